@@ -1,0 +1,14 @@
+"""fp64 CPU oracle for fused linear cross-entropy. TEST INFRASTRUCTURE ONLY.
+
+Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline and reference
+legs may import this package. The CUDA library and its Python binding never
+import it and share no code with it.
+
+Parity status: every function is pinned. There is no "parity unpinned" entry.
+tests/test_oracle_pins.py holds the pins: torch fp64 autograd, finite
+differences, closed forms, invariants and hand-derived golden values.
+"""
+from .flce_oracle import (  # noqa: F401
+    REDUCTIONS, backward, check_targets, dlogits, forward, forward_rows,
+    grad_hidden_rows, grad_weight_rows, row_gamma, row_terms, transformed_logits,
+)
