@@ -1,0 +1,418 @@
+"""Throughput of fused linear cross-entropy forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one forward + backward (all three gradients) of the workload on
+one batch of synthetic, seeded inputs. The default workload is
+bf16_v128256_bias_zloss: N=8192 tokens, H=4096, V=128256, bias, Zipf targets,
+5% ignored, z-loss 1e-4, mean reduction.
+
+Timing:
+- ``value`` is tokens/s with the inputs already resident in HBM. It is
+  measured with CUDA events over K steps on the launching stream, with a
+  barrier and a device synchronize on both sides, max over ranks.
+- ``e2e`` is the same metric through the public PyTorch API with host
+  buffers. Each step copies the step's inputs from pinned host memory and
+  reads the loss back.
+- The inputs are larger than L2 (W alone is 1.05 GB), so no L2 flush is
+  needed between steps.
+
+For N > 1 ranks (torchrun) every rank runs its own batch (weak scaling) and
+there is no collective on the data path. The only collective is the timing
+reduction.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
+same workload. The oracle is the only reference implementation in this
+project. That leg and the ``cpu_baseline`` field are the only places
+bench.py runs the oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_cross_entropy_tiled_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fwd+bwd tokens/s and TFLOP/s (8NHV) vs GB300 bf16 peak, N=8192 H=4096 V=128k"
+UNIT = "tokens/s"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(bf16_burst=d.get("bf16_tflops"), bf16_sustained=d.get("bf16_tflops_sustained"),
+                    hbm=d.get("hbm_gbs"), source="measured")
+    return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (read-only queries)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if "Active" in v and "Not" not in v:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def kernel_flops(name: str, w: wl.Workload, chunk_rows: list[int]) -> float:
+    """Algorithmic FLOPs of one launch of each tensor-core kernel."""
+    N, H, V = w.N, w.H, w.V
+    if name == "flce_fwd_tc":
+        return 2.0 * N * H * V
+    if name in ("flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
+        # one launch per row chunk; the chunks are equal except possibly the last
+        return 2.0 * (N / len(chunk_rows)) * H * V
+    return 0.0
+
+
+def sources_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_cross_entropy_tiled_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary.
+
+    Returns None if there is no summary, or if the kernel sources have changed
+    since the summary was captured.
+    """
+    p = os.path.join(PROFILES, "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("sources_digest") != sources_digest():
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    if not e or e.get("workload") != workload:
+        return None
+    return e.get("bytes_per_launch")
+
+
+def cpu_oracle_rate(w: wl.Workload, inputs: dict, target_s: float = 15.0):
+    """fp64 oracle fwd+bwd on a bounded row sample. Returns (tokens/s, rows, seconds, threads)."""
+    import oracle
+
+    kw = dict(ignore_index=wl.IGNORE_INDEX, logit_scale=w.logit_scale, softcap=w.softcap,
+              z_loss_multiplier=w.z_loss_multiplier, reduction=w.reduction)
+
+    def run(n):
+        rows = np.arange(n)
+        t0 = time.perf_counter()
+        oracle.forward(inputs["hidden"][rows], inputs["weight"], inputs["targets"][rows],
+                       bias=inputs["bias"], **kw)
+        oracle.backward(inputs["hidden"][rows], inputs["weight"], inputs["targets"][rows],
+                        bias=inputs["bias"], **kw)
+        return time.perf_counter() - t0
+
+    n0 = 16
+    t0 = run(n0)
+    n = int(min(w.N, max(n0, n0 * target_s / max(t0, 1e-3))))
+    t = run(n) if n != n0 else t0
+    return n / t, n, t, os.cpu_count() or 1
+
+
+def reference_main(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    inputs = wl.generate(w)
+    per_step = max(5.0, 150.0 / max(1, args.steps + args.warmup))
+    rate, n, t, cores = cpu_oracle_rate(w, inputs, target_s=per_step)
+    import oracle
+    kw = dict(ignore_index=wl.IGNORE_INDEX, logit_scale=w.logit_scale, softcap=w.softcap,
+              z_loss_multiplier=w.z_loss_multiplier, reduction=w.reduction)
+    rows = np.arange(n)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(inputs["hidden"][rows], inputs["weight"], inputs["targets"][rows],
+                       bias=inputs["bias"], **kw)
+        oracle.backward(inputs["hidden"][rows], inputs["weight"], inputs["targets"][rows],
+                        bias=inputs["bias"], **kw)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    step_s = max(times) if times else t
+    value = n / step_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "sample_rows": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def ours_main(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from linear_cross_entropy_tiled_gb300 import _lib, fused_linear_cross_entropy
+    from linear_cross_entropy_tiled_gb300.functional import flce_backward, flce_forward
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # weak scaling: every rank draws its own batch
+    wr = w.replace(seed=w.seed + 7919 * rank)
+    inputs = wl.generate(wr)
+
+    def dev_tensor(name):
+        if w.dtype == "bf16":
+            return torch.from_numpy(inputs[name + "_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(inputs[name]).to(dev)
+
+    h = dev_tensor("hidden")
+    W = dev_tensor("weight")
+    b = dev_tensor("bias") if w.bias else None
+    t = torch.from_numpy(inputs["targets"]).to(dev)
+    p = _lib.make_params(N=w.N, H=w.H, V=w.V,
+                         dtype=_lib.FLCE_BF16 if w.dtype == "bf16" else _lib.FLCE_F32,
+                         reduction=w.reduction, ignore_index=wl.IGNORE_INDEX,
+                         logit_scale=w.logit_scale, softcap=w.softcap,
+                         z_loss_multiplier=w.z_loss_multiplier, has_bias=w.bias,
+                         deterministic=w.deterministic)
+    fws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD), dtype=torch.uint8, device=dev)
+    bws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD), dtype=torch.uint8, device=dev)
+    gh, gw = torch.empty_like(h), torch.empty_like(W)
+    gb = torch.empty_like(b) if b is not None else None
+    gl = torch.ones(w.N if w.reduction == "none" else 1, dtype=torch.float32, device=dev)
+
+    def step():
+        loss, lse, nc, ent, _ = flce_forward(p, h, W, t, b, return_metrics=w.metrics, workspace=fws)
+        flce_backward(p, h, W, t, lse, gl, b, workspace=bws, out=(gh, gw, gb))
+        return loss
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    _lib.check(_lib.check_status(bws.data_ptr(), torch.cuda.current_stream(dev).cuda_stream),
+               "warm-up backward")
+
+    # ---------------- device-resident timed region ----------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    barrier()
+    n_launch0 = _lib.launch_count()
+    _lib.profiling_enable(True)
+    _lib.profiling_read()  # clear
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    _lib.profiling_enable(False)
+    launches = _lib.launch_count() - n_launch0
+    kernels = _lib.profiling_read()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    _lib.check(_lib.check_status(bws.data_ptr(), stream.cuda_stream), "timed backward")
+
+    # ---------------- end to end, host buffers ----------------
+    e2e = None
+    if not args.no_e2e:
+        hp = h.cpu().pin_memory()
+        Wp = W.cpu().pin_memory()
+        bp = b.cpu().pin_memory() if b is not None else None
+        tp = t.cpu().pin_memory()
+        h2d = hp.numel() * hp.element_size() + Wp.numel() * Wp.element_size() + \
+            tp.numel() * tp.element_size() + (bp.numel() * bp.element_size() if bp is not None else 0)
+        loss_host = torch.empty(1 if w.reduction != "none" else w.N, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            hd = hp.to(dev, non_blocking=True).requires_grad_(True)
+            Wd = Wp.to(dev, non_blocking=True).requires_grad_(True)
+            bd = bp.to(dev, non_blocking=True).requires_grad_(True) if bp is not None else None
+            td = tp.to(dev, non_blocking=True)
+            loss = fused_linear_cross_entropy(
+                hd, Wd, td, bias=bd, ignore_index=wl.IGNORE_INDEX, logit_scale=w.logit_scale,
+                softcap=w.softcap, z_loss_multiplier=w.z_loss_multiplier, reduction=w.reduction,
+                return_metrics=w.metrics, deterministic=w.deterministic)
+            if isinstance(loss, tuple):
+                loss = loss[0]
+            loss.sum().backward() if w.reduction == "none" else loss.backward()
+            loss_host.copy_(loss.detach().reshape(-1), non_blocking=True)
+
+        e2e_steps = max(3, args.steps // 2)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        ems = f0.elapsed_time(f1) / e2e_steps
+        if world > 1:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": world * w.N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(loss_host.numel() * 4), "ms_per_step": ems,
+               "steps": e2e_steps, "api": "fused_linear_cross_entropy + backward"}
+
+    if rank == 0:
+        peaks = load_peaks()
+        flops = w.flops_fwd_bwd
+        tflops = flops / (ms * 1e-3) / 1e12
+        chunk_rows = bwd_chunks(p)
+        kern = []
+        for name, n, tot in kernels:
+            per = tot / n if n else 0.0
+            f = kernel_flops(name, w, chunk_rows)
+            kern.append({"name": name, "launches": n, "ms_per_launch": per,
+                         "share": tot / max(sum(k[2] for k in kernels), 1e-9),
+                         "tflops": (f / (per * 1e-3) / 1e12) if (f and per) else None})
+        kern.sort(key=lambda k: -k["share"])
+        dom = kern[0] if kern else None
+        roof = None
+        if dom is not None and dom["tflops"] is not None:
+            roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
+                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": dom["tflops"] / peaks["bf16_sustained"],
+                    "peak_kind": f"bf16 sustained ({peaks['source']})",
+                    "traffic": traffic_for(dom["name"], w.name)}
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            rate, n, tcpu, cores = cpu_oracle_rate(w, inputs)
+            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64 ({tcpu:.1f} s)"}
+        line = {
+            "metric": METRIC, "value": world * w.N / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; inputs generated on the host)",
+            "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "bias": w.bias,
+                       "targets": w.targets, "ignore_frac": w.ignore_frac,
+                       "z_loss_multiplier": w.z_loss_multiplier, "logit_scale": w.logit_scale,
+                       "softcap": w.softcap, "reduction": w.reduction, "metrics": w.metrics,
+                       "l2": "inputs larger than L2 (W alone is 1.05 GB); no flush"},
+            "tflops": tflops, "tflops_per_gpu": tflops,
+            "frac_of_peak": {"bf16_burst": tflops / peaks["bf16_burst"],
+                             "bf16_sustained": tflops / peaks["bf16_sustained"],
+                             "source": peaks["source"]},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "kernels": kern,
+            "logits_bytes_avoided": w.logits_bytes_avoided,
+            "peak_device_bytes": int(torch.cuda.max_memory_allocated(dev)),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def bwd_chunks(p) -> list[int]:
+    N = p.N
+    if N <= 128:
+        return [N]
+    half = -(-(-(-N // 2)) // 128) * 128
+    rows, r = [], 0
+    while r < N:
+        rows.append(min(half, N - r))
+        r += half
+    return rows
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=wl.HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_main(args, w)
+    return ours_main(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

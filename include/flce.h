@@ -1,0 +1,200 @@
+/*
+ * flce.h -- C ABI of the GB300 (sm_103a) fused linear cross-entropy library.
+ *
+ * What the library computes. hidden is h[N,H], weight is W[V,H], bias is b[V]
+ * (optional) and targets is t[N]. With s = logit_scale, c = softcap and
+ * zeta = z_loss_multiplier:
+ *
+ *   a_ij = sum_k h_ik W_jk
+ *   u_ij = (a_ij + b_j) * s
+ *   z_ij = c * tanh(u_ij / c)   if c > 0, else u_ij
+ *   lse_i = log sum_j exp z_ij
+ *   loss_i = lse_i - z_{i,t_i} + zeta * lse_i^2   (valid rows, t_i != ignore_index)
+ *   loss_i = 0                                    (ignored rows)
+ *
+ * Sources, by passage:
+ * - The linear + cross-entropy definition: quack-kernels diff,
+ *   quack/linear_cross_entropy.py, linear_cross_entropy_func_ref.
+ * - bias, logit_scale, softcap and the metrics: fused-linear-ce README,
+ *   sections "Full signature" and "Metrics for free".
+ * - z-loss: "Chunked Linear Cross-Entropy", section "Usage". The page gives
+ *   the keyword but not the formula; zeta * lse^2 is this library's reading.
+ * - The global-mean semantics: "Chunked Linear Loss", section "Reduction
+ *   semantics".
+ *
+ * The N x V logits are never stored.
+ * - The forward sweeps vocabulary tiles and keeps an online log-sum-exp
+ *   (fused-linear-ce README, "Algorithm").
+ * - The backward recomputes each logit tile and forms dlogits from it in
+ *   registers (same section). dlogits goes to HBM as bf16 for a bounded row
+ *   chunk of at most ceil(N/2) rows (at most ceil(N/2) x V elements, or
+ *   fewer when that would exceed 4 GiB), never for all N rows. Two tensor-core
+ *   contractions then accumulate grad_hidden = dlogits W and
+ *   grad_weight = dlogits^T h, as the quack diff and "Chunked Linear Loss",
+ *   section "Gradient handling", do per chunk.
+ *
+ * Conventions common to every entry point:
+ * - Pointers named "device" must point to device memory of the current CUDA
+ *   device. All tensors are dense and row-major (the last index moves
+ *   fastest) and 16-byte aligned.
+ * - The caller owns every buffer. The library allocates no device memory. It
+ *   keeps only small per-device host state: attributes, tensor-map encoder,
+ *   profiling events.
+ * - Every call is asynchronous on `stream` and never synchronises the host,
+ *   except flce_check_status and flce_profiling_read.
+ * - Return codes are the FLCE_* values below. An argument error is reported
+ *   before any work is enqueued. Errors the device detects (a target out of
+ *   range, an expired bounded wait) are written to a status word at the start
+ *   of the workspace. flce_check_status reads it.
+ * - Outputs are overwritten, never accumulated into.
+ * - Results do not depend on launch timing. Every reduction runs in a fixed
+ *   order, so repeated calls on the same inputs give bit-identical outputs.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. NULL is the legacy default stream. */
+typedef struct CUstream_st* flce_stream_t;
+
+typedef enum {
+  FLCE_F32 = 0,  /* fp32 hidden/weight/bias/grads; SIMT fp32 arithmetic        */
+  FLCE_BF16 = 1  /* bf16 hidden/weight/bias/grads; tcgen05 bf16 MMA, fp32 acc. */
+} flce_dtype;
+
+typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1, FLCE_NONE = 2 } flce_reduction;
+
+typedef enum { FLCE_PASS_FORWARD = 0, FLCE_PASS_BACKWARD = 1 } flce_pass;
+
+enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, dtype, reduction or scalar   */
+  FLCE_ERR_UNSUPPORTED = 2,  /* the current device is not sm_103 (GB300)            */
+  FLCE_ERR_ALIGNMENT = 3,    /* a pointer is not 16-B aligned, or H % 8 != 0       */
+  FLCE_ERR_WORKSPACE = 4,    /* NULL workspace or ws_bytes below the required size */
+  FLCE_ERR_CUDA = 5,         /* a CUDA runtime call failed                          */
+  FLCE_ERR_TARGET_RANGE = 6, /* device: a target outside [0,V) and != ignore_index  */
+  FLCE_ERR_TIMEOUT = 7       /* device: a bounded wait in a kernel expired          */
+};
+
+typedef struct {
+  int64_t N;                 /* rows (tokens), >= 0                                   */
+  int64_t H;                 /* hidden size, >= 1; bf16 needs H % 8 == 0 (16-B rows)  */
+  int64_t V;                 /* vocabulary size, >= 1                                 */
+  int32_t dtype;             /* flce_dtype of hidden, weight, bias and all gradients  */
+  int32_t reduction;         /* flce_reduction                                        */
+  int64_t ignore_index;      /* rows whose target equals it are ignored (usually -100)*/
+  float logit_scale;         /* s: finite and nonzero (1.0 = off)                     */
+  float softcap;             /* c: > 0 enables the tanh softcap; <= 0 disables it     */
+  float z_loss_multiplier;   /* zeta: finite, >= 0 (0.0 = off)                        */
+  int32_t has_bias;          /* 1 if a bias vector is given                           */
+  int32_t deterministic;     /* accepted for API parity; every reduction here is
+                                already in fixed order, so both values give the same
+                                bits                                                  */
+} flce_params;
+
+/*
+ * Device bytes the caller must provide as `workspace` for one pass. The
+ * forward and backward need different amounts, and one workspace may serve
+ * both passes in turn. For the headline size (N=8192, H=4096, V=128256,
+ * bf16) the forward needs a few MB. The backward needs about 3.2 GB:
+ * - a 4096-row bf16 dlogits chunk (1.05 GB);
+ * - an fp32 grad_weight partial (2.1 GB);
+ * - per-128-row bias partial sums.
+ * Returns FLCE_OK and sets *bytes, or an argument error.
+ */
+int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
+
+/*
+ * Forward: loss, per-row log-sum-exp and optional metrics.
+ *   hidden    device [N,H] dtype
+ *   weight    device [V,H] dtype
+ *   bias      device [V] dtype, or NULL when has_bias == 0
+ *   targets   device [N] int64
+ *   loss      device float: [1] for SUM and MEAN, [N] for NONE (ignored rows 0).
+ *             MEAN divides by the number of valid rows in this call. With no
+ *             valid row it is NaN (0/0, as F.cross_entropy gives).
+ *   lse       device float [N]: lse_i of every row, ignored rows included.
+ *             flce_backward needs it.
+ *   num_correct  device int64 [1] or NULL: #{valid i : argmax_j z_ij == t_i}.
+ *             Ties go to the lowest j.
+ *   entropy_sum  device float [1] or NULL: sum over valid rows of the softmax
+ *             entropy of z_i in nats.
+ *   Whether or not the metric pointers are given, loss and lse are
+ *   bit-identical (fused-linear-ce README, "Metrics for free").
+ *   workspace device, >= flce_workspace_bytes(p, FLCE_PASS_FORWARD) bytes.
+ *   With N == 0, hidden, targets and lse may be NULL (and loss too for NONE).
+ *   SUM then gives 0 and MEAN gives NaN.
+ */
+int flce_forward(const flce_params* p, const void* hidden, const void* weight,
+                 const void* bias, const int64_t* targets, float* loss, float* lse,
+                 int64_t* num_correct, float* entropy_sum, void* workspace,
+                 size_t ws_bytes, flce_stream_t stream);
+
+/*
+ * Backward: gradients of the reduced loss, recomputing every logit tile.
+ *   lse         device float [N], as written by flce_forward on the same inputs
+ *   grad_loss   device float: [1] for SUM and MEAN, [N] for NONE. This is the
+ *               upstream gradient of the loss output.
+ *   grad_hidden device [N,H] dtype, or NULL to skip it
+ *   grad_weight device [V,H] dtype, or NULL to skip it
+ *   grad_bias   device [V] dtype, or NULL to skip it (requires has_bias == 1
+ *               when given)
+ * dlogits is rounded to bf16 before the two bf16 contractions. grad_weight is
+ * accumulated in fp32 across row chunks, in chunk order, and cast once
+ * ("Chunked Linear Loss", section "Weight-gradient accumulation dtype", the
+ * "fp32" default).
+ *   workspace   device, >= flce_workspace_bytes(p, FLCE_PASS_BACKWARD) bytes
+ * With N == 0, the row-indexed pointers may be NULL. grad_weight and grad_bias
+ * are then zero-filled.
+ */
+int flce_backward(const flce_params* p, const void* hidden, const void* weight,
+                  const void* bias, const int64_t* targets, const float* lse,
+                  const float* grad_loss, void* grad_hidden, void* grad_weight,
+                  void* grad_bias, void* workspace, size_t ws_bytes,
+                  flce_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device-detected status of the last
+ * pass that used `workspace`. The status is FLCE_OK, FLCE_ERR_TARGET_RANGE or
+ * FLCE_ERR_TIMEOUT, or FLCE_ERR_CUDA if the synchronisation itself failed.
+ */
+int flce_check_status(const void* workspace, flce_stream_t stream);
+
+/* Static English description of a return code. Never NULL. */
+const char* flce_error_string(int code);
+
+/* Static text naming the last CUDA or tensor-map failure on this host
+ * thread (empty if none). It is meant for diagnostics after FLCE_ERR_CUDA or
+ * FLCE_ERR_UNSUPPORTED. Never NULL. */
+const char* flce_last_error_detail(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t flce_launch_count(void);
+
+/*
+ * Per-kernel timing on the launching stream. While enabled, each launch is
+ * bracketed by two CUDA events. flce_profiling_read synchronises those events.
+ * It fills up to `max` records, in first-launch order, with the kernel name,
+ * the number of launches and their total duration in milliseconds. It then
+ * clears the counts. *count is set to the number of distinct kernels.
+ */
+typedef struct {
+  char name[48];
+  uint64_t launches;
+  double total_ms;
+} flce_kernel_time;
+
+int flce_profiling_enable(int on);
+int flce_profiling_read(flce_kernel_time* out, int max, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLCE_H_ */

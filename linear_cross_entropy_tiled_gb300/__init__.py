@@ -1,0 +1,10 @@
+"""Fused linear cross-entropy for GB300 (sm_103a).
+
+The CUDA library libflce.so does all of the computation. Its C ABI is in
+include/flce.h and ``_lib`` binds it with ctypes. ``functional`` wraps it for
+PyTorch tensors and autograd. Importing this package loads nothing: the
+library is loaded on the first call, and that call raises if it is missing.
+"""
+from .functional import fused_linear_cross_entropy, flce_backward, flce_forward  # noqa: F401
+
+__all__ = ["fused_linear_cross_entropy", "flce_forward", "flce_backward"]

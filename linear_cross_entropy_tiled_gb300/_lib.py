@@ -1,0 +1,166 @@
+"""ctypes binding of libflce.so, the C ABI declared in include/flce.h.
+
+This module only marshals arguments. Every step of the computation runs in
+the library's CUDA kernels. There is no Python or CPU fallback: if the library
+is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
+
+FLCE_F32, FLCE_BF16 = 0, 1
+FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
+FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD = 0, 1
+REDUCTIONS = {"sum": FLCE_SUM, "mean": FLCE_MEAN, "none": FLCE_NONE}
+
+ERRORS = {
+    0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
+    4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
+}
+
+# Every exported symbol of include/flce.h.
+EXPORTS = (
+    "flce_workspace_bytes", "flce_forward", "flce_backward", "flce_check_status",
+    "flce_error_string", "flce_last_error_detail", "flce_launch_count",
+    "flce_profiling_enable", "flce_profiling_read",
+)
+
+
+class FlceParams(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int64),
+        ("H", ctypes.c_int64),
+        ("V", ctypes.c_int64),
+        ("dtype", ctypes.c_int32),
+        ("reduction", ctypes.c_int32),
+        ("ignore_index", ctypes.c_int64),
+        ("logit_scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+        ("z_loss_multiplier", ctypes.c_float),
+        ("has_bias", ctypes.c_int32),
+        ("deterministic", ctypes.c_int32),
+    ]
+
+
+class FlceKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_uint64),
+                ("total_ms", ctypes.c_double)]
+
+
+class FlceError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        msg = f"{where}: {ERRORS.get(code, code)} ({error_string(code)})"
+        if detail:
+            msg += f" [{detail}]"
+        super().__init__(msg)
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libflce.so. It raises if the library is missing: the extension must be built first."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -m linear_cross_entropy_tiled_gb300.build). There is no fallback path.")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER(FlceParams)
+    lib.flce_workspace_bytes.argtypes = [P, ctypes.c_int, ctypes.POINTER(sz)]
+    lib.flce_workspace_bytes.restype = ctypes.c_int
+    lib.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward.restype = ctypes.c_int
+    lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_backward.restype = ctypes.c_int
+    lib.flce_check_status.argtypes = [vp, vp]
+    lib.flce_check_status.restype = ctypes.c_int
+    lib.flce_error_string.argtypes = [ctypes.c_int]
+    lib.flce_error_string.restype = ctypes.c_char_p
+    lib.flce_last_error_detail.argtypes = []
+    lib.flce_last_error_detail.restype = ctypes.c_char_p
+    lib.flce_launch_count.argtypes = []
+    lib.flce_launch_count.restype = ctypes.c_uint64
+    lib.flce_profiling_enable.argtypes = [ctypes.c_int]
+    lib.flce_profiling_enable.restype = ctypes.c_int
+    lib.flce_profiling_read.argtypes = [ctypes.POINTER(FlceKernelTime), ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_int)]
+    lib.flce_profiling_read.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load().flce_error_string(code).decode()
+
+
+def last_error_detail() -> str:
+    return load().flce_last_error_detail().decode()
+
+
+def check(code: int, where: str) -> None:
+    if code != 0:
+        raise FlceError(code, where, last_error_detail())
+
+
+def make_params(N: int, H: int, V: int, dtype: int, reduction: str = "mean",
+                ignore_index: int = -100, logit_scale: float = 1.0,
+                softcap: Optional[float] = None, z_loss_multiplier: float = 0.0,
+                has_bias: bool = False, deterministic: bool = False) -> FlceParams:
+    if reduction not in REDUCTIONS:
+        raise ValueError(f"reduction must be one of {tuple(REDUCTIONS)}, got {reduction!r}")
+    return FlceParams(N=N, H=H, V=V, dtype=dtype, reduction=REDUCTIONS[reduction],
+                      ignore_index=ignore_index, logit_scale=logit_scale,
+                      softcap=softcap if softcap else 0.0,
+                      z_loss_multiplier=z_loss_multiplier, has_bias=1 if has_bias else 0,
+                      deterministic=1 if deterministic else 0)
+
+
+def workspace_bytes(p: FlceParams, pass_: int) -> int:
+    n = ctypes.c_size_t(0)
+    check(load().flce_workspace_bytes(ctypes.byref(p), pass_, ctypes.byref(n)),
+          "flce_workspace_bytes")
+    return n.value
+
+
+def forward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int, loss: int,
+                lse: int, num_correct: int, entropy_sum: int, ws: int, ws_bytes: int,
+                stream: int) -> int:
+    return load().flce_forward(ctypes.byref(p), hidden, weight, bias, targets, loss, lse,
+                               num_correct, entropy_sum, ws, ws_bytes, stream)
+
+
+def backward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int, lse: int,
+                 grad_loss: int, grad_hidden: int, grad_weight: int, grad_bias: int, ws: int,
+                 ws_bytes: int, stream: int) -> int:
+    return load().flce_backward(ctypes.byref(p), hidden, weight, bias, targets, lse, grad_loss,
+                                grad_hidden, grad_weight, grad_bias, ws, ws_bytes, stream)
+
+
+def check_status(ws: int, stream: int) -> int:
+    return load().flce_check_status(ws, stream)
+
+
+def launch_count() -> int:
+    return int(load().flce_launch_count())
+
+
+def profiling_enable(on: bool) -> None:
+    check(load().flce_profiling_enable(1 if on else 0), "flce_profiling_enable")
+
+
+def profiling_read(max_kernels: int = 64) -> list[tuple[str, int, float]]:
+    arr = (FlceKernelTime * max_kernels)()
+    n = ctypes.c_int(0)
+    check(load().flce_profiling_read(arr, max_kernels, ctypes.byref(n)), "flce_profiling_read")
+    return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms))
+            for i in range(min(n.value, max_kernels))]

@@ -1,0 +1,672 @@
+// Host runtime behind the C ABI declared in include/flce.h: argument
+// validation, workspace layout, TMA tensor maps, tile-schedule selection and
+// the launch sequence of each pass.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "flce.h"
+#include "kernels.h"
+
+using namespace flce;
+
+namespace {
+
+// ------------------------------------------------------------ device state
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_detail[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s", what, cudaGetErrorString(e));
+  return FLCE_ERR_CUDA;
+}
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return FLCE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.init = true;
+  }
+  *out = d;
+  if (d.major != 10 || d.minor != 3) {
+    snprintf(g_detail, sizeof(g_detail), "device is sm_%d%d; this library is built for sm_103a",
+             d.major, d.minor);
+    return FLCE_ERR_UNSUPPORTED;
+  }
+  return FLCE_OK;
+}
+
+// -------------------------------------------------------------- profiling
+struct Pending {
+  int name;
+  cudaEvent_t e0, e1;
+};
+std::mutex g_prof_mu;
+bool g_prof = false;
+std::vector<std::string> g_names;
+std::vector<uint64_t> g_counts;
+std::vector<double> g_ms;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+int name_index(const char* n) {
+  for (size_t i = 0; i < g_names.size(); ++i)
+    if (g_names[i] == n) return static_cast<int>(i);
+  g_names.emplace_back(n);
+  g_counts.push_back(0);
+  g_ms.push_back(0.0);
+  return static_cast<int>(g_names.size() - 1);
+}
+
+template <class F>
+int launch(const char* name, cudaStream_t s, F&& f) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  std::unique_lock<std::mutex> lk(g_prof_mu);
+  const bool prof = g_prof;
+  Pending p{};
+  if (prof) {
+    p.name = name_index(name);
+    p.e0 = pool_event();
+    cudaEventRecord(p.e0, s);
+  }
+  lk.unlock();
+  const cudaError_t e = f();
+  if (prof) {
+    lk.lock();
+    p.e1 = pool_event();
+    cudaEventRecord(p.e1, s);
+    g_pending.push_back(p);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return FLCE_OK;
+}
+
+// ------------------------------------------------------------ validation
+int validate(const flce_params* p) {
+  if (p == nullptr) return FLCE_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 30);
+  if (p->N < 0 || p->H < 1 || p->V < 1 || p->N > lim || p->H > lim || p->V > lim)
+    return FLCE_ERR_INVALID_ARG;
+  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16) return FLCE_ERR_INVALID_ARG;
+  if (p->reduction < FLCE_SUM || p->reduction > FLCE_NONE) return FLCE_ERR_INVALID_ARG;
+  if (!isfinite(p->logit_scale) || p->logit_scale == 0.f) return FLCE_ERR_INVALID_ARG;
+  if (!isfinite(p->softcap)) return FLCE_ERR_INVALID_ARG;
+  if (!isfinite(p->z_loss_multiplier) || p->z_loss_multiplier < 0.f) return FLCE_ERR_INVALID_ARG;
+  if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
+  if (p->dtype == FLCE_BF16 && (p->H % 8) != 0) return FLCE_ERR_ALIGNMENT;
+  return FLCE_OK;
+}
+
+bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------ workspace layouts
+constexpr int kMinPanelTiles = 4;
+constexpr int kMaxPanelTiles = 32;
+constexpr size_t kHeader = 256;
+constexpr size_t kChunkByteCap = size_t(4) << 30;
+
+struct FwdLayout {
+  int num_panels_max;
+  int nblk;
+  size_t partials, zt, blk_loss, blk_ent, blk_correct, blk_valid, total;
+};
+
+FwdLayout fwd_layout(const flce_params* p) {
+  FwdLayout L{};
+  const int64_t N = p->N, V = p->V;
+  if (p->dtype == FLCE_BF16)
+    L.num_panels_max = static_cast<int>(ceil_div(ceil_div(V, kBN), kMinPanelTiles));
+  else
+    L.num_panels_max = static_cast<int>(ceil_div(V, kSimtPanelCols));
+  L.nblk = static_cast<int>(ceil_div(N, kMergeThreads));
+  size_t o = kHeader;
+  L.partials = o;
+  o = align_up(o + size_t(L.num_panels_max) * N * sizeof(float4), 256);
+  L.zt = o;
+  o = align_up(o + size_t(N) * 4, 256);
+  L.blk_loss = o;
+  o = align_up(o + size_t(L.nblk) * 8, 256);
+  L.blk_ent = o;
+  o = align_up(o + size_t(L.nblk) * 8, 256);
+  L.blk_correct = o;
+  o = align_up(o + size_t(L.nblk) * 8, 256);
+  L.blk_valid = o;
+  o = align_up(o + size_t(L.nblk) * 8, 256);
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  int64_t chunk, V_pad;
+  int nchunks, rowblk, n_rowblocks;
+  size_t coef, ds, dw, bias_part, total;
+};
+
+BwdLayout bwd_layout(const flce_params* p) {
+  BwdLayout L{};
+  const int64_t N = p->N, V = p->V, H = p->H;
+  const size_t elem = p->dtype == FLCE_BF16 ? 2 : 4;
+  L.V_pad = (V + 7) / 8 * 8;
+  if (N <= kBM) {
+    L.chunk = N;
+  } else {
+    const int64_t half = ceil_div(ceil_div(N, 2), kBM) * kBM;
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem)) / kBM * kBM;
+    if (cap < kBM) cap = kBM;
+    // FLCE_MAX_CHUNK_ROWS (a multiple of 128) lowers the row-chunk cap. The
+    // work and the result are the same; it is there so tests can reach the
+    // three-or-more-chunk schedule at small sizes.
+    if (const char* env = getenv("FLCE_MAX_CHUNK_ROWS")) {
+      const long long r = atoll(env) / kBM * kBM;
+      if (r >= kBM && r < cap) cap = r;
+    }
+    L.chunk = half < cap ? half : cap;
+  }
+  L.nchunks = N > 0 ? static_cast<int>(ceil_div(N, L.chunk)) : 0;
+  L.rowblk = p->dtype == FLCE_BF16 ? kBM : kSimtTile;
+  L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
+  size_t o = kHeader;
+  L.coef = o;
+  o = align_up(o + size_t(N) * sizeof(float4), 256);
+  L.ds = o;
+  o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
+  L.dw = o;
+  if (p->dtype == FLCE_BF16 && L.nchunks > 1) o = align_up(o + size_t(V) * H * 4, 1024);
+  L.bias_part = o;
+  if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
+  L.total = o;
+  return L;
+}
+
+// Vocabulary tiles per panel. Units are (panel, row block) pairs in
+// panel-major order, handed out round-robin to `sms` persistent CTAs. So at
+// any moment the CTAs work on the same few panels: the W panel is read from
+// HBM about once and shared through L2. The panel length is chosen to
+// minimise the largest tile count of any CTA, which is the critical path.
+int choose_panel_tiles(int n_blocks, int v_tiles, int sms, int* grid_out) {
+  int best = kMinPanelTiles;
+  long long best_cost = -1;
+  int best_grid = 1;
+  for (int pt = kMinPanelTiles; pt <= kMaxPanelTiles; ++pt) {
+    const long long P = ceil_div(v_tiles, pt);
+    const long long U = P * n_blocks;
+    const long long G = U < sms ? U : sms;
+    const long long full_end = (P - 1) * n_blocks;
+    const long long last_len = v_tiles - (P - 1) * pt;
+    long long cost = 0;
+    for (long long c = 0; c < G; ++c) {
+      auto cnt = [&](long long x) { return x > c ? (x - c - 1) / G + 1 : 0; };
+      const long long t = cnt(full_end) * pt + (cnt(U) - cnt(full_end)) * last_len;
+      if (t > cost) cost = t;
+    }
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && pt > best)) {
+      best_cost = cost;
+      best = pt;
+      best_grid = static_cast<int>(G);
+    }
+  }
+  *grid_out = best_grid;
+  return best;
+}
+
+// ------------------------------------------------------------ tensor maps
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_detail, sizeof(g_detail), "cuTensorMapEncodeTiled failed (%d) dims %llu x %llu",
+             static_cast<int>(r), static_cast<unsigned long long>(inner),
+             static_cast<unsigned long long>(outer));
+    return FLCE_ERR_CUDA;
+  }
+  return FLCE_OK;
+}
+
+float inv_cap(const flce_params* p) { return p->softcap > 0.f ? 1.f / p->softcap : 0.f; }
+
+}  // namespace
+
+// ===================================================================== ABI
+extern "C" {
+
+const char* flce_error_string(int code) {
+  switch (code) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_INVALID_ARG: return "invalid argument";
+    case FLCE_ERR_UNSUPPORTED: return "unsupported device (needs sm_103 / GB300)";
+    case FLCE_ERR_ALIGNMENT: return "misaligned pointer or H not a multiple of 8";
+    case FLCE_ERR_WORKSPACE: return "workspace missing or too small";
+    case FLCE_ERR_CUDA: return "CUDA runtime error";
+    case FLCE_ERR_TARGET_RANGE: return "target outside [0, V) and not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    default: return "unknown error code";
+  }
+}
+
+const char* flce_last_error_detail(void) { return g_detail; }
+
+uint64_t flce_launch_count(void) { return g_launches.load(); }
+
+int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes) {
+  const int v = validate(p);
+  if (v != FLCE_OK) return v;
+  if (bytes == nullptr) return FLCE_ERR_INVALID_ARG;
+  if (pass == FLCE_PASS_FORWARD) {
+    *bytes = fwd_layout(p).total;
+  } else if (pass == FLCE_PASS_BACKWARD) {
+    *bytes = bwd_layout(p).total;
+  } else {
+    return FLCE_ERR_INVALID_ARG;
+  }
+  return FLCE_OK;
+}
+
+int flce_forward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
+                 const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
+                 float* entropy_sum, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  // Row-indexed pointers may be NULL only when there are no rows.
+  const bool rows = p->N > 0;
+  if (weight == nullptr || (rows && (hidden == nullptr || targets == nullptr || lse == nullptr)) ||
+      (loss == nullptr && (rows || p->reduction != FLCE_NONE)))
+    return FLCE_ERR_INVALID_ARG;
+  if ((p->has_bias != 0) != (bias != nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (workspace == nullptr) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(weight) || (bias && !aligned16(bias)) ||
+      !aligned16(workspace) || !aligned16(targets))
+    return FLCE_ERR_ALIGNMENT;
+  const FwdLayout L = fwd_layout(p);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+
+  const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  FwdArgs fa{};
+  fa.N = N;
+  fa.H = H;
+  fa.V = V;
+  fa.scale = p->logit_scale;
+  fa.softcap = p->softcap > 0.f ? p->softcap : 0.f;
+  fa.inv_softcap = inv_cap(p);
+  fa.bias = bias;
+  fa.targets = targets;
+  fa.ignore_index = p->ignore_index;
+  fa.partials = reinterpret_cast<float4*>(ws + L.partials);
+  fa.zt = reinterpret_cast<float*>(ws + L.zt);
+  fa.status = status;
+
+  if (N > 0) {
+    if (p->dtype == FLCE_BF16) {
+      fa.n_blocks = static_cast<int>(ceil_div(N, kBM));
+      fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
+      int grid = 1;
+      fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.sms, &grid);
+      fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
+      fa.num_units = fa.num_panels * fa.n_blocks;
+      CUtensorMap tm_h, tm_w;
+      if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
+      if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBN)) != FLCE_OK) return v;
+      v = launch("flce_fwd_tc", st, [&] {
+        return launch_fwd_tc(tm_h, tm_w, fa, bias != nullptr, p->softcap > 0.f, grid, st);
+      });
+    } else {
+      fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
+      fa.num_panels = static_cast<int>(ceil_div(V, kSimtPanelCols));
+      fa.num_units = fa.num_panels * fa.n_blocks;
+      v = launch("flce_fwd_simt", st, [&] {
+        return launch_fwd_simt(static_cast<const float*>(hidden),
+                               static_cast<const float*>(weight), fa, st);
+      });
+    }
+    if (v != FLCE_OK) return v;
+    MergeArgs ma{};
+    ma.N = N;
+    ma.V = V;
+    ma.num_panels = fa.num_panels;
+    ma.reduction = p->reduction;
+    ma.ignore_index = p->ignore_index;
+    ma.zeta = p->z_loss_multiplier;
+    ma.partials = fa.partials;
+    ma.zt = fa.zt;
+    ma.targets = targets;
+    ma.lse = lse;
+    ma.loss_rows = p->reduction == FLCE_NONE ? loss : nullptr;
+    ma.blk_loss = reinterpret_cast<double*>(ws + L.blk_loss);
+    ma.blk_ent = reinterpret_cast<double*>(ws + L.blk_ent);
+    ma.blk_correct = reinterpret_cast<long long*>(ws + L.blk_correct);
+    ma.blk_valid = reinterpret_cast<long long*>(ws + L.blk_valid);
+    ma.status = status;
+    v = launch("flce_merge", st, [&] { return launch_merge(ma, L.nblk, st); });
+    if (v != FLCE_OK) return v;
+  }
+  FinalizeArgs fz{};
+  fz.nblk = N > 0 ? L.nblk : 0;
+  fz.reduction = p->reduction;
+  fz.blk_loss = reinterpret_cast<const double*>(ws + L.blk_loss);
+  fz.blk_ent = reinterpret_cast<const double*>(ws + L.blk_ent);
+  fz.blk_correct = reinterpret_cast<const long long*>(ws + L.blk_correct);
+  fz.blk_valid = reinterpret_cast<const long long*>(ws + L.blk_valid);
+  fz.loss = p->reduction == FLCE_NONE ? nullptr : loss;
+  fz.num_correct = num_correct;
+  fz.entropy_sum = entropy_sum;
+  return launch("flce_finalize", st, [&] { return launch_finalize(fz, st); });
+}
+
+int flce_backward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
+                  const int64_t* targets, const float* lse, const float* grad_loss,
+                  void* grad_hidden, void* grad_weight, void* grad_bias, void* workspace,
+                  size_t ws_bytes, flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  const bool rows = p->N > 0;
+  if (weight == nullptr ||
+      (rows && (hidden == nullptr || targets == nullptr || lse == nullptr || grad_loss == nullptr)))
+    return FLCE_ERR_INVALID_ARG;
+  if ((p->has_bias != 0) != (bias != nullptr)) return FLCE_ERR_INVALID_ARG;
+  if (grad_bias != nullptr && !p->has_bias) return FLCE_ERR_INVALID_ARG;
+  if (workspace == nullptr) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(weight) || (bias && !aligned16(bias)) ||
+      !aligned16(workspace) || !aligned16(targets) || (grad_hidden && !aligned16(grad_hidden)) ||
+      (grad_weight && !aligned16(grad_weight)) || (grad_bias && !aligned16(grad_bias)))
+    return FLCE_ERR_ALIGNMENT;
+  const BwdLayout L = bwd_layout(p);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  const size_t elem = p->dtype == FLCE_BF16 ? 2 : 4;
+
+  if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return FLCE_OK;
+  if (N == 0) {
+    if (grad_weight && (e = cudaMemsetAsync(grad_weight, 0, size_t(V) * H * elem, st)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync");
+    if (grad_bias && (e = cudaMemsetAsync(grad_bias, 0, size_t(V) * elem, st)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync");
+    return FLCE_OK;
+  }
+
+  float4* coef = reinterpret_cast<float4*>(ws + L.coef);
+  RowCoefArgs ra{};
+  ra.N = N;
+  ra.V = V;
+  ra.reduction = p->reduction;
+  ra.ignore_index = p->ignore_index;
+  ra.scale = p->logit_scale;
+  ra.zeta = p->z_loss_multiplier;
+  ra.targets = targets;
+  ra.lse = lse;
+  ra.grad_loss = grad_loss;
+  ra.coef = coef;
+  ra.status = status;
+  v = launch("flce_row_coef", st, [&] { return launch_row_coef(ra, st); });
+  if (v != FLCE_OK) return v;
+
+  float* bias_part = grad_bias ? reinterpret_cast<float*>(ws + L.bias_part) : nullptr;
+  DsArgs da{};
+  da.H = H;
+  da.V = V;
+  da.V_pad = static_cast<int>(L.V_pad);
+  da.scale = p->logit_scale;
+  da.softcap = p->softcap > 0.f ? p->softcap : 0.f;
+  da.inv_softcap = inv_cap(p);
+  da.bias = bias;
+  da.coef = coef;
+  da.ds = ws + L.ds;
+  da.bias_part = bias_part;
+  da.status = status;
+
+  if (p->dtype == FLCE_BF16) {
+    CUtensorMap tm_h, tm_w, tm_w_mn;
+    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBN)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w_mn, weight, H, V, uint64_t(H) * 2, 64, 64)) != FLCE_OK) return v;
+    float* dw_part = reinterpret_cast<float*>(ws + L.dw);
+    for (int c = 0; c < L.nchunks; ++c) {
+      const int row0 = static_cast<int>(c * L.chunk);
+      const int rows = static_cast<int>(N - row0 < L.chunk ? N - row0 : L.chunk);
+      da.rows = rows;
+      da.row0 = row0;
+      da.n_blocks = static_cast<int>(ceil_div(rows, kBM));
+      da.v_tiles = static_cast<int>(ceil_div(V, kBN));
+      int grid = 1;
+      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.v_tiles, d.sms, &grid);
+      da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
+      da.num_units = da.num_panels * da.n_blocks;
+      da.bias_blk0 = row0 / kBM;
+      v = launch("flce_dlogits_tc", st, [&] {
+        return launch_ds_tc(tm_h, tm_w, da, bias != nullptr, p->softcap > 0.f, grid, st);
+      });
+      if (v != FLCE_OK) return v;
+      const uint64_t ds_row_bytes = uint64_t(L.V_pad) * 2;
+      if (grad_hidden) {
+        // grad_hidden[rows, H] = dS[rows, V] (K-major) x W[V, H] (MN-major)
+        CUtensorMap tm_a;
+        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, kBK, kBM)) != FLCE_OK) return v;
+        GemmArgs ga{};
+        ga.M = rows;
+        ga.N = H;
+        ga.K = V;
+        ga.m_tiles = static_cast<int>(ceil_div(rows, kBM));
+        ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(V, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.a_mn = 0;
+        ga.b_mn = 1;
+        ga.mode = kStoreOut;
+        ga.out = static_cast<uint8_t*>(grad_hidden) + size_t(row0) * H * 2;
+        ga.ld_out = H;
+        ga.status = status;
+        const int g2 = ga.num_tiles < d.sms ? ga.num_tiles : d.sms;
+        v = launch("flce_grad_hidden_tc", st, [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, g2, st); });
+        if (v != FLCE_OK) return v;
+      }
+      if (grad_weight) {
+        // grad_weight[V, H] (+)= dS^T[V, rows] (MN-major) x h[rows, H] (MN-major)
+        CUtensorMap tm_a, tm_b;
+        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, 64, 64)) != FLCE_OK) return v;
+        const void* hc = static_cast<const uint8_t*>(hidden) + size_t(row0) * H * 2;
+        if ((v = make_map(&tm_b, hc, H, rows, uint64_t(H) * 2, 64, 64)) != FLCE_OK) return v;
+        GemmArgs ga{};
+        ga.M = V;
+        ga.N = H;
+        ga.K = rows;
+        ga.m_tiles = static_cast<int>(ceil_div(V, kBM));
+        ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(rows, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.a_mn = 1;
+        ga.b_mn = 1;
+        if (L.nchunks == 1)
+          ga.mode = kStoreOut;
+        else if (c == 0)
+          ga.mode = kStorePart;
+        else if (c == L.nchunks - 1)
+          ga.mode = kAddPartToOut;
+        else
+          ga.mode = kAddPart;
+        ga.out = grad_weight;
+        ga.ld_out = H;
+        ga.part = dw_part;
+        ga.ld_part = H;
+        ga.status = status;
+        const int g2 = ga.num_tiles < d.sms ? ga.num_tiles : d.sms;
+        v = launch("flce_grad_weight_tc", st, [&] { return launch_gemm_tc(tm_a, tm_b, ga, g2, st); });
+        if (v != FLCE_OK) return v;
+      }
+    }
+  } else {
+    const float* hf = static_cast<const float*>(hidden);
+    const float* wf = static_cast<const float*>(weight);
+    for (int c = 0; c < L.nchunks; ++c) {
+      const int row0 = static_cast<int>(c * L.chunk);
+      const int rows = static_cast<int>(N - row0 < L.chunk ? N - row0 : L.chunk);
+      da.rows = rows;
+      da.row0 = row0;
+      da.bias_blk0 = row0 / kSimtTile;
+      v = launch("flce_dlogits_simt", st, [&] { return launch_ds_simt(hf, wf, da, st); });
+      if (v != FLCE_OK) return v;
+      const float* ds = reinterpret_cast<const float*>(da.ds);
+      if (grad_hidden) {
+        SimtGemmArgs ga{};
+        ga.M = rows;
+        ga.N = H;
+        ga.K = V;
+        ga.A = ds;
+        ga.sam = L.V_pad;
+        ga.sak = 1;
+        ga.B = wf;
+        ga.sbk = H;
+        ga.sbn = 1;
+        ga.C = static_cast<float*>(grad_hidden) + size_t(row0) * H;
+        ga.ldc = H;
+        ga.accumulate = 0;
+        v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
+        if (v != FLCE_OK) return v;
+      }
+      if (grad_weight) {
+        SimtGemmArgs ga{};
+        ga.M = V;
+        ga.N = H;
+        ga.K = rows;
+        ga.A = ds;
+        ga.sam = 1;
+        ga.sak = L.V_pad;
+        ga.B = hf + size_t(row0) * H;
+        ga.sbk = H;
+        ga.sbn = 1;
+        ga.C = static_cast<float*>(grad_weight);
+        ga.ldc = H;
+        ga.accumulate = c > 0 ? 1 : 0;
+        v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
+        if (v != FLCE_OK) return v;
+      }
+    }
+  }
+  if (grad_bias) {
+    BiasReduceArgs ba{};
+    ba.V = V;
+    ba.V_pad = static_cast<int>(L.V_pad);
+    ba.nblk = L.n_rowblocks;
+    ba.bias_part = bias_part;
+    ba.grad_bias = grad_bias;
+    v = launch("flce_bias_reduce", st, [&] { return launch_bias_reduce(ba, p->dtype, st); });
+    if (v != FLCE_OK) return v;
+  }
+  return FLCE_OK;
+}
+
+int flce_check_status(const void* workspace, flce_stream_t stream) {
+  if (workspace == nullptr) return FLCE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (word & kDevErrTimeout) return FLCE_ERR_TIMEOUT;
+  if (word & kDevErrTargetRange) return FLCE_ERR_TARGET_RANGE;
+  return FLCE_OK;
+}
+
+int flce_profiling_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof = on != 0;
+  return FLCE_OK;
+}
+
+int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const Pending& p : g_pending) {
+    cudaError_t e = cudaEventSynchronize(p.e1);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, p.e0, p.e1);
+    g_counts[p.name] += 1;
+    g_ms[p.name] += ms;
+    g_pool.push_back(p.e0);
+    g_pool.push_back(p.e1);
+  }
+  g_pending.clear();
+  int n = 0;
+  for (size_t i = 0; i < g_names.size(); ++i) {
+    if (g_counts[i] == 0) continue;
+    if (out != nullptr && n < max) {
+      memset(&out[n], 0, sizeof(out[n]));
+      strncpy(out[n].name, g_names[i].c_str(), sizeof(out[n].name) - 1);
+      out[n].launches = g_counts[i];
+      out[n].total_ms = g_ms[i];
+    }
+    ++n;
+    g_counts[i] = 0;
+    g_ms[i] = 0.0;
+  }
+  if (count != nullptr) *count = n;
+  return FLCE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+// Internal interface between the host runtime (flce.cu) and the kernel
+// translation units. It is not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flce {
+
+// Device status bits written to the workspace status word. The host maps
+// them to FLCE_ERR_* codes.
+enum : int { kDevErrTargetRange = 1, kDevErrTimeout = 2 };
+
+// ---- tcgen05 tile shape shared by every bf16 kernel -----------------------
+// One CTA per SM owns a 128 x 256 fp32 accumulator in TMEM, double-buffered
+// (2 x 256 of the 512 TMEM columns). Operands arrive in 64-deep K slices
+// (one 128-byte swizzle row of bf16) through a 4-stage TMA ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kStageA = kBM * kBK * 2;           // 16 KB
+constexpr int kStageB = kBN * kBK * 2;           // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;   // 48 KB
+constexpr int kTcThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kTmemCols = 512;
+// dynamic shared memory: 1 KB alignment slack + stages + control block
+constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;
+
+// ---- fp32 SIMT path tile shape -------------------------------------------
+constexpr int kSimtTile = 64;        // 64 x 64 logit tiles
+constexpr int kSimtPanelCols = 512;  // columns per partial-state panel
+constexpr int kSimtThreads = 256;
+
+// Per (panel, row) partial state of the online log-sum-exp:
+// x = running max m, y = sum exp(z - m), z = sum z exp(z - m), w = argmax (int bits).
+
+struct FwdArgs {
+  int N, H, V;
+  int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
+  float scale, softcap, inv_softcap;
+  const void* bias;            // dtype of the pass, or nullptr
+  const int64_t* targets;
+  long long ignore_index;
+  float4* partials;            // [num_panels][N]
+  float* zt;                   // [N] transformed target logit
+  int* status;
+};
+
+struct MergeArgs {
+  int N, V, num_panels, reduction;
+  long long ignore_index;
+  float zeta;
+  const float4* partials;
+  const float* zt;
+  const int64_t* targets;
+  float* lse;                  // [N]
+  float* loss_rows;            // [N] when reduction == none, else nullptr
+  double* blk_loss;            // [gridDim]
+  double* blk_ent;
+  long long* blk_correct;
+  long long* blk_valid;
+  int* status;
+};
+
+struct FinalizeArgs {
+  int nblk, reduction;
+  const double* blk_loss;
+  const double* blk_ent;
+  const long long* blk_correct;
+  const long long* blk_valid;
+  float* loss;                 // [1] for sum/mean, nullptr for none
+  int64_t* num_correct;        // nullable
+  float* entropy_sum;          // nullable
+};
+
+// Backward per-row coefficients: x = s*gamma*(1 + 2 zeta lse), y = s*gamma,
+// z = lse, w = target (int bits; -1 if ignored or out of the row range).
+struct RowCoefArgs {
+  int N, V, reduction;
+  long long ignore_index;
+  float scale, zeta;
+  const int64_t* targets;
+  const float* lse;
+  const float* grad_loss;
+  float4* coef;
+  int* status;
+};
+
+struct DsArgs {
+  int rows, row0, H, V, V_pad;
+  int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
+  float scale, softcap, inv_softcap;
+  const void* bias;
+  const float4* coef;          // indexed by global row
+  void* ds;                    // chunk buffer [rows][V_pad], bf16 or f32
+  float* bias_part;            // [row blocks][V_pad] or nullptr
+  int bias_blk0;               // first row block of this chunk
+  int* status;
+};
+
+enum GemmMode : int {
+  kStoreOut = 0,      // out  = acc (output dtype)
+  kStorePart = 1,     // part = acc (fp32)
+  kAddPart = 2,       // part = part + acc
+  kAddPartToOut = 3   // out  = part + acc
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks, num_tiles;
+  int a_mn, b_mn;              // 1: operand is MN-major in memory
+  int mode;
+  void* out;
+  long long ld_out;
+  float* part;
+  long long ld_part;
+  int* status;
+};
+
+struct SimtGemmArgs {
+  int M, N, K;
+  const float* A;              // A(m,k) = A[m*sam + k*sak]
+  long long sam, sak;
+  const float* B;              // B(k,n) = B[k*sbk + n*sbn]
+  long long sbk, sbn;
+  float* C;                    // C[m*ldc + n]
+  long long ldc;
+  int accumulate;              // 1: C += A B, 0: C = A B
+};
+
+struct BiasReduceArgs {
+  int V, V_pad, nblk;
+  const float* bias_part;      // [nblk][V_pad]
+  void* grad_bias;             // dtype of the pass
+};
+
+// tcgen05 / TMA kernels (bf16)
+cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
+                          bool has_bias, bool softcap, int grid, cudaStream_t s);
+cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
+                         bool has_bias, bool softcap, int grid, cudaStream_t s);
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+                           int grid, cudaStream_t s);
+
+// SIMT kernels (fp32)
+cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s);
+
+// dtype-generic small kernels (dtype: 0 = f32, 1 = bf16)
+cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
+cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);
+
+constexpr int kMergeThreads = 256;
+
+}  // namespace flce

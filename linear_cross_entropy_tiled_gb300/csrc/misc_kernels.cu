@@ -1,0 +1,193 @@
+// Small kernels shared by both dtypes:
+//   merge       per-row merge of the vocabulary-panel partial states into
+//               lse, loss_i, entropy_i and correct_i, plus per-block sums;
+//   finalize    fixed-order sum of the block sums into the reduced outputs;
+//   row_coef    per-row backward coefficients (gamma with the reduction and
+//               the z-loss folded in);
+//   bias_reduce fixed-order sum of per-row-block grad_bias partials.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+// Deterministic block sum: warp shuffles, then warp 0 over the warp sums.
+template <typename Tv>
+__device__ __forceinline__ Tv block_sum(Tv v, Tv* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  Tv r = 0;
+  if (warp == 0) {
+    r = (lane < static_cast<int>(blockDim.x >> 5)) ? sh[lane] : Tv(0);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  }
+  __syncthreads();
+  return r;  // valid in thread 0
+}
+
+// Merge of the online-softmax states of all vocabulary panels of one row, in
+// panel order (fused-linear-ce README, "Algorithm": the flash-attention style
+// rescaling). Panels are merged in increasing column order. A later panel
+// takes the argmax only with a strictly larger max, so ties keep the lowest
+// column index.
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
+  __shared__ double sh_d[32];
+  __shared__ long long sh_i[32];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  double loss_i = 0.0, ent_i = 0.0;
+  long long corr = 0, valid = 0;
+  if (i < a.N) {
+    float M = -INFINITY, S = 0.f, Tt = 0.f;
+    int A = 0;
+    for (int p = 0; p < a.num_panels; ++p) {
+      const float4 st = a.partials[static_cast<size_t>(p) * a.N + i];
+      if (st.x > M) {
+        const float f = expf(M - st.x);
+        S = fmaf(S, f, st.y);
+        Tt = fmaf(Tt, f, st.z);
+        M = st.x;
+        A = __float_as_int(st.w);
+      } else {
+        const float f = expf(st.x - M);
+        S = fmaf(st.y, f, S);
+        Tt = fmaf(st.z, f, Tt);
+      }
+    }
+    const float lse = M + logf(S);
+    a.lse[i] = lse;
+    const long long t = a.targets[i];
+    float li = 0.f;
+    if (t != a.ignore_index) {
+      valid = 1;
+      if (t < 0 || t >= a.V) {
+        atomicOr(a.status, kDevErrTargetRange);
+        li = NAN;
+      } else {
+        li = lse - a.zt[i] + a.zeta * lse * lse;
+        ent_i = static_cast<double>(lse - Tt / S);
+        corr = (static_cast<long long>(A) == t) ? 1 : 0;
+      }
+    }
+    loss_i = li;
+    if (a.loss_rows != nullptr) a.loss_rows[i] = li;
+  }
+  const double bl = block_sum(loss_i, sh_d);
+  const double be = block_sum(ent_i, sh_d);
+  const long long bc = block_sum(corr, sh_i);
+  const long long bv = block_sum(valid, sh_i);
+  if (threadIdx.x == 0) {
+    a.blk_loss[blockIdx.x] = bl;
+    a.blk_ent[blockIdx.x] = be;
+    a.blk_correct[blockIdx.x] = bc;
+    a.blk_valid[blockIdx.x] = bv;
+  }
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
+  __shared__ double sh_d[32];
+  __shared__ long long sh_i[32];
+  double l = 0.0, e = 0.0;
+  long long c = 0, v = 0;
+  for (int b = threadIdx.x; b < a.nblk; b += blockDim.x) {
+    l += a.blk_loss[b];
+    e += a.blk_ent[b];
+    c += a.blk_correct[b];
+    v += a.blk_valid[b];
+  }
+  l = block_sum(l, sh_d);
+  e = block_sum(e, sh_d);
+  c = block_sum(c, sh_i);
+  v = block_sum(v, sh_i);
+  if (threadIdx.x == 0) {
+    if (a.loss != nullptr) {
+      if (a.reduction == 0) {
+        *a.loss = static_cast<float>(l);
+      } else {
+        *a.loss = v > 0 ? static_cast<float>(l / static_cast<double>(v)) : NAN;
+      }
+    }
+    if (a.num_correct != nullptr) *a.num_correct = c;
+    if (a.entropy_sum != nullptr) *a.entropy_sum = static_cast<float>(e);
+  }
+}
+
+// One block. It first counts the valid rows (needed for the mean), then
+// writes the coefficients of every row.
+__global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
+  __shared__ long long sh_i[32];
+  __shared__ long long s_valid;
+  long long v = 0;
+  for (int i = threadIdx.x; i < a.N; i += blockDim.x) v += (a.targets[i] != a.ignore_index) ? 1 : 0;
+  v = block_sum(v, sh_i);
+  if (threadIdx.x == 0) s_valid = v;
+  __syncthreads();
+  const long long num_valid = s_valid;
+  float g_all = 0.f;
+  if (a.reduction == 0) g_all = a.grad_loss[0];
+  if (a.reduction == 1) g_all = num_valid > 0 ? a.grad_loss[0] / static_cast<float>(num_valid) : 0.f;
+  for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
+    const long long t = a.targets[i];
+    const float lse = a.lse[i];
+    float4 c = make_float4(0.f, 0.f, lse, __int_as_float(-1));
+    if (t != a.ignore_index) {
+      if (t < 0 || t >= a.V) {
+        atomicOr(a.status, kDevErrTargetRange);
+      } else {
+        const float gam = (a.reduction == 2) ? a.grad_loss[i] : g_all;
+        const float sg = a.scale * gam;
+        c.x = sg * fmaf(2.f * a.zeta, lse, 1.f);
+        c.y = sg;
+        c.w = __int_as_float(static_cast<int>(t));
+      }
+    }
+    a.coef[i] = c;
+  }
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(256) bias_reduce_kernel(const BiasReduceArgs a) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= a.V) return;
+  float s = 0.f;
+  for (int b = 0; b < a.nblk; ++b) s += a.bias_part[static_cast<size_t>(b) * a.V_pad + j];
+  if constexpr (sizeof(Tout) == 2) {
+    static_cast<__nv_bfloat16*>(a.grad_bias)[j] = __float2bfloat16_rn(s);
+  } else {
+    static_cast<float*>(a.grad_bias)[j] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s) {
+  merge_kernel<<<nblk, kMergeThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
+  finalize_kernel<<<1, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s) {
+  row_coef_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s) {
+  const int grid = (a.V + 255) / 256;
+  if (dtype == 1)
+    bias_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+  else
+    bias_reduce_kernel<float><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

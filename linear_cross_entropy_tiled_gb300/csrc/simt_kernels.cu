@@ -1,0 +1,235 @@
+// fp32 kernels. This is the path for fp32 hidden/weight: plain FFMA
+// arithmetic, no tensor cores.
+//
+// The fused-linear-ce README ("Full signature") accepts fp32 inputs. A loss
+// accurate to 1e-5 relative needs fp32 products. TF32 tensor cores round the
+// operands to 10 mantissa bits, which is not enough. The schedule is the same
+// as the bf16 path: vocabulary panels with an online log-sum-exp (forward),
+// and a recompute -> dlogits -> two contractions backward. Only the tile
+// arithmetic differs. Speed is not a goal here. The fp32 workload is the small
+// 256 x 512 x 8192 case.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr int T = kSimtTile;   // 64
+constexpr int TK = 32;
+
+// Computes the 64 x 64 tile acc[i][j] += sum_k h[r0+4ty+i][k] * w[c0+4tx+j][k].
+// Rows >= nrows and columns >= ncols read as 0.
+__device__ __forceinline__ void simt_logit_tile(const float* __restrict__ h,
+                                                const float* __restrict__ w, int H, int r0,
+                                                int nrows, int c0, int ncols, float (&As)[TK][T + 4],
+                                                float (&Bs)[TK][T + 4], float (&acc)[4][4]) {
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < H; k0 += TK) {
+    for (int e = tid; e < T * TK; e += kSimtThreads) {
+      const int rr = e / TK, kk = e % TK;
+      const int k = k0 + kk;
+      As[kk][rr] = (r0 + rr < nrows && k < H) ? h[static_cast<size_t>(r0 + rr) * H + k] : 0.f;
+      Bs[kk][rr] = (c0 + rr < ncols && k < H) ? w[static_cast<size_t>(c0 + rr) * H + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < TK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ float transform_f32(float a, const float* bias, int col, float scale,
+                                               float cap, float inv_cap) {
+  float u = (bias != nullptr) ? (a + bias[col]) * scale : a * scale;
+  if (cap > 0.f) u = cap * tanhf(u * inv_cap);
+  return u;
+}
+
+// One block per (panel of kSimtPanelCols columns, block of 64 rows).
+__global__ void __launch_bounds__(kSimtThreads)
+    fwd_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const FwdArgs a) {
+  __shared__ float As[TK][T + 4];
+  __shared__ float Bs[TK][T + 4];
+  __shared__ float Z[T][T + 1];
+  const int panel = blockIdx.x / a.n_blocks;
+  const int rb = blockIdx.x - panel * a.n_blocks;
+  const int r0 = rb * T;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* bias = static_cast<const float*>(a.bias);
+  float m = -INFINITY, ssum = 0.f, tsum = 0.f;
+  int amax = 0;
+  const int row = r0 + tid;
+  const long long tgt = (tid < T && row < a.N) ? a.targets[row] : a.ignore_index;
+  const int c_begin = panel * kSimtPanelCols;
+  const int c_end = min(a.V, c_begin + kSimtPanelCols);
+  for (int c0 = c_begin; c0 < c_end; c0 += T) {
+    float acc[4][4];
+    simt_logit_tile(h, w, a.H, r0, a.N, c0, a.V, As, Bs, acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = c0 + tx * 4 + j;
+        Z[ty * 4 + i][tx * 4 + j] =
+            col < a.V ? transform_f32(acc[i][j], bias, col, a.scale, a.softcap, a.inv_softcap)
+                      : -INFINITY;
+      }
+    __syncthreads();
+    if (tid < T && row < a.N) {
+      const int nc = min(T, a.V - c0);
+      for (int j = 0; j < nc; ++j) {
+        const float z = Z[tid][j];
+        if (c0 + j == tgt) a.zt[row] = z;
+        if (z > m) {
+          const float f = expf(m - z);
+          ssum = ssum * f + 1.f;
+          tsum = tsum * f + z;
+          m = z;
+          amax = c0 + j;
+        } else {
+          const float e = expf(z - m);
+          ssum += e;
+          tsum = fmaf(z, e, tsum);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (tid < T && row < a.N)
+    a.partials[static_cast<size_t>(panel) * a.N + row] =
+        make_float4(m, ssum, tsum, __int_as_float(amax));
+}
+
+// One block per (64-column tile, 64-row block of the chunk).
+__global__ void __launch_bounds__(kSimtThreads)
+    ds_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const DsArgs a) {
+  __shared__ float As[TK][T + 4];
+  __shared__ float Bs[TK][T + 4];
+  __shared__ float G[T][T + 1];
+  const int c0 = blockIdx.x * T;
+  const int rb = blockIdx.y;
+  const int r0 = rb * T;  // local to the chunk
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const float* bias = static_cast<const float*>(a.bias);
+  float acc[4][4];
+  simt_logit_tile(h + static_cast<size_t>(a.row0) * a.H, w, a.H, r0, a.rows, c0, a.V, As, Bs, acc);
+  float* ds = static_cast<float*>(a.ds);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rl = r0 + ty * 4 + i;
+    const bool row_ok = rl < a.rows;
+    const float4 cf = row_ok ? a.coef[a.row0 + rl] : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+    const int tgt = __float_as_int(cf.w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + tx * 4 + j;
+      float g = 0.f;
+      if (row_ok && col < a.V) {
+        const float z = transform_f32(acc[i][j], bias, col, a.scale, a.softcap, a.inv_softcap);
+        const float p = expf(z - cf.z);
+        g = cf.x * p;
+        if (col == tgt) g -= cf.y;
+        if (a.softcap > 0.f) {
+          const float zc = z * a.inv_softcap;
+          g *= (1.f - zc * zc);
+        }
+        ds[static_cast<size_t>(rl) * a.V_pad + col] = g;
+      }
+      G[ty * 4 + i][tx * 4 + j] = g;
+    }
+  }
+  if (a.bias_part != nullptr) {
+    __syncthreads();
+    if (tid < T && c0 + tid < a.V) {
+      float sum = 0.f;
+      for (int i = 0; i < T; ++i) sum += G[i][tid];
+      a.bias_part[static_cast<size_t>(a.bias_blk0 + rb) * a.V_pad + c0 + tid] = sum;
+    }
+  }
+}
+
+constexpr int GK = 16;
+
+__global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmArgs a) {
+  __shared__ float As[GK][T + 4];
+  __shared__ float Bs[GK][T + 4];
+  const int m0 = blockIdx.y * T, n0 = blockIdx.x * T;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < a.K; k0 += GK) {
+    for (int e = tid; e < T * GK; e += kSimtThreads) {
+      const int kk = e / T, mm = e % T;
+      const int k = k0 + kk;
+      As[kk][mm] = (m0 + mm < a.M && k < a.K) ? a.A[(m0 + mm) * a.sam + k * a.sak] : 0.f;
+      Bs[kk][mm] = (n0 + mm < a.N && k < a.K) ? a.B[k * a.sbk + (n0 + mm) * a.sbn] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < GK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= a.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= a.N) continue;
+      float* c = a.C + m * a.ldc + n;
+      *c = a.accumulate ? *c + acc[i][j] : acc[i][j];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cudaStream_t s) {
+  fwd_simt_kernel<<<a.num_units, kSimtThreads, 0, s>>>(h, w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s) {
+  dim3 grid((a.V + T - 1) / T, (a.rows + T - 1) / T);
+  ds_simt_kernel<<<grid, kSimtThreads, 0, s>>>(h, w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s) {
+  dim3 grid((a.N + T - 1) / T, (a.M + T - 1) / T);
+  gemm_simt_kernel<<<grid, kSimtThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,742 @@
+// tcgen05 / TMA kernels of the bf16 path (sm_103a).
+//
+// Every kernel here is a persistent, warp-specialised CTA (one per SM):
+//   warp 0     one thread issues TMA tile loads into a 4-stage shared ring;
+//   warp 1     one thread issues tcgen05.mma into a double-buffered TMEM
+//              accumulator (2 x 128 lanes x 256 fp32 columns). This warp
+//              also owns the TMEM allocation;
+//   warps 2-5  the epilogue. Each thread owns one accumulator row, which is
+//              one TMEM lane, and reads it with tcgen05.ld.
+// The kernels differ only in the tile sequence, the operand layouts and the
+// epilogue:
+//   fwd_tc   logits tile -> bias, scale, softcap -> online max / sum-exp /
+//            sum z*exp / argmax per row, plus the target logit
+//            (fused-linear-ce README, "Algorithm" and "Metrics for free").
+//   ds_tc    recomputed logits tile -> dlogits = (softmax (1 + 2 zeta lse)
+//            - onehot) x softcap' x scale x gamma -> bf16 row chunk, plus
+//            per-128-row column sums for grad_bias (same README, "Algorithm";
+//            the z-loss term is this library's reading of "Chunked Linear
+//            Cross-Entropy", "Usage").
+//   gemm_tc  plain D = A B with fp32 accumulation. It serves the two
+//            gradient contractions grad_hidden = dS W and grad_weight =
+//            dS^T h ("Chunked Linear Loss", "Gradient handling"), and the
+//            fp32 accumulation of grad_weight across row chunks ("Chunked
+//            Linear Loss", "Weight-gradient accumulation dtype").
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kFull = 0xffffffffu;
+
+// --------------------------------------------------------------- smem map
+struct TcSmem {
+  uint8_t* a;            // kStages x kStageA
+  uint8_t* b;            // kStages x kStageB
+  float* scratch;        // 8 KB: column sums of the dlogits epilogue
+  uint64_t* full;        // kStages: TMA bytes landed
+  uint64_t* empty;       // kStages: MMAs done reading the stage
+  uint64_t* tfull;       // 2: accumulator complete
+  uint64_t* tempty;      // 2: epilogue done reading the accumulator
+  uint64_t* mma_done;    // 1: all MMAs complete (teardown)
+  uint32_t* tmem_slot;
+  int* abort;
+};
+
+__device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
+  TcSmem s;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  s.a = base;
+  s.b = base + kStages * kStageA;
+  s.scratch = reinterpret_cast<float*>(s.b + kStages * kStageB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.scratch) + 8192);
+  s.full = bars;
+  s.empty = bars + kStages;
+  s.tfull = bars + 2 * kStages;
+  s.tempty = s.tfull + 2;
+  s.mma_done = s.tempty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
+  s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+  return s;
+}
+
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(s.mma_done, 1);
+    *s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *s.tmem_slot;
+}
+
+__device__ __forceinline__ void tc_teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Bounded wait that ignores the abort flag. It is used only to drain
+// operations that are already in flight before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+// --------------------------------------------------------- producer / MMA
+// ForEachTile(f) calls f(ta, tb) for every tile of this CTA, in order.
+// Issue(ta, tb, kb, a_dst, b_dst, bar) issues the TMA loads of one K slice.
+template <class ForEachTile, class Issue>
+__device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& g, int kblocks,
+                                              ForEachTile for_each_tile, Issue issue) {
+  int stage = 0;
+  uint32_t phase = 0;
+  bool dead = false;
+  long long issued = 0;
+  for_each_tile([&](int ta, int tb) {
+    for (int kb = 0; kb < kblocks && !dead; ++kb) {
+      if (!mbar_wait(&s.empty[stage], phase ^ 1u, g)) {
+        dead = true;
+        break;
+      }
+      mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
+      issue(ta, tb, kb, s.a + stage * kStageA, s.b + stage * kStageB, &s.full[stage]);
+      ++issued;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  });
+  if (dead) {
+    // Let the loads already in flight land before shared memory is released.
+    const long long first = issued > kStages ? issued - kStages : 0;
+    for (long long i = first; i < issued; ++i)
+      drain_wait(&s.full[i % kStages], static_cast<uint32_t>((i / kStages) & 1));
+  }
+}
+
+// Descs(sa, sb, kk, adesc, bdesc) builds the descriptors of the kk-th
+// 16-deep K step within a 64-deep stage.
+template <class ForEachTile, class Descs>
+__device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, uint32_t tmem,
+                                         int kblocks, uint32_t idesc, ForEachTile for_each_tile,
+                                         Descs descs) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool dead = false;
+  for_each_tile([&](int, int) {
+    if (dead) return;
+    if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, g)) {
+      dead = true;
+      return;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
+    for (int kb = 0; kb < kblocks; ++kb) {
+      if (!mbar_wait(&s.full[stage], phase, g)) {
+        dead = true;
+        return;
+      }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(s.a + stage * kStageA);
+      const uint32_t sb = smem_u32(s.b + stage * kStageB);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        uint64_t ad, bd;
+        descs(sa, sb, kk, ad, bd);
+        umma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      umma_commit(&s.empty[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    umma_commit(&s.tfull[acc]);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  });
+  // Every MMA must have finished before TMEM is released.
+  umma_commit(s.mma_done);
+  drain_wait(s.mma_done, 0);
+}
+
+__device__ __forceinline__ void kmajor_descs(uint32_t sa, uint32_t sb, int kk, uint64_t& ad,
+                                             uint64_t& bd) {
+  ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+  bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
+}
+
+// Epilogue: wait until accumulator `acc` is full. The result is warp-uniform,
+// so a warp either reads TMEM with every lane or not at all.
+__device__ __forceinline__ bool epi_wait_full(const TcSmem& s, int acc, uint32_t acc_phase,
+                                              const WaitGuard& g, bool dead) {
+  bool ok = !dead && mbar_wait(&s.tfull[acc], acc_phase, g);
+  ok = __all_sync(kFull, ok);
+  if (ok) tc_fence_after();
+  return ok;
+}
+
+__device__ __forceinline__ void epi_release(const TcSmem& s, int acc, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&s.tempty[acc]);
+}
+
+// 32 bias values times scale, for columns col0 .. col0+31. Columns at or
+// beyond V read as 0.
+template <bool kRagged>
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int col0, int V,
+                                            float scale, float (&bs)[32]) {
+  if (!kRagged) {
+    const uint4* p = reinterpret_cast<const uint4*>(bias + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(p + q);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+        bs[q * 8 + 2 * h] = __uint_as_float(ws[h] << 16) * scale;
+        bs[q * 8 + 2 * h + 1] = __uint_as_float(ws[h] & 0xffff0000u) * scale;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      bs[j] = (col0 + j < V) ? __bfloat162float(bias[col0 + j]) * scale : 0.f;
+  }
+}
+
+// Transformed logit z from the raw accumulator value.
+template <bool kBias, bool kSoftcap>
+__device__ __forceinline__ float transform(uint32_t raw, float bs, float scale, float cap,
+                                           float inv_cap) {
+  float u = kBias ? fmaf(__uint_as_float(raw), scale, bs) : __uint_as_float(raw) * scale;
+  if (kSoftcap) u = cap * tanhf(u * inv_cap);
+  return u;
+}
+
+// ======================================================= forward kernel
+// One level of a pairwise (max, first index) tree over W pairs. The left
+// element wins ties, so the lowest index survives.
+template <int W>
+__device__ __forceinline__ void argmax_level(float (&mv)[16], int (&mi)[16]) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    const bool l = mv[2 * j] >= mv[2 * j + 1];
+    mv[j] = l ? mv[2 * j] : mv[2 * j + 1];
+    mi[j] = l ? mi[2 * j] : mi[2 * j + 1];
+  }
+}
+
+// One level of a pairwise sum tree over W pairs, for two arrays at once.
+template <int W>
+__device__ __forceinline__ void sum_level(float (&e)[32], float (&ze)[32]) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    e[j] = e[j] + e[j + W];
+    ze[j] = ze[j] + ze[j + W];
+  }
+}
+// x[i] for a runtime i in [0, 32), as a 5-level multiplexer on the bits of
+// i. Every array index stays a compile-time constant, so x stays in
+// registers.
+__device__ __forceinline__ float select32(const float (&x)[32], int i) {
+  float t16[16], t8[8], t4[4], t2[2];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t16[j] = (i & 16) ? x[j + 16] : x[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) t8[j] = (i & 8) ? t16[j + 8] : t16[j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t4[j] = (i & 4) ? t8[j + 4] : t8[j];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) t2[j] = (i & 2) ? t4[j + 2] : t4[j];
+  return (i & 1) ? t2[1] : t2[0];
+}
+
+template <bool kRagged, bool kBias, bool kSoftcap>
+__device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs& a, int col0,
+                                          long long tgt, int row, bool row_ok, float& m,
+                                          float& ssum, float& tsum, int& amax) {
+  float bs[32];
+  if (kBias) load_bias32<kRagged>(static_cast<const __nv_bfloat16*>(a.bias), col0, a.V,
+                                  a.scale, bs);
+  float z[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float zz = transform<kBias, kSoftcap>(v[j], kBias ? bs[j] : 0.f, a.scale, a.softcap,
+                                          a.inv_softcap);
+    if (kRagged && col0 + j >= a.V) zz = -INFINITY;
+    z[j] = zz;
+  }
+  // The target logit lives in exactly one chunk of the whole vocabulary sweep.
+  const long long rel = tgt - col0;
+  if (row_ok && rel >= 0 && rel < 32) {
+    a.zt[row] = select32(z, static_cast<int>(rel));
+  }
+  // Chunk max and first index that attains it, as a pairwise tree. The left
+  // operand wins ties, so the lowest index is kept.
+  float mv[16];
+  int mi[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool l = z[2 * j] >= z[2 * j + 1];
+    mv[j] = l ? z[2 * j] : z[2 * j + 1];
+    mi[j] = l ? 2 * j : 2 * j + 1;
+  }
+  argmax_level<8>(mv, mi);
+  argmax_level<4>(mv, mi);
+  argmax_level<2>(mv, mi);
+  argmax_level<1>(mv, mi);
+  const float cmax = mv[0];
+  const float mnew = fmaxf(m, cmax);
+  if (cmax > m) amax = col0 + mi[0];  // strict: an earlier chunk keeps a tie
+  const float alpha = ex2_approx((m - mnew) * kLog2e);
+  const float nb = -mnew * kLog2e;
+  float e[32], ze[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    e[j] = ex2_approx(fmaf(z[j], kLog2e, nb));
+    const float zc = (kRagged && col0 + j >= a.V) ? 0.f : z[j];
+    ze[j] = zc * e[j];
+  }
+  sum_level<16>(e, ze);
+  sum_level<8>(e, ze);
+  sum_level<4>(e, ze);
+  sum_level<2>(e, ze);
+  sum_level<1>(e, ze);
+  ssum = fmaf(ssum, alpha, e[0]);
+  tsum = fmaf(tsum, alpha, ze[0]);
+  m = mnew;
+}
+
+template <bool kBias, bool kSoftcap>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                  const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const TcSmem s = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tmem = tc_setup(s, warp);
+  const WaitGuard g{a.status, s.abort};
+  const int kblocks = (a.H + kBK - 1) / kBK;
+
+  auto for_each_tile = [&](auto&& f) {
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      const int vt0 = panel * a.panel_tiles;
+      const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
+      for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_h);
+      tma_prefetch_desc(&tm_w);
+      const uint64_t pol_h = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_normal();
+      producer_role(s, g, kblocks, for_each_tile,
+                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
+                      tma_load_2d(da, &tm_h, bar, kb * kBK, nb * kBM, pol_h);
+                      tma_load_2d(db, &tm_w, bar, kb * kBK, vt * kBN, pol_w);
+                    });
+    }
+  } else if (warp == 1) {
+    if (lane == 0)
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, false, false), for_each_tile,
+               kmajor_descs);
+  } else {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool dead = false;
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      const int row = nb * kBM + r;
+      const bool row_ok = row < a.N;
+      const long long tgt = row_ok ? a.targets[row] : a.ignore_index;
+      float m = -INFINITY, ssum = 0.f, tsum = 0.f;
+      int amax = 0;
+      const int vt0 = panel * a.panel_tiles;
+      const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
+      for (int vt = vt0; vt < vt1; ++vt) {
+        dead = !epi_wait_full(s, acc, acc_phase, g, dead);
+        if (!dead) {
+          const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * kBN);
+          const bool ragged = (vt + 1) * kBN > a.V;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait(v);
+            const int col0 = vt * kBN + c * 32;
+            if (!ragged) {
+              fwd_chunk<false, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum, amax);
+            } else if (col0 < a.V) {
+              fwd_chunk<true, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum, amax);
+            }
+          }
+          epi_release(s, acc, lane);
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (row_ok && !dead)
+        a.partials[static_cast<size_t>(panel) * a.N + row] =
+            make_float4(m, ssum, tsum, __int_as_float(amax));
+    }
+  }
+  tc_teardown(tmem, warp);
+}
+
+// ====================================================== dlogits kernel
+__device__ __forceinline__ float warp_transpose_sum32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int k = 0; k < off; ++k) {
+      const float send = upper ? x[k] : x[k + off];
+      const float keep = upper ? x[k + off] : x[k];
+      x[k] = keep + __shfl_xor_sync(kFull, send, off);
+    }
+  }
+  return x[0];  // lane L now holds the sum of column L over the warp's 32 rows
+}
+
+template <bool kRagged, bool kBias, bool kSoftcap>
+__device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& a, int col0,
+                                         float4 cf, bool row_ok, int row_local, float (&gout)[32]) {
+  float bs[32];
+  if (kBias) load_bias32<kRagged>(static_cast<const __nv_bfloat16*>(a.bias), col0, a.V,
+                                  a.scale, bs);
+  const int tgt = __float_as_int(cf.w);
+  const float nlse = -cf.z * kLog2e;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float z = transform<kBias, kSoftcap>(v[j], kBias ? bs[j] : 0.f, a.scale, a.softcap,
+                                               a.inv_softcap);
+    const float p = ex2_approx(fmaf(z, kLog2e, nlse));
+    float gj = cf.x * p;
+    if (col0 + j == tgt) gj -= cf.y;
+    if (kSoftcap) {
+      const float zc = z * a.inv_softcap;
+      gj *= fmaf(-zc, zc, 1.f);
+    }
+    if (kRagged && col0 + j >= a.V) gj = 0.f;
+    gout[j] = row_ok ? gj : 0.f;
+  }
+  if (row_ok) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.ds) +
+                         static_cast<size_t>(row_local) * a.V_pad + col0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (kRagged && col0 + q * 8 >= a.V) break;
+      uint4 w;
+      w.x = pack_bf16x2(gout[q * 8 + 0], gout[q * 8 + 1]);
+      w.y = pack_bf16x2(gout[q * 8 + 2], gout[q * 8 + 3]);
+      w.z = pack_bf16x2(gout[q * 8 + 4], gout[q * 8 + 5]);
+      w.w = pack_bf16x2(gout[q * 8 + 6], gout[q * 8 + 7]);
+      *reinterpret_cast<uint4*>(dst + q * 8) = w;
+    }
+  }
+}
+
+template <bool kBias, bool kSoftcap>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                 const DsArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const TcSmem s = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tmem = tc_setup(s, warp);
+  const WaitGuard g{a.status, s.abort};
+  const int kblocks = (a.H + kBK - 1) / kBK;
+
+  auto for_each_tile = [&](auto&& f) {
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      const int vt0 = panel * a.panel_tiles;
+      const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
+      for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_h);
+      tma_prefetch_desc(&tm_w);
+      const uint64_t pol_h = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_normal();
+      producer_role(s, g, kblocks, for_each_tile,
+                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
+                      tma_load_2d(da, &tm_h, bar, kb * kBK, a.row0 + nb * kBM, pol_h);
+                      tma_load_2d(db, &tm_w, bar, kb * kBK, vt * kBN, pol_w);
+                    });
+    }
+  } else if (warp == 1) {
+    if (lane == 0)
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, false, false), for_each_tile,
+               kmajor_descs);
+  } else {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool dead = false;
+    int tile_par = 0;
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      const int row_local = nb * kBM + r;
+      const bool row_ok = row_local < a.rows;
+      const float4 cf = row_ok ? a.coef[a.row0 + row_local] : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+      const int vt0 = panel * a.panel_tiles;
+      const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
+      for (int vt = vt0; vt < vt1; ++vt) {
+        float* colsum = s.scratch + tile_par * (4 * kBN);
+        dead = !epi_wait_full(s, acc, acc_phase, g, dead);
+        const bool ragged = (vt + 1) * kBN > a.V;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          float gv[32];
+          const int col0 = vt * kBN + c * 32;
+          if (!dead) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(acc * kBN + c * 32),
+                      v);
+            tmem_ld_wait(v);
+            if (!ragged) {
+              ds_chunk<false, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, gv);
+            } else if (col0 < a.V) {
+              ds_chunk<true, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, gv);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) gv[j] = 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gv[j] = 0.f;
+          }
+          if (a.bias_part != nullptr) {
+            const float cs = warp_transpose_sum32(gv, lane);
+            colsum[q * kBN + c * 32 + lane] = cs;
+          }
+        }
+        if (!dead) epi_release(s, acc, lane);
+        if (a.bias_part != nullptr) {
+          // Every epilogue thread reaches this barrier once per tile, also
+          // after an abort, so the barrier cannot hang.
+          named_barrier(1, 128);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = et + h * 128;
+            const int col = vt * kBN + j;
+            if (col < a.V) {
+              const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
+                              colsum[3 * kBN + j];
+              a.bias_part[static_cast<size_t>(a.bias_blk0 + nb) * a.V_pad + col] = t;
+            }
+          }
+        }
+        tile_par ^= 1;
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_teardown(tmem, warp);
+}
+
+// ========================================================= plain GEMM
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const TcSmem s = carve_smem(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t tmem = tc_setup(s, warp);
+  const WaitGuard g{a.status, s.abort};
+  const int kblocks = a.k_blocks;
+
+  auto for_each_tile = [&](auto&& f) {
+    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+      const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
+      f(mt, nt);
+    }
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      const uint64_t pol = l2_policy_evict_normal();
+      const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
+      producer_role(s, g, kblocks, for_each_tile,
+                    [&](int mt, int nt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
+                      if (a_mn) {
+                        // [K rows][M cols] in memory: two 64 x 64 boxes cover M = 128
+                        tma_load_2d(da, &tm_a, bar, mt * kBM, kb * kBK, pol);
+                        tma_load_2d(da + 8192, &tm_a, bar, mt * kBM + 64, kb * kBK, pol);
+                      } else {
+                        tma_load_2d(da, &tm_a, bar, kb * kBK, mt * kBM, pol);
+                      }
+                      if (b_mn) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                          tma_load_2d(db + i * 8192, &tm_b, bar, nt * kBN + i * 64, kb * kBK, pol);
+                      } else {
+                        tma_load_2d(db, &tm_b, bar, kb * kBK, nt * kBN, pol);
+                      }
+                    });
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, a_mn, b_mn), for_each_tile,
+               [&](uint32_t sa, uint32_t sb, int kk, uint64_t& ad, uint64_t& bd) {
+                 ad = a_mn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                           : smem_desc_sw128(sa + kk * 32, 16, 1024);
+                 bd = b_mn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                           : smem_desc_sw128(sb + kk * 32, 16, 1024);
+               });
+    }
+  } else {
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool dead = false;
+    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+      const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
+      dead = !epi_wait_full(s, acc, acc_phase, g, dead);
+      if (!dead) {
+        const int m = mt * kBM + r;
+        const bool row_ok = m < a.M;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                        static_cast<uint32_t>(acc * kBN + c * 32),
+                    v);
+          tmem_ld_wait(v);
+          const int col0 = nt * kBN + c * 32;
+          if (!row_ok || col0 >= a.N) continue;
+          float d[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
+          if (a.mode == kAddPart || a.mode == kAddPartToOut) {
+            const float4* src =
+                reinterpret_cast<const float4*>(a.part + static_cast<size_t>(m) * a.ld_part + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (col0 + i * 4 < a.N) {
+                const float4 p4 = src[i];
+                d[4 * i] += p4.x;
+                d[4 * i + 1] += p4.y;
+                d[4 * i + 2] += p4.z;
+                d[4 * i + 3] += p4.w;
+              }
+            }
+          }
+          if (a.mode == kStorePart || a.mode == kAddPart) {
+            float4* dst = reinterpret_cast<float4*>(a.part + static_cast<size_t>(m) * a.ld_part + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (col0 + i * 4 < a.N)
+                dst[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+          } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                 static_cast<size_t>(m) * a.ld_out + col0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (col0 + i * 8 < a.N) {
+                uint4 w;
+                w.x = pack_bf16x2(d[8 * i + 0], d[8 * i + 1]);
+                w.y = pack_bf16x2(d[8 * i + 2], d[8 * i + 3]);
+                w.z = pack_bf16x2(d[8 * i + 4], d[8 * i + 5]);
+                w.w = pack_bf16x2(d[8 * i + 6], d[8 * i + 7]);
+                *reinterpret_cast<uint4*>(dst + i * 8) = w;
+              }
+            }
+          }
+        }
+        epi_release(s, acc, lane);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  tc_teardown(tmem, warp);
+}
+
+template <class K>
+cudaError_t set_smem_attr(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
+                          bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  auto k = has_bias ? (softcap ? fwd_tc_kernel<true, true> : fwd_tc_kernel<true, false>)
+                    : (softcap ? fwd_tc_kernel<false, true> : fwd_tc_kernel<false, false>);
+  cudaError_t e = set_smem_attr(k);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
+                         bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  auto k = has_bias ? (softcap ? ds_tc_kernel<true, true> : ds_tc_kernel<true, false>)
+                    : (softcap ? ds_tc_kernel<false, true> : ds_tc_kernel<false, false>);
+  cudaError_t e = set_smem_attr(k);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+                           int grid, cudaStream_t st) {
+  cudaError_t e = set_smem_attr(gemm_tc_kernel);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -148,16 +148,22 @@ def forward(hidden, weight, targets, bias=None, ignore_index: int = -100,
     entropy = np.empty(N)
     argmax = np.empty(N, dtype=np.int64)
     correct = np.zeros(N, dtype=bool)
+    top2_gap = np.full(N, np.inf)
     valid = targets != ignore_index
+    Wf = _f64(weight)
+    bf = None if bias is None else _f64(bias)
     for r0 in range(0, N, rb):
         r1 = min(N, r0 + rb)
-        z = transformed_logits(np.asarray(hidden)[r0:r1], weight, bias, logit_scale, softcap)
+        z = transformed_logits(np.asarray(hidden)[r0:r1], Wf, bf, logit_scale, softcap)
         rt = row_terms(z, targets[r0:r1], ignore_index, z_loss_multiplier)
         lse[r0:r1] = rt["lse"]
         loss_rows[r0:r1] = rt["loss"]
         entropy[r0:r1] = rt["entropy"]
         argmax[r0:r1] = rt["argmax"]
         correct[r0:r1] = rt["correct"]
+        if V > 1:
+            top2 = np.partition(z, V - 2, axis=1)[:, V - 2:]
+            top2_gap[r0:r1] = np.abs(top2[:, 1] - top2[:, 0])
     num_valid = int(valid.sum())
     return dict(
         loss=_reduce(loss_rows, num_valid, reduction),
@@ -168,6 +174,8 @@ def forward(hidden, weight, targets, bias=None, ignore_index: int = -100,
         entropy_sum=float(entropy[valid].sum()),
         entropy_rows=entropy,
         argmax=argmax,
+        correct=correct,
+        top2_gap=top2_gap,
     )
 
 

@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol,
+sizes workspaces, and rejects bad arguments before it enqueues any work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_tiled_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "flce.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\**\s+\**(flce_[a-z_]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    decl = declared_functions()
+    assert set(decl) == set(_lib.EXPORTS), decl
+    for name in decl:
+        assert getattr(lib, name) is not None
+
+
+def test_error_strings(lib):
+    for code in range(8):
+        assert _lib.error_string(code)
+    assert "unknown" in _lib.error_string(99)
+
+
+def params(**kw):
+    base = dict(N=256, H=512, V=1000, dtype=_lib.FLCE_BF16)
+    base.update(kw)
+    return _lib.make_params(**base)
+
+
+def test_workspace_sizes(lib):
+    p = params(N=8192, H=4096, V=128256, has_bias=True)
+    fwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
+    bwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
+    assert fwd < 64 << 20                       # a few MB of partial states
+    chunk = 4096 * 128256 * 2                   # one bf16 dlogits chunk of N/2 rows
+    dw = 128256 * 4096 * 4                      # fp32 grad_weight partial
+    assert chunk + dw < bwd < chunk + dw + (64 << 20)
+    assert bwd < 8192 * 128256 * 2 + dw         # never an N x V buffer
+    small = params(N=100, H=64, V=50)
+    assert _lib.workspace_bytes(small, _lib.FLCE_PASS_BACKWARD) > 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(N=-1), dict(H=0), dict(V=0), dict(dtype=7), dict(logit_scale=0.0),
+    dict(logit_scale=float("nan")), dict(z_loss_multiplier=-1.0), dict(softcap=float("inf")),
+])
+def test_invalid_params_rejected(lib, bad):
+    p = params(**bad)
+    n = ctypes.c_size_t(0)
+    assert lib.flce_workspace_bytes(ctypes.byref(p), 0, ctypes.byref(n)) == 1
+
+
+def test_bad_reduction_rejected(lib):
+    p = params()
+    p.reduction = 5
+    n = ctypes.c_size_t(0)
+    assert lib.flce_workspace_bytes(ctypes.byref(p), 0, ctypes.byref(n)) == 1
+    assert lib.flce_workspace_bytes(ctypes.byref(params()), 9, ctypes.byref(n)) == 1
+
+
+def test_bf16_needs_h_multiple_of_8(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.flce_workspace_bytes(ctypes.byref(params(H=100)), 0, ctypes.byref(n)) == 3
+    assert lib.flce_workspace_bytes(ctypes.byref(params(H=100, dtype=_lib.FLCE_F32)), 0,
+                                    ctypes.byref(n)) == 0
+
+
+def test_null_and_misaligned_pointers_rejected_before_any_gpu_work(lib):
+    p = params()
+    fake = 1 << 20   # never dereferenced: every case below fails validation first
+    # NULL hidden
+    assert _lib.forward_raw(p, 0, fake, 0, fake, fake, fake, 0, 0, fake, 1 << 30, 0) == 1
+    # bias pointer given while has_bias == 0
+    assert _lib.forward_raw(p, fake, fake, fake, fake, fake, fake, 0, 0, fake, 1 << 30, 0) == 1
+    # NULL workspace, then a workspace that is too small
+    assert _lib.forward_raw(p, fake, fake, 0, fake, fake, fake, 0, 0, 0, 1 << 30, 0) == 4
+    assert _lib.forward_raw(p, fake, fake, 0, fake, fake, fake, 0, 0, fake, 16, 0) == 4
+    # misaligned hidden
+    assert _lib.forward_raw(p, fake + 2, fake, 0, fake, fake, fake, 0, 0, fake, 1 << 30, 0) == 3
+    # backward: NULL grad_loss; grad_bias without a bias
+    assert _lib.backward_raw(p, fake, fake, 0, fake, fake, 0, fake, fake, 0, fake, 1 << 34, 0) == 1
+    assert _lib.backward_raw(p, fake, fake, 0, fake, fake, fake, fake, fake, fake, fake,
+                             1 << 34, 0) == 1
+    assert lib.flce_check_status(None, None) == 4
+
+
+def test_launch_counter_starts_at_zero_without_work(lib):
+    assert _lib.launch_count() >= 0
