@@ -161,6 +161,41 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
                   flce_stream_t stream);
 
 /*
+ * flce_forward without a workspace argument, for callers that cannot
+ * allocate device memory. The pages have no counterpart; this entry point is
+ * this library's own.
+ *
+ * Who needs it. Some callers cannot call cudaMalloc or any allocator:
+ * - code inside a CUDA-graph capture or a runtime that forbids allocation on
+ *   the hot path;
+ * - runtimes that own every byte of device memory through a fixed arena;
+ * - plain C hosts that only hold pointers to tensors they already have.
+ *
+ * Behaviour.
+ * - Same arguments and results as flce_forward, minus the workspace. The
+ *   kernels are identical, so the outputs are bit-identical too.
+ * - The scratch (partial states, target logits, block sums) lives in one
+ *   fixed 48 MiB device array inside this library. Every GPU that loads the
+ *   library holds it until the process exits.
+ * - Sizes whose forward scratch (flce_workspace_bytes with
+ *   FLCE_PASS_FORWARD) exceeds 48 MiB are rejected with FLCE_ERR_WORKSPACE
+ *   and a message on stderr, before any work is enqueued. The headline size
+ *   N=8192, V=128256 needs about 17 MB.
+ * - The first call on each device looks up the array's device address, with
+ *   that device current. Make that first call before any stream capture.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents. The call zeroes the status word itself, and every other
+ *   scratch byte is written before it is read. Calls that overlap on the GPU
+ *   (different streams, or several host threads) race on the array, so
+ *   serialise them.
+ * - flce_check_status cannot reach the array. Device-detected errors of this
+ *   entry point show up as NaN losses only.
+ */
+int flce_forward_noalloc(const flce_params* p, const void* hidden, const void* weight,
+                         const void* bias, const int64_t* targets, float* loss, float* lse,
+                         int64_t* num_correct, float* entropy_sum, flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device-detected status of the last
  * pass that used `workspace`. The status is FLCE_OK, FLCE_ERR_TARGET_RANGE or
  * FLCE_ERR_TIMEOUT, or FLCE_ERR_CUDA if the synchronisation itself failed.

@@ -27,7 +27,7 @@ ERRORS = {
 EXPORTS = (
     "flce_workspace_bytes", "flce_forward", "flce_backward", "flce_check_status",
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
-    "flce_profiling_enable", "flce_profiling_read",
+    "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
 )
 
 
@@ -82,6 +82,8 @@ def load() -> ctypes.CDLL:
     lib.flce_forward.restype = ctypes.c_int
     lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_backward.restype = ctypes.c_int
+    lib.flce_forward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.flce_forward_noalloc.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
     lib.flce_error_string.argtypes = [ctypes.c_int]
@@ -137,6 +139,14 @@ def forward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int
                 stream: int) -> int:
     return load().flce_forward(ctypes.byref(p), hidden, weight, bias, targets, loss, lse,
                                num_correct, entropy_sum, ws, ws_bytes, stream)
+
+
+def forward_noalloc_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int,
+                        loss: int, lse: int, num_correct: int, entropy_sum: int,
+                        stream: int) -> int:
+    """flce_forward_noalloc: the forward with the library's fixed 48 MiB scratch array."""
+    return load().flce_forward_noalloc(ctypes.byref(p), hidden, weight, bias, targets, loss, lse,
+                                       num_correct, entropy_sum, stream)
 
 
 def backward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int, lse: int,
