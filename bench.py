@@ -386,9 +386,9 @@ def ours_main(args, w):
 
 def bwd_chunks(p) -> list[int]:
     N = p.N
-    if N <= 128:
+    if N <= 256:
         return [N]
-    half = -(-(-(-N // 2)) // 128) * 128
+    half = -(-(-(-N // 2)) // 256) * 256
     rows, r = [], 0
     while r < N:
         rows.append(min(half, N - r))

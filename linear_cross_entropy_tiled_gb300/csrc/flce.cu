@@ -25,6 +25,7 @@ namespace {
 struct DeviceInfo {
   bool init = false;
   int sms = 0;
+  int pairs = 0;  // co-resident CTA pairs of the tcgen05 kernels
   int major = 0, minor = 0;
 };
 std::mutex g_mu;
@@ -58,6 +59,9 @@ int device_info(DeviceInfo* out) {
       if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
         return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (d.major == 10 && d.minor == 3) {
+      if ((e = tc_max_active_pairs(&d.pairs)) != cudaSuccess || d.pairs <= 0) d.pairs = d.sms / 2;
     }
     d.init = true;
   }
@@ -195,18 +199,19 @@ BwdLayout bwd_layout(const flce_params* p) {
   const int64_t N = p->N, V = p->V, H = p->H;
   const size_t elem = p->dtype == FLCE_BF16 ? 2 : 4;
   L.V_pad = (V + 7) / 8 * 8;
-  if (N <= kBM) {
+  if (N <= kPairM) {
     L.chunk = N;
   } else {
-    const int64_t half = ceil_div(ceil_div(N, 2), kBM) * kBM;
-    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem)) / kBM * kBM;
-    if (cap < kBM) cap = kBM;
-    // FLCE_MAX_CHUNK_ROWS (a multiple of 128) lowers the row-chunk cap. The
+    // chunk boundaries fall on 256-row pair blocks
+    const int64_t half = ceil_div(ceil_div(N, 2), kPairM) * kPairM;
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem)) / kPairM * kPairM;
+    if (cap < kPairM) cap = kPairM;
+    // FLCE_MAX_CHUNK_ROWS (a multiple of 256) lowers the row-chunk cap. The
     // work and the result are the same; it is there so tests can reach the
     // three-or-more-chunk schedule at small sizes.
     if (const char* env = getenv("FLCE_MAX_CHUNK_ROWS")) {
-      const long long r = atoll(env) / kBM * kBM;
-      if (r >= kBM && r < cap) cap = r;
+      const long long r = atoll(env) / kPairM * kPairM;
+      if (r >= kPairM && r < cap) cap = r;
     }
     L.chunk = half < cap ? half : cap;
   }
@@ -358,15 +363,15 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
 
   if (N > 0) {
     if (p->dtype == FLCE_BF16) {
-      fa.n_blocks = static_cast<int>(ceil_div(N, kBM));
+      fa.n_blocks = static_cast<int>(ceil_div(N, kPairM));
       fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
       int grid = 1;
-      fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.sms, &grid);
+      fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.pairs, &grid);
       fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
       fa.num_units = fa.num_panels * fa.n_blocks;
       CUtensorMap tm_h, tm_w;
       if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
-      if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBN)) != FLCE_OK) return v;
+      if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
       v = launch("flce_fwd_tc", st, [&] {
         return launch_fwd_tc(tm_h, tm_w, fa, bias != nullptr, p->softcap > 0.f, grid, st);
       });
@@ -484,7 +489,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   if (p->dtype == FLCE_BF16) {
     CUtensorMap tm_h, tm_w, tm_w_mn;
     if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
-    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBN)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
     if ((v = make_map(&tm_w_mn, weight, H, V, uint64_t(H) * 2, 64, 64)) != FLCE_OK) return v;
     float* dw_part = reinterpret_cast<float*>(ws + L.dw);
     for (int c = 0; c < L.nchunks; ++c) {
@@ -492,10 +497,10 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       const int rows = static_cast<int>(N - row0 < L.chunk ? N - row0 : L.chunk);
       da.rows = rows;
       da.row0 = row0;
-      da.n_blocks = static_cast<int>(ceil_div(rows, kBM));
+      da.n_blocks = static_cast<int>(ceil_div(rows, kPairM));
       da.v_tiles = static_cast<int>(ceil_div(V, kBN));
       int grid = 1;
-      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.v_tiles, d.sms, &grid);
+      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.v_tiles, d.pairs, &grid);
       da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
       da.num_units = da.num_panels * da.n_blocks;
       da.bias_blk0 = row0 / kBM;
@@ -512,7 +517,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.M = rows;
         ga.N = H;
         ga.K = V;
-        ga.m_tiles = static_cast<int>(ceil_div(rows, kBM));
+        ga.m_tiles = static_cast<int>(ceil_div(rows, kPairM));
         ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
         ga.k_blocks = static_cast<int>(ceil_div(V, kBK));
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
@@ -522,7 +527,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.out = static_cast<uint8_t*>(grad_hidden) + size_t(row0) * H * 2;
         ga.ld_out = H;
         ga.status = status;
-        const int g2 = ga.num_tiles < d.sms ? ga.num_tiles : d.sms;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_hidden_tc", st, [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, g2, st); });
         if (v != FLCE_OK) return v;
       }
@@ -536,7 +541,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.M = V;
         ga.N = H;
         ga.K = rows;
-        ga.m_tiles = static_cast<int>(ceil_div(V, kBM));
+        ga.m_tiles = static_cast<int>(ceil_div(V, kPairM));
         ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
         ga.k_blocks = static_cast<int>(ceil_div(rows, kBK));
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
@@ -555,7 +560,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.part = dw_part;
         ga.ld_part = H;
         ga.status = status;
-        const int g2 = ga.num_tiles < d.sms ? ga.num_tiles : d.sms;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st, [&] { return launch_gemm_tc(tm_a, tm_b, ga, g2, st); });
         if (v != FLCE_OK) return v;
       }

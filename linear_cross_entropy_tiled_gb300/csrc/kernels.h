@@ -13,19 +13,23 @@ namespace flce {
 enum : int { kDevErrTargetRange = 1, kDevErrTimeout = 2 };
 
 // ---- tcgen05 tile shape shared by every bf16 kernel -----------------------
-// One CTA per SM owns a 128 x 256 fp32 accumulator in TMEM, double-buffered
-// (2 x 256 of the 512 TMEM columns). Operands arrive in 64-deep K slices
-// (one 128-byte swizzle row of bf16) through a 4-stage TMA ring.
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+// CTAs run in pairs (clusters of 2) with the 2-SM MMA (cta_group::2).
+// - A pair computes a 256 x 256 fp32 tile. Each CTA owns 128 rows of it in
+//   its own TMEM, double-buffered (2 x 256 of its 512 TMEM columns).
+// - Each CTA stages its 128 rows of A and its half (128 rows) of B in 64-deep
+//   K slices, one 128-byte swizzle row of bf16, through a 6-stage TMA ring.
+constexpr int kBM = 128;                         // rows of the tile per CTA
+constexpr int kPairM = 256;                      // rows of the tile per pair
+constexpr int kBN = 256;                         // columns of the tile
+constexpr int kBNHalf = 128;                     // B rows staged per CTA
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kStageA = kBM * kBK * 2;           // 16 KB
-constexpr int kStageB = kBN * kBK * 2;           // 32 KB
-constexpr int kStageBytes = kStageA + kStageB;   // 48 KB
+constexpr int kStageB = kBNHalf * kBK * 2;       // 16 KB
+constexpr int kStageBytes = kStageA + kStageB;   // 32 KB per CTA
 constexpr int kTcThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTmemCols = 512;
-// dynamic shared memory: 1 KB alignment slack + stages + control block
+// dynamic shared memory: 1 KB alignment slack + stages + 8 KB scratch + control block
 constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;
 
 // ---- fp32 SIMT path tile shape -------------------------------------------
@@ -136,7 +140,8 @@ struct BiasReduceArgs {
   void* grad_bias;             // dtype of the pass
 };
 
-// tcgen05 / TMA kernels (bf16)
+// tcgen05 / TMA kernels (bf16). `grid` is the number of CTA pairs.
+cudaError_t tc_max_active_pairs(int* pairs);
 cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
                           bool has_bias, bool softcap, int grid, cudaStream_t s);
 cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,

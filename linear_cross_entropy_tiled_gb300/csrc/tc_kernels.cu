@@ -1,10 +1,15 @@
 // tcgen05 / TMA kernels of the bf16 path (sm_103a).
 //
-// Every kernel here is a persistent, warp-specialised CTA (one per SM):
-//   warp 0     one thread issues TMA tile loads into a 4-stage shared ring;
-//   warp 1     one thread issues tcgen05.mma into a double-buffered TMEM
-//              accumulator (2 x 128 lanes x 256 fp32 columns). This warp
-//              also owns the TMEM allocation;
+// Every kernel here is persistent and warp-specialised. CTAs run in pairs
+// (clusters of 2) that share one 2-SM MMA (tcgen05.mma.cta_group::2) per
+// 256 x 256 tile. Roles in each CTA of a pair:
+//   warp 0     one thread issues TMA loads of this CTA's 128 rows of A and
+//              its half of B into a 6-stage shared ring. The completion
+//              bytes of both CTAs go to the even CTA's "full" barriers;
+//   warp 1     in the even CTA, one thread issues the pair's MMAs into
+//              double-buffered TMEM accumulators (each CTA holds its 128
+//              rows x 256 fp32 columns) and commits to both CTAs' barriers.
+//              In both CTAs this warp owns the TMEM allocation;
 //   warps 2-5  the epilogue. Each thread owns one accumulator row, which is
 //              one TMEM lane, and reads it with tcgen05.ld.
 // The kernels differ only in the tile sequence, the operand layouts and the
@@ -66,36 +71,41 @@ __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
   return s;
 }
 
+// Barriers and TMEM of both CTAs of the pair. The cluster barrier at the end
+// makes every barrier initialised before any remote arrive or
+// remote-signalling TMA can target it.
 __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
+      mbar_init(&s.full[i], 1);   // even CTA: its own arrive.expect_tx
+      mbar_init(&s.empty[i], 1);  // the MMA commit, multicast to both CTAs
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);  // one arrival per epilogue warp
+      mbar_init(&s.tfull[i], 1);   // the MMA commit, multicast to both CTAs
+      mbar_init(&s.tempty[i], 8);  // even CTA: 4 epilogue warps x 2 CTAs
     }
     mbar_init(s.mma_done, 1);
     *s.abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(s.tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(s.tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   tc_fence_after();
   return *s.tmem_slot;
 }
 
+// The even CTA's MMAs read the odd CTA's shared memory and write its TMEM.
+// So neither CTA releases TMEM or exits before the whole pair is done.
 __device__ __forceinline__ void tc_teardown(uint32_t tmem, int warp) {
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -110,11 +120,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // --------------------------------------------------------- producer / MMA
-// ForEachTile(f) calls f(ta, tb) for every tile of this CTA, in order.
-// Issue(ta, tb, kb, a_dst, b_dst, bar) issues the TMA loads of one K slice.
+// ForEachTile(f) calls f(ta, tb) for every tile of this pair, in order.
+// Issue(ta, tb, kb, a_dst, b_dst, mbar) issues this CTA's TMA loads of one
+// K slice; `mbar` is the shared::cluster address of the even CTA's barrier.
 template <class ForEachTile, class Issue>
 __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& g, int kblocks,
-                                              ForEachTile for_each_tile, Issue issue) {
+                                              bool leader, ForEachTile for_each_tile,
+                                              Issue issue) {
   int stage = 0;
   uint32_t phase = 0;
   bool dead = false;
@@ -125,8 +137,10 @@ __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& 
         dead = true;
         break;
       }
-      mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-      issue(ta, tb, kb, s.a + stage * kStageA, s.b + stage * kStageB, &s.full[stage]);
+      // The even CTA expects the bytes of both CTAs' loads on its barrier.
+      if (leader) mbar_arrive_expect_tx(&s.full[stage], 2 * kStageBytes);
+      issue(ta, tb, kb, s.a + stage * kStageA, s.b + stage * kStageB,
+            mapa_shared(smem_u32(&s.full[stage]), 0));
       ++issued;
       if (++stage == kStages) {
         stage = 0;
@@ -134,7 +148,7 @@ __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& 
       }
     }
   });
-  if (dead) {
+  if (dead && leader) {
     // Let the loads already in flight land before shared memory is released.
     const long long first = issued > kStages ? issued - kStages : 0;
     for (long long i = first; i < issued; ++i)
@@ -142,8 +156,8 @@ __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& 
   }
 }
 
-// Descs(sa, sb, kk, adesc, bdesc) builds the descriptors of the kk-th
-// 16-deep K step within a 64-deep stage.
+// Runs in the even CTA only. Descs(sa, sb, kk, adesc, bdesc) builds the
+// descriptors of the kk-th 16-deep K step within a 64-deep stage.
 template <class ForEachTile, class Descs>
 __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, uint32_t tmem,
                                          int kblocks, uint32_t idesc, ForEachTile for_each_tile,
@@ -173,20 +187,20 @@ __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, ui
       for (int kk = 0; kk < kBK / 16; ++kk) {
         uint64_t ad, bd;
         descs(sa, sb, kk, ad, bd);
-        umma_f16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        umma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      umma_commit(&s.empty[stage]);
+      umma_commit_pair_multicast(&s.empty[stage], 0x3);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    umma_commit(&s.tfull[acc]);
+    umma_commit_pair_multicast(&s.tfull[acc], 0x3);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   });
   // Every MMA must have finished before TMEM is released.
-  umma_commit(s.mma_done);
+  umma_commit_pair(s.mma_done);
   drain_wait(s.mma_done, 0);
 }
 
@@ -206,10 +220,12 @@ __device__ __forceinline__ bool epi_wait_full(const TcSmem& s, int acc, uint32_t
   return ok;
 }
 
+// Tells the even CTA's MMA thread that this warp is done with accumulator
+// `acc`. Both CTAs' epilogue warps arrive on the even CTA's barrier.
 __device__ __forceinline__ void epi_release(const TcSmem& s, int acc, int lane) {
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&s.tempty[acc]);
+  if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[acc]), 0));
 }
 
 // 32 bias values times scale, for columns col0 .. col0+31. Columns at or
@@ -341,18 +357,20 @@ __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs
 }
 
 template <bool kBias, bool kSoftcap>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                   const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tmem = tc_setup(s, warp);
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
   const int kblocks = (a.H + kBK - 1) / kBK;
 
   auto for_each_tile = [&](auto&& f) {
-    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    for (int u = pair; u < a.num_units; u += npairs) {
       const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
@@ -366,15 +384,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol_h = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_normal();
-      producer_role(s, g, kblocks, for_each_tile,
-                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
-                      tma_load_2d(da, &tm_h, bar, kb * kBK, nb * kBM, pol_h);
-                      tma_load_2d(db, &tm_w, bar, kb * kBK, vt * kBN, pol_w);
+      producer_role(s, g, kblocks, rank == 0, for_each_tile,
+                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      tma_load_2d_pair(da, &tm_h, bar, kb * kBK, nb * kPairM + rank * kBM, pol_h);
+                      tma_load_2d_pair(db, &tm_w, bar, kb * kBK, vt * kBN + rank * kBNHalf, pol_w);
                     });
     }
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, false, false), for_each_tile,
+    if (lane == 0 && rank == 0)
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, false, false), for_each_tile,
                kmajor_descs);
   } else {
     const int q = warp & 3;
@@ -382,9 +400,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
-    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    for (int u = pair; u < a.num_units; u += npairs) {
       const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
-      const int row = nb * kBM + r;
+      const int row = nb * kPairM + static_cast<int>(rank) * kBM + r;
       const bool row_ok = row < a.N;
       const long long tgt = row_ok ? a.targets[row] : a.ignore_index;
       float m = -INFINITY, ssum = 0.f, tsum = 0.f;
@@ -476,18 +494,20 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
 }
 
 template <bool kBias, bool kSoftcap>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const DsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tmem = tc_setup(s, warp);
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
   const int kblocks = (a.H + kBK - 1) / kBK;
 
   auto for_each_tile = [&](auto&& f) {
-    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    for (int u = pair; u < a.num_units; u += npairs) {
       const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
@@ -501,15 +521,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol_h = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_normal();
-      producer_role(s, g, kblocks, for_each_tile,
-                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
-                      tma_load_2d(da, &tm_h, bar, kb * kBK, a.row0 + nb * kBM, pol_h);
-                      tma_load_2d(db, &tm_w, bar, kb * kBK, vt * kBN, pol_w);
+      producer_role(s, g, kblocks, rank == 0, for_each_tile,
+                    [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      tma_load_2d_pair(da, &tm_h, bar, kb * kBK,
+                                       a.row0 + nb * kPairM + rank * kBM, pol_h);
+                      tma_load_2d_pair(db, &tm_w, bar, kb * kBK, vt * kBN + rank * kBNHalf, pol_w);
                     });
     }
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, false, false), for_each_tile,
+    if (lane == 0 && rank == 0)
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, false, false), for_each_tile,
                kmajor_descs);
   } else {
     const int q = warp & 3;
@@ -519,10 +540,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t acc_phase = 0;
     bool dead = false;
     int tile_par = 0;
-    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    for (int u = pair; u < a.num_units; u += npairs) {
       const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
-      const int row_local = nb * kBM + r;
+      const int blk_local = nb * 2 + static_cast<int>(rank);  // this CTA's 128-row block
+      const int row_local = blk_local * kBM + r;
       const bool row_ok = row_local < a.rows;
+      const bool blk_ok = blk_local * kBM < a.rows;
       const float4 cf = row_ok ? a.coef[a.row0 + row_local] : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
@@ -566,10 +589,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int h = 0; h < 2; ++h) {
             const int j = et + h * 128;
             const int col = vt * kBN + j;
-            if (col < a.V) {
+            if (col < a.V && blk_ok) {
               const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
                               colsum[3 * kBN + j];
-              a.bias_part[static_cast<size_t>(a.bias_blk0 + nb) * a.V_pad + col] = t;
+              a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.V_pad + col] = t;
             }
           }
         }
@@ -583,18 +606,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ========================================================= plain GEMM
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tmem = tc_setup(s, warp);
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
   const int kblocks = a.k_blocks;
 
   auto for_each_tile = [&](auto&& f) {
-    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    for (int t = pair; t < a.num_tiles; t += npairs) {
       const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
       f(mt, nt);
     }
@@ -606,28 +631,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_b);
       const uint64_t pol = l2_policy_evict_normal();
       const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
-      producer_role(s, g, kblocks, for_each_tile,
-                    [&](int mt, int nt, int kb, uint8_t* da, uint8_t* db, uint64_t* bar) {
+      const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
+      producer_role(s, g, kblocks, rank == 0, for_each_tile,
+                    [&](int mt, int nt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      const int m0 = mt * kPairM + m_off, n0 = nt * kBN + n_off;
                       if (a_mn) {
-                        // [K rows][M cols] in memory: two 64 x 64 boxes cover M = 128
-                        tma_load_2d(da, &tm_a, bar, mt * kBM, kb * kBK, pol);
-                        tma_load_2d(da + 8192, &tm_a, bar, mt * kBM + 64, kb * kBK, pol);
+                        // [K rows][M cols] in memory: two 64 x 64 boxes cover 128 rows of M
+                        tma_load_2d_pair(da, &tm_a, bar, m0, kb * kBK, pol);
+                        tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, kb * kBK, pol);
                       } else {
-                        tma_load_2d(da, &tm_a, bar, kb * kBK, mt * kBM, pol);
+                        tma_load_2d_pair(da, &tm_a, bar, kb * kBK, m0, pol);
                       }
                       if (b_mn) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                          tma_load_2d(db + i * 8192, &tm_b, bar, nt * kBN + i * 64, kb * kBK, pol);
+                        // [K rows][N cols] in memory: two 64 x 64 boxes cover this CTA's 128 columns
+                        tma_load_2d_pair(db, &tm_b, bar, n0, kb * kBK, pol);
+                        tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, kb * kBK, pol);
                       } else {
-                        tma_load_2d(db, &tm_b, bar, kb * kBK, nt * kBN, pol);
+                        tma_load_2d_pair(db, &tm_b, bar, kb * kBK, n0, pol);
                       }
                     });
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kBM, kBN, a_mn, b_mn), for_each_tile,
+      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, a_mn, b_mn), for_each_tile,
                [&](uint32_t sa, uint32_t sb, int kk, uint64_t& ad, uint64_t& bd) {
                  ad = a_mn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
                            : smem_desc_sw128(sa + kk * 32, 16, 1024);
@@ -641,11 +668,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
-    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+    for (int t = pair; t < a.num_tiles; t += npairs) {
       const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
       dead = !epi_wait_full(s, acc, acc_phase, g, dead);
       if (!dead) {
-        const int m = mt * kBM + r;
+        const int m = mt * kPairM + static_cast<int>(rank) * kBM + r;
         const bool row_ok = m < a.M;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
@@ -711,13 +738,29 @@ cudaError_t set_smem_attr(K kernel) {
 
 }  // namespace
 
+cudaError_t tc_max_active_pairs(int* pairs) {
+  auto k = fwd_tc_kernel<false, false>;
+  cudaError_t e = set_smem_attr(k);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kTcSmemBytes;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+  if (e != cudaSuccess) return e;
+  *pairs = n;
+  return cudaSuccess;
+}
+
+// `grid` counts CTA pairs; the launch has 2 * grid CTAs.
 cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
                           bool has_bias, bool softcap, int grid, cudaStream_t st) {
   auto k = has_bias ? (softcap ? fwd_tc_kernel<true, true> : fwd_tc_kernel<true, false>)
                     : (softcap ? fwd_tc_kernel<false, true> : fwd_tc_kernel<false, false>);
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
-  k<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
   return cudaGetLastError();
 }
 
@@ -727,7 +770,7 @@ cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const
                     : (softcap ? ds_tc_kernel<false, true> : ds_tc_kernel<false, false>);
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
-  k<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
   return cudaGetLastError();
 }
 
@@ -735,7 +778,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, con
                            int grid, cudaStream_t st) {
   cudaError_t e = set_smem_attr(gemm_tc_kernel);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
+  gemm_tc_kernel<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
   return cudaGetLastError();
 }
 

@@ -82,7 +82,7 @@ def test_fullsize_bf16(name):
     assert sure <= out["num_correct"] <= sure + int((near & valid).sum())
     assert_entropy_close(out["entropy_sum"], ref["entropy_sum"])
 
-    half = -(-(-(-w.N // 2)) // 128) * 128
+    half = -(-(-(-w.N // 2)) // 256) * 256
     rows = sample_rows(w.N, [half], seed=w.seed)
     gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows, bias=d["bias"],
                                  reduction=w.reduction, **okw)
