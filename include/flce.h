@@ -103,9 +103,10 @@ typedef struct {
  * Device bytes the caller must provide as `workspace` for one pass. The
  * forward and backward need different amounts, and one workspace may serve
  * both passes in turn. For the headline size (N=8192, H=4096, V=128256,
- * bf16) the forward needs a few MB. The backward needs about 3.2 GB:
+ * bf16) the forward needs a few MB. The backward needs about 3.3 GB:
  * - a 4096-row bf16 dlogits chunk (1.05 GB);
  * - an fp32 grad_weight partial (2.1 GB);
+ * - two fp32 K-split partials of the grad_hidden chunk (134 MB);
  * - per-128-row bias partial sums.
  * Returns FLCE_OK and sets *bytes, or an argument error.
  */

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+
+#include <cmath>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -156,6 +158,7 @@ constexpr int kMinPanelTiles = 4;
 constexpr int kMaxPanelTiles = 32;
 constexpr size_t kHeader = 256;
 constexpr size_t kChunkByteCap = size_t(4) << 30;
+constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_splits)
 
 struct FwdLayout {
   int num_panels_max;
@@ -191,7 +194,7 @@ FwdLayout fwd_layout(const flce_params* p) {
 struct BwdLayout {
   int64_t chunk, V_pad;
   int nchunks, rowblk, n_rowblocks;
-  size_t coef, ds, dw, bias_part, total;
+  size_t coef, ds, dw, dh_part, bias_part, total;
 };
 
 BwdLayout bwd_layout(const flce_params* p) {
@@ -225,6 +228,8 @@ BwdLayout bwd_layout(const flce_params* p) {
   o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
   L.dw = o;
   if (p->dtype == FLCE_BF16 && L.nchunks > 1) o = align_up(o + size_t(V) * H * 4, 1024);
+  L.dh_part = o;
+  if (p->dtype == FLCE_BF16) o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
   L.bias_part = o;
   if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
   L.total = o;
@@ -259,6 +264,22 @@ int choose_panel_tiles(int n_blocks, int v_tiles, int sms, int* grid_out) {
     }
   }
   *grid_out = best_grid;
+  return best;
+}
+
+// K splits of the grad_hidden GEMM. Its long tiles (K = V) number only
+// rows/256 x H/256 (256 at the headline size), which is 3.37 waves on 76
+// pairs: the last wave runs a third full. Two K halves give 6.74 waves
+// (96 % full). The partials cost an extra fp32 write and read of
+// rows x H per split.
+int choose_k_splits(int tiles, int k_blocks, int pairs) {
+  auto eff = [&](int s) {
+    const double w = double(tiles) * s / pairs;
+    return w / std::ceil(w);
+  };
+  int best = 1;
+  for (int s = 2; s <= kMaxKSplits; ++s)
+    if (k_blocks / s >= 128 && eff(s) > eff(best) + 0.04) best = s;
   return best;
 }
 
@@ -521,15 +542,34 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
         ga.k_blocks = static_cast<int>(ceil_div(V, kBK));
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = choose_k_splits(ga.num_tiles, ga.k_blocks, d.pairs);
+        ga.kb_per_split = static_cast<int>(ceil_div(ga.k_blocks, ga.k_splits));
         ga.a_mn = 0;
         ga.b_mn = 1;
         ga.mode = kStoreOut;
         ga.out = static_cast<uint8_t*>(grad_hidden) + size_t(row0) * H * 2;
         ga.ld_out = H;
+        ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.ld_part = H;
+        ga.split_stride = static_cast<long long>(L.chunk) * H;
         ga.status = status;
-        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+        const int units = ga.num_tiles * ga.k_splits;
+        const int g2 = units < d.pairs ? units : d.pairs;
         v = launch("flce_grad_hidden_tc", st, [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, g2, st); });
         if (v != FLCE_OK) return v;
+        if (ga.k_splits > 1) {
+          SplitReduceArgs ra2{};
+          ra2.M = rows;
+          ra2.N = H;
+          ra2.splits = ga.k_splits;
+          ra2.part = ga.part;
+          ra2.ld_part = H;
+          ra2.split_stride = ga.split_stride;
+          ra2.out = ga.out;
+          ra2.ld_out = H;
+          v = launch("flce_split_reduce", st, [&] { return launch_split_reduce(ra2, st); });
+          if (v != FLCE_OK) return v;
+        }
       }
       if (grad_weight) {
         // grad_weight[V, H] (+)= dS^T[V, rows] (MN-major) x h[rows, H] (MN-major)
@@ -545,6 +585,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
         ga.k_blocks = static_cast<int>(ceil_div(rows, kBK));
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = 1;
+        ga.kb_per_split = ga.k_blocks;
         ga.a_mn = 1;
         ga.b_mn = 1;
         if (L.nchunks == 1)

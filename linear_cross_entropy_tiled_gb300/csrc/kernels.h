@@ -111,16 +111,33 @@ enum GemmMode : int {
   kAddPartToOut = 3   // out  = part + acc
 };
 
+// One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With
+// k_splits > 1 the K loop of every tile is cut into k_splits contiguous
+// ranges. Split s of tile (m, n) writes its fp32 result to
+// part + s * split_stride, and split_reduce_kernel later sums the splits in
+// order. Units are ordered split-major, so the units that run at the same
+// time share their K range.
 struct GemmArgs {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks, num_tiles;
+  int k_splits, kb_per_split;
   int a_mn, b_mn;              // 1: operand is MN-major in memory
-  int mode;
+  int mode;                    // GemmMode (kStorePart when k_splits > 1)
   void* out;
   long long ld_out;
   float* part;
   long long ld_part;
+  long long split_stride;      // elements between split partial buffers
   int* status;
+};
+
+// out[m, n] (bf16) = sum over s of part[s][m, n], in split order.
+struct SplitReduceArgs {
+  int M, N, splits;
+  const float* part;
+  long long ld_part, split_stride;
+  void* out;
+  long long ld_out;
 };
 
 struct SimtGemmArgs {
@@ -159,6 +176,7 @@ cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s);
 
 constexpr int kMergeThreads = 256;
 

@@ -4,7 +4,8 @@
 //   finalize    fixed-order sum of the block sums into the reduced outputs;
 //   row_coef    per-row backward coefficients (gamma with the reduction and
 //               the z-loss folded in);
-//   bias_reduce fixed-order sum of per-row-block grad_bias partials.
+//   bias_reduce fixed-order sum of per-row-block grad_bias partials;
+//   split_reduce fixed-order sum of the K-split partials of grad_hidden.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -164,7 +165,37 @@ __global__ void __launch_bounds__(256) bias_reduce_kernel(const BiasReduceArgs a
   }
 }
 
+// Sums the fp32 K-split partials of a GEMM in split order and casts to bf16.
+// Each thread handles 4 consecutive columns (N is a multiple of 8).
+__global__ void __launch_bounds__(256) split_reduce_kernel(const SplitReduceArgs a) {
+  const long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long per_row = a.N / 4;
+  if (q >= static_cast<long long>(a.M) * per_row) return;
+  const long long m = q / per_row;
+  const long long n = (q - m * per_row) * 4;
+  float4 acc = *reinterpret_cast<const float4*>(a.part + m * a.ld_part + n);
+  for (int s = 1; s < a.splits; ++s) {
+    const float4 p = *reinterpret_cast<const float4*>(a.part + s * a.split_stride + m * a.ld_part + n);
+    acc.x += p.x;
+    acc.y += p.y;
+    acc.z += p.z;
+    acc.w += p.w;
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&lo);
+  w.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + m * a.ld_out + n) = w;
+}
+
 }  // namespace
+
+cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s) {
+  const long long n = static_cast<long long>(a.M) * (a.N / 4);
+  split_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s) {
   merge_kernel<<<nblk, kMergeThreads, 0, s>>>(a);

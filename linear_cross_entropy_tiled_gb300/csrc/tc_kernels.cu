@@ -121,17 +121,19 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // --------------------------------------------------------- producer / MMA
 // ForEachTile(f) calls f(ta, tb) for every tile of this pair, in order.
+// KBlocks(ta, tb) is the number of 64-deep K slices of that tile.
 // Issue(ta, tb, kb, a_dst, b_dst, mbar) issues this CTA's TMA loads of one
 // K slice; `mbar` is the shared::cluster address of the even CTA's barrier.
-template <class ForEachTile, class Issue>
-__device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& g, int kblocks,
-                                              bool leader, ForEachTile for_each_tile,
-                                              Issue issue) {
+template <class ForEachTile, class KBlocks, class Issue>
+__device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& g,
+                                              KBlocks kblocks_of, bool leader,
+                                              ForEachTile for_each_tile, Issue issue) {
   int stage = 0;
   uint32_t phase = 0;
   bool dead = false;
   long long issued = 0;
   for_each_tile([&](int ta, int tb) {
+    const int kblocks = kblocks_of(ta, tb);
     for (int kb = 0; kb < kblocks && !dead; ++kb) {
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, g)) {
         dead = true;
@@ -156,19 +158,21 @@ __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& 
   }
 }
 
-// Runs in the even CTA only. Descs(sa, sb, kk, adesc, bdesc) builds the
-// descriptors of the kk-th 16-deep K step within a 64-deep stage.
-template <class ForEachTile, class Descs>
+// Runs in the even CTA only. Descs(ta, tb, sa, sb, kk, adesc, bdesc, idesc)
+// builds the operand and instruction descriptors of the kk-th 16-deep K
+// step within a 64-deep stage of tile (ta, tb).
+template <class ForEachTile, class KBlocks, class Descs>
 __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, uint32_t tmem,
-                                         int kblocks, uint32_t idesc, ForEachTile for_each_tile,
+                                         KBlocks kblocks_of, ForEachTile for_each_tile,
                                          Descs descs) {
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool dead = false;
-  for_each_tile([&](int, int) {
+  for_each_tile([&](int ta, int tb) {
     if (dead) return;
+    const int kblocks = kblocks_of(ta, tb);
     if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, g)) {
       dead = true;
       return;
@@ -186,7 +190,8 @@ __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, ui
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         uint64_t ad, bd;
-        descs(sa, sb, kk, ad, bd);
+        uint32_t idesc;
+        descs(ta, tb, sa, sb, kk, ad, bd, idesc);
         umma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
       }
       umma_commit_pair_multicast(&s.empty[stage], 0x3);
@@ -204,10 +209,20 @@ __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, ui
   drain_wait(s.mma_done, 0);
 }
 
-__device__ __forceinline__ void kmajor_descs(uint32_t sa, uint32_t sb, int kk, uint64_t& ad,
-                                             uint64_t& bd) {
+// Both operands K-major; the pair computes M = 256, N = 256.
+__device__ __forceinline__ void kmajor_descs(int, int, uint32_t sa, uint32_t sb, int kk,
+                                             uint64_t& ad, uint64_t& bd, uint32_t& idesc) {
   ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
   bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
+  idesc = idesc_bf16_f32(kPairM, kBN, false, false);
+}
+
+// Operand descriptor of the kk-th 16-deep K step: K-major rows advance 32 B
+// within the swizzle row; MN-major tiles advance 16 k-rows (two 1 KB atoms),
+// with the two 64-wide MN atoms 8 KB apart.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool mn_major, int kk) {
+  return mn_major ? smem_desc_sw128(base + kk * 2048, 8192, 1024)
+                  : smem_desc_sw128(base + kk * 32, 16, 1024);
 }
 
 // Epilogue: wait until accumulator `acc` is full. The result is warp-uniform,
@@ -384,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol_h = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_normal();
-      producer_role(s, g, kblocks, rank == 0, for_each_tile,
+      producer_role(s, g, [&](int, int) { return kblocks; }, rank == 0, for_each_tile,
                     [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
                       tma_load_2d_pair(da, &tm_h, bar, kb * kBK, nb * kPairM + rank * kBM, pol_h);
                       tma_load_2d_pair(db, &tm_w, bar, kb * kBK, vt * kBN + rank * kBNHalf, pol_w);
@@ -392,8 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, false, false), for_each_tile,
-               kmajor_descs);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -521,7 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_w);
       const uint64_t pol_h = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_normal();
-      producer_role(s, g, kblocks, rank == 0, for_each_tile,
+      producer_role(s, g, [&](int, int) { return kblocks; }, rank == 0, for_each_tile,
                     [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
                       tma_load_2d_pair(da, &tm_h, bar, kb * kBK,
                                        a.row0 + nb * kPairM + rank * kBM, pol_h);
@@ -530,8 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, false, false), for_each_tile,
-               kmajor_descs);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -606,6 +619,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 }
 
 // ========================================================= plain GEMM
+// D = A B with fp32 accumulation; the two gradient contractions. Units
+// (split, tile) go round-robin over the pairs: consecutive units are
+// neighbouring tiles of the same K range, which share an operand strip in L2.
+// The arguments are copied into registers up front; the role loops read no
+// kernel parameters.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const GemmArgs a) {
@@ -616,13 +634,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
-  const int kblocks = a.k_blocks;
+  const int M = a.M, N = a.N, n_tiles = a.n_tiles, num_tiles = a.num_tiles;
+  const int k_blocks = a.k_blocks, kb_per_split = a.kb_per_split;
+  const int units = num_tiles * a.k_splits;
+  const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
 
+  // (split, tile) of every unit of this pair
   auto for_each_tile = [&](auto&& f) {
-    for (int t = pair; t < a.num_tiles; t += npairs) {
-      const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
-      f(mt, nt);
+    for (int u = pair; u < units; u += npairs) {
+      const int sp = u / num_tiles;
+      f(sp, u - sp * num_tiles);
     }
+  };
+  auto kblocks_of = [&](int sp, int) {
+    return min(k_blocks, (sp + 1) * kb_per_split) - sp * kb_per_split;
   };
 
   if (warp == 0) {
@@ -630,50 +655,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
       const uint64_t pol = l2_policy_evict_normal();
-      const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
       const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
-      producer_role(s, g, kblocks, rank == 0, for_each_tile,
-                    [&](int mt, int nt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
+      producer_role(s, g, kblocks_of, rank == 0, for_each_tile,
+                    [&](int sp, int t, int kb_rel, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      const int mt = t / n_tiles, nt = t - mt * n_tiles;
                       const int m0 = mt * kPairM + m_off, n0 = nt * kBN + n_off;
+                      const int k0 = (sp * kb_per_split + kb_rel) * kBK;
                       if (a_mn) {
                         // [K rows][M cols] in memory: two 64 x 64 boxes cover 128 rows of M
-                        tma_load_2d_pair(da, &tm_a, bar, m0, kb * kBK, pol);
-                        tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, kb * kBK, pol);
+                        tma_load_2d_pair(da, &tm_a, bar, m0, k0, pol);
+                        tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, k0, pol);
                       } else {
-                        tma_load_2d_pair(da, &tm_a, bar, kb * kBK, m0, pol);
+                        tma_load_2d_pair(da, &tm_a, bar, k0, m0, pol);
                       }
                       if (b_mn) {
                         // [K rows][N cols] in memory: two 64 x 64 boxes cover this CTA's 128 columns
-                        tma_load_2d_pair(db, &tm_b, bar, n0, kb * kBK, pol);
-                        tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, kb * kBK, pol);
+                        tma_load_2d_pair(db, &tm_b, bar, n0, k0, pol);
+                        tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, k0, pol);
                       } else {
-                        tma_load_2d_pair(db, &tm_b, bar, kb * kBK, n0, pol);
+                        tma_load_2d_pair(db, &tm_b, bar, k0, n0, pol);
                       }
                     });
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
-      mma_role(s, g, tmem, kblocks, idesc_bf16_f32(kPairM, kBN, a_mn, b_mn), for_each_tile,
-               [&](uint32_t sa, uint32_t sb, int kk, uint64_t& ad, uint64_t& bd) {
-                 ad = a_mn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
-                           : smem_desc_sw128(sa + kk * 32, 16, 1024);
-                 bd = b_mn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
-                           : smem_desc_sw128(sb + kk * 32, 16, 1024);
+      const uint32_t id = idesc_bf16_f32(kPairM, kBN, a_mn, b_mn);
+      mma_role(s, g, tmem, kblocks_of, for_each_tile,
+               [&](int, int, uint32_t sa, uint32_t sb, int kk, uint64_t& ad, uint64_t& bd,
+                   uint32_t& idesc) {
+                 ad = operand_desc(sa, a_mn, kk);
+                 bd = operand_desc(sb, b_mn, kk);
+                 idesc = id;
                });
     }
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const int mode0 = a.k_splits > 1 ? static_cast<int>(kStorePart) : a.mode;
+    const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
+    const bool to_part = mode0 == kStorePart || mode0 == kAddPart;
+    float* const part0 = a.part;
+    const long long ld_part = a.ld_part, split_stride = a.split_stride, ld_out = a.ld_out;
+    __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
-    for (int t = pair; t < a.num_tiles; t += npairs) {
-      const int mt = t / a.n_tiles, nt = t - mt * a.n_tiles;
+    for (int u = pair; u < units; u += npairs) {
+      const int sp = u / num_tiles, t = u - sp * num_tiles;
+      const int mt = t / n_tiles, nt = t - mt * n_tiles;
+      float* const part = part0 + static_cast<size_t>(sp) * split_stride;
       dead = !epi_wait_full(s, acc, acc_phase, g, dead);
       if (!dead) {
         const int m = mt * kPairM + static_cast<int>(rank) * kBM + r;
-        const bool row_ok = m < a.M;
+        const bool row_ok = m < M;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -682,16 +716,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     v);
           tmem_ld_wait(v);
           const int col0 = nt * kBN + c * 32;
-          if (!row_ok || col0 >= a.N) continue;
+          if (!row_ok || col0 >= N) continue;
           float d[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
-          if (a.mode == kAddPart || a.mode == kAddPartToOut) {
+          if (add_part) {
             const float4* src =
-                reinterpret_cast<const float4*>(a.part + static_cast<size_t>(m) * a.ld_part + col0);
+                reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * ld_part + col0);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              if (col0 + i * 4 < a.N) {
+              if (col0 + i * 4 < N) {
                 const float4 p4 = src[i];
                 d[4 * i] += p4.x;
                 d[4 * i + 1] += p4.y;
@@ -700,18 +734,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
               }
             }
           }
-          if (a.mode == kStorePart || a.mode == kAddPart) {
-            float4* dst = reinterpret_cast<float4*>(a.part + static_cast<size_t>(m) * a.ld_part + col0);
+          if (to_part) {
+            float4* dst = reinterpret_cast<float4*>(part + static_cast<size_t>(m) * ld_part + col0);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (col0 + i * 4 < a.N)
+              if (col0 + i * 4 < N)
                 dst[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
           } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                                 static_cast<size_t>(m) * a.ld_out + col0;
+            __nv_bfloat16* dst = out + static_cast<size_t>(m) * ld_out + col0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              if (col0 + i * 8 < a.N) {
+              if (col0 + i * 8 < N) {
                 uint4 w;
                 w.x = pack_bf16x2(d[8 * i + 0], d[8 * i + 1]);
                 w.y = pack_bf16x2(d[8 * i + 2], d[8 * i + 3]);

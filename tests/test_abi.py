@@ -52,7 +52,8 @@ def test_workspace_sizes(lib):
     assert fwd < 64 << 20                       # a few MB of partial states
     chunk = 4096 * 128256 * 2                   # one bf16 dlogits chunk of N/2 rows
     dw = 128256 * 4096 * 4                      # fp32 grad_weight partial
-    assert chunk + dw < bwd < chunk + dw + (64 << 20)
+    dh = 2 * 4096 * 4096 * 4                    # two fp32 K-split partials of grad_hidden
+    assert chunk + dw + dh < bwd < chunk + dw + dh + (64 << 20)
     assert bwd < 8192 * 128256 * 2 + dw         # never an N x V buffer
     small = params(N=100, H=64, V=50)
     assert _lib.workspace_bytes(small, _lib.FLCE_PASS_BACKWARD) > 0
