@@ -46,7 +46,8 @@
  *   before any work is enqueued. Errors the device detects (a target out of
  *   range, an expired bounded wait) are written to a status word at the start
  *   of the workspace. flce_check_status reads it.
- * - Outputs are overwritten, never accumulated into.
+ * - Outputs are overwritten, unless flce_params.accumulate asks the backward
+ *   to add its gradients into the buffers it is given.
  * - Results do not depend on launch timing. Every reduction runs in a fixed
  *   order, so repeated calls on the same inputs give bit-identical outputs.
  */
@@ -71,6 +72,12 @@ typedef enum {
 typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1, FLCE_NONE = 2 } flce_reduction;
 
 typedef enum { FLCE_PASS_FORWARD = 0, FLCE_PASS_BACKWARD = 1 } flce_pass;
+
+/* Accumulator of grad_weight across row chunks ("Chunked Linear Loss",
+ * section "Weight-gradient accumulation dtype"). FP32 keeps an fp32 partial
+ * and casts once (the default). WEIGHT accumulates in the weight dtype, which
+ * rounds between chunks but needs no fp32 [V,H] partial. */
+typedef enum { FLCE_ACCUM_FP32 = 0, FLCE_ACCUM_WEIGHT = 1 } flce_accum;
 
 enum {
   FLCE_OK = 0,
@@ -97,6 +104,14 @@ typedef struct {
   int32_t deterministic;     /* accepted for API parity; every reduction here is
                                 already in fixed order, so both values give the same
                                 bits                                                  */
+  int32_t accumulate;        /* 1: the backward adds into grad_hidden, grad_weight and
+                                grad_bias (beta = 1) instead of overwriting them, as
+                                quack's fused accumulation into weight.grad does       */
+  int32_t grad_weight_accum; /* flce_accum; FLCE_ACCUM_FP32 by default               */
+  int64_t vocab_start;       /* vocabulary shards: `weight` (and bias) hold global ids
+                                vocab_start .. vocab_start+V-1 of vocab_total. targets
+                                are global ids. 0 when not sharded                     */
+  int64_t vocab_total;       /* global vocabulary size; 0 means V (not sharded)       */
 } flce_params;
 
 /*
@@ -132,6 +147,8 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
  *   workspace device, >= flce_workspace_bytes(p, FLCE_PASS_FORWARD) bytes.
  *   With N == 0, hidden, targets and lse may be NULL (and loss too for NONE).
  *   SUM then gives 0 and MEAN gives NaN.
+ *   The loss needs the whole vocabulary, so vocab_total must be 0 or V (see
+ *   flce_forward_partial for shards).
  */
 int flce_forward(const flce_params* p, const void* hidden, const void* weight,
                  const void* bias, const int64_t* targets, float* loss, float* lse,
@@ -160,6 +177,53 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight,
                   const float* grad_loss, void* grad_hidden, void* grad_weight,
                   void* grad_bias, void* workspace, size_t ws_bytes,
                   flce_stream_t stream);
+
+/*
+ * Vocabulary-parallel use (a W split by rows across ranks, or across calls).
+ *
+ * The per-row online state of one shard (20 bytes). Gathered from every shard,
+ * these states give the exact loss, lse and metrics. The fused-linear-ce
+ * README ("Metrics for free") asks for results that recombine across ranks;
+ * the vocabulary-tiled forward merges exactly these states across vocabulary
+ * tiles ("Algorithm").
+ *   max_logit    largest z_ij of the row within the shard
+ *   sum_exp      sum_j exp(z_ij - max_logit) over the shard
+ *   sum_z_exp    sum_j z_ij exp(z_ij - max_logit) over the shard
+ *   argmax       global vocabulary id of the first maximum within the shard
+ *   target_logit z_{i,t_i} if t_i lies in the shard, else 0
+ */
+typedef struct {
+  float max_logit;
+  float sum_exp;
+  float sum_z_exp;
+  int32_t argmax;
+  float target_logit;
+} flce_row_state;
+
+/*
+ * The vocabulary sweep of one shard. p->V is the shard size. p->vocab_start
+ * and p->vocab_total place the shard in the global vocabulary. targets hold
+ * global ids. Writes states[N] (device, 4-byte aligned).
+ * workspace: flce_workspace_bytes(p, FLCE_PASS_FORWARD) bytes.
+ */
+int flce_forward_partial(const flce_params* p, const void* hidden, const void* weight,
+                         const void* bias, const int64_t* targets, flce_row_state* states,
+                         void* workspace, size_t ws_bytes, flce_stream_t stream);
+
+/*
+ * Merges the states of num_shards shards into flce_forward's outputs. states is
+ * [num_shards][N] (device), with the shards in increasing vocabulary order, so
+ * that argmax ties go to the lowest global id. p->vocab_total (or p->V when 0)
+ * is the global vocabulary size used to validate targets. The backward of a
+ * shard is flce_backward with the same p and the merged lse. Its grad_hidden
+ * is that shard's share, to be summed over shards (for example with
+ * accumulate = 1 into one buffer). Its grad_weight and grad_bias are the
+ * shard's rows.
+ */
+int flce_forward_combine(const flce_params* p, const flce_row_state* states, int32_t num_shards,
+                         const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
+                         float* entropy_sum, void* workspace, size_t ws_bytes,
+                         flce_stream_t stream);
 
 /*
  * flce_forward without a workspace argument, for callers that cannot

@@ -16,6 +16,8 @@ LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
 FLCE_F32, FLCE_BF16 = 0, 1
 FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
 FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD = 0, 1
+FLCE_ACCUM_FP32, FLCE_ACCUM_WEIGHT = 0, 1
+ACCUM_DTYPES = {"fp32": FLCE_ACCUM_FP32, "weight": FLCE_ACCUM_WEIGHT}
 REDUCTIONS = {"sum": FLCE_SUM, "mean": FLCE_MEAN, "none": FLCE_NONE}
 
 ERRORS = {
@@ -28,6 +30,7 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_forward", "flce_backward", "flce_check_status",
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
+    "flce_forward_partial", "flce_forward_combine",
 )
 
 
@@ -44,7 +47,21 @@ class FlceParams(ctypes.Structure):
         ("z_loss_multiplier", ctypes.c_float),
         ("has_bias", ctypes.c_int32),
         ("deterministic", ctypes.c_int32),
+        ("accumulate", ctypes.c_int32),
+        ("grad_weight_accum", ctypes.c_int32),
+        ("vocab_start", ctypes.c_int64),
+        ("vocab_total", ctypes.c_int64),
     ]
+
+
+class FlceRowState(ctypes.Structure):
+    """One vocabulary shard's state of one row (include/flce.h, flce_row_state)."""
+    _fields_ = [("max_logit", ctypes.c_float), ("sum_exp", ctypes.c_float),
+                ("sum_z_exp", ctypes.c_float), ("argmax", ctypes.c_int32),
+                ("target_logit", ctypes.c_float)]
+
+
+ROW_STATE_BYTES = ctypes.sizeof(FlceRowState)
 
 
 class FlceKernelTime(ctypes.Structure):
@@ -84,6 +101,10 @@ def load() -> ctypes.CDLL:
     lib.flce_backward.restype = ctypes.c_int
     lib.flce_forward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.flce_forward_noalloc.restype = ctypes.c_int
+    lib.flce_forward_partial.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_partial.restype = ctypes.c_int
+    lib.flce_forward_combine.argtypes = [P, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_combine.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
     lib.flce_error_string.argtypes = [ctypes.c_int]
@@ -117,14 +138,21 @@ def check(code: int, where: str) -> None:
 def make_params(N: int, H: int, V: int, dtype: int, reduction: str = "mean",
                 ignore_index: int = -100, logit_scale: float = 1.0,
                 softcap: Optional[float] = None, z_loss_multiplier: float = 0.0,
-                has_bias: bool = False, deterministic: bool = False) -> FlceParams:
+                has_bias: bool = False, deterministic: bool = False, accumulate: bool = False,
+                grad_weight_accum: str = "fp32", vocab_start: int = 0,
+                vocab_total: int = 0) -> FlceParams:
     if reduction not in REDUCTIONS:
         raise ValueError(f"reduction must be one of {tuple(REDUCTIONS)}, got {reduction!r}")
+    if grad_weight_accum not in ACCUM_DTYPES:
+        raise ValueError(f"grad_weight_accum must be one of {tuple(ACCUM_DTYPES)}")
     return FlceParams(N=N, H=H, V=V, dtype=dtype, reduction=REDUCTIONS[reduction],
                       ignore_index=ignore_index, logit_scale=logit_scale,
                       softcap=softcap if softcap else 0.0,
                       z_loss_multiplier=z_loss_multiplier, has_bias=1 if has_bias else 0,
-                      deterministic=1 if deterministic else 0)
+                      deterministic=1 if deterministic else 0,
+                      accumulate=1 if accumulate else 0,
+                      grad_weight_accum=ACCUM_DTYPES[grad_weight_accum],
+                      vocab_start=vocab_start, vocab_total=vocab_total)
 
 
 def workspace_bytes(p: FlceParams, pass_: int) -> int:
@@ -147,6 +175,19 @@ def forward_noalloc_raw(p: FlceParams, hidden: int, weight: int, bias: int, targ
     """flce_forward_noalloc: the forward with the library's fixed 48 MiB scratch array."""
     return load().flce_forward_noalloc(ctypes.byref(p), hidden, weight, bias, targets, loss, lse,
                                        num_correct, entropy_sum, stream)
+
+
+def forward_partial_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int,
+                        states: int, ws: int, ws_bytes: int, stream: int) -> int:
+    return load().flce_forward_partial(ctypes.byref(p), hidden, weight, bias, targets, states, ws,
+                                       ws_bytes, stream)
+
+
+def forward_combine_raw(p: FlceParams, states: int, num_shards: int, targets: int, loss: int,
+                        lse: int, num_correct: int, entropy_sum: int, ws: int, ws_bytes: int,
+                        stream: int) -> int:
+    return load().flce_forward_combine(ctypes.byref(p), states, num_shards, targets, loss, lse,
+                                       num_correct, entropy_sum, ws, ws_bytes, stream)
 
 
 def backward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int, lse: int,

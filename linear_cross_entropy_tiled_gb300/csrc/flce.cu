@@ -144,6 +144,14 @@ int validate(const flce_params* p) {
   if (!isfinite(p->softcap)) return FLCE_ERR_INVALID_ARG;
   if (!isfinite(p->z_loss_multiplier) || p->z_loss_multiplier < 0.f) return FLCE_ERR_INVALID_ARG;
   if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
+  if (p->accumulate != 0 && p->accumulate != 1) return FLCE_ERR_INVALID_ARG;
+  if (p->grad_weight_accum != FLCE_ACCUM_FP32 && p->grad_weight_accum != FLCE_ACCUM_WEIGHT)
+    return FLCE_ERR_INVALID_ARG;
+  if (p->vocab_total == 0) {
+    if (p->vocab_start != 0) return FLCE_ERR_INVALID_ARG;
+  } else if (p->vocab_start < 0 || p->vocab_total > lim || p->vocab_start + p->V > p->vocab_total) {
+    return FLCE_ERR_INVALID_ARG;
+  }
   if (p->dtype == FLCE_BF16 && (p->H % 8) != 0) return FLCE_ERR_ALIGNMENT;
   return FLCE_OK;
 }
@@ -227,7 +235,8 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.ds = o;
   o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
   L.dw = o;
-  if (p->dtype == FLCE_BF16 && L.nchunks > 1) o = align_up(o + size_t(V) * H * 4, 1024);
+  if (p->dtype == FLCE_BF16 && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
+    o = align_up(o + size_t(V) * H * 4, 1024);
   L.dh_part = o;
   if (p->dtype == FLCE_BF16) o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
   L.bias_part = o;
@@ -342,36 +351,37 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes) {
   return FLCE_OK;
 }
 
-int flce_forward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
-                 const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
-                 float* entropy_sum, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+// Checks and set-up shared by the forward entry points. `rows_out` is the
+// per-row output that must be non-NULL when N > 0 (lse or the shard states).
+static int forward_prologue(const flce_params* p, const void* hidden, const void* weight,
+                            const void* bias, const int64_t* targets, const void* rows_out,
+                            void* workspace, size_t ws_bytes, FwdLayout* L, DeviceInfo* d) {
   int v = validate(p);
   if (v != FLCE_OK) return v;
   // Row-indexed pointers may be NULL only when there are no rows.
   const bool rows = p->N > 0;
-  if (weight == nullptr || (rows && (hidden == nullptr || targets == nullptr || lse == nullptr)) ||
-      (loss == nullptr && (rows || p->reduction != FLCE_NONE)))
+  if (weight == nullptr || (rows && (hidden == nullptr || targets == nullptr || rows_out == nullptr)))
     return FLCE_ERR_INVALID_ARG;
   if ((p->has_bias != 0) != (bias != nullptr)) return FLCE_ERR_INVALID_ARG;
   if (workspace == nullptr) return FLCE_ERR_WORKSPACE;
   if (!aligned16(hidden) || !aligned16(weight) || (bias && !aligned16(bias)) ||
       !aligned16(workspace) || !aligned16(targets))
     return FLCE_ERR_ALIGNMENT;
-  const FwdLayout L = fwd_layout(p);
-  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
-  DeviceInfo d;
-  if ((v = device_info(&d)) != FLCE_OK) return v;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* status = reinterpret_cast<int*>(ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  *L = fwd_layout(p);
+  if (ws_bytes < L->total) return FLCE_ERR_WORKSPACE;
+  return FLCE_OK;
+}
 
+// The vocabulary sweep: per-panel online states and the target logits.
+static int forward_tiles(const flce_params* p, const void* hidden, const void* weight,
+                         const void* bias, const int64_t* targets, uint8_t* ws, const FwdLayout& L,
+                         const DeviceInfo& d, cudaStream_t st, FwdArgs* out) {
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   FwdArgs fa{};
   fa.N = N;
   fa.H = H;
   fa.V = V;
+  fa.vocab_start = p->vocab_start;
   fa.scale = p->logit_scale;
   fa.softcap = p->softcap > 0.f ? p->softcap : 0.f;
   fa.inv_softcap = inv_cap(p);
@@ -380,35 +390,79 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
   fa.ignore_index = p->ignore_index;
   fa.partials = reinterpret_cast<float4*>(ws + L.partials);
   fa.zt = reinterpret_cast<float*>(ws + L.zt);
-  fa.status = status;
+  fa.status = reinterpret_cast<int*>(ws);
+  int v;
+  if (p->dtype == FLCE_BF16) {
+    fa.n_blocks = static_cast<int>(ceil_div(N, kPairM));
+    fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
+    int grid = 1;
+    fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.pairs, &grid);
+    fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
+    fa.num_units = fa.num_panels * fa.n_blocks;
+    CUtensorMap tm_h, tm_w;
+    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
+    v = launch("flce_fwd_tc", st, [&] {
+      return launch_fwd_tc(tm_h, tm_w, fa, bias != nullptr, p->softcap > 0.f, grid, st);
+    });
+  } else {
+    fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
+    fa.num_panels = static_cast<int>(ceil_div(V, kSimtPanelCols));
+    fa.num_units = fa.num_panels * fa.n_blocks;
+    v = launch("flce_fwd_simt", st, [&] {
+      return launch_fwd_simt(static_cast<const float*>(hidden), static_cast<const float*>(weight),
+                             fa, st);
+    });
+  }
+  *out = fa;
+  return v;
+}
 
+static int forward_finalize(const flce_params* p, uint8_t* ws, const FwdLayout& L, int nblk,
+                            float* loss, int64_t* num_correct, float* entropy_sum,
+                            cudaStream_t st) {
+  FinalizeArgs fz{};
+  fz.nblk = nblk;
+  fz.reduction = p->reduction;
+  fz.blk_loss = reinterpret_cast<const double*>(ws + L.blk_loss);
+  fz.blk_ent = reinterpret_cast<const double*>(ws + L.blk_ent);
+  fz.blk_correct = reinterpret_cast<const long long*>(ws + L.blk_correct);
+  fz.blk_valid = reinterpret_cast<const long long*>(ws + L.blk_valid);
+  fz.loss = p->reduction == FLCE_NONE ? nullptr : loss;
+  fz.num_correct = num_correct;
+  fz.entropy_sum = entropy_sum;
+  return launch("flce_finalize", st, [&] { return launch_finalize(fz, st); });
+}
+
+int flce_forward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
+                 const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
+                 float* entropy_sum, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  FwdLayout L;
+  DeviceInfo d;
+  int v = forward_prologue(p, hidden, weight, bias, targets, lse, workspace, ws_bytes, &L, &d);
+  if (v != FLCE_OK) return v;
+  if (loss == nullptr && (p->N > 0 || p->reduction != FLCE_NONE)) return FLCE_ERR_INVALID_ARG;
+  // The loss needs the whole vocabulary. Shards go through flce_forward_partial
+  // and flce_forward_combine.
+  if (p->vocab_total != 0 && (p->vocab_total != p->V || p->vocab_start != 0)) {
+    snprintf(g_detail, sizeof(g_detail),
+             "flce_forward needs the whole vocabulary; use flce_forward_partial + combine");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  const int N = static_cast<int>(p->N);
   if (N > 0) {
-    if (p->dtype == FLCE_BF16) {
-      fa.n_blocks = static_cast<int>(ceil_div(N, kPairM));
-      fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
-      int grid = 1;
-      fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.pairs, &grid);
-      fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
-      fa.num_units = fa.num_panels * fa.n_blocks;
-      CUtensorMap tm_h, tm_w;
-      if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
-      if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
-      v = launch("flce_fwd_tc", st, [&] {
-        return launch_fwd_tc(tm_h, tm_w, fa, bias != nullptr, p->softcap > 0.f, grid, st);
-      });
-    } else {
-      fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
-      fa.num_panels = static_cast<int>(ceil_div(V, kSimtPanelCols));
-      fa.num_units = fa.num_panels * fa.n_blocks;
-      v = launch("flce_fwd_simt", st, [&] {
-        return launch_fwd_simt(static_cast<const float*>(hidden),
-                               static_cast<const float*>(weight), fa, st);
-      });
-    }
-    if (v != FLCE_OK) return v;
+    FwdArgs fa;
+    if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, st, &fa)) != FLCE_OK) return v;
     MergeArgs ma{};
     ma.N = N;
-    ma.V = V;
+    ma.V = static_cast<int>(p->V);
+    ma.vocab_start = 0;
+    ma.vocab_total = p->V;
     ma.num_panels = fa.num_panels;
     ma.reduction = p->reduction;
     ma.ignore_index = p->ignore_index;
@@ -422,21 +476,85 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
     ma.blk_ent = reinterpret_cast<double*>(ws + L.blk_ent);
     ma.blk_correct = reinterpret_cast<long long*>(ws + L.blk_correct);
     ma.blk_valid = reinterpret_cast<long long*>(ws + L.blk_valid);
-    ma.status = status;
+    ma.status = reinterpret_cast<int*>(ws);
     v = launch("flce_merge", st, [&] { return launch_merge(ma, L.nblk, st); });
     if (v != FLCE_OK) return v;
   }
-  FinalizeArgs fz{};
-  fz.nblk = N > 0 ? L.nblk : 0;
-  fz.reduction = p->reduction;
-  fz.blk_loss = reinterpret_cast<const double*>(ws + L.blk_loss);
-  fz.blk_ent = reinterpret_cast<const double*>(ws + L.blk_ent);
-  fz.blk_correct = reinterpret_cast<const long long*>(ws + L.blk_correct);
-  fz.blk_valid = reinterpret_cast<const long long*>(ws + L.blk_valid);
-  fz.loss = p->reduction == FLCE_NONE ? nullptr : loss;
-  fz.num_correct = num_correct;
-  fz.entropy_sum = entropy_sum;
-  return launch("flce_finalize", st, [&] { return launch_finalize(fz, st); });
+  return forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct, entropy_sum, st);
+}
+
+int flce_forward_partial(const flce_params* p, const void* hidden, const void* weight,
+                         const void* bias, const int64_t* targets, flce_row_state* states,
+                         void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  static_assert(sizeof(flce_row_state) == sizeof(ShardState), "row state layout");
+  FwdLayout L;
+  DeviceInfo d;
+  int v = forward_prologue(p, hidden, weight, bias, targets, states, workspace, ws_bytes, &L, &d);
+  if (v != FLCE_OK) return v;
+  if (reinterpret_cast<uintptr_t>(states) & 3u) return FLCE_ERR_ALIGNMENT;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  if (p->N == 0) return FLCE_OK;
+  FwdArgs fa;
+  if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, st, &fa)) != FLCE_OK) return v;
+  ShardStateArgs sa{};
+  sa.N = static_cast<int>(p->N);
+  sa.V = static_cast<int>(p->V);
+  sa.num_panels = fa.num_panels;
+  sa.vocab_start = p->vocab_start;
+  sa.ignore_index = p->ignore_index;
+  sa.partials = fa.partials;
+  sa.zt = fa.zt;
+  sa.targets = targets;
+  sa.out = reinterpret_cast<ShardState*>(states);
+  return launch("flce_shard_state", st, [&] { return launch_shard_state(sa, st); });
+}
+
+int flce_forward_combine(const flce_params* p, const flce_row_state* states, int32_t num_shards,
+                         const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
+                         float* entropy_sum, void* workspace, size_t ws_bytes,
+                         flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  const bool rows = p->N > 0;
+  if (num_shards < 1 || (rows && (states == nullptr || targets == nullptr || lse == nullptr)) ||
+      (loss == nullptr && (rows || p->reduction != FLCE_NONE)))
+    return FLCE_ERR_INVALID_ARG;
+  if (workspace == nullptr) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(targets)) return FLCE_ERR_ALIGNMENT;
+  const FwdLayout L = fwd_layout(p);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  const int N = static_cast<int>(p->N);
+  if (N > 0) {
+    CombineArgs ca{};
+    ca.N = N;
+    ca.R = num_shards;
+    ca.reduction = p->reduction;
+    ca.vocab_total = p->vocab_total ? p->vocab_total : p->V;
+    ca.ignore_index = p->ignore_index;
+    ca.zeta = p->z_loss_multiplier;
+    ca.states = reinterpret_cast<const ShardState*>(states);
+    ca.targets = targets;
+    ca.lse = lse;
+    ca.loss_rows = p->reduction == FLCE_NONE ? loss : nullptr;
+    ca.blk_loss = reinterpret_cast<double*>(ws + L.blk_loss);
+    ca.blk_ent = reinterpret_cast<double*>(ws + L.blk_ent);
+    ca.blk_correct = reinterpret_cast<long long*>(ws + L.blk_correct);
+    ca.blk_valid = reinterpret_cast<long long*>(ws + L.blk_valid);
+    ca.status = reinterpret_cast<int*>(ws);
+    v = launch("flce_combine", st, [&] { return launch_combine(ca, L.nblk, st); });
+    if (v != FLCE_OK) return v;
+  }
+  return forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct, entropy_sum, st);
 }
 
 int flce_backward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
@@ -470,6 +588,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
 
   if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return FLCE_OK;
   if (N == 0) {
+    if (p->accumulate) return FLCE_OK;  // nothing to add
     if (grad_weight && (e = cudaMemsetAsync(grad_weight, 0, size_t(V) * H * elem, st)) != cudaSuccess)
       return cuda_fail(e, "cudaMemsetAsync");
     if (grad_bias && (e = cudaMemsetAsync(grad_bias, 0, size_t(V) * elem, st)) != cudaSuccess)
@@ -482,6 +601,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   ra.N = N;
   ra.V = V;
   ra.reduction = p->reduction;
+  ra.vocab_start = p->vocab_start;
+  ra.vocab_total = p->vocab_total ? p->vocab_total : p->V;
   ra.ignore_index = p->ignore_index;
   ra.scale = p->logit_scale;
   ra.zeta = p->z_loss_multiplier;
@@ -546,7 +667,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.kb_per_split = static_cast<int>(ceil_div(ga.k_blocks, ga.k_splits));
         ga.a_mn = 0;
         ga.b_mn = 1;
-        ga.mode = kStoreOut;
+        ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
         ga.out = static_cast<uint8_t*>(grad_hidden) + size_t(row0) * H * 2;
         ga.ld_out = H;
         ga.part = reinterpret_cast<float*>(ws + L.dh_part);
@@ -562,6 +683,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
           ra2.M = rows;
           ra2.N = H;
           ra2.splits = ga.k_splits;
+          ra2.accumulate = p->accumulate;
           ra2.part = ga.part;
           ra2.ld_part = H;
           ra2.split_stride = ga.split_stride;
@@ -589,10 +711,14 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.kb_per_split = ga.k_blocks;
         ga.a_mn = 1;
         ga.b_mn = 1;
-        if (L.nchunks == 1)
-          ga.mode = kStoreOut;
+        // grad_weight across row chunks. fp32: the first chunk starts the fp32
+        // partial (from the existing gradient when accumulating), the middle
+        // chunks add to it, and the last adds and casts. Weight dtype: every
+        // chunk after the first reads, adds and rewrites the output.
+        if (p->grad_weight_accum == FLCE_ACCUM_WEIGHT || L.nchunks == 1)
+          ga.mode = (c > 0 || p->accumulate) ? kAddOutToOut : kStoreOut;
         else if (c == 0)
-          ga.mode = kStorePart;
+          ga.mode = p->accumulate ? kAddOutToPart : kStorePart;
         else if (c == L.nchunks - 1)
           ga.mode = kAddPartToOut;
         else
@@ -632,7 +758,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.sbn = 1;
         ga.C = static_cast<float*>(grad_hidden) + size_t(row0) * H;
         ga.ldc = H;
-        ga.accumulate = 0;
+        ga.accumulate = p->accumulate;
         v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
@@ -649,7 +775,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.sbn = 1;
         ga.C = static_cast<float*>(grad_weight);
         ga.ldc = H;
-        ga.accumulate = c > 0 ? 1 : 0;
+        ga.accumulate = (c > 0 || p->accumulate) ? 1 : 0;
         v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
@@ -662,6 +788,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     ba.nblk = L.n_rowblocks;
     ba.bias_part = bias_part;
     ba.grad_bias = grad_bias;
+    ba.accumulate = p->accumulate;
     v = launch("flce_bias_reduce", st, [&] { return launch_bias_reduce(ba, p->dtype, st); });
     if (v != FLCE_OK) return v;
   }

@@ -42,6 +42,7 @@ constexpr int kSimtThreads = 256;
 
 struct FwdArgs {
   int N, H, V;
+  long long vocab_start;       // global id of this call's first vocabulary row
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
   float scale, softcap, inv_softcap;
   const void* bias;            // dtype of the pass, or nullptr
@@ -54,6 +55,7 @@ struct FwdArgs {
 
 struct MergeArgs {
   int N, V, num_panels, reduction;
+  long long vocab_start, vocab_total;   // shard placement; vocab_total = V when not sharded
   long long ignore_index;
   float zeta;
   const float4* partials;
@@ -62,6 +64,42 @@ struct MergeArgs {
   float* lse;                  // [N]
   float* loss_rows;            // [N] when reduction == none, else nullptr
   double* blk_loss;            // [gridDim]
+  double* blk_ent;
+  long long* blk_correct;
+  long long* blk_valid;
+  int* status;
+};
+
+// Exported per-row state of one vocabulary shard (20 bytes): running max,
+// sum of exp(z - max), sum of z exp(z - max), global argmax, and the target
+// logit if this shard holds the target (0 otherwise).
+struct ShardState {
+  float m, s, t;
+  int argmax;
+  float zt;
+};
+
+struct ShardStateArgs {
+  int N, V, num_panels;
+  long long vocab_start;
+  long long ignore_index;
+  const float4* partials;
+  const float* zt;
+  const int64_t* targets;
+  ShardState* out;             // [N]
+};
+
+// Merge of R shards' states into the same outputs merge_kernel produces.
+struct CombineArgs {
+  int N, R, reduction;
+  long long vocab_total;
+  long long ignore_index;
+  float zeta;
+  const ShardState* states;    // [R][N]
+  const int64_t* targets;
+  float* lse;
+  float* loss_rows;
+  double* blk_loss;
   double* blk_ent;
   long long* blk_correct;
   long long* blk_valid;
@@ -83,6 +121,7 @@ struct FinalizeArgs {
 // z = lse, w = target (int bits; -1 if ignored or out of the row range).
 struct RowCoefArgs {
   int N, V, reduction;
+  long long vocab_start, vocab_total;   // shard placement; vocab_total = V when not sharded
   long long ignore_index;
   float scale, zeta;
   const int64_t* targets;
@@ -108,7 +147,9 @@ enum GemmMode : int {
   kStoreOut = 0,      // out  = acc (output dtype)
   kStorePart = 1,     // part = acc (fp32)
   kAddPart = 2,       // part = part + acc
-  kAddPartToOut = 3   // out  = part + acc
+  kAddPartToOut = 3,  // out  = part + acc
+  kAddOutToOut = 4,   // out  = out + acc (read-modify-write in the output dtype)
+  kAddOutToPart = 5   // part = out + acc
 };
 
 // One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With
@@ -134,6 +175,7 @@ struct GemmArgs {
 // out[m, n] (bf16) = sum over s of part[s][m, n], in split order.
 struct SplitReduceArgs {
   int M, N, splits;
+  int accumulate;              // 1: out += sum (read-modify-write)
   const float* part;
   long long ld_part, split_stride;
   void* out;
@@ -153,6 +195,7 @@ struct SimtGemmArgs {
 
 struct BiasReduceArgs {
   int V, V_pad, nblk;
+  int accumulate;              // 1: grad_bias += sum
   const float* bias_part;      // [nblk][V_pad]
   void* grad_bias;             // dtype of the pass
 };
@@ -173,6 +216,8 @@ cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s);
 
 // dtype-generic small kernels (dtype: 0 = f32, 1 = bf16)
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);
+cudaError_t launch_shard_state(const ShardStateArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);

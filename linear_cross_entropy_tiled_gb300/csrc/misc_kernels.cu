@@ -5,7 +5,9 @@
 //   row_coef    per-row backward coefficients (gamma with the reduction and
 //               the z-loss folded in);
 //   bias_reduce fixed-order sum of per-row-block grad_bias partials;
-//   split_reduce fixed-order sum of the K-split partials of grad_hidden.
+//   split_reduce fixed-order sum of the K-split partials of grad_hidden;
+//   shard_state / combine  export of one vocabulary shard's per-row state and
+//               the merge of several shards' states (vocabulary-parallel use).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -67,11 +69,105 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     float li = 0.f;
     if (t != a.ignore_index) {
       valid = 1;
-      if (t < 0 || t >= a.V) {
+      if (t < 0 || t >= a.vocab_total) {
         atomicOr(a.status, kDevErrTargetRange);
         li = NAN;
       } else {
         li = lse - a.zt[i] + a.zeta * lse * lse;
+        ent_i = static_cast<double>(lse - Tt / S);
+        corr = (static_cast<long long>(A) + a.vocab_start == t) ? 1 : 0;
+      }
+    }
+    loss_i = li;
+    if (a.loss_rows != nullptr) a.loss_rows[i] = li;
+  }
+  const double bl = block_sum(loss_i, sh_d);
+  const double be = block_sum(ent_i, sh_d);
+  const long long bc = block_sum(corr, sh_i);
+  const long long bv = block_sum(valid, sh_i);
+  if (threadIdx.x == 0) {
+    a.blk_loss[blockIdx.x] = bl;
+    a.blk_ent[blockIdx.x] = be;
+    a.blk_correct[blockIdx.x] = bc;
+    a.blk_valid[blockIdx.x] = bv;
+  }
+}
+
+// Per-row state of one vocabulary shard: the panels of this call merged in
+// panel order (as in merge_kernel), with the argmax made a global id. The
+// target logit is kept only if the target lies in this shard.
+__global__ void __launch_bounds__(256) shard_state_kernel(const ShardStateArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.N) return;
+  float M = -INFINITY, S = 0.f, Tt = 0.f;
+  int A = 0;
+  for (int p = 0; p < a.num_panels; ++p) {
+    const float4 st = a.partials[static_cast<size_t>(p) * a.N + i];
+    if (st.x > M) {
+      const float f = expf(M - st.x);
+      S = fmaf(S, f, st.y);
+      Tt = fmaf(Tt, f, st.z);
+      M = st.x;
+      A = __float_as_int(st.w);
+    } else {
+      const float f = expf(st.x - M);
+      S = fmaf(st.y, f, S);
+      Tt = fmaf(st.z, f, Tt);
+    }
+  }
+  const long long t = a.targets[i];
+  const long long local = t - a.vocab_start;
+  const bool owned = t != a.ignore_index && local >= 0 && local < a.V;
+  ShardState o;
+  o.m = M;
+  o.s = S;
+  o.t = Tt;
+  o.argmax = static_cast<int>(A + a.vocab_start);
+  o.zt = owned ? a.zt[i] : 0.f;
+  a.out[i] = o;
+}
+
+// Merge of the states of R vocabulary shards, in shard order, into lse,
+// loss_i, entropy_i and correct_i per row, plus per-block sums for
+// finalize_kernel. The shards must be given in increasing vocabulary order:
+// a later shard takes the argmax only with a strictly larger max, so ties keep
+// the lowest global id. The target logit is the sum over shards; only the owning
+// shard contributes a nonzero value.
+__global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArgs a) {
+  __shared__ double sh_d[32];
+  __shared__ long long sh_i[32];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  double loss_i = 0.0, ent_i = 0.0;
+  long long corr = 0, valid = 0;
+  if (i < a.N) {
+    float M = -INFINITY, S = 0.f, Tt = 0.f, zt = 0.f;
+    int A = 0;
+    for (int r = 0; r < a.R; ++r) {
+      const ShardState st = a.states[static_cast<size_t>(r) * a.N + i];
+      zt += st.zt;
+      if (st.m > M) {
+        const float f = expf(M - st.m);
+        S = fmaf(S, f, st.s);
+        Tt = fmaf(Tt, f, st.t);
+        M = st.m;
+        A = st.argmax;
+      } else {
+        const float f = expf(st.m - M);
+        S = fmaf(st.s, f, S);
+        Tt = fmaf(st.t, f, Tt);
+      }
+    }
+    const float lse = M + logf(S);
+    a.lse[i] = lse;
+    const long long t = a.targets[i];
+    float li = 0.f;
+    if (t != a.ignore_index) {
+      valid = 1;
+      if (t < 0 || t >= a.vocab_total) {
+        atomicOr(a.status, kDevErrTargetRange);
+        li = NAN;
+      } else {
+        li = lse - zt + a.zeta * lse * lse;
         ent_i = static_cast<double>(lse - Tt / S);
         corr = (static_cast<long long>(A) == t) ? 1 : 0;
       }
@@ -138,14 +234,16 @@ __global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
     const float lse = a.lse[i];
     float4 c = make_float4(0.f, 0.f, lse, __int_as_float(-1));
     if (t != a.ignore_index) {
-      if (t < 0 || t >= a.V) {
+      if (t < 0 || t >= a.vocab_total) {
         atomicOr(a.status, kDevErrTargetRange);
       } else {
         const float gam = (a.reduction == 2) ? a.grad_loss[i] : g_all;
         const float sg = a.scale * gam;
         c.x = sg * fmaf(2.f * a.zeta, lse, 1.f);
         c.y = sg;
-        c.w = __int_as_float(static_cast<int>(t));
+        // the onehot term belongs to the shard that holds the target
+        const long long local = t - a.vocab_start;
+        if (local >= 0 && local < a.V) c.w = __int_as_float(static_cast<int>(local));
       }
     }
     a.coef[i] = c;
@@ -159,9 +257,12 @@ __global__ void __launch_bounds__(256) bias_reduce_kernel(const BiasReduceArgs a
   float s = 0.f;
   for (int b = 0; b < a.nblk; ++b) s += a.bias_part[static_cast<size_t>(b) * a.V_pad + j];
   if constexpr (sizeof(Tout) == 2) {
-    static_cast<__nv_bfloat16*>(a.grad_bias)[j] = __float2bfloat16_rn(s);
+    __nv_bfloat16* gb = static_cast<__nv_bfloat16*>(a.grad_bias);
+    if (a.accumulate) s += __bfloat162float(gb[j]);
+    gb[j] = __float2bfloat16_rn(s);
   } else {
-    static_cast<float*>(a.grad_bias)[j] = s;
+    float* gb = static_cast<float*>(a.grad_bias);
+    gb[j] = a.accumulate ? gb[j] + s : s;
   }
 }
 
@@ -181,12 +282,20 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const SplitReduceArgs
     acc.z += p.z;
     acc.w += p.w;
   }
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + m * a.ld_out + n);
+  if (a.accumulate) {
+    const uint2 o = *dst;
+    acc.x += __uint_as_float(o.x << 16);
+    acc.y += __uint_as_float(o.x & 0xffff0000u);
+    acc.z += __uint_as_float(o.y << 16);
+    acc.w += __uint_as_float(o.y & 0xffff0000u);
+  }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 w;
   w.x = *reinterpret_cast<uint32_t*>(&lo);
   w.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + m * a.ld_out + n) = w;
+  *dst = w;
 }
 
 }  // namespace
@@ -199,6 +308,16 @@ cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s) {
 
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s) {
   merge_kernel<<<nblk, kMergeThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_state(const ShardStateArgs& a, cudaStream_t s) {
+  shard_state_kernel<<<(a.N + 255) / 256, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s) {
+  combine_kernel<<<nblk, kMergeThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kSimtThreads)
   float m = -INFINITY, ssum = 0.f, tsum = 0.f;
   int amax = 0;
   const int row = r0 + tid;
-  const long long tgt = (tid < T && row < a.N) ? a.targets[row] : a.ignore_index;
+  long long tgt = (tid < T && row < a.N) ? a.targets[row] : a.ignore_index;
+  tgt = (tgt == a.ignore_index) ? -(1ll << 40) : tgt - a.vocab_start;  // shard-local id
   const int c_begin = panel * kSimtPanelCols;
   const int c_end = min(a.V, c_begin + kSimtPanelCols);
   for (int c0 = c_begin; c0 < c_end; c0 += T) {

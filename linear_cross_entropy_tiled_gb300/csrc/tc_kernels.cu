@@ -418,7 +418,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
       const int row = nb * kPairM + static_cast<int>(rank) * kBM + r;
       const bool row_ok = row < a.N;
-      const long long tgt = row_ok ? a.targets[row] : a.ignore_index;
+      // shard-local target id; an ignored row gets one that never matches a column
+      long long tgt = row_ok ? a.targets[row] : a.ignore_index;
+      tgt = (tgt == a.ignore_index) ? -(1ll << 40) : tgt - a.vocab_start;
       float m = -INFINITY, ssum = 0.f, tsum = 0.f;
       int amax = 0;
       const int vt0 = panel * a.panel_tiles;
@@ -693,7 +695,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const int r = q * 32 + lane;
     const int mode0 = a.k_splits > 1 ? static_cast<int>(kStorePart) : a.mode;
     const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
-    const bool to_part = mode0 == kStorePart || mode0 == kAddPart;
+    const bool add_out = mode0 == kAddOutToOut || mode0 == kAddOutToPart;
+    const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
     float* const part0 = a.part;
     const long long ld_part = a.ld_part, split_stride = a.split_stride, ld_out = a.ld_out;
     __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
@@ -731,6 +734,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                 d[4 * i + 1] += p4.y;
                 d[4 * i + 2] += p4.z;
                 d[4 * i + 3] += p4.w;
+              }
+            }
+          }
+          if (add_out) {
+            const uint4* src = reinterpret_cast<const uint4*>(out + static_cast<size_t>(m) * ld_out + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (col0 + i * 8 < N) {
+                const uint4 w = src[i];
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+                  d[8 * i + 2 * h] += __uint_as_float(ws[h] << 16);
+                  d[8 * i + 2 * h + 1] += __uint_as_float(ws[h] & 0xffff0000u);
+                }
               }
             }
           }

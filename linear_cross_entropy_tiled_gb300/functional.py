@@ -88,16 +88,66 @@ def flce_forward(p: _lib.FlceParams, hidden: torch.Tensor, weight: torch.Tensor,
     return loss, lse, nc, ent, workspace
 
 
+def flce_forward_partial(p: _lib.FlceParams, hidden: torch.Tensor, weight_shard: torch.Tensor,
+                         targets: torch.Tensor, bias_shard: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The vocabulary sweep of one shard. Returns its per-row states as a [N, 5] int32 tensor.
+
+    Its 20-byte rows are ``flce_row_state``. Gather the states of every shard
+    (for example with an all-gather) and pass them to ``flce_forward_combine``.
+    """
+    dev = hidden.device
+    states = torch.empty((p.N, 5), dtype=torch.int32, device=dev)
+    need = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = _lib.forward_partial_raw(p, _ptr(hidden), _ptr(weight_shard), _ptr(bias_shard),
+                                  _ptr(targets), _ptr(states), _ptr(workspace), workspace.numel(),
+                                  _stream(dev))
+    _lib.check(rc, "flce_forward_partial")
+    _maybe_check(workspace, "flce_forward_partial")
+    return states
+
+
+def flce_forward_combine(p: _lib.FlceParams, states: torch.Tensor, targets: torch.Tensor,
+                         return_metrics: bool = False,
+                         workspace: Optional[torch.Tensor] = None):
+    """Merges [R, N, 5] shard states (in vocabulary order). Returns (loss, lse, num_correct, entropy_sum)."""
+    dev = targets.device
+    R = states.shape[0]
+    states = states.contiguous()
+    nloss = p.N if p.reduction == _lib.FLCE_NONE else 1
+    loss = torch.empty(nloss, dtype=torch.float32, device=dev)
+    lse = torch.empty(p.N, dtype=torch.float32, device=dev)
+    nc = torch.empty(1, dtype=torch.int64, device=dev) if return_metrics else None
+    ent = torch.empty(1, dtype=torch.float32, device=dev) if return_metrics else None
+    need = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = _lib.forward_combine_raw(p, _ptr(states), R, _ptr(targets), _ptr(loss), _ptr(lse),
+                                  _ptr(nc), _ptr(ent), _ptr(workspace), workspace.numel(),
+                                  _stream(dev))
+    _lib.check(rc, "flce_forward_combine")
+    _maybe_check(workspace, "flce_forward_combine")
+    return loss, lse, nc, ent
+
+
 def flce_backward(p: _lib.FlceParams, hidden: torch.Tensor, weight: torch.Tensor,
                   targets: torch.Tensor, lse: torch.Tensor, grad_loss: torch.Tensor,
                   bias: Optional[torch.Tensor] = None, need_hidden: bool = True,
                   need_weight: bool = True, need_bias: bool = True,
-                  workspace: Optional[torch.Tensor] = None, out=None):
+                  workspace: Optional[torch.Tensor] = None, out=None, accumulate: bool = False):
     """One call of the C ABI backward. Returns (grad_hidden, grad_weight, grad_bias, workspace).
 
     ``out`` may pass preallocated (grad_hidden, grad_weight, grad_bias) tensors.
+    With ``accumulate`` the gradients are added into ``out`` (beta = 1).
     """
     dev = hidden.device
+    if accumulate:
+        if out is None:
+            raise ValueError("accumulate=True needs the out=(...) tensors to add into")
+        p = _lib.FlceParams.from_buffer_copy(p)
+        p.accumulate = 1
     if out is not None:
         gh, gw, gb = out
     else:
@@ -120,11 +170,14 @@ class _FLCE(torch.autograd.Function):
     @staticmethod
     def forward(ctx, hidden, weight, bias, targets, opts):
         (reduction, ignore_index, logit_scale, softcap, z_loss, return_metrics,
-         deterministic) = opts
+         deterministic, accum_dtype, fuse_grad_accum) = opts
         shape = targets.shape
         h2, w, t1, b = _prepare(hidden, weight, targets, bias)
         p = _params(h2, w, b, reduction, ignore_index, logit_scale, softcap, z_loss,
                     deterministic)
+        p.grad_weight_accum = _lib.ACCUM_DTYPES[accum_dtype]
+        ctx.fuse_grad_accum = fuse_grad_accum
+        ctx.weight = weight if fuse_grad_accum else None
         loss, lse, nc, ent, _ = flce_forward(p, h2, w, t1, b, return_metrics)
         ctx.save_for_backward(h2, w, t1, lse, b)
         ctx.p = p
@@ -140,9 +193,21 @@ class _FLCE(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_loss, _g1=None, _g2=None):
         h2, w, t1, lse, b = ctx.saved_tensors
-        gh, gw, gb, _ = flce_backward(
-            ctx.p, h2, w, t1, lse, grad_loss, b, need_hidden=ctx.needs_input_grad[0],
-            need_weight=ctx.needs_input_grad[1], need_bias=ctx.needs_input_grad[2])
+        weight = ctx.weight
+        if ctx.fuse_grad_accum and ctx.needs_input_grad[1] and weight.grad is not None \
+                and weight.grad.is_contiguous() and weight.grad.dtype == weight.dtype:
+            # Add grad_weight straight into the existing weight.grad (beta = 1) and
+            # return None for it, as quack's fused gradient accumulation does. The
+            # other two gradients start from zero in the same call.
+            gh = torch.zeros_like(h2) if ctx.needs_input_grad[0] else None
+            gb = torch.zeros_like(b) if (b is not None and ctx.needs_input_grad[2]) else None
+            flce_backward(ctx.p, h2, w, t1, lse, grad_loss, b, accumulate=True,
+                          out=(gh, weight.grad, gb))
+            gw = None
+        else:
+            gh, gw, gb, _ = flce_backward(
+                ctx.p, h2, w, t1, lse, grad_loss, b, need_hidden=ctx.needs_input_grad[0],
+                need_weight=ctx.needs_input_grad[1], need_bias=ctx.needs_input_grad[2])
         if gh is not None:
             gh = gh.reshape(ctx.hidden_shape)
         return gh, gw, gb, None, None
@@ -152,16 +217,26 @@ def fused_linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, targe
                                bias: Optional[torch.Tensor] = None, ignore_index: int = -100,
                                logit_scale: float = 1.0, softcap: Optional[float] = None,
                                z_loss_multiplier: float = 0.0, reduction: str = "mean",
-                               return_metrics: bool = False, deterministic: bool = False):
+                               return_metrics: bool = False, deterministic: bool = False,
+                               grad_weight_accum_dtype: str = "fp32",
+                               fuse_grad_accum: bool = False):
     """Cross-entropy of ``hidden @ weight.T (+ bias)`` against ``targets``. The logits are never stored.
 
     Returns ``loss``, or ``(loss, {"num_correct_tokens", "entropy_sum"})``
     when ``return_metrics``. The metrics are int64 / float32 scalar sums over
     non-ignored rows (fused-linear-ce README, "Metrics for free"). hidden,
     weight and bias all receive gradients.
+
+    ``grad_weight_accum_dtype`` selects the accumulator of grad_weight across
+    row chunks ("Chunked Linear Loss", "Weight-gradient accumulation dtype"):
+    "fp32" (default) or "weight". With ``fuse_grad_accum``, an existing
+    ``weight.grad`` gets the gradient added in place by the backward kernel
+    instead of a separate add.
     """
+    if grad_weight_accum_dtype not in _lib.ACCUM_DTYPES:
+        raise ValueError("grad_weight_accum_dtype must be 'fp32' or 'weight'")
     opts = (reduction, ignore_index, logit_scale, softcap, z_loss_multiplier, return_metrics,
-            deterministic)
+            deterministic, grad_weight_accum_dtype, fuse_grad_accum)
     loss, nc, ent = _FLCE.apply(hidden, weight, bias, targets, opts)
     if return_metrics:
         return loss, {"num_correct_tokens": nc, "entropy_sum": ent}

@@ -69,6 +69,34 @@ def test_invalid_params_rejected(lib, bad):
     assert lib.flce_workspace_bytes(ctypes.byref(p), 0, ctypes.byref(n)) == 1
 
 
+@pytest.mark.parametrize("bad", [
+    dict(accumulate=2), dict(vocab_start=5), dict(vocab_start=-1, vocab_total=2000),
+    dict(vocab_start=1500, vocab_total=2000),   # 1500 + V(1000) > 2000
+])
+def test_invalid_new_fields_rejected(lib, bad):
+    p = params()
+    for k, v in bad.items():
+        setattr(p, k, v)
+    n = ctypes.c_size_t(0)
+    assert lib.flce_workspace_bytes(ctypes.byref(p), 0, ctypes.byref(n)) == 1
+    p2 = params()
+    p2.grad_weight_accum = 7
+    assert lib.flce_workspace_bytes(ctypes.byref(p2), 0, ctypes.byref(n)) == 1
+
+
+def test_forward_refuses_a_vocabulary_shard_before_any_gpu_work(lib):
+    p = params(vocab_start=1000, vocab_total=3000)
+    fake = 1 << 20
+    assert _lib.forward_raw(p, fake, fake, 0, fake, fake, fake, 0, 0, fake, 1 << 30, 0) == 1
+    assert "flce_forward_partial" in _lib.last_error_detail()
+    # combine: zero shards is an argument error
+    assert _lib.forward_combine_raw(params(), fake, 0, fake, fake, fake, 0, 0, fake, 1 << 30, 0) == 1
+
+
+def test_row_state_is_20_bytes(lib):
+    assert _lib.ROW_STATE_BYTES == 20
+
+
 def test_bad_reduction_rejected(lib):
     p = params()
     p.reduction = 5
