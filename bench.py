@@ -225,8 +225,9 @@ def ours_main(args, w):
     inputs = wl.generate(wr)
 
     def dev_tensor(name):
-        if w.dtype == "bf16":
-            return torch.from_numpy(inputs[name + "_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+        if w.sixteen_bit:
+            tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+            return torch.from_numpy(inputs[name + "_bits"].view(np.int16)).to(dev).view(tdt)
         return torch.from_numpy(inputs[name]).to(dev)
 
     h = dev_tensor("hidden")
@@ -234,7 +235,8 @@ def ours_main(args, w):
     b = dev_tensor("bias") if w.bias else None
     t = torch.from_numpy(inputs["targets"]).to(dev)
     p = _lib.make_params(N=w.N, H=w.H, V=w.V,
-                         dtype=_lib.FLCE_BF16 if w.dtype == "bf16" else _lib.FLCE_F32,
+                         dtype={"bf16": _lib.FLCE_BF16, "f16": _lib.FLCE_F16,
+                                "f32": _lib.FLCE_F32}[w.dtype],
                          reduction=w.reduction, ignore_index=wl.IGNORE_INDEX,
                          logit_scale=w.logit_scale, softcap=w.softcap,
                          z_loss_multiplier=w.z_loss_multiplier, has_bias=w.bias,

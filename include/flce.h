@@ -65,8 +65,11 @@ extern "C" {
 typedef struct CUstream_st* flce_stream_t;
 
 typedef enum {
-  FLCE_F32 = 0,  /* fp32 hidden/weight/bias/grads; SIMT fp32 arithmetic        */
-  FLCE_BF16 = 1  /* bf16 hidden/weight/bias/grads; tcgen05 bf16 MMA, fp32 acc. */
+  FLCE_F32 = 0,  /* fp32 hidden/weight/bias/grads; SIMT fp32 arithmetic         */
+  FLCE_BF16 = 1, /* bf16 hidden/weight/bias/grads; tcgen05 bf16 MMA, fp32 acc.  */
+  FLCE_F16 = 2   /* fp16 hidden/weight/bias/grads; tcgen05 fp16 MMA, fp32 acc.
+                    dlogits are stored in fp16 times an exact power of two that
+                    keeps them out of the fp16 subnormal range                  */
 } flce_dtype;
 
 typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1, FLCE_NONE = 2 } flce_reduction;
@@ -92,7 +95,7 @@ enum {
 
 typedef struct {
   int64_t N;                 /* rows (tokens), >= 0                                   */
-  int64_t H;                 /* hidden size, >= 1; bf16 needs H % 8 == 0 (16-B rows)  */
+  int64_t H;                 /* hidden size, >= 1; bf16/fp16 need H % 8 == 0 (16-B rows) */
   int64_t V;                 /* vocabulary size, >= 1                                 */
   int32_t dtype;             /* flce_dtype of hidden, weight, bias and all gradients  */
   int32_t reduction;         /* flce_reduction                                        */

@@ -13,7 +13,7 @@ from typing import Optional
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
 
-FLCE_F32, FLCE_BF16 = 0, 1
+FLCE_F32, FLCE_BF16, FLCE_F16 = 0, 1, 2
 FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
 FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD = 0, 1
 FLCE_ACCUM_FP32, FLCE_ACCUM_WEIGHT = 0, 1

@@ -138,7 +138,8 @@ int validate(const flce_params* p) {
   const int64_t lim = (int64_t(1) << 30);
   if (p->N < 0 || p->H < 1 || p->V < 1 || p->N > lim || p->H > lim || p->V > lim)
     return FLCE_ERR_INVALID_ARG;
-  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16) return FLCE_ERR_INVALID_ARG;
+  if (p->dtype != FLCE_F32 && p->dtype != FLCE_BF16 && p->dtype != FLCE_F16)
+    return FLCE_ERR_INVALID_ARG;
   if (p->reduction < FLCE_SUM || p->reduction > FLCE_NONE) return FLCE_ERR_INVALID_ARG;
   if (!isfinite(p->logit_scale) || p->logit_scale == 0.f) return FLCE_ERR_INVALID_ARG;
   if (!isfinite(p->softcap)) return FLCE_ERR_INVALID_ARG;
@@ -152,11 +153,14 @@ int validate(const flce_params* p) {
   } else if (p->vocab_start < 0 || p->vocab_total > lim || p->vocab_start + p->V > p->vocab_total) {
     return FLCE_ERR_INVALID_ARG;
   }
-  if (p->dtype == FLCE_BF16 && (p->H % 8) != 0) return FLCE_ERR_ALIGNMENT;
+  if (p->dtype != FLCE_F32 && (p->H % 8) != 0) return FLCE_ERR_ALIGNMENT;
   return FLCE_OK;
 }
 
 bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+// bf16 and fp16 run on the tensor cores; fp32 on the SIMT path.
+bool tensor_path(const flce_params* p) { return p->dtype != FLCE_F32; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -164,7 +168,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // ------------------------------------------------------ workspace layouts
 constexpr int kMinPanelTiles = 4;
 constexpr int kMaxPanelTiles = 32;
-constexpr size_t kHeader = 256;
+constexpr size_t kHeader = 256;   // status word at 0, fp16 dlogits scale {S, 1/S} at 64
+constexpr size_t kScaleOffset = 64;
 constexpr size_t kChunkByteCap = size_t(4) << 30;
 constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_splits)
 
@@ -177,7 +182,7 @@ struct FwdLayout {
 FwdLayout fwd_layout(const flce_params* p) {
   FwdLayout L{};
   const int64_t N = p->N, V = p->V;
-  if (p->dtype == FLCE_BF16)
+  if (tensor_path(p))
     L.num_panels_max = static_cast<int>(ceil_div(ceil_div(V, kBN), kMinPanelTiles));
   else
     L.num_panels_max = static_cast<int>(ceil_div(V, kSimtPanelCols));
@@ -208,7 +213,7 @@ struct BwdLayout {
 BwdLayout bwd_layout(const flce_params* p) {
   BwdLayout L{};
   const int64_t N = p->N, V = p->V, H = p->H;
-  const size_t elem = p->dtype == FLCE_BF16 ? 2 : 4;
+  const size_t elem = tensor_path(p) ? 2 : 4;
   L.V_pad = (V + 7) / 8 * 8;
   if (N <= kPairM) {
     L.chunk = N;
@@ -227,7 +232,7 @@ BwdLayout bwd_layout(const flce_params* p) {
     L.chunk = half < cap ? half : cap;
   }
   L.nchunks = N > 0 ? static_cast<int>(ceil_div(N, L.chunk)) : 0;
-  L.rowblk = p->dtype == FLCE_BF16 ? kBM : kSimtTile;
+  L.rowblk = tensor_path(p) ? kBM : kSimtTile;
   L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
   size_t o = kHeader;
   L.coef = o;
@@ -235,10 +240,10 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.ds = o;
   o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
   L.dw = o;
-  if (p->dtype == FLCE_BF16 && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
+  if (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
     o = align_up(o + size_t(V) * H * 4, 1024);
   L.dh_part = o;
-  if (p->dtype == FLCE_BF16) o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
+  if (tensor_path(p)) o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
   L.bias_part = o;
   if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
   L.total = o;
@@ -294,12 +299,13 @@ int choose_k_splits(int tiles, int k_blocks, int pairs) {
 
 // ------------------------------------------------------------ tensor maps
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -313,6 +319,10 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 }
 
 float inv_cap(const flce_params* p) { return p->softcap > 0.f ? 1.f / p->softcap : 0.f; }
+
+CUtensorMapDataType map_type(const flce_params* p) {
+  return p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
 
 }  // namespace
 
@@ -392,7 +402,8 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   fa.zt = reinterpret_cast<float*>(ws + L.zt);
   fa.status = reinterpret_cast<int*>(ws);
   int v;
-  if (p->dtype == FLCE_BF16) {
+  if (tensor_path(p)) {
+    const CUtensorMapDataType dt = map_type(p);
     fa.n_blocks = static_cast<int>(ceil_div(N, kPairM));
     fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
     int grid = 1;
@@ -400,10 +411,11 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
     fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
     fa.num_units = fa.num_panels * fa.n_blocks;
     CUtensorMap tm_h, tm_w;
-    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
-    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM, dt)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
+    const bool f16 = p->dtype == FLCE_F16;
     v = launch("flce_fwd_tc", st, [&] {
-      return launch_fwd_tc(tm_h, tm_w, fa, bias != nullptr, p->softcap > 0.f, grid, st);
+      return launch_fwd_tc(tm_h, tm_w, fa, f16, bias != nullptr, p->softcap > 0.f, grid, st);
     });
   } else {
     fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
@@ -584,7 +596,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
-  const size_t elem = p->dtype == FLCE_BF16 ? 2 : 4;
+  const size_t elem = tensor_path(p) ? 2 : 4;
 
   if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return FLCE_OK;
   if (N == 0) {
@@ -610,6 +622,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   ra.lse = lse;
   ra.grad_loss = grad_loss;
   ra.coef = coef;
+  float* ds_scale = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + kScaleOffset) : nullptr;
+  ra.ds_scale = ds_scale;
   ra.status = status;
   v = launch("flce_row_coef", st, [&] { return launch_row_coef(ra, st); });
   if (v != FLCE_OK) return v;
@@ -624,15 +638,20 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   da.inv_softcap = inv_cap(p);
   da.bias = bias;
   da.coef = coef;
+  da.ds_scale = ds_scale;
   da.ds = ws + L.ds;
   da.bias_part = bias_part;
   da.status = status;
 
-  if (p->dtype == FLCE_BF16) {
+  if (tensor_path(p)) {
+    const CUtensorMapDataType dt = map_type(p);
+    const bool f16 = p->dtype == FLCE_F16;
+    // fp16 dlogits are stored times S; the contractions multiply by 1/S
+    const float* acc_scale = ds_scale != nullptr ? ds_scale + 1 : nullptr;
     CUtensorMap tm_h, tm_w, tm_w_mn;
-    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM)) != FLCE_OK) return v;
-    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf)) != FLCE_OK) return v;
-    if ((v = make_map(&tm_w_mn, weight, H, V, uint64_t(H) * 2, 64, 64)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM, dt)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
+    if ((v = make_map(&tm_w_mn, weight, H, V, uint64_t(H) * 2, 64, 64, dt)) != FLCE_OK) return v;
     float* dw_part = reinterpret_cast<float*>(ws + L.dw);
     for (int c = 0; c < L.nchunks; ++c) {
       const int row0 = static_cast<int>(c * L.chunk);
@@ -647,14 +666,14 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.num_units = da.num_panels * da.n_blocks;
       da.bias_blk0 = row0 / kBM;
       v = launch("flce_dlogits_tc", st, [&] {
-        return launch_ds_tc(tm_h, tm_w, da, bias != nullptr, p->softcap > 0.f, grid, st);
+        return launch_ds_tc(tm_h, tm_w, da, f16, bias != nullptr, p->softcap > 0.f, grid, st);
       });
       if (v != FLCE_OK) return v;
       const uint64_t ds_row_bytes = uint64_t(L.V_pad) * 2;
       if (grad_hidden) {
         // grad_hidden[rows, H] = dS[rows, V] (K-major) x W[V, H] (MN-major)
         CUtensorMap tm_a;
-        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, kBK, kBM)) != FLCE_OK) return v;
+        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, kBK, kBM, dt)) != FLCE_OK) return v;
         GemmArgs ga{};
         ga.M = rows;
         ga.N = H;
@@ -673,10 +692,12 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.part = reinterpret_cast<float*>(ws + L.dh_part);
         ga.ld_part = H;
         ga.split_stride = static_cast<long long>(L.chunk) * H;
+        ga.acc_scale = acc_scale;
         ga.status = status;
         const int units = ga.num_tiles * ga.k_splits;
         const int g2 = units < d.pairs ? units : d.pairs;
-        v = launch("flce_grad_hidden_tc", st, [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, g2, st); });
+        v = launch("flce_grad_hidden_tc", st,
+                   [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
         if (ga.k_splits > 1) {
           SplitReduceArgs ra2{};
@@ -684,6 +705,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
           ra2.N = H;
           ra2.splits = ga.k_splits;
           ra2.accumulate = p->accumulate;
+          ra2.f16 = f16 ? 1 : 0;
           ra2.part = ga.part;
           ra2.ld_part = H;
           ra2.split_stride = ga.split_stride;
@@ -696,9 +718,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       if (grad_weight) {
         // grad_weight[V, H] (+)= dS^T[V, rows] (MN-major) x h[rows, H] (MN-major)
         CUtensorMap tm_a, tm_b;
-        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, 64, 64)) != FLCE_OK) return v;
+        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, 64, 64, dt)) != FLCE_OK) return v;
         const void* hc = static_cast<const uint8_t*>(hidden) + size_t(row0) * H * 2;
-        if ((v = make_map(&tm_b, hc, H, rows, uint64_t(H) * 2, 64, 64)) != FLCE_OK) return v;
+        if ((v = make_map(&tm_b, hc, H, rows, uint64_t(H) * 2, 64, 64, dt)) != FLCE_OK) return v;
         GemmArgs ga{};
         ga.M = V;
         ga.N = H;
@@ -727,9 +749,11 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.ld_out = H;
         ga.part = dw_part;
         ga.ld_part = H;
+        ga.acc_scale = acc_scale;
         ga.status = status;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
-        v = launch("flce_grad_weight_tc", st, [&] { return launch_gemm_tc(tm_a, tm_b, ga, g2, st); });
+        v = launch("flce_grad_weight_tc", st,
+                   [&] { return launch_gemm_tc(tm_a, tm_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
     }

@@ -128,6 +128,7 @@ struct RowCoefArgs {
   const float* lse;
   const float* grad_loss;
   float4* coef;
+  float* ds_scale;             // nullable: receives {S, 1/S}, S = 2^k with max |dlogits| * S <= 2^14
   int* status;
 };
 
@@ -137,7 +138,8 @@ struct DsArgs {
   float scale, softcap, inv_softcap;
   const void* bias;
   const float4* coef;          // indexed by global row
-  void* ds;                    // chunk buffer [rows][V_pad], bf16 or f32
+  const float* ds_scale;       // fp16: power of two that dlogits is stored times; else nullptr
+  void* ds;                    // chunk buffer [rows][V_pad] in the input dtype (f32 for fp32)
   float* bias_part;            // [row blocks][V_pad] or nullptr
   int bias_blk0;               // first row block of this chunk
   int* status;
@@ -169,6 +171,7 @@ struct GemmArgs {
   float* part;
   long long ld_part;
   long long split_stride;      // elements between split partial buffers
+  const float* acc_scale;      // nullable: the accumulator is multiplied by *acc_scale first
   int* status;
 };
 
@@ -176,6 +179,7 @@ struct GemmArgs {
 struct SplitReduceArgs {
   int M, N, splits;
   int accumulate;              // 1: out += sum (read-modify-write)
+  int f16;                     // output dtype: 1 fp16, 0 bf16
   const float* part;
   long long ld_part, split_stride;
   void* out;
@@ -202,19 +206,20 @@ struct BiasReduceArgs {
 
 // tcgen05 / TMA kernels (bf16). `grid` is the number of CTA pairs.
 cudaError_t tc_max_active_pairs(int* pairs);
+// f16 selects fp16 operands and outputs; otherwise bf16.
 cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
-                          bool has_bias, bool softcap, int grid, cudaStream_t s);
+                          bool f16, bool has_bias, bool softcap, int grid, cudaStream_t s);
 cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
-                         bool has_bias, bool softcap, int grid, cudaStream_t s);
+                         bool f16, bool has_bias, bool softcap, int grid, cudaStream_t s);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
-                           int grid, cudaStream_t s);
+                           bool f16, int grid, cudaStream_t s);
 
 // SIMT kernels (fp32)
 cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s);
 
-// dtype-generic small kernels (dtype: 0 = f32, 1 = bf16)
+// dtype-generic small kernels (dtype: 0 = f32, 1 = bf16, 2 = fp16)
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);
 cudaError_t launch_shard_state(const ShardStateArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s);

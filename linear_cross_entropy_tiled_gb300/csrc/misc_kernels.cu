@@ -9,6 +9,7 @@
 //   shard_state / combine  export of one vocabulary shard's per-row state and
 //               the merge of several shards' states (vocabulary-parallel use).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "kernels.h"
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
 __global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
   __shared__ long long sh_i[32];
   __shared__ long long s_valid;
+  __shared__ float sh_max[32];
   long long v = 0;
   for (int i = threadIdx.x; i < a.N; i += blockDim.x) v += (a.targets[i] != a.ignore_index) ? 1 : 0;
   v = block_sum(v, sh_i);
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
   float g_all = 0.f;
   if (a.reduction == 0) g_all = a.grad_loss[0];
   if (a.reduction == 1) g_all = num_valid > 0 ? a.grad_loss[0] / static_cast<float>(num_valid) : 0.f;
+  float cmax = 0.f;  // bound on |dlogits|: |g| <= max(|x|, |y|) because 0 <= p <= 1
   for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
     const long long t = a.targets[i];
     const float lse = a.lse[i];
@@ -247,8 +250,42 @@ __global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
       }
     }
     a.coef[i] = c;
+    cmax = fmaxf(cmax, fmaxf(fabsf(c.x), fabsf(c.y)));
+  }
+  if (a.ds_scale != nullptr) {
+    // fp16 dlogits are stored times S = 2^k with max |dlogits| * S <= 2^14:
+    // large values stay below the fp16 maximum (65504) and small probabilities
+    // stay above its subnormal range. S is a power of two, so scaling and
+    // unscaling are exact.
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    if ((threadIdx.x & 31) == 0) sh_max[threadIdx.x >> 5] = cmax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, sh_max[w]);
+      int k = 0;
+      if (m > 0.f && isfinite(m)) {
+        int e;
+        frexpf(m, &e);          // m = f * 2^e with 0.5 <= f < 1, so m < 2^e
+        k = 14 - e;
+        k = k > 120 ? 120 : (k < -120 ? -120 : k);
+      }
+      a.ds_scale[0] = ldexpf(1.f, k);
+      a.ds_scale[1] = ldexpf(1.f, -k);
+    }
   }
 }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
 template <typename Tout>
 __global__ void __launch_bounds__(256) bias_reduce_kernel(const BiasReduceArgs a) {
@@ -256,18 +293,15 @@ __global__ void __launch_bounds__(256) bias_reduce_kernel(const BiasReduceArgs a
   if (j >= a.V) return;
   float s = 0.f;
   for (int b = 0; b < a.nblk; ++b) s += a.bias_part[static_cast<size_t>(b) * a.V_pad + j];
-  if constexpr (sizeof(Tout) == 2) {
-    __nv_bfloat16* gb = static_cast<__nv_bfloat16*>(a.grad_bias);
-    if (a.accumulate) s += __bfloat162float(gb[j]);
-    gb[j] = __float2bfloat16_rn(s);
-  } else {
-    float* gb = static_cast<float*>(a.grad_bias);
-    gb[j] = a.accumulate ? gb[j] + s : s;
-  }
+  Tout* gb = static_cast<Tout*>(a.grad_bias);
+  if (a.accumulate) s += to_f32(gb[j]);
+  gb[j] = from_f32<Tout>(s);
 }
 
-// Sums the fp32 K-split partials of a GEMM in split order and casts to bf16.
-// Each thread handles 4 consecutive columns (N is a multiple of 8).
+// Sums the fp32 K-split partials of a GEMM in split order and casts to the
+// 16-bit output type. Each thread handles 4 consecutive columns (N is a
+// multiple of 8).
+template <typename Tout>
 __global__ void __launch_bounds__(256) split_reduce_kernel(const SplitReduceArgs a) {
   const long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long per_row = a.N / 4;
@@ -282,27 +316,28 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const SplitReduceArgs
     acc.z += p.z;
     acc.w += p.w;
   }
-  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + m * a.ld_out + n);
+  Tout* dst = static_cast<Tout*>(a.out) + m * a.ld_out + n;
   if (a.accumulate) {
-    const uint2 o = *dst;
-    acc.x += __uint_as_float(o.x << 16);
-    acc.y += __uint_as_float(o.x & 0xffff0000u);
-    acc.z += __uint_as_float(o.y << 16);
-    acc.w += __uint_as_float(o.y & 0xffff0000u);
+    acc.x += to_f32(dst[0]);
+    acc.y += to_f32(dst[1]);
+    acc.z += to_f32(dst[2]);
+    acc.w += to_f32(dst[3]);
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 w;
-  w.x = *reinterpret_cast<uint32_t*>(&lo);
-  w.y = *reinterpret_cast<uint32_t*>(&hi);
-  *dst = w;
+  dst[0] = from_f32<Tout>(acc.x);
+  dst[1] = from_f32<Tout>(acc.y);
+  dst[2] = from_f32<Tout>(acc.z);
+  dst[3] = from_f32<Tout>(acc.w);
 }
 
 }  // namespace
 
 cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s) {
   const long long n = static_cast<long long>(a.M) * (a.N / 4);
-  split_reduce_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
+  const unsigned grid = static_cast<unsigned>((n + 255) / 256);
+  if (a.f16)
+    split_reduce_kernel<__half><<<grid, 256, 0, s>>>(a);
+  else
+    split_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -335,6 +370,8 @@ cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t 
   const int grid = (a.V + 255) / 256;
   if (dtype == 1)
     bias_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+  else if (dtype == 2)
+    bias_reduce_kernel<__half><<<grid, 256, 0, s>>>(a);
   else
     bias_reduce_kernel<float><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();

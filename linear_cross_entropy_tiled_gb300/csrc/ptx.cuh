@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kernels.h"
@@ -202,12 +203,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (2ull << 61);    // 128-byte swizzle
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
+// Instruction descriptor of kind::f16 with 16-bit A/B (both bf16 or both fp16)
+// and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major, bool bf16) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | ((bf16 ? 1u : 0u) << 7)                  // A format: 1 = bf16, 0 = fp16
+         | ((bf16 ? 1u : 0u) << 10)                 // B format: same as A
          | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
@@ -301,6 +303,11 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return idesc_f16kind_f32(M, N, a_mn_major, b_mn_major, true);
+}
+
 // ------------------------------------------------------------- arithmetic
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -312,5 +319,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// The two 16-bit storage types of the tensor-core path. lo/hi convert the two
+// halves of a 32-bit word; pack rounds two floats to nearest even.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr bool kBf16 = true;
+  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+  __device__ static __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ static __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+  __device__ static __forceinline__ uint32_t pack(float a, float b) { return pack_bf16x2(a, b); }
+  __device__ static __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr bool kBf16 = false;
+  __device__ static __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+  }
+  __device__ static __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  }
+  __device__ static __forceinline__ uint32_t pack(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __device__ static __forceinline__ float to_float(__half x) { return __half2float(x); }
+};
 
 }  // namespace flce

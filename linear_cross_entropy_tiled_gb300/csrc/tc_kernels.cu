@@ -1,4 +1,4 @@
-// tcgen05 / TMA kernels of the bf16 path (sm_103a).
+// tcgen05 / TMA kernels of the 16-bit path (bf16 or fp16 operands; sm_103a).
 //
 // Every kernel here is persistent and warp-specialised. CTAs run in pairs
 // (clusters of 2) that share one 2-SM MMA (tcgen05.mma.cta_group::2) per
@@ -28,6 +28,7 @@
 //            fp32 accumulation of grad_weight across row chunks ("Chunked
 //            Linear Loss", "Weight-gradient accumulation dtype").
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "kernels.h"
@@ -210,11 +211,12 @@ __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, ui
 }
 
 // Both operands K-major; the pair computes M = 256, N = 256.
+template <typename T>
 __device__ __forceinline__ void kmajor_descs(int, int, uint32_t sa, uint32_t sb, int kk,
                                              uint64_t& ad, uint64_t& bd, uint32_t& idesc) {
   ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
   bd = smem_desc_sw128(sb + kk * 32, 16, 1024);
-  idesc = idesc_bf16_f32(kPairM, kBN, false, false);
+  idesc = idesc_f16kind_f32(kPairM, kBN, false, false, Elem<T>::kBf16);
 }
 
 // Operand descriptor of the kk-th 16-deep K step: K-major rows advance 32 B
@@ -245,9 +247,9 @@ __device__ __forceinline__ void epi_release(const TcSmem& s, int acc, int lane) 
 
 // 32 bias values times scale, for columns col0 .. col0+31. Columns at or
 // beyond V read as 0.
-template <bool kRagged>
-__device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int col0, int V,
-                                            float scale, float (&bs)[32]) {
+template <typename T, bool kRagged>
+__device__ __forceinline__ void load_bias32(const T* bias, int col0, int V, float scale,
+                                            float (&bs)[32]) {
   if (!kRagged) {
     const uint4* p = reinterpret_cast<const uint4*>(bias + col0);
 #pragma unroll
@@ -256,15 +258,14 @@ __device__ __forceinline__ void load_bias32(const __nv_bfloat16* bias, int col0,
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
-        bs[q * 8 + 2 * h] = __uint_as_float(ws[h] << 16) * scale;
-        bs[q * 8 + 2 * h + 1] = __uint_as_float(ws[h] & 0xffff0000u) * scale;
+        bs[q * 8 + 2 * h] = Elem<T>::lo(ws[h]) * scale;
+        bs[q * 8 + 2 * h + 1] = Elem<T>::hi(ws[h]) * scale;
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      bs[j] = (col0 + j < V) ? __bfloat162float(bias[col0 + j]) * scale : 0.f;
+      bs[j] = (col0 + j < V) ? Elem<T>::to_float(bias[col0 + j]) * scale : 0.f;
   }
 }
 
@@ -315,13 +316,12 @@ __device__ __forceinline__ float select32(const float (&x)[32], int i) {
   return (i & 1) ? t2[1] : t2[0];
 }
 
-template <bool kRagged, bool kBias, bool kSoftcap>
+template <typename T, bool kRagged, bool kBias, bool kSoftcap>
 __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs& a, int col0,
                                           long long tgt, int row, bool row_ok, float& m,
                                           float& ssum, float& tsum, int& amax) {
   float bs[32];
-  if (kBias) load_bias32<kRagged>(static_cast<const __nv_bfloat16*>(a.bias), col0, a.V,
-                                  a.scale, bs);
+  if (kBias) load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
   float z[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -371,7 +371,7 @@ __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs
   m = mnew;
 }
 
-template <bool kBias, bool kSoftcap>
+template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                   const FwdArgs a) {
@@ -407,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -438,9 +438,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             tmem_ld_wait(v);
             const int col0 = vt * kBN + c * 32;
             if (!ragged) {
-              fwd_chunk<false, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum, amax);
+              fwd_chunk<T, false, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
+                                                   amax);
             } else if (col0 < a.V) {
-              fwd_chunk<true, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum, amax);
+              fwd_chunk<T, true, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
+                                                  amax);
             }
           }
           epi_release(s, acc, lane);
@@ -471,12 +473,12 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&x)[32], int lane) 
   return x[0];  // lane L now holds the sum of column L over the warp's 32 rows
 }
 
-template <bool kRagged, bool kBias, bool kSoftcap>
+template <typename T, bool kRagged, bool kBias, bool kSoftcap>
 __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& a, int col0,
-                                         float4 cf, bool row_ok, int row_local, float (&gout)[32]) {
+                                         float4 cf, bool row_ok, int row_local, float ds_mul,
+                                         float (&gout)[32]) {
   float bs[32];
-  if (kBias) load_bias32<kRagged>(static_cast<const __nv_bfloat16*>(a.bias), col0, a.V,
-                                  a.scale, bs);
+  if (kBias) load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
   const int tgt = __float_as_int(cf.w);
   const float nlse = -cf.z * kLog2e;
 #pragma unroll
@@ -494,22 +496,23 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
     gout[j] = row_ok ? gj : 0.f;
   }
   if (row_ok) {
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.ds) +
-                         static_cast<size_t>(row_local) * a.V_pad + col0;
+    // fp16 stores dlogits times a power of two (ds_mul), which keeps the small
+    // probabilities out of the fp16 subnormal range; the GEMMs undo it exactly.
+    T* dst = static_cast<T*>(a.ds) + static_cast<size_t>(row_local) * a.V_pad + col0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if (kRagged && col0 + q * 8 >= a.V) break;
       uint4 w;
-      w.x = pack_bf16x2(gout[q * 8 + 0], gout[q * 8 + 1]);
-      w.y = pack_bf16x2(gout[q * 8 + 2], gout[q * 8 + 3]);
-      w.z = pack_bf16x2(gout[q * 8 + 4], gout[q * 8 + 5]);
-      w.w = pack_bf16x2(gout[q * 8 + 6], gout[q * 8 + 7]);
+      w.x = Elem<T>::pack(gout[q * 8 + 0] * ds_mul, gout[q * 8 + 1] * ds_mul);
+      w.y = Elem<T>::pack(gout[q * 8 + 2] * ds_mul, gout[q * 8 + 3] * ds_mul);
+      w.z = Elem<T>::pack(gout[q * 8 + 4] * ds_mul, gout[q * 8 + 5] * ds_mul);
+      w.w = Elem<T>::pack(gout[q * 8 + 6] * ds_mul, gout[q * 8 + 7] * ds_mul);
       *reinterpret_cast<uint4*>(dst + q * 8) = w;
     }
   }
 }
 
-template <bool kBias, bool kSoftcap>
+template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const DsArgs a) {
@@ -546,11 +549,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int et = threadIdx.x - 64;  // 0..127
+    const float ds_mul = a.ds_scale != nullptr ? *a.ds_scale : 1.f;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
@@ -579,9 +583,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                       v);
             tmem_ld_wait(v);
             if (!ragged) {
-              ds_chunk<false, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, gv);
+              ds_chunk<T, false, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, ds_mul, gv);
             } else if (col0 < a.V) {
-              ds_chunk<true, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, gv);
+              ds_chunk<T, true, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, ds_mul, gv);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) gv[j] = 0.f;
@@ -626,6 +630,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 // neighbouring tiles of the same K range, which share an operand strip in L2.
 // The arguments are copied into registers up front; the role loops read no
 // kernel parameters.
+template <typename T>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const GemmArgs a) {
@@ -681,7 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      const uint32_t id = idesc_bf16_f32(kPairM, kBN, a_mn, b_mn);
+      const uint32_t id = idesc_f16kind_f32(kPairM, kBN, a_mn, b_mn, Elem<T>::kBf16);
       mma_role(s, g, tmem, kblocks_of, for_each_tile,
                [&](int, int, uint32_t sa, uint32_t sb, int kk, uint64_t& ad, uint64_t& bd,
                    uint32_t& idesc) {
@@ -699,7 +704,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
     float* const part0 = a.part;
     const long long ld_part = a.ld_part, split_stride = a.split_stride, ld_out = a.ld_out;
-    __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
+    T* const out = static_cast<T*>(a.out);
+    const float acc_mul = a.acc_scale != nullptr ? *a.acc_scale : 1.f;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
@@ -722,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           if (!row_ok || col0 >= N) continue;
           float d[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
           if (add_part) {
             const float4* src =
                 reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * ld_part + col0);
@@ -746,9 +752,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
-                  d[8 * i + 2 * h] += __uint_as_float(ws[h] << 16);
-                  d[8 * i + 2 * h + 1] += __uint_as_float(ws[h] & 0xffff0000u);
+                  d[8 * i + 2 * h] += Elem<T>::lo(ws[h]);
+                  d[8 * i + 2 * h + 1] += Elem<T>::hi(ws[h]);
                 }
               }
             }
@@ -760,15 +765,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
               if (col0 + i * 4 < N)
                 dst[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
           } else {
-            __nv_bfloat16* dst = out + static_cast<size_t>(m) * ld_out + col0;
+            T* dst = out + static_cast<size_t>(m) * ld_out + col0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               if (col0 + i * 8 < N) {
                 uint4 w;
-                w.x = pack_bf16x2(d[8 * i + 0], d[8 * i + 1]);
-                w.y = pack_bf16x2(d[8 * i + 2], d[8 * i + 3]);
-                w.z = pack_bf16x2(d[8 * i + 4], d[8 * i + 5]);
-                w.w = pack_bf16x2(d[8 * i + 6], d[8 * i + 7]);
+                w.x = Elem<T>::pack(d[8 * i + 0], d[8 * i + 1]);
+                w.y = Elem<T>::pack(d[8 * i + 2], d[8 * i + 3]);
+                w.z = Elem<T>::pack(d[8 * i + 4], d[8 * i + 5]);
+                w.w = Elem<T>::pack(d[8 * i + 6], d[8 * i + 7]);
                 *reinterpret_cast<uint4*>(dst + i * 8) = w;
               }
             }
@@ -791,7 +796,7 @@ cudaError_t set_smem_attr(K kernel) {
 }  // namespace
 
 cudaError_t tc_max_active_pairs(int* pairs) {
-  auto k = fwd_tc_kernel<false, false>;
+  auto k = fwd_tc_kernel<__nv_bfloat16, false, false>;
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -805,33 +810,56 @@ cudaError_t tc_max_active_pairs(int* pairs) {
   return cudaSuccess;
 }
 
-// `grid` counts CTA pairs; the launch has 2 * grid CTAs.
-cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
-                          bool has_bias, bool softcap, int grid, cudaStream_t st) {
-  auto k = has_bias ? (softcap ? fwd_tc_kernel<true, true> : fwd_tc_kernel<true, false>)
-                    : (softcap ? fwd_tc_kernel<false, true> : fwd_tc_kernel<false, false>);
+namespace {
+template <typename T>
+cudaError_t launch_fwd_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
+                         bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  auto k = has_bias ? (softcap ? fwd_tc_kernel<T, true, true> : fwd_tc_kernel<T, true, false>)
+                    : (softcap ? fwd_tc_kernel<T, false, true> : fwd_tc_kernel<T, false, false>);
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_ds_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
+                        bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  auto k = has_bias ? (softcap ? ds_tc_kernel<T, true, true> : ds_tc_kernel<T, true, false>)
+                    : (softcap ? ds_tc_kernel<T, false, true> : ds_tc_kernel<T, false, false>);
+  cudaError_t e = set_smem_attr(k);
+  if (e != cudaSuccess) return e;
+  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_gemm_t(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+                          int grid, cudaStream_t st) {
+  cudaError_t e = set_smem_attr(gemm_tc_kernel<T>);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<T><<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+// `grid` counts CTA pairs; the launch has 2 * grid CTAs.
+cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
+                          bool f16, bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  return f16 ? launch_fwd_t<__half>(tm_h, tm_w, a, has_bias, softcap, grid, st)
+             : launch_fwd_t<__nv_bfloat16>(tm_h, tm_w, a, has_bias, softcap, grid, st);
 }
 
 cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
-                         bool has_bias, bool softcap, int grid, cudaStream_t st) {
-  auto k = has_bias ? (softcap ? ds_tc_kernel<true, true> : ds_tc_kernel<true, false>)
-                    : (softcap ? ds_tc_kernel<false, true> : ds_tc_kernel<false, false>);
-  cudaError_t e = set_smem_attr(k);
-  if (e != cudaSuccess) return e;
-  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
-  return cudaGetLastError();
+                         bool f16, bool has_bias, bool softcap, int grid, cudaStream_t st) {
+  return f16 ? launch_ds_t<__half>(tm_h, tm_w, a, has_bias, softcap, grid, st)
+             : launch_ds_t<__nv_bfloat16>(tm_h, tm_w, a, has_bias, softcap, grid, st);
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
-                           int grid, cudaStream_t st) {
-  cudaError_t e = set_smem_attr(gemm_tc_kernel);
-  if (e != cudaSuccess) return e;
-  gemm_tc_kernel<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
-  return cudaGetLastError();
+                           bool f16, int grid, cudaStream_t st) {
+  return f16 ? launch_gemm_t<__half>(tm_a, tm_b, a, grid, st)
+             : launch_gemm_t<__nv_bfloat16>(tm_a, tm_b, a, grid, st);
 }
 
 }  // namespace flce

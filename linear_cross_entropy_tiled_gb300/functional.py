@@ -17,7 +17,8 @@ import torch
 
 from . import _lib
 
-_DTYPES = {torch.float32: _lib.FLCE_F32, torch.bfloat16: _lib.FLCE_BF16}
+_DTYPES = {torch.float32: _lib.FLCE_F32, torch.bfloat16: _lib.FLCE_BF16,
+           torch.float16: _lib.FLCE_F16}
 _CHECK = os.environ.get("FLCE_CHECK", "0") not in ("", "0")
 
 
@@ -33,7 +34,7 @@ def _prepare(hidden, weight, targets, bias):
     if not (hidden.is_cuda and weight.is_cuda and targets.is_cuda):
         raise ValueError("hidden, weight and targets must be CUDA tensors (there is no CPU path)")
     if hidden.dtype not in _DTYPES:
-        raise TypeError(f"hidden must be float32 or bfloat16, got {hidden.dtype}")
+        raise TypeError(f"hidden must be float32, bfloat16 or float16, got {hidden.dtype}")
     if weight.dtype != hidden.dtype or (bias is not None and bias.dtype != hidden.dtype):
         raise TypeError("weight and bias must have the dtype of hidden")
     H = hidden.shape[-1]

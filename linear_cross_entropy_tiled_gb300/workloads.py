@@ -15,8 +15,8 @@ in its "Full signature" section. The distributions are:
   (k + 1)^-s. The ids are taken rank-for-rank and drawn by inverse-CDF.
 * Exactly round(f * N) rows are set to ignore_index. A seeded permutation picks them.
 
-Every tensor is drawn in fp32. For bf16 workloads each value is rounded to the
-nearest bf16 (ties to even). The fp32 array that is returned holds those rounded
+Every tensor is drawn in fp32. For bf16 and fp16 inputs each value is rounded
+to the nearest value of that type (ties to even). The fp32 array that is returned holds those rounded
 values exactly, so fp64 arithmetic on it sees the same numbers the GPU sees.
 """
 from __future__ import annotations
@@ -41,7 +41,7 @@ class Workload:
     N: int
     H: int
     V: int
-    dtype: str = "bf16"            # "bf16" or "f32"
+    dtype: str = "bf16"            # "bf16", "f16" or "f32"
     bias: bool = False
     bias_var: float = 0.1
     targets: str = "uniform"       # "uniform" or "zipf"
@@ -67,6 +67,10 @@ class Workload:
     def logits_bytes_avoided(self) -> int:
         """Bytes of one N x V logits tensor in the input dtype. This tensor is never allocated."""
         return self.N * self.V * (4 if self.dtype == "f32" else 2)
+
+    @property
+    def sixteen_bit(self) -> bool:
+        return self.dtype in ("bf16", "f16")
 
 
 SWEEP_V = (32000, 50304, 65536, 100352, 128256, 256000)
@@ -107,13 +111,22 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def round_to_16bit(x: np.ndarray, dtype: str):
+    """(uint16 bit patterns, fp32 values) of x rounded to bf16 or fp16 (nearest, ties to even)."""
+    if dtype == "bf16":
+        bits = round_to_bf16_bits(x)
+        return bits, bf16_bits_to_f32(bits)
+    h = np.asarray(x, dtype=np.float32).astype(np.float16)
+    return h.view(np.uint16), h.astype(np.float32)
+
+
 def _normal_matrix(seed_seq: np.random.SeedSequence, rows: int, cols: int,
                    std: float, dtype: str, threads: int):
     """N(0, std^2) matrix in fixed row blocks. Returns (fp32 values, bf16 bits or None)."""
     nblk = max(1, -(-rows // _BLOCK_ROWS))
     children = seed_seq.spawn(nblk)
     vals = np.empty((rows, cols), dtype=np.float32)
-    bits = np.empty((rows, cols), dtype=np.uint16) if dtype == "bf16" else None
+    bits = np.empty((rows, cols), dtype=np.uint16) if dtype in ("bf16", "f16") else None
 
     def fill(b):
         r0 = b * _BLOCK_ROWS
@@ -123,9 +136,9 @@ def _normal_matrix(seed_seq: np.random.SeedSequence, rows: int, cols: int,
         if std != 1.0:
             x *= np.float32(std)
         if bits is not None:
-            bb = round_to_bf16_bits(x)
+            bb, vv = round_to_16bit(x, dtype)
             bits[r0:r1] = bb
-            vals[r0:r1] = bf16_bits_to_f32(bb)
+            vals[r0:r1] = vv
         else:
             vals[r0:r1] = x
 
@@ -151,7 +164,7 @@ def generate(w: Workload, threads: Optional[int] = None) -> dict:
       weight  float32 [V, H]
       bias    float32 [V] or None
       targets int64 [N]        ignore_index = -100 on the ignored rows
-      hidden_bits / weight_bits / bias_bits   uint16 bf16 patterns (bf16 only)
+      hidden_bits / weight_bits / bias_bits   uint16 bit patterns (bf16 and fp16 only)
     """
     threads = threads or min(16, os.cpu_count() or 1)
     root = np.random.SeedSequence(w.seed)
@@ -176,7 +189,7 @@ def generate(w: Workload, threads: Optional[int] = None) -> dict:
         gi = np.random.Generator(np.random.PCG64(s_ign))
         targets[gi.permutation(w.N)[:n_ign]] = IGNORE_INDEX
     out = dict(hidden=hidden, weight=weight, bias=bias, targets=targets)
-    if w.dtype == "bf16":
+    if w.sixteen_bit:
         out.update(hidden_bits=hidden_bits, weight_bits=weight_bits, bias_bits=bias_bits)
     return out
 
@@ -191,9 +204,8 @@ def small_case(N: int, H: int, V: int, seed: int, dtype: str = "bf16", bias: boo
     d = generate(w, threads=4)
     if hidden_std != 1.0:
         x = d["hidden"] * np.float32(hidden_std)
-        if dtype == "bf16":
-            d["hidden_bits"] = round_to_bf16_bits(x)
-            d["hidden"] = bf16_bits_to_f32(d["hidden_bits"])
+        if dtype in ("bf16", "f16"):
+            d["hidden_bits"], d["hidden"] = round_to_16bit(x, dtype)
         else:
             d["hidden"] = x
     return d

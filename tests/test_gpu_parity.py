@@ -94,6 +94,22 @@ def test_f32_parity(N, H, V, bias, ign, kw):
     check_case(d, "f32", kw, grad_loss=gl)
 
 
+F16_CASES = [
+    (300, 136, 1000, True, 0.1, dict(reduction="mean", logit_scale=0.7, softcap=10.0,
+                                     z_loss_multiplier=1e-3)),
+    (513, 264, 2053, True, 0.05, dict(reduction="none")),
+    (8192, 256, 4099, False, 0.2, dict(reduction="mean")),   # 1/N-sized dlogits: tests the fp16 scaling
+]
+
+
+@pytest.mark.parametrize("N,H,V,bias,ign,kw", F16_CASES)
+def test_f16_parity(N, H, V, bias, ign, kw):
+    d = small_case(N, H, V, seed=N * 5 + V, dtype="f16", bias=bias, ignore_frac=ign)
+    d = with_argmax_targets(d, kw)
+    gl = np.random.default_rng(2).standard_normal(N).astype(np.float32) if kw["reduction"] == "none" else 1.0
+    check_case(d, "f16", kw, grad_loss=gl)
+
+
 def test_three_chunk_backward(monkeypatch):
     """Force 256-row chunks (3 of them): the grad_weight partial is stored, added to, then cast."""
     monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS", "256")

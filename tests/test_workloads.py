@@ -57,3 +57,11 @@ def test_headline_workload_matches_the_printed_logits_size():
     gib = w.logits_bytes_avoided / 2 ** 30
     assert abs(gib - g["approx_gib_bf16"]) / g["approx_gib_bf16"] < g["rel_tol"]
     assert w.flops_fwd_bwd == 8 * 8192 * 4096 * 128256
+
+
+def test_fp16_rounding_matches_torch():
+    x = np.random.default_rng(3).standard_normal(50000).astype(np.float32) * 10
+    bits, vals = wl.round_to_16bit(x, "f16")
+    ref = torch.from_numpy(x).to(torch.float16)
+    np.testing.assert_array_equal(bits, ref.view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(vals, ref.float().numpy())
