@@ -18,6 +18,7 @@
 
 #include "flce.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 using namespace flce;
 
@@ -250,34 +251,59 @@ BwdLayout bwd_layout(const flce_params* p) {
   return L;
 }
 
-// Vocabulary tiles per panel. Units are (panel, row block) pairs in
-// panel-major order, handed out round-robin to `sms` persistent CTAs. So at
-// any moment the CTAs work on the same few panels: the W panel is read from
-// HBM about once and shared through L2. The panel length is chosen to
-// minimise the largest tile count of any CTA, which is the critical path.
-int choose_panel_tiles(int n_blocks, int v_tiles, int sms, int* grid_out) {
-  int best = kMinPanelTiles;
+// Pair blocks per unit group: about 32 MB of h rows (256 x H x 2 bytes per
+// block). Measured at the headline size, a group of 16 blocks (4096 rows x
+// 4096) stays in L2. The forward over all 32 blocks (67 MB of h) read 6.1x
+// its algorithmic bytes from DRAM.
+int group_blocks_for(int n_blocks, int H) {
+  const long long per_block = static_cast<long long>(kPairM) * H * 2;
+  long long g = (32ll << 20) / per_block;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < n_blocks ? g : n_blocks);
+}
+
+// Vocabulary tiles per panel. Units (panel, pair block) are handed out
+// round-robin to `pairs` persistent CTA pairs, in groups of `group` pair
+// blocks, panel-major within a group (decode_unit). So at any moment the pairs
+// work on the same few panels of the same group: a W panel is read from HBM
+// once per group and shared through L2, and the group's rows of h stay
+// resident. The criterion is the busiest pair's tile count (the critical
+// path). Among panel lengths within 1 % of the best, the shortest wins,
+// because it keeps the W working set small next to h.
+int choose_panel_tiles(int n_blocks, int group, int v_tiles, int pairs, int* grid_out) {
+  long long cost_of[kMaxPanelTiles + 1];
+  int grid_of[kMaxPanelTiles + 1];
   long long best_cost = -1;
-  int best_grid = 1;
   for (int pt = kMinPanelTiles; pt <= kMaxPanelTiles; ++pt) {
     const long long P = ceil_div(v_tiles, pt);
     const long long U = P * n_blocks;
-    const long long G = U < sms ? U : sms;
-    const long long full_end = (P - 1) * n_blocks;
+    const long long G = U < pairs ? U : pairs;
     const long long last_len = v_tiles - (P - 1) * pt;
     long long cost = 0;
     for (long long c = 0; c < G; ++c) {
+      // units of pair c: c, c + G, ...; count those in [lo, hi)
       auto cnt = [&](long long x) { return x > c ? (x - c - 1) / G + 1 : 0; };
-      const long long t = cnt(full_end) * pt + (cnt(U) - cnt(full_end)) * last_len;
+      long long t = 0, pos = 0;
+      for (long long b0 = 0; b0 < n_blocks; b0 += group) {
+        const long long gb = n_blocks - b0 < group ? n_blocks - b0 : group;
+        const long long full = gb * (P - 1);  // units of full panels, then gb of the last panel
+        t += (cnt(pos + full) - cnt(pos)) * pt + (cnt(pos + full + gb) - cnt(pos + full)) * last_len;
+        pos += full + gb;
+      }
       if (t > cost) cost = t;
     }
-    if (best_cost < 0 || cost < best_cost || (cost == best_cost && pt > best)) {
-      best_cost = cost;
+    cost_of[pt] = cost;
+    grid_of[pt] = static_cast<int>(G);
+    if (best_cost < 0 || cost < best_cost) best_cost = cost;
+  }
+  int best = kMinPanelTiles;
+  for (int pt = kMinPanelTiles; pt <= kMaxPanelTiles; ++pt) {
+    if (cost_of[pt] * 100 <= best_cost * 101) {
       best = pt;
-      best_grid = static_cast<int>(G);
+      break;
     }
   }
-  *grid_out = best_grid;
+  *grid_out = grid_of[best];
   return best;
 }
 
@@ -401,13 +427,24 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   fa.partials = reinterpret_cast<float4*>(ws + L.partials);
   fa.zt = reinterpret_cast<float*>(ws + L.zt);
   fa.status = reinterpret_cast<int*>(ws);
+  fa.wait_ns = kWaitLimitNs;
+  fa.drop_kb = -1;
+  // Fault injection for the bounded-wait test (tests/test_gpu_faults.py):
+  // FLCE_TEST_DROP_KBLOCK names a K slice whose loads the forward never issues,
+  // and FLCE_TEST_WAIT_MS shortens every wait of that launch.
+  if (const char* e = getenv("FLCE_TEST_DROP_KBLOCK")) fa.drop_kb = atoi(e);
+  if (const char* e = getenv("FLCE_TEST_WAIT_MS")) {
+    const long long ms = atoll(e);
+    if (ms > 0) fa.wait_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+  }
   int v;
   if (tensor_path(p)) {
     const CUtensorMapDataType dt = map_type(p);
     fa.n_blocks = static_cast<int>(ceil_div(N, kPairM));
     fa.v_tiles = static_cast<int>(ceil_div(V, kBN));
+    fa.group_blocks = group_blocks_for(fa.n_blocks, H);
     int grid = 1;
-    fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.v_tiles, d.pairs, &grid);
+    fa.panel_tiles = choose_panel_tiles(fa.n_blocks, fa.group_blocks, fa.v_tiles, d.pairs, &grid);
     fa.num_panels = static_cast<int>(ceil_div(fa.v_tiles, fa.panel_tiles));
     fa.num_units = fa.num_panels * fa.n_blocks;
     CUtensorMap tm_h, tm_w;
@@ -660,8 +697,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.row0 = row0;
       da.n_blocks = static_cast<int>(ceil_div(rows, kPairM));
       da.v_tiles = static_cast<int>(ceil_div(V, kBN));
+      da.group_blocks = group_blocks_for(da.n_blocks, H);
       int grid = 1;
-      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.v_tiles, d.pairs, &grid);
+      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.group_blocks, da.v_tiles, d.pairs, &grid);
       da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
       da.num_units = da.num_panels * da.n_blocks;
       da.bias_blk0 = row0 / kBM;

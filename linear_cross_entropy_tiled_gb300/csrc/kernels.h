@@ -40,9 +40,28 @@ constexpr int kSimtThreads = 256;
 // Per (panel, row) partial state of the online log-sum-exp:
 // x = running max m, y = sum exp(z - m), z = sum z exp(z - m), w = argmax (int bits).
 
+// The vocabulary sweeps (forward, dlogits) hand out units (panel, pair block)
+// in groups of `group_blocks` pair blocks: within a group panel-major, one
+// group after the other. A group's rows of h (group_blocks x 256 x H x 2 bytes,
+// about 32 MB) stay in L2 while the W panels stream through once per group.
+__host__ __device__ inline void decode_unit(int u, int n_blocks, int group_blocks,
+                                            int num_panels, int& panel, int& nb) {
+  const int per_group = group_blocks * num_panels;
+  const int g = u / per_group;
+  const int r = u - g * per_group;
+  const int rest = n_blocks - g * group_blocks;
+  const int gb = rest < group_blocks ? rest : group_blocks;  // the last group may be smaller
+  panel = r / gb;
+  nb = g * group_blocks + (r - panel * gb);
+}
+
 struct FwdArgs {
   int N, H, V;
+  int group_blocks;
   long long vocab_start;       // global id of this call's first vocabulary row
+  unsigned long long wait_ns;  // limit of every bounded wait (kWaitLimitNs unless testing)
+  int drop_kb;                 // fault injection, off (-1) unless testing: the even CTA of pair 0
+                               // arms but never issues the loads of this K slice of its first tile
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
   float scale, softcap, inv_softcap;
   const void* bias;            // dtype of the pass, or nullptr
@@ -134,6 +153,7 @@ struct RowCoefArgs {
 
 struct DsArgs {
   int rows, row0, H, V, V_pad;
+  int group_blocks;
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
   float scale, softcap, inv_softcap;
   const void* bias;

@@ -59,6 +59,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 struct WaitGuard {
   int* status;           // global status word (bit mask of kDevErr*)
   volatile int* abort;   // shared-memory flag, nonzero once any role gave up
+  unsigned long long limit_ns = kWaitLimitNs;
 };
 
 // Waits for the phase of `bar` with parity `parity` to complete.
@@ -70,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*g.abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > g.limit_ns) {
       *g.abort = 1;
       atomicOr(g.status, kDevErrTimeout);
       return false;

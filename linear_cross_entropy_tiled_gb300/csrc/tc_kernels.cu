@@ -381,12 +381,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = tc_setup(s, warp);
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const WaitGuard g{a.status, s.abort};
+  const WaitGuard g{a.status, s.abort, a.wait_ns};
   const int kblocks = (a.H + kBK - 1) / kBK;
 
   auto for_each_tile = [&](auto&& f) {
     for (int u = pair; u < a.num_units; u += npairs) {
-      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      int panel, nb;
+      decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
       for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
@@ -401,6 +402,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_w = l2_policy_evict_normal();
       producer_role(s, g, [&](int, int) { return kblocks; }, rank == 0, for_each_tile,
                     [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      // Fault injection for the bounded-wait test: the stage is armed
+                      // but its loads never come, so the MMA's wait must time out.
+                      if (kb == a.drop_kb && pair == 0 && rank == 0 &&
+                          nb == 0 && vt == 0)
+                        return;
                       tma_load_2d_pair(da, &tm_h, bar, kb * kBK, nb * kPairM + rank * kBM, pol_h);
                       tma_load_2d_pair(db, &tm_w, bar, kb * kBK, vt * kBN + rank * kBNHalf, pol_w);
                     });
@@ -415,7 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     uint32_t acc_phase = 0;
     bool dead = false;
     for (int u = pair; u < a.num_units; u += npairs) {
-      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      int panel, nb;
+      decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int row = nb * kPairM + static_cast<int>(rank) * kBM + r;
       const bool row_ok = row < a.N;
       // shard-local target id; an ignored row gets one that never matches a column
@@ -527,7 +534,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 
   auto for_each_tile = [&](auto&& f) {
     for (int u = pair; u < a.num_units; u += npairs) {
-      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      int panel, nb;
+      decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
       for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
@@ -560,7 +568,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     bool dead = false;
     int tile_par = 0;
     for (int u = pair; u < a.num_units; u += npairs) {
-      const int panel = u / a.n_blocks, nb = u - panel * a.n_blocks;
+      int panel, nb;
+      decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int blk_local = nb * 2 + static_cast<int>(rank);  // this CTA's 128-row block
       const int row_local = blk_local * kBM + r;
       const bool row_ok = row_local < a.rows;
