@@ -165,10 +165,22 @@ def cpu_oracle_rate(w: wl.Workload, inputs: dict, target_s: float = 15.0):
                         bias=inputs["bias"], **kw)
         return time.perf_counter() - t0
 
-    n0 = 16
+    # Two-point calibration: every call has a fixed cost (the fp64 conversion of
+    # W) plus a per-row cost. Size the sample so that the timed call takes
+    # about target_s.
+    run(8)  # warm-up: thread pools and the first touch of the grad_weight buffer
+    n0, n1 = 32, 128
     t0 = run(n0)
-    n = int(min(w.N, max(n0, n0 * target_s / max(t0, 1e-3))))
-    t = run(n) if n != n0 else t0
+    t1 = run(n1)
+    per_row = max((t1 - t0) / (n1 - n0), 1e-6)
+    fixed = max(t0 - n0 * per_row, 0.0)
+    n = int(min(w.N, max(n1, (target_s - fixed) / per_row)))
+    t = run(n)
+    for _ in range(2):  # the cost is not quite linear in the rows; refine twice at most
+        if t >= 0.6 * target_s or n >= w.N:
+            break
+        n = int(min(w.N, n * target_s / max(t, 1e-3)))
+        t = run(n)
     return n / t, n, t, os.cpu_count() or 1
 
 
