@@ -184,6 +184,15 @@ def cpu_oracle_rate(w: wl.Workload, inputs: dict, target_s: float = 15.0):
     return n / t, n, t, os.cpu_count() or 1
 
 
+def workload_config(w: wl.Workload) -> dict:
+    """The `config` object of the JSON line: the same for both arms."""
+    return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "bias": w.bias,
+            "targets": w.targets, "ignore_frac": w.ignore_frac,
+            "z_loss_multiplier": w.z_loss_multiplier, "logit_scale": w.logit_scale,
+            "softcap": w.softcap, "reduction": w.reduction, "metrics": w.metrics,
+            "l2": "inputs larger than L2 (W alone is 1.05 GB); no flush"}
+
+
 def reference_main(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -211,7 +220,7 @@ def reference_main(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "sample_rows": n},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -377,11 +386,7 @@ def ours_main(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; inputs generated on the host)",
-            "config": {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "bias": w.bias,
-                       "targets": w.targets, "ignore_frac": w.ignore_frac,
-                       "z_loss_multiplier": w.z_loss_multiplier, "logit_scale": w.logit_scale,
-                       "softcap": w.softcap, "reduction": w.reduction, "metrics": w.metrics,
-                       "l2": "inputs larger than L2 (W alone is 1.05 GB); no flush"},
+            "config": workload_config(w),
             "tflops": tflops, "tflops_per_gpu": tflops,
             "frac_of_peak": {"bf16_burst": tflops / peaks["bf16_burst"],
                              "bf16_sustained": tflops / peaks["bf16_sustained"],
