@@ -234,8 +234,8 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
  * this library's own.
  *
  * Who needs it. Some callers cannot call cudaMalloc or any allocator:
- * - code inside a CUDA-graph capture or a runtime that forbids allocation on
- *   the hot path;
+ * - frameworks that forbid allocation on the hot path once their memory
+ *   plan is fixed;
  * - runtimes that own every byte of device memory through a fixed arena;
  * - plain C hosts that only hold pointers to tensors they already have.
  *

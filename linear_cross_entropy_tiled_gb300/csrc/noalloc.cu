@@ -2,9 +2,10 @@
 // device memory.
 //
 // Some callers cannot call cudaMalloc or any allocator of their own. Examples
-// are code running inside a CUDA-graph capture that forbids allocation, a
-// runtime that owns every byte of device memory through a fixed arena, and
-// C hosts that only hand over pointers to tensors they already have. This
+// are a training loop whose framework forbids allocation once its memory plan
+// is fixed, a runtime that owns every byte of device memory through a fixed
+// arena, and C hosts that only hand over pointers to tensors they already
+// have. This
 // entry point runs the same kernels as flce_forward. It takes its scratch
 // memory (the per-panel partial states, the target logits and the block sums)
 // from a fixed array that lives in this library's device image, not from a

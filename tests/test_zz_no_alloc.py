@@ -1,8 +1,8 @@
 """flce_forward_noalloc: the forward for callers that cannot allocate device memory.
 
-Some callers cannot call cudaMalloc: code under a graph capture that forbids
-allocation, runtimes that hand out memory only from a fixed arena, plain C
-hosts holding only their tensors' pointers. For them the library keeps the
+Some callers cannot call cudaMalloc: frameworks that forbid allocation once
+their memory plan is fixed, runtimes that hand out memory only from a fixed
+arena, plain C hosts holding only their tensors' pointers. For them the library keeps the
 forward scratch in one fixed device array of its own instead of a caller
 workspace. This test calls that entry point through the C ABI twice in a row,
 on different inputs, so stale scratch would show. It compares each result
