@@ -112,14 +112,16 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def kernel_flops(name: str, w: wl.Workload, chunk_rows: list[int]) -> float:
-    """Algorithmic FLOPs of one launch of each tensor-core kernel."""
-    N, H, V = w.N, w.H, w.V
-    if name == "flce_fwd_tc":
-        return 2.0 * N * H * V
-    if name in ("flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
-        # one launch per row chunk; the chunks are equal except possibly the last
-        return 2.0 * (N / len(chunk_rows)) * H * V
+def kernel_flops(name: str, w: wl.Workload) -> float:
+    """Algorithmic FLOPs one step spends in each tensor-core kernel.
+
+    Each of the four contractions is 2*N*H*V per step, however it is split
+    into launches (row or vocabulary chunks, vocabulary shards). Divided by the
+    kernel's total time per step this is its throughput; with launches of equal
+    shape it equals FLOPs per launch over the mean launch time.
+    """
+    if name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
+        return 2.0 * w.N * w.H * w.V
     return 0.0
 
 
@@ -234,7 +236,9 @@ def ours_main(args, w):
     import torch.distributed as dist
 
     from linear_cross_entropy_tiled_gb300 import _lib, fused_linear_cross_entropy
-    from linear_cross_entropy_tiled_gb300.functional import flce_backward, flce_forward
+    from linear_cross_entropy_tiled_gb300.functional import (flce_backward, flce_forward,
+                                                             flce_forward_combine,
+                                                             flce_forward_partial)
 
     rank, world, local = dist_env()
     if world > 1:
@@ -243,6 +247,9 @@ def ours_main(args, w):
     dev = torch.device("cuda", local)
     # weak scaling: every rank draws its own batch
     wr = w.replace(seed=w.seed + 7919 * rank)
+    if args.dtype:
+        wr = wr.replace(dtype=args.dtype)
+        w = w.replace(dtype=args.dtype)
     inputs = wl.generate(wr)
 
     def dev_tensor(name):
@@ -261,7 +268,7 @@ def ours_main(args, w):
                          reduction=w.reduction, ignore_index=wl.IGNORE_INDEX,
                          logit_scale=w.logit_scale, softcap=w.softcap,
                          z_loss_multiplier=w.z_loss_multiplier, has_bias=w.bias,
-                         deterministic=w.deterministic)
+                         deterministic=w.deterministic, grad_weight_accum=args.grad_weight_accum)
     fws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD), dtype=torch.uint8, device=dev)
     bws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD), dtype=torch.uint8, device=dev)
     gh, gw = torch.empty_like(h), torch.empty_like(W)
@@ -272,6 +279,36 @@ def ours_main(args, w):
         loss, lse, nc, ent, _ = flce_forward(p, h, W, t, b, return_metrics=w.metrics, workspace=fws)
         flce_backward(p, h, W, t, lse, gl, b, workspace=bws, out=(gh, gw, gb))
         return loss
+
+    if args.vocab_shards > 1:
+        # The work of every rank of a vocabulary-parallel head, run on one GPU:
+        # each shard's sweep, the merge of the gathered states (done once
+        # here; every rank would do it), then each shard's backward with the
+        # merged lse into that rank's own grad_hidden share. The all-gather of
+        # the states and the all-reduce of grad_hidden are collectives between
+        # GPUs and are not part of this single-GPU step. Shard boundaries are
+        # multiples of 8 so every slice of W and b stays 16-byte aligned.
+        R = args.vocab_shards
+        bounds = [min(w.V, (w.V * r // R) // 8 * 8) for r in range(R)] + [w.V]
+        shards = []
+        for v0, v1 in zip(bounds[:-1], bounds[1:]):
+            ps = _lib.FlceParams.from_buffer_copy(p)
+            ps.V, ps.vocab_start, ps.vocab_total = v1 - v0, v0, w.V
+            shards.append((ps, W[v0:v1], None if b is None else b[v0:v1],
+                           torch.empty_like(h), gw[v0:v1], None if gb is None else gb[v0:v1]))
+        sws = torch.empty(max(_lib.workspace_bytes(sp[0], _lib.FLCE_PASS_FORWARD) for sp in shards),
+                          dtype=torch.uint8, device=dev)
+        bws = torch.empty(max(_lib.workspace_bytes(sp[0], _lib.FLCE_PASS_BACKWARD) for sp in shards),
+                          dtype=torch.uint8, device=dev)
+
+        def step():  # noqa: F811
+            states = torch.stack([flce_forward_partial(ps, h, Ws, t, bs, workspace=sws)
+                                  for ps, Ws, bs, _, _, _ in shards])
+            loss, lse, nc, ent = flce_forward_combine(p, states, t, return_metrics=w.metrics,
+                                                      workspace=fws)
+            for ps, Ws, bs, ghs, gws, gbs in shards:
+                flce_backward(ps, h, Ws, t, lse, gl, bs, workspace=bws, out=(ghs, gws, gbs))
+            return loss
 
     def barrier():
         if world > 1:
@@ -312,7 +349,7 @@ def ours_main(args, w):
 
     # ---------------- end to end, host buffers ----------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.vocab_shards == 1:
         hp = h.cpu().pin_memory()
         Wp = W.cpu().pin_memory()
         bp = b.cpu().pin_memory() if b is not None else None
@@ -329,7 +366,8 @@ def ours_main(args, w):
             loss = fused_linear_cross_entropy(
                 hd, Wd, td, bias=bd, ignore_index=wl.IGNORE_INDEX, logit_scale=w.logit_scale,
                 softcap=w.softcap, z_loss_multiplier=w.z_loss_multiplier, reduction=w.reduction,
-                return_metrics=w.metrics, deterministic=w.deterministic)
+                return_metrics=w.metrics, deterministic=w.deterministic,
+                grad_weight_accum_dtype=args.grad_weight_accum)
             if isinstance(loss, tuple):
                 loss = loss[0]
             loss.sum().backward() if w.reduction == "none" else loss.backward()
@@ -359,14 +397,15 @@ def ours_main(args, w):
         peaks = load_peaks()
         flops = w.flops_fwd_bwd
         tflops = flops / (ms * 1e-3) / 1e12
-        chunk_rows = bwd_chunks(p)
         kern = []
         for name, n, tot in kernels:
             per = tot / n if n else 0.0
-            f = kernel_flops(name, w, chunk_rows)
+            f = kernel_flops(name, w)
             kern.append({"name": name, "launches": n, "ms_per_launch": per,
                          "share": tot / max(sum(k[2] for k in kernels), 1e-9),
-                         "tflops": (f / (per * 1e-3) / 1e12) if (f and per) else None})
+                         "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
+        default_variant = args.grad_weight_accum == "fp32" and args.vocab_shards == 1 and \
+            w.dtype == wl.WORKLOADS[w.name].dtype
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None
         roof = None
@@ -375,7 +414,7 @@ def ours_main(args, w):
                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                     "frac": dom["tflops"] / peaks["bf16_sustained"],
                     "peak_kind": f"bf16 sustained ({peaks['source']})",
-                    "traffic": traffic_for(dom["name"], w.name)}
+                    "traffic": traffic_for(dom["name"], w.name) if default_variant else None}
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             rate, n, tcpu, cores = cpu_oracle_rate(w, inputs)
@@ -393,6 +432,8 @@ def ours_main(args, w):
                              "source": peaks["source"]},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "kernels": kern,
+            "variant": {"dtype": w.dtype, "grad_weight_accum": args.grad_weight_accum,
+                        "vocab_shards": args.vocab_shards},
             "logits_bytes_avoided": w.logits_bytes_avoided,
             "peak_device_bytes": int(torch.cuda.max_memory_allocated(dev)),
         }
@@ -401,18 +442,6 @@ def ours_main(args, w):
         dist.barrier()
         dist.destroy_process_group()
     return 0
-
-
-def bwd_chunks(p) -> list[int]:
-    N = p.N
-    if N <= 256:
-        return [N]
-    half = -(-(-(-N // 2)) // 256) * 256
-    rows, r = [], 0
-    while r < N:
-        rows.append(min(half, N - r))
-        r += half
-    return rows
 
 
 def main():
@@ -424,6 +453,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=("bf16", "f16"), default=None,
+                    help="override the workload's 16-bit input dtype")
+    ap.add_argument("--grad-weight-accum", choices=("fp32", "weight"), default="fp32")
+    ap.add_argument("--vocab-shards", type=int, default=1,
+                    help="run the vocabulary-parallel flow with this many shards on one GPU")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
