@@ -206,16 +206,69 @@ FwdLayout fwd_layout(const flce_params* p) {
 }
 
 struct BwdLayout {
-  int64_t chunk, V_pad;
+  bool vocab;               // chunks are column ranges of the vocabulary (else row ranges)
+  int64_t chunk, V_pad;     // rows (or columns) per chunk
+  int64_t ds_ld;            // row stride of the dlogits buffer, in elements
   int nchunks, rowblk, n_rowblocks;
   size_t coef, ds, dw, dh_part, bias_part, total;
 };
+
+// The backward stores dlogits for one chunk at a time, about half of the N x V
+// logits, and contracts it into both gradients. Whatever crosses chunks is
+// summed in an fp32 partial: grad_weight [V, H] when the chunks are row
+// ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
+// chunks the vocabulary when N < V, where that partial is the smaller one:
+// each chunk's grad_weight rows are then complete after one GEMM over all N
+// rows. FLCE_BWD_CHUNKS=rows or =vocab fixes the axis, so that tests reach
+// both schedules at any size; the result is the same either way.
+bool vocab_chunked(const flce_params* p) {
+  if (!tensor_path(p) || p->N == 0) return false;
+  if (const char* env = getenv("FLCE_BWD_CHUNKS")) {
+    if (strcmp(env, "rows") == 0) return false;
+    if (strcmp(env, "vocab") == 0) return true;
+  }
+  return p->N > kPairM && p->N < p->V;
+}
 
 BwdLayout bwd_layout(const flce_params* p) {
   BwdLayout L{};
   const int64_t N = p->N, V = p->V, H = p->H;
   const size_t elem = tensor_path(p) ? 2 : 4;
   L.V_pad = (V + 7) / 8 * 8;
+  L.vocab = vocab_chunked(p);
+  if (L.vocab) {
+    // Two column chunks of whole 256-column tiles, fewer columns per chunk if
+    // N rows of them would pass the 4 GiB cap; then the columns are spread
+    // evenly over the chunks. FLCE_MAX_CHUNK_COLS (a multiple of 256) lowers
+    // the cap, like FLCE_MAX_CHUNK_ROWS for row chunks.
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem)) / kBN * kBN;
+    if (cap < kBN) cap = kBN;
+    if (const char* env = getenv("FLCE_MAX_CHUNK_COLS")) {
+      const long long c = atoll(env) / kBN * kBN;
+      if (c >= kBN && c < cap) cap = c;
+    }
+    int64_t w = ceil_div(ceil_div(V, 2), kBN) * kBN;
+    if (w > cap) w = cap;
+    L.nchunks = static_cast<int>(ceil_div(V, w));
+    L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), kBN) * kBN;
+    L.nchunks = static_cast<int>(ceil_div(V, L.chunk));
+    L.ds_ld = (L.chunk + 7) / 8 * 8;
+    L.rowblk = kBM;
+    L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
+    size_t o = kHeader;
+    L.coef = o;
+    o = align_up(o + size_t(N) * sizeof(float4), 256);
+    L.ds = o;
+    o = align_up(o + size_t(N) * L.ds_ld * elem, 1024);
+    L.dw = o;
+    L.dh_part = o;
+    if (L.nchunks > 1) o = align_up(o + size_t(N) * H * 4, 1024);
+    L.bias_part = o;
+    if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
+    L.total = o;
+    return L;
+  }
+  L.ds_ld = L.V_pad;
   if (N <= kPairM) {
     L.chunk = N;
   } else {
@@ -341,6 +394,51 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
              static_cast<unsigned long long>(outer));
     return FLCE_ERR_CUDA;
   }
+  return FLCE_OK;
+}
+
+// A K-major GEMM operand [rows][k]: the 2-D map with 64 x box_rows boxes.
+int make_k_operand(GemmOperand* op, const void* base, uint64_t k, uint64_t rows, uint64_t row_bytes,
+                   uint32_t box_rows, CUtensorMapDataType dt) {
+  const int v = make_map(&op->map, base, k, rows, row_bytes, kBK, box_rows, dt);
+  op->map3 = op->map;
+  return v;
+}
+
+// An MN-major GEMM operand [k rows][mn cols] of 16-bit elements: the 2-D map
+// with 64 x 64 boxes and, if `view3` and it has two or more full 64-column
+// atoms, the 3-D view of those atoms. Element (x, y, z) of the view is column
+// 64 z + x of row y, so its strides are row_bytes (y) and 128 bytes (z).
+// *atoms is the view's atom count, 0 without a view.
+//
+// The view is taken for B operands only (W in grad_hidden, h in
+// grad_weight). Timed on one GB300 in the full backward at N = 8192, H = 4096
+// and 64128-column vocabulary chunks, it took grad_hidden from 2.80 to 2.76 ms
+// and grad_weight from 3.04 to 3.00 ms per launch. Taking it for the A
+// operand of grad_weight as well (dlogits read transposed, rows 128 KB
+// apart) made grad_weight slower, 3.39 ms.
+int make_mn_operand(GemmOperand* op, int* atoms, const void* base, uint64_t mn, uint64_t k,
+                    uint64_t row_bytes, CUtensorMapDataType dt, bool view3) {
+  int v = make_map(&op->map, base, mn, k, row_bytes, 64, 64, dt);
+  if (v != FLCE_OK) return v;
+  op->map3 = op->map;
+  *atoms = 0;
+  const uint64_t full = mn / 64;
+  if (!view3 || full < 2) return FLCE_OK;
+  const cuuint64_t dims[3] = {64, k, full};
+  const cuuint64_t strides[2] = {row_bytes, 128};
+  const cuuint32_t box[3] = {64, 64, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(&op->map3, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_detail, sizeof(g_detail), "cuTensorMapEncodeTiled (3-D) failed (%d) atoms %llu x %llu",
+             static_cast<int>(r), static_cast<unsigned long long>(full),
+             static_cast<unsigned long long>(k));
+    return FLCE_ERR_CUDA;
+  }
+  *atoms = static_cast<int>(full);
   return FLCE_OK;
 }
 
@@ -678,6 +776,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   da.ds_scale = ds_scale;
   da.ds = ws + L.ds;
   da.bias_part = bias_part;
+  da.bias_ld = static_cast<int>(L.V_pad);
+  da.tgt_base = 0;
   da.status = status;
 
   if (tensor_path(p)) {
@@ -685,12 +785,111 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     const bool f16 = p->dtype == FLCE_F16;
     // fp16 dlogits are stored times S; the contractions multiply by 1/S
     const float* acc_scale = ds_scale != nullptr ? ds_scale + 1 : nullptr;
-    CUtensorMap tm_h, tm_w, tm_w_mn;
+    CUtensorMap tm_h, tm_w;
     if ((v = make_map(&tm_h, hidden, H, N, uint64_t(H) * 2, kBK, kBM, dt)) != FLCE_OK) return v;
     if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
-    if ((v = make_map(&tm_w_mn, weight, H, V, uint64_t(H) * 2, 64, 64, dt)) != FLCE_OK) return v;
     float* dw_part = reinterpret_cast<float*>(ws + L.dw);
-    for (int c = 0; c < L.nchunks; ++c) {
+    const int nchunks_rows = L.vocab ? 0 : L.nchunks;
+    for (int c = 0; L.vocab && c < L.nchunks; ++c) {
+      // Columns [v0, v0 + vc) of the vocabulary, all N rows.
+      const int v0 = static_cast<int>(c * L.chunk);
+      const int vc = static_cast<int>(V - v0 < L.chunk ? V - v0 : L.chunk);
+      const uint8_t* wc = static_cast<const uint8_t*>(weight) + size_t(v0) * H * 2;
+      const uint64_t ds_row_bytes = uint64_t(L.ds_ld) * 2;
+      CUtensorMap tm_wc;
+      if ((v = make_map(&tm_wc, wc, H, vc, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
+      da.rows = N;
+      da.row0 = 0;
+      da.V = vc;
+      da.V_pad = static_cast<int>(L.ds_ld);
+      da.bias = bias != nullptr ? static_cast<const uint8_t*>(bias) + size_t(v0) * 2 : nullptr;
+      da.bias_part = bias_part != nullptr ? bias_part + v0 : nullptr;
+      da.bias_blk0 = 0;
+      da.tgt_base = v0;
+      da.n_blocks = static_cast<int>(ceil_div(N, kPairM));
+      da.v_tiles = static_cast<int>(ceil_div(vc, kBN));
+      da.group_blocks = group_blocks_for(da.n_blocks, H);
+      int grid = 1;
+      da.panel_tiles = choose_panel_tiles(da.n_blocks, da.group_blocks, da.v_tiles, d.pairs, &grid);
+      da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
+      da.num_units = da.num_panels * da.n_blocks;
+      v = launch("flce_dlogits_tc", st, [&] {
+        return launch_ds_tc(tm_h, tm_wc, da, f16, bias != nullptr, p->softcap > 0.f, grid, st);
+      });
+      if (v != FLCE_OK) return v;
+      if (grad_hidden) {
+        // grad_hidden[N, H] (+)= dS[N, vc] (K-major) x W[v0:v0+vc, H] (MN-major). The
+        // first chunk starts the fp32 partial (from the existing gradient when
+        // accumulating), the middle chunks add to it, and the last adds and casts.
+        GemmOperand op_a, op_b;
+        GemmArgs ga{};
+        if ((v = make_k_operand(&op_a, da.ds, vc, N, ds_row_bytes, kBM, dt)) != FLCE_OK) return v;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, wc, H, vc, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+          return v;
+        ga.M = N;
+        ga.N = H;
+        ga.K = vc;
+        ga.m_tiles = static_cast<int>(ceil_div(N, kPairM));
+        ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(vc, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = 1;
+        ga.kb_per_split = ga.k_blocks;
+        ga.a_mn = 0;
+        ga.b_mn = 1;
+        if (L.nchunks == 1)
+          ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
+        else if (c == 0)
+          ga.mode = p->accumulate ? kAddOutToPart : kStorePart;
+        else if (c == L.nchunks - 1)
+          ga.mode = kAddPartToOut;
+        else
+          ga.mode = kAddPart;
+        ga.out = grad_hidden;
+        ga.ld_out = H;
+        ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.ld_part = H;
+        ga.acc_scale = acc_scale;
+        ga.status = status;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+        v = launch("flce_grad_hidden_tc", st,
+                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+        if (v != FLCE_OK) return v;
+      }
+      if (grad_weight) {
+        // grad_weight[v0:v0+vc, H] = dS^T[vc, N] (MN-major) x h[N, H] (MN-major):
+        // complete after this one GEMM, so it goes straight to the output.
+        GemmOperand op_a, op_b;
+        GemmArgs ga{};
+        if ((v = make_mn_operand(&op_a, &ga.a_atoms, da.ds, vc, N, ds_row_bytes, dt, false)) != FLCE_OK)
+          return v;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+          return v;
+        ga.M = vc;
+        ga.N = H;
+        ga.K = N;
+        ga.m_tiles = static_cast<int>(ceil_div(vc, kPairM));
+        ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(N, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = 1;
+        ga.kb_per_split = ga.k_blocks;
+        ga.a_mn = 1;
+        ga.b_mn = 1;
+        ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
+        ga.out = static_cast<uint8_t*>(grad_weight) + size_t(v0) * H * 2;
+        ga.ld_out = H;
+        ga.part = nullptr;
+        ga.ld_part = H;
+        ga.acc_scale = acc_scale;
+        ga.status = status;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+        v = launch("flce_grad_weight_tc", st,
+                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+        if (v != FLCE_OK) return v;
+      }
+    }
+    for (int c = 0; c < nchunks_rows; ++c) {
       const int row0 = static_cast<int>(c * L.chunk);
       const int rows = static_cast<int>(N - row0 < L.chunk ? N - row0 : L.chunk);
       da.rows = rows;
@@ -710,9 +909,11 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       const uint64_t ds_row_bytes = uint64_t(L.V_pad) * 2;
       if (grad_hidden) {
         // grad_hidden[rows, H] = dS[rows, V] (K-major) x W[V, H] (MN-major)
-        CUtensorMap tm_a;
-        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, kBK, kBM, dt)) != FLCE_OK) return v;
+        GemmOperand op_a, op_b;
         GemmArgs ga{};
+        if ((v = make_k_operand(&op_a, da.ds, V, rows, ds_row_bytes, kBM, dt)) != FLCE_OK) return v;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, weight, H, V, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+          return v;
         ga.M = rows;
         ga.N = H;
         ga.K = V;
@@ -735,7 +936,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         const int units = ga.num_tiles * ga.k_splits;
         const int g2 = units < d.pairs ? units : d.pairs;
         v = launch("flce_grad_hidden_tc", st,
-                   [&] { return launch_gemm_tc(tm_a, tm_w_mn, ga, f16, g2, st); });
+                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
         if (ga.k_splits > 1) {
           SplitReduceArgs ra2{};
@@ -755,11 +956,13 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       }
       if (grad_weight) {
         // grad_weight[V, H] (+)= dS^T[V, rows] (MN-major) x h[rows, H] (MN-major)
-        CUtensorMap tm_a, tm_b;
-        if ((v = make_map(&tm_a, da.ds, V, rows, ds_row_bytes, 64, 64, dt)) != FLCE_OK) return v;
-        const void* hc = static_cast<const uint8_t*>(hidden) + size_t(row0) * H * 2;
-        if ((v = make_map(&tm_b, hc, H, rows, uint64_t(H) * 2, 64, 64, dt)) != FLCE_OK) return v;
+        GemmOperand op_a, op_b;
         GemmArgs ga{};
+        if ((v = make_mn_operand(&op_a, &ga.a_atoms, da.ds, V, rows, ds_row_bytes, dt, false)) != FLCE_OK)
+          return v;
+        const void* hc = static_cast<const uint8_t*>(hidden) + size_t(row0) * H * 2;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hc, H, rows, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+          return v;
         ga.M = V;
         ga.N = H;
         ga.K = rows;
@@ -791,7 +994,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.status = status;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
-                   [&] { return launch_gemm_tc(tm_a, tm_b, ga, f16, g2, st); });
+                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
     }

@@ -259,6 +259,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// The same for a 3-D tensor map (coordinates x, y, z from the innermost).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m,
+                                                 uint32_t mbar_cluster_addr, int32_t x, int32_t y,
+                                                 int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_cluster_addr), "r"(x), "r"(y), "r"(z),
+      "l"(policy)
+      : "memory");
+}
+
 // ------------------------------------------------- tcgen05, CTA pairs
 // TMEM allocation for a CTA pair: one warp in each of the two CTAs issues it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kSimtThreads)
     const int rl = r0 + ty * 4 + i;
     const bool row_ok = rl < a.rows;
     const float4 cf = row_ok ? a.coef[a.row0 + rl] : make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
-    const int tgt = __float_as_int(cf.w);
+    const int tgt = __float_as_int(cf.w) - a.tgt_base;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int col = c0 + tx * 4 + j;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kSimtThreads)
     if (tid < T && c0 + tid < a.V) {
       float sum = 0.f;
       for (int i = 0; i < T; ++i) sum += G[i][tid];
-      a.bias_part[static_cast<size_t>(a.bias_blk0 + rb) * a.V_pad + c0 + tid] = sum;
+      a.bias_part[static_cast<size_t>(a.bias_blk0 + rb) * a.bias_ld + c0 + tid] = sum;
     }
   }
 }

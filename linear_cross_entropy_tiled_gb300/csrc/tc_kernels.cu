@@ -486,7 +486,7 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
                                          float (&gout)[32]) {
   float bs[32];
   if (kBias) load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
-  const int tgt = __float_as_int(cf.w);
+  const int tgt = __float_as_int(cf.w) - a.tgt_base;  // no target (-1) stays negative
   const float nlse = -cf.z * kLog2e;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -620,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             if (col < a.V && blk_ok) {
               const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
                               colsum[3 * kBN + j];
-              a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.V_pad + col] = t;
+              a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.bias_ld + col] = t;
             }
           }
         }
@@ -642,7 +642,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 template <typename T>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tm_a3,
+                   const __grid_constant__ CUtensorMap tm_b3, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -654,6 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const int k_blocks = a.k_blocks, kb_per_split = a.kb_per_split;
   const int units = num_tiles * a.k_splits;
   const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
+  const int a_atoms = a.a_atoms, b_atoms = a.b_atoms;
 
   // (split, tile) of every unit of this pair
   auto for_each_tile = [&](auto&& f) {
@@ -670,6 +672,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
+      if (a_atoms > 0) tma_prefetch_desc(&tm_a3);
+      if (b_atoms > 0) tma_prefetch_desc(&tm_b3);
       const uint64_t pol = l2_policy_evict_normal();
       const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
       producer_role(s, g, kblocks_of, rank == 0, for_each_tile,
@@ -678,16 +682,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                       const int m0 = mt * kPairM + m_off, n0 = nt * kBN + n_off;
                       const int k0 = (sp * kb_per_split + kb_rel) * kBK;
                       if (a_mn) {
-                        // [K rows][M cols] in memory: two 64 x 64 boxes cover 128 rows of M
-                        tma_load_2d_pair(da, &tm_a, bar, m0, k0, pol);
-                        tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, k0, pol);
+                        // [K rows][M cols] in memory: the atoms m0/64 and m0/64 + 1 cover
+                        // this CTA's 128 rows of M, one 64 x 64 box each
+                        const int at = m0 >> 6;
+                        if (at + 2 <= a_atoms) {
+                          tma_load_3d_pair(da, &tm_a3, bar, 0, k0, at, pol);
+                        } else {
+                          tma_load_2d_pair(da, &tm_a, bar, m0, k0, pol);
+                          tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, k0, pol);
+                        }
                       } else {
                         tma_load_2d_pair(da, &tm_a, bar, k0, m0, pol);
                       }
                       if (b_mn) {
-                        // [K rows][N cols] in memory: two 64 x 64 boxes cover this CTA's 128 columns
-                        tma_load_2d_pair(db, &tm_b, bar, n0, k0, pol);
-                        tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, k0, pol);
+                        // [K rows][N cols] in memory: two atoms cover this CTA's 128 columns
+                        const int at = n0 >> 6;
+                        if (at + 2 <= b_atoms) {
+                          tma_load_3d_pair(db, &tm_b3, bar, 0, k0, at, pol);
+                        } else {
+                          tma_load_2d_pair(db, &tm_b, bar, n0, k0, pol);
+                          tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, k0, pol);
+                        }
                       } else {
                         tma_load_2d_pair(db, &tm_b, bar, k0, n0, pol);
                       }
@@ -843,11 +858,12 @@ cudaError_t launch_ds_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const 
 }
 
 template <typename T>
-cudaError_t launch_gemm_t(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+cudaError_t launch_gemm_t(const GemmOperand& op_a, const GemmOperand& op_b, const GemmArgs& a,
                           int grid, cudaStream_t st) {
   cudaError_t e = set_smem_attr(gemm_tc_kernel<T>);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<T><<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_a, tm_b, a);
+  gemm_tc_kernel<T><<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(op_a.map, op_b.map, op_a.map3,
+                                                                 op_b.map3, a);
   return cudaGetLastError();
 }
 }  // namespace
@@ -865,10 +881,10 @@ cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const
              : launch_ds_t<__nv_bfloat16>(tm_h, tm_w, a, has_bias, softcap, grid, st);
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+cudaError_t launch_gemm_tc(const GemmOperand& op_a, const GemmOperand& op_b, const GemmArgs& a,
                            bool f16, int grid, cudaStream_t st) {
-  return f16 ? launch_gemm_t<__half>(tm_a, tm_b, a, grid, st)
-             : launch_gemm_t<__nv_bfloat16>(tm_a, tm_b, a, grid, st);
+  return f16 ? launch_gemm_t<__half>(op_a, op_b, a, grid, st)
+             : launch_gemm_t<__nv_bfloat16>(op_a, op_b, a, grid, st);
 }
 
 }  // namespace flce

@@ -45,16 +45,33 @@ def params(**kw):
     return _lib.make_params(**base)
 
 
-def test_workspace_sizes(lib):
+def test_workspace_sizes(lib, monkeypatch):
     p = params(N=8192, H=4096, V=128256, has_bias=True)
     fwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
-    bwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
     assert fwd < 64 << 20                       # a few MB of partial states
-    chunk = 4096 * 128256 * 2                   # one bf16 dlogits chunk of N/2 rows
-    dw = 128256 * 4096 * 4                      # fp32 grad_weight partial
-    dh = 2 * 4096 * 4096 * 4                    # two fp32 K-split partials of grad_hidden
-    assert chunk + dw + dh < bwd < chunk + dw + dh + (64 << 20)
-    assert bwd < 8192 * 128256 * 2 + dw         # never an N x V buffer
+    # N < V: vocabulary chunks. dlogits for all rows and half of the columns
+    # (64128 rounded up to whole 256-column tiles), and the fp32 grad_hidden
+    # partial that crosses the two chunks.
+    bwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
+    chunk = 8192 * 64256 * 2
+    dh = 8192 * 4096 * 4
+    assert chunk + dh < bwd < chunk + dh + (64 << 20)
+    assert bwd < 8192 * 128256 * 2              # never an N x V buffer
+    # row chunks: N/2 rows of dlogits, the fp32 grad_weight partial and two
+    # fp32 K-split partials of grad_hidden
+    monkeypatch.setenv("FLCE_BWD_CHUNKS", "rows")
+    bwd_rows = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
+    chunk = 4096 * 128256 * 2
+    dw = 128256 * 4096 * 4
+    dh = 2 * 4096 * 4096 * 4
+    assert chunk + dw + dh < bwd_rows < chunk + dw + dh + (64 << 20)
+    assert bwd_rows < 8192 * 128256 * 2 + dw
+    monkeypatch.delenv("FLCE_BWD_CHUNKS")
+    # N > V: row chunks by default
+    q = params(N=65536, H=1024, V=32000)
+    chunk = 32768 * 32000 * 2
+    dw = 32000 * 1024 * 4
+    assert chunk + dw < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < chunk + dw + (600 << 20)
     small = params(N=100, H=64, V=50)
     assert _lib.workspace_bytes(small, _lib.FLCE_PASS_BACKWARD) > 0
 

@@ -4,6 +4,8 @@
   fuses the accumulation into weight.grad; here all three gradients support it.
 * grad_weight_accum = weight: grad_weight accumulated across row chunks in the
   weight dtype ("Chunked Linear Loss", "Weight-gradient accumulation dtype").
+  Vocabulary chunks finish each grad_weight row in one GEMM, so the option
+  only changes the row-chunk schedule.
 * vocabulary shards: flce_forward_partial per shard, flce_forward_combine, and
   the backward of each shard with the combined lse. The metrics are sums that
   recombine across ranks (fused-linear-ce README, "Metrics for free").
@@ -42,14 +44,20 @@ def dev_tensor(x, dtype):
     return torch.from_numpy(x).cuda()
 
 
-@pytest.mark.parametrize("dtype,N,H,V,chunk_cap", [
-    ("bf16", 600, 256, 16500, None),   # grad_hidden with 2 K splits, 2 chunks
-    ("bf16", 700, 136, 900, "256"),    # 3 chunks
-    ("f32", 150, 64, 700, None),
+@pytest.mark.parametrize("dtype,N,H,V,axis,chunk_cap", [
+    ("bf16", 600, 256, 16500, "rows", None),    # grad_hidden with 2 K splits, 2 row chunks
+    ("bf16", 700, 136, 900, "rows", "256"),     # 3 row chunks
+    ("bf16", 600, 256, 16500, "vocab", None),   # 2 vocabulary chunks
+    ("bf16", 700, 136, 900, "vocab", "256"),    # 4 vocabulary chunks
+    ("bf16", 200, 64, 250, "vocab", None),      # 1 vocabulary chunk (V < 256)
+    ("f32", 150, 64, 700, None, None),
 ])
-def test_accumulate_into_existing_gradients(dtype, N, H, V, chunk_cap, monkeypatch):
+def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap, monkeypatch):
+    if axis:
+        monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
     if chunk_cap:
-        monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS", chunk_cap)
+        monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS" if axis == "rows" else "FLCE_MAX_CHUNK_COLS",
+                           chunk_cap)
     d = small_case(N, H, V, seed=N + V, dtype=dtype, bias=True, ignore_frac=0.1)
     kw = dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3)
     gh, gw, gb = oracle.backward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **kw)
@@ -69,6 +77,8 @@ def test_accumulate_into_existing_gradients(dtype, N, H, V, chunk_cap, monkeypat
 
 
 def test_grad_weight_accumulated_in_weight_dtype(monkeypatch):
+    # Only row chunks accumulate grad_weight across chunks.
+    monkeypatch.setenv("FLCE_BWD_CHUNKS", "rows")
     monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS", "256")
     d = small_case(800, 136, 1100, seed=77, dtype="bf16", bias=True, ignore_frac=0.1)
     kw = dict(reduction="sum", logit_scale=0.8)

@@ -132,30 +132,39 @@ def test_sweep_sampled(V):
     assert_sampled_grad(out["grad_hidden"][rows], gh, "grad_hidden rows")
 
 
-def test_more_than_2_to_the_32_logits():
+def test_more_than_2_to_the_32_logits(monkeypatch):
     """N x V = 65536 x 65537 > 2^32 logits (8.6 GB in bf16, never stored).
 
-    Half the rows would exceed the 4 GiB cap of the dlogits chunk, so the
-    backward runs 3 chunks (32512, 32512 and 512 rows). That drives the fp32
-    grad_weight partial through store, add and add-and-cast at scale. V = 65537
-    leaves one column in the last vocabulary tile.
+    The backward runs both ways, on the same inputs:
+
+    * row chunks: half the rows would pass the 4 GiB cap of the dlogits chunk,
+      so it runs 3 chunks (32512, 32512 and 512 rows), and the dlogits chunk
+      holds more than 2^31 elements. That drives the fp32 grad_weight partial
+      through store, add and add-and-cast at scale;
+    * vocabulary chunks: 3 chunks of 22016, 22016 and 21505 columns, with the
+      fp32 grad_hidden partial through the same three steps.
+
+    V = 65537 leaves one column in the last vocabulary tile.
     """
     w = wl.Workload("big_nv", N=65536, H=256, V=65537, bias=True, ignore_frac=0.05,
                     reduction="mean", z_loss_multiplier=1e-4, seed=4242)
     d = wl.generate(w)
-    out = run_gpu(d, "bf16", kw_of(w))
-    assert out["status_fwd"] == 0 and out["status_bwd"] == 0
     okw = oracle_kw(w)
     ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"],
                          reduction=w.reduction, row_block=2048, **okw)
-    assert_loss_close(out["loss"], ref["loss"], "bf16")
-    assert_lse_close(out["lse"], ref["lse"])
-    rows = sample_rows(w.N, [32768], seed=1)
+    rows = sample_rows(w.N, [32512, 65024], seed=1)
     gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows, bias=d["bias"],
                                  reduction=w.reduction, **okw)
-    assert_sampled_grad(out["grad_hidden"][rows], gh, "grad_hidden rows")
     J = sample_vocab(w.V, d["targets"], seed=2)
+    J = np.union1d(J, [22015, 22016, 44031, 44032])
     gw, gb = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
                                      bias=d["bias"], reduction=w.reduction, **okw)
-    assert_sampled_grad(out["grad_weight"][J], gw, "grad_weight rows")
-    assert_sampled_grad(out["grad_bias"][J], gb, "grad_bias entries")
+    for axis in ("rows", "vocab"):
+        monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
+        out = run_gpu(d, "bf16", kw_of(w))
+        assert out["status_fwd"] == 0 and out["status_bwd"] == 0
+        assert_loss_close(out["loss"], ref["loss"], "bf16")
+        assert_lse_close(out["lse"], ref["lse"])
+        assert_sampled_grad(out["grad_hidden"][rows], gh, f"grad_hidden rows ({axis})")
+        assert_sampled_grad(out["grad_weight"][J], gw, f"grad_weight rows ({axis})")
+        assert_sampled_grad(out["grad_bias"][J], gb, f"grad_bias entries ({axis})")

@@ -2,8 +2,9 @@
 
 The shapes are small enough for the oracle to finish in seconds. They still
 span several 128-row, 256-vocabulary and 64-deep tiles, and they have ragged
-tails in N, V and H. The backward always runs as two or more row chunks, so
-the fp32 grad_weight partial path is exercised.
+tails in N, V and H. Each 16-bit case runs the backward both ways: as row
+chunks (the fp32 grad_weight partial crosses them) and as vocabulary chunks
+(the fp32 grad_hidden partial crosses them). FLCE_BWD_CHUNKS picks the axis.
 """
 import os
 
@@ -70,8 +71,10 @@ BF16_CASES = [
 ]
 
 
+@pytest.mark.parametrize("axis", ["rows", "vocab"])
 @pytest.mark.parametrize("N,H,V,bias,ign,kw", BF16_CASES)
-def test_bf16_parity(N, H, V, bias, ign, kw):
+def test_bf16_parity(N, H, V, bias, ign, kw, axis, monkeypatch):
+    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
     d = small_case(N, H, V, seed=N * 7 + V, dtype="bf16", bias=bias, ignore_frac=ign,
                    hidden_std=1.0)
     d = with_argmax_targets(d, kw)
@@ -102,17 +105,26 @@ F16_CASES = [
 ]
 
 
+@pytest.mark.parametrize("axis", ["rows", "vocab"])
 @pytest.mark.parametrize("N,H,V,bias,ign,kw", F16_CASES)
-def test_f16_parity(N, H, V, bias, ign, kw):
+def test_f16_parity(N, H, V, bias, ign, kw, axis, monkeypatch):
+    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
     d = small_case(N, H, V, seed=N * 5 + V, dtype="f16", bias=bias, ignore_frac=ign)
     d = with_argmax_targets(d, kw)
     gl = np.random.default_rng(2).standard_normal(N).astype(np.float32) if kw["reduction"] == "none" else 1.0
     check_case(d, "f16", kw, grad_loss=gl)
 
 
-def test_three_chunk_backward(monkeypatch):
-    """Force 256-row chunks (3 of them): the grad_weight partial is stored, added to, then cast."""
-    monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS", "256")
+@pytest.mark.parametrize("axis,cap_env", [("rows", "FLCE_MAX_CHUNK_ROWS"),
+                                          ("vocab", "FLCE_MAX_CHUNK_COLS")])
+def test_three_or_more_chunk_backward(axis, cap_env, monkeypatch):
+    """Force 256-row chunks (3 of them) or 256-column chunks (4 of them).
+
+    The fp32 partial that crosses the chunks (grad_weight for rows, grad_hidden
+    for columns) is stored, added to, then added and cast.
+    """
+    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
+    monkeypatch.setenv(cap_env, "256")
     d = small_case(700, 136, 900, seed=11, dtype="bf16", bias=True, ignore_frac=0.1)
     check_case(d, "bf16", dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3))
 
