@@ -209,12 +209,16 @@ struct BwdLayout {
   bool vocab;               // chunks are column ranges of the vocabulary (else row ranges)
   int64_t chunk, V_pad;     // rows (or columns) per chunk
   int64_t ds_ld;            // row stride of the dlogits buffer, in elements
+  int64_t ds_t_ld;          // row stride of the transposed dlogits buffer (tensor path)
   int nchunks, rowblk, n_rowblocks;
-  size_t coef, ds, dw, dh_part, bias_part, total;
+  size_t coef, ds, ds_t, dw, dh_part, bias_part, total;
 };
 
-// The backward stores dlogits for one chunk at a time, about half of the N x V
-// logits, and contracts it into both gradients. Whatever crosses chunks is
+// The backward stores dlogits for one chunk at a time and contracts it into
+// both gradients. The tensor path keeps two copies: row-major for grad_hidden
+// (K = vocabulary) and transposed for grad_weight (K = rows), so that both
+// GEMMs read their dlogits operand K-major. Together the copies hold about
+// half of the N x V logits, and at most 4 GiB. Whatever crosses chunks is
 // summed in an fp32 partial: grad_weight [V, H] when the chunks are row
 // ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
 // chunks the vocabulary when N < V, where that partial is the smaller one:
@@ -237,22 +241,24 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.V_pad = (V + 7) / 8 * 8;
   L.vocab = vocab_chunked(p);
   if (L.vocab) {
-    // Two column chunks of whole 256-column tiles, fewer columns per chunk if
-    // N rows of them would pass the 4 GiB cap; then the columns are spread
-    // evenly over the chunks. FLCE_MAX_CHUNK_COLS (a multiple of 256) lowers
-    // the cap, like FLCE_MAX_CHUNK_ROWS for row chunks.
-    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem)) / kBN * kBN;
+    // Four column chunks of whole 256-column tiles (two copies of a quarter
+    // of the columns), fewer columns per chunk if N rows of them would pass
+    // the 4 GiB cap; then the columns are spread evenly over the chunks.
+    // FLCE_MAX_CHUNK_COLS (a multiple of 256) lowers the cap, like
+    // FLCE_MAX_CHUNK_ROWS for row chunks.
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * 2)) / kBN * kBN;
     if (cap < kBN) cap = kBN;
     if (const char* env = getenv("FLCE_MAX_CHUNK_COLS")) {
       const long long c = atoll(env) / kBN * kBN;
       if (c >= kBN && c < cap) cap = c;
     }
-    int64_t w = ceil_div(ceil_div(V, 2), kBN) * kBN;
+    int64_t w = ceil_div(ceil_div(V, 4), kBN) * kBN;
     if (w > cap) w = cap;
     L.nchunks = static_cast<int>(ceil_div(V, w));
     L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), kBN) * kBN;
     L.nchunks = static_cast<int>(ceil_div(V, L.chunk));
     L.ds_ld = (L.chunk + 7) / 8 * 8;
+    L.ds_t_ld = (N + 7) / 8 * 8;
     L.rowblk = kBM;
     L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
     size_t o = kHeader;
@@ -260,6 +266,8 @@ BwdLayout bwd_layout(const flce_params* p) {
     o = align_up(o + size_t(N) * sizeof(float4), 256);
     L.ds = o;
     o = align_up(o + size_t(N) * L.ds_ld * elem, 1024);
+    L.ds_t = o;
+    o = align_up(o + size_t(L.chunk) * L.ds_t_ld * elem, 1024);
     L.dw = o;
     L.dh_part = o;
     if (L.nchunks > 1) o = align_up(o + size_t(N) * H * 4, 1024);
@@ -269,12 +277,16 @@ BwdLayout bwd_layout(const flce_params* p) {
     return L;
   }
   L.ds_ld = L.V_pad;
+  const int copies = tensor_path(p) ? 2 : 1;
   if (N <= kPairM) {
     L.chunk = N;
   } else {
-    // chunk boundaries fall on 256-row pair blocks
-    const int64_t half = ceil_div(ceil_div(N, 2), kPairM) * kPairM;
-    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem)) / kPairM * kPairM;
+    // chunk boundaries fall on 256-row pair blocks; each copy of dlogits
+    // holds a quarter of the rows (half of them on the fp32 path, which keeps
+    // one copy)
+    const int64_t half = ceil_div(ceil_div(N, 2 * copies), kPairM) * kPairM;
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem * copies)) /
+                  kPairM * kPairM;
     if (cap < kPairM) cap = kPairM;
     // FLCE_MAX_CHUNK_ROWS (a multiple of 256) lowers the row-chunk cap. The
     // work and the result are the same; it is there so tests can reach the
@@ -293,6 +305,9 @@ BwdLayout bwd_layout(const flce_params* p) {
   o = align_up(o + size_t(N) * sizeof(float4), 256);
   L.ds = o;
   o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
+  L.ds_t = o;
+  L.ds_t_ld = (L.chunk + 7) / 8 * 8;
+  if (tensor_path(p)) o = align_up(o + size_t(V) * L.ds_t_ld * elem, 1024);
   L.dw = o;
   if (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
     o = align_up(o + size_t(V) * H * 4, 1024);
@@ -406,25 +421,19 @@ int make_k_operand(GemmOperand* op, const void* base, uint64_t k, uint64_t rows,
 }
 
 // An MN-major GEMM operand [k rows][mn cols] of 16-bit elements: the 2-D map
-// with 64 x 64 boxes and, if `view3` and it has two or more full 64-column
-// atoms, the 3-D view of those atoms. Element (x, y, z) of the view is column
-// 64 z + x of row y, so its strides are row_bytes (y) and 128 bytes (z).
-// *atoms is the view's atom count, 0 without a view.
-//
-// The view is taken for B operands only (W in grad_hidden, h in
-// grad_weight). Timed on one GB300 in the full backward at N = 8192, H = 4096
-// and 64128-column vocabulary chunks, it took grad_hidden from 2.80 to 2.76 ms
-// and grad_weight from 3.04 to 3.00 ms per launch. Taking it for the A
-// operand of grad_weight as well (dlogits read transposed, rows 128 KB
-// apart) made grad_weight slower, 3.39 ms.
+// with 64 x 64 boxes and, when it has two or more full 64-column atoms, the
+// 3-D view of those atoms. Element (x, y, z) of the view is column 64 z + x of
+// row y, so its strides are row_bytes (y) and 128 bytes (z). *atoms is the
+// view's atom count, 0 without a view. The MN-major operands are the B sides
+// of both gradient GEMMs: W in grad_hidden and h in grad_weight.
 int make_mn_operand(GemmOperand* op, int* atoms, const void* base, uint64_t mn, uint64_t k,
-                    uint64_t row_bytes, CUtensorMapDataType dt, bool view3) {
+                    uint64_t row_bytes, CUtensorMapDataType dt) {
   int v = make_map(&op->map, base, mn, k, row_bytes, 64, 64, dt);
   if (v != FLCE_OK) return v;
   op->map3 = op->map;
   *atoms = 0;
   const uint64_t full = mn / 64;
-  if (!view3 || full < 2) return FLCE_OK;
+  if (full < 2) return FLCE_OK;
   const cuuint64_t dims[3] = {64, k, full};
   const cuuint64_t strides[2] = {row_bytes, 128};
   const cuuint32_t box[3] = {64, 64, 2};
@@ -806,6 +815,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.bias_part = bias_part != nullptr ? bias_part + v0 : nullptr;
       da.bias_blk0 = 0;
       da.tgt_base = v0;
+      da.ds_t = grad_weight != nullptr ? ws + L.ds_t : nullptr;
+      da.ld_t = L.ds_t_ld;
       da.n_blocks = static_cast<int>(ceil_div(N, kPairM));
       da.v_tiles = static_cast<int>(ceil_div(vc, kBN));
       da.group_blocks = group_blocks_for(da.n_blocks, H);
@@ -824,7 +835,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         GemmOperand op_a, op_b;
         GemmArgs ga{};
         if ((v = make_k_operand(&op_a, da.ds, vc, N, ds_row_bytes, kBM, dt)) != FLCE_OK) return v;
-        if ((v = make_mn_operand(&op_b, &ga.b_atoms, wc, H, vc, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, wc, H, vc, uint64_t(H) * 2, dt)) != FLCE_OK)
           return v;
         ga.M = N;
         ga.N = H;
@@ -857,13 +868,14 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         if (v != FLCE_OK) return v;
       }
       if (grad_weight) {
-        // grad_weight[v0:v0+vc, H] = dS^T[vc, N] (MN-major) x h[N, H] (MN-major):
-        // complete after this one GEMM, so it goes straight to the output.
+        // grad_weight[v0:v0+vc, H] = dS^T[vc, N] (K-major, the transposed copy)
+        // x h[N, H] (MN-major): complete after this one GEMM, so it goes
+        // straight to the output.
         GemmOperand op_a, op_b;
         GemmArgs ga{};
-        if ((v = make_mn_operand(&op_a, &ga.a_atoms, da.ds, vc, N, ds_row_bytes, dt, false)) != FLCE_OK)
+        if ((v = make_k_operand(&op_a, da.ds_t, N, vc, uint64_t(L.ds_t_ld) * 2, kBM, dt)) != FLCE_OK)
           return v;
-        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt)) != FLCE_OK)
           return v;
         ga.M = vc;
         ga.N = H;
@@ -874,7 +886,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
         ga.k_splits = 1;
         ga.kb_per_split = ga.k_blocks;
-        ga.a_mn = 1;
+        ga.a_mn = 0;
         ga.b_mn = 1;
         ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
         ga.out = static_cast<uint8_t*>(grad_weight) + size_t(v0) * H * 2;
@@ -902,6 +914,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
       da.num_units = da.num_panels * da.n_blocks;
       da.bias_blk0 = row0 / kBM;
+      da.ds_t = grad_weight != nullptr ? ws + L.ds_t : nullptr;
+      da.ld_t = L.ds_t_ld;
       v = launch("flce_dlogits_tc", st, [&] {
         return launch_ds_tc(tm_h, tm_w, da, f16, bias != nullptr, p->softcap > 0.f, grid, st);
       });
@@ -912,7 +926,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         GemmOperand op_a, op_b;
         GemmArgs ga{};
         if ((v = make_k_operand(&op_a, da.ds, V, rows, ds_row_bytes, kBM, dt)) != FLCE_OK) return v;
-        if ((v = make_mn_operand(&op_b, &ga.b_atoms, weight, H, V, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, weight, H, V, uint64_t(H) * 2, dt)) != FLCE_OK)
           return v;
         ga.M = rows;
         ga.N = H;
@@ -955,13 +969,14 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         }
       }
       if (grad_weight) {
-        // grad_weight[V, H] (+)= dS^T[V, rows] (MN-major) x h[rows, H] (MN-major)
+        // grad_weight[V, H] (+)= dS^T[V, rows] (K-major, the transposed copy)
+        // x h[rows, H] (MN-major)
         GemmOperand op_a, op_b;
         GemmArgs ga{};
-        if ((v = make_mn_operand(&op_a, &ga.a_atoms, da.ds, V, rows, ds_row_bytes, dt, false)) != FLCE_OK)
+        if ((v = make_k_operand(&op_a, da.ds_t, rows, V, uint64_t(L.ds_t_ld) * 2, kBM, dt)) != FLCE_OK)
           return v;
         const void* hc = static_cast<const uint8_t*>(hidden) + size_t(row0) * H * 2;
-        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hc, H, rows, uint64_t(H) * 2, dt, true)) != FLCE_OK)
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hc, H, rows, uint64_t(H) * 2, dt)) != FLCE_OK)
           return v;
         ga.M = V;
         ga.N = H;
@@ -972,7 +987,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.num_tiles = ga.m_tiles * ga.n_tiles;
         ga.k_splits = 1;
         ga.kb_per_split = ga.k_blocks;
-        ga.a_mn = 1;
+        ga.a_mn = 0;
         ga.b_mn = 1;
         // grad_weight across row chunks. fp32: the first chunk starts the fp32
         // partial (from the existing gradient when accumulating), the middle

@@ -160,6 +160,8 @@ struct DsArgs {
   const float4* coef;          // indexed by global row
   const float* ds_scale;       // fp16: power of two that dlogits is stored times; else nullptr
   void* ds;                    // chunk buffer [rows][V_pad] in the input dtype (f32 for fp32)
+  void* ds_t;                  // the same values transposed, [V][ld_t] (16-bit types); or nullptr
+  long long ld_t;              // row stride of ds_t, in elements
   float* bias_part;            // [row blocks][bias_ld], offset to this chunk's first column; or nullptr
   int bias_ld;                 // row stride of bias_part
   int bias_blk0;               // first row block of this chunk

@@ -519,6 +519,29 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
   }
 }
 
+// Stores a warp's 32 rows x 32 columns of dlogits transposed: row v of ds_t
+// holds column v for every row of the chunk. Each lane pair swaps one value,
+// so that every lane writes two neighbouring rows of one column as one 32-bit
+// word and a warp store covers 64 contiguous bytes of two ds_t rows. All 32
+// lanes must call it (it shuffles).
+template <typename T>
+__device__ __forceinline__ void store_ds_t(const float (&g)[32], const DsArgs& a, int col0,
+                                          int row_w, int lane, float ds_mul, bool live) {
+  const bool odd = (lane & 1) != 0;
+  const int row_pair = row_w + (lane & ~1);  // the first of this lane's two rows
+  T* const base = static_cast<T*>(a.ds_t) + row_pair;
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    const float recv = __shfl_xor_sync(kFull, odd ? g[2 * jj] : g[2 * jj + 1], 1);
+    const float lo = odd ? recv : g[2 * jj];
+    const float hi = odd ? g[2 * jj + 1] : recv;
+    const int col = col0 + 2 * jj + (odd ? 1 : 0);
+    if (live && row_pair < a.rows && col < a.V)
+      *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(col) * a.ld_t) =
+          Elem<T>::pack(lo * ds_mul, hi * ds_mul);
+  }
+}
+
 template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
@@ -603,6 +626,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) gv[j] = 0.f;
           }
+          if (a.ds_t != nullptr)
+            store_ds_t<T>(gv, a, col0, row_local - lane, lane, ds_mul, !dead);
           if (a.bias_part != nullptr) {
             const float cs = warp_transpose_sum32(gv, lane);
             colsum[q * kBN + c * 32 + lane] = cs;

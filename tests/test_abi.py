@@ -49,29 +49,34 @@ def test_workspace_sizes(lib, monkeypatch):
     p = params(N=8192, H=4096, V=128256, has_bias=True)
     fwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
     assert fwd < 64 << 20                       # a few MB of partial states
-    # N < V: vocabulary chunks. dlogits for all rows and half of the columns
-    # (64128 rounded up to whole 256-column tiles), and the fp32 grad_hidden
-    # partial that crosses the two chunks.
+    # N < V: vocabulary chunks. Two bf16 copies of dlogits (row-major and
+    # transposed) for all rows and a quarter of the columns (32064 rounded up
+    # to whole 256-column tiles), and the fp32 grad_hidden partial that
+    # crosses the four chunks.
     bwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
-    chunk = 8192 * 64256 * 2
+    chunk = 2 * 8192 * 32256 * 2
     dh = 8192 * 4096 * 4
     assert chunk + dh < bwd < chunk + dh + (64 << 20)
-    assert bwd < 8192 * 128256 * 2              # never an N x V buffer
-    # row chunks: N/2 rows of dlogits, the fp32 grad_weight partial and two
-    # fp32 K-split partials of grad_hidden
+    assert bwd < 8192 * 128256 * 2              # less than one N x V buffer
+    # row chunks: two copies of a quarter of the rows, the fp32 grad_weight
+    # partial and two fp32 K-split partials of grad_hidden
     monkeypatch.setenv("FLCE_BWD_CHUNKS", "rows")
     bwd_rows = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
-    chunk = 4096 * 128256 * 2
+    chunk = 2 * 2048 * 128256 * 2
     dw = 128256 * 4096 * 4
-    dh = 2 * 4096 * 4096 * 4
+    dh = 2 * 2048 * 4096 * 4
     assert chunk + dw + dh < bwd_rows < chunk + dw + dh + (64 << 20)
     assert bwd_rows < 8192 * 128256 * 2 + dw
     monkeypatch.delenv("FLCE_BWD_CHUNKS")
     # N > V: row chunks by default
     q = params(N=65536, H=1024, V=32000)
-    chunk = 32768 * 32000 * 2
+    chunk = 2 * 16384 * 32000 * 2
     dw = 32000 * 1024 * 4
-    assert chunk + dw < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < chunk + dw + (600 << 20)
+    assert chunk + dw < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < chunk + dw + (300 << 20)
+    # the fp32 path keeps one copy of half of the rows
+    f = params(N=4096, H=1024, V=3000, dtype=_lib.FLCE_F32)
+    chunk = 2048 * 3000 * 4
+    assert chunk < _lib.workspace_bytes(f, _lib.FLCE_PASS_BACKWARD) < chunk + (64 << 20)
     small = params(N=100, H=64, V=50)
     assert _lib.workspace_bytes(small, _lib.FLCE_PASS_BACKWARD) > 0
 

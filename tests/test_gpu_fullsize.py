@@ -137,11 +137,11 @@ def test_more_than_2_to_the_32_logits(monkeypatch):
 
     The backward runs both ways, on the same inputs:
 
-    * row chunks: half the rows would pass the 4 GiB cap of the dlogits chunk,
-      so it runs 3 chunks (32512, 32512 and 512 rows), and the dlogits chunk
-      holds more than 2^31 elements. That drives the fp32 grad_weight partial
-      through store, add and add-and-cast at scale;
-    * vocabulary chunks: 3 chunks of 22016, 22016 and 21505 columns, with the
+    * row chunks: a quarter of the rows would pass the 4 GiB cap of the two
+      dlogits copies, so it runs 5 chunks (4 of 16128 rows, then 1024). That
+      drives the fp32 grad_weight partial through store, add and add-and-cast
+      at scale;
+    * vocabulary chunks: 5 chunks (4 of 13312 columns, then 12289), with the
       fp32 grad_hidden partial through the same three steps.
 
     V = 65537 leaves one column in the last vocabulary tile.
@@ -152,11 +152,11 @@ def test_more_than_2_to_the_32_logits(monkeypatch):
     okw = oracle_kw(w)
     ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"],
                          reduction=w.reduction, row_block=2048, **okw)
-    rows = sample_rows(w.N, [32512, 65024], seed=1)
+    rows = sample_rows(w.N, [16128, 32256, 64512], seed=1)
     gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows, bias=d["bias"],
                                  reduction=w.reduction, **okw)
     J = sample_vocab(w.V, d["targets"], seed=2)
-    J = np.union1d(J, [22015, 22016, 44031, 44032])
+    J = np.union1d(J, [13311, 13312, 26623, 26624, 53247, 53248])
     gw, gb = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
                                      bias=d["bias"], reduction=w.reduction, **okw)
     for axis in ("rows", "vocab"):
