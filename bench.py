@@ -404,8 +404,11 @@ def ours_main(args, w):
             kern.append({"name": name, "launches": n, "ms_per_launch": per,
                          "share": tot / max(sum(k[2] for k in kernels), 1e-9),
                          "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
+        # the committed DRAM counts hold for the default schedule only
         default_variant = args.grad_weight_accum == "fp32" and args.vocab_shards == 1 and \
-            w.dtype == wl.WORKLOADS[w.name].dtype
+            w.dtype == wl.WORKLOADS[w.name].dtype and not any(
+                os.environ.get(k) for k in ("FLCE_BWD_CHUNKS", "FLCE_MAX_CHUNK_ROWS",
+                                            "FLCE_MAX_CHUNK_COLS"))
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None
         roof = None
