@@ -28,6 +28,10 @@ constexpr int kStageA = kBM * kBK * 2;           // 16 KB
 constexpr int kStageB = kBNHalf * kBK * 2;       // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;   // 32 KB per CTA
 constexpr int kTcThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// The dlogits kernel has two epilogue warps per TMEM lane quarter (warps 2-9),
+// each on half of a tile's 256 columns: its epilogue (exp, softcap, two
+// stores, bias sums) outlasts the MMAs of a tile when H is small.
+constexpr int kDsThreads = 320;
 constexpr int kTmemCols = 512;
 // dynamic shared memory: 1 KB alignment slack + stages + 8 KB scratch + control block
 constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;

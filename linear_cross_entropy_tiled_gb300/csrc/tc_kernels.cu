@@ -75,7 +75,7 @@ __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
 // Barriers and TMEM of both CTAs of the pair. The cluster barrier at the end
 // makes every barrier initialised before any remote arrive or
 // remote-signalling TMA can target it.
-__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp) {
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_warps = 4) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);   // even CTA: its own arrive.expect_tx
@@ -83,7 +83,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);   // the MMA commit, multicast to both CTAs
-      mbar_init(&s.tempty[i], 8);  // even CTA: 4 epilogue warps x 2 CTAs
+      mbar_init(&s.tempty[i], 2 * epi_warps);  // even CTA: every epilogue warp of both CTAs
     }
     mbar_init(s.mma_done, 1);
     *s.abort = 0;
@@ -554,13 +554,13 @@ __device__ __forceinline__ void store_ds_t(const float (&g)[32], const DsArgs& a
 }
 
 template <typename T, bool kBias, bool kSoftcap>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const DsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tmem = tc_setup(s, warp);
+  const uint32_t tmem = tc_setup(s, warp, 8);
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
@@ -593,9 +593,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     if (lane == 0 && rank == 0)
       mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>);
   } else {
+    // warps 2-5 take columns 0-127 of each tile, warps 6-9 columns 128-255
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..127
+    const int et = threadIdx.x - 64;  // 0..255
     const float ds_mul = a.ds_scale != nullptr ? *a.ds_scale : 1.f;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -616,7 +618,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         dead = !epi_wait_full(s, acc, acc_phase, g, dead);
         const bool ragged = (vt + 1) * kBN > a.V;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int cc = 0; cc < kBN / 64; ++cc) {
+          const int c = half * (kBN / 64) + cc;
           float gv[32];
           const int col0 = vt * kBN + c * 32;
           if (!dead) {
@@ -648,16 +651,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         if (a.bias_part != nullptr) {
           // Every epilogue thread reaches this barrier once per tile, also
           // after an abort, so the barrier cannot hang.
-          named_barrier(1, 128);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = et + h * 128;
-            const int col = vt * kBN + j;
-            if (col < a.V && blk_ok) {
-              const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
-                              colsum[3 * kBN + j];
-              a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.bias_ld + col] = t;
-            }
+          named_barrier(1, 256);
+          const int j = et;
+          const int col = vt * kBN + j;
+          if (col < a.V && blk_ok) {
+            const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
+                            colsum[3 * kBN + j];
+            a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.bias_ld + col] = t;
           }
         }
         tile_par ^= 1;
@@ -889,7 +889,7 @@ cudaError_t launch_ds_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const 
                     : (softcap ? ds_tc_kernel<T, false, true> : ds_tc_kernel<T, false, false>);
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
-  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  k<<<2 * grid, kDsThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
   return cudaGetLastError();
 }
 
