@@ -26,10 +26,11 @@
  * - The forward sweeps vocabulary tiles and keeps an online log-sum-exp
  *   (fused-linear-ce README, "Algorithm").
  * - The backward recomputes each logit tile and forms dlogits from it in
- *   registers (same section). dlogits goes to HBM as bf16 for a bounded row
- *   chunk of at most ceil(N/2) rows (at most ceil(N/2) x V elements, or
- *   fewer when that would exceed 4 GiB), never for all N rows. Two tensor-core
- *   contractions then accumulate grad_hidden = dlogits W and
+ *   registers (same section). dlogits goes to HBM in 16 bits for one chunk
+ *   at a time: a range of vocabulary columns for all rows when N < V, else
+ *   a range of rows. Each chunk is stored row-major and transposed. The two
+ *   copies together hold about half of the N x V logits, and at most 4 GiB.
+ *   Two tensor-core contractions then accumulate grad_hidden = dlogits W and
  *   grad_weight = dlogits^T h, as the quack diff and "Chunked Linear Loss",
  *   section "Gradient handling", do per chunk.
  *
@@ -74,7 +75,23 @@ typedef enum {
 
 typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1, FLCE_NONE = 2 } flce_reduction;
 
-typedef enum { FLCE_PASS_FORWARD = 0, FLCE_PASS_BACKWARD = 1 } flce_pass;
+typedef enum {
+  FLCE_PASS_FORWARD = 0,      /* flce_forward, flce_forward_partial, flce_forward_combine */
+  FLCE_PASS_BACKWARD = 1,     /* flce_backward                                           */
+  FLCE_PASS_CHUNK_LOGITS = 2, /* flce_chunk_logits (the status word only)                */
+  FLCE_PASS_CHUNK_GRADS = 3   /* flce_chunk_grads; N is the largest chunk's row count;
+                                 the same workspace must be passed to every chunk of
+                                 one loss, because it carries the fp32 grad_weight
+                                 partial from chunk to chunk                            */
+} flce_pass;
+
+/* Position of a row chunk in flce_chunk_grads' accumulation of grad_weight. */
+typedef enum {
+  FLCE_CHUNK_ONLY = 0,  /* the loss has one chunk                                  */
+  FLCE_CHUNK_FIRST = 1, /* first of several chunks                                 */
+  FLCE_CHUNK_NEXT = 2,  /* neither first nor last                                  */
+  FLCE_CHUNK_LAST = 3   /* last of several chunks: grad_weight is written here     */
+} flce_chunk_phase;
 
 /* Accumulator of grad_weight across row chunks ("Chunked Linear Loss",
  * section "Weight-gradient accumulation dtype"). FP32 keeps an fp32 partial
@@ -262,6 +279,58 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
 int flce_forward_noalloc(const flce_params* p, const void* hidden, const void* weight,
                          const void* bias, const int64_t* targets, float* loss, float* lse,
                          int64_t* num_correct, float* entropy_sum, flce_stream_t stream);
+
+/*
+ * Generic chunked linear loss ("Chunked Linear Loss": sections "Why chunk the
+ * projection?", "What is fused?", "Loss function contract"). For a loss that
+ * the caller evaluates one row chunk at a time, the library runs the parts
+ * the strategy owns there: the projection of the chunk, and the folding of
+ * the chunk's logits gradient into grad_input and grad_weight. Between the two
+ * calls the caller's own code turns the logits chunk into the chunk's loss and
+ * dlogits. Only one chunk of logits exists at a time.
+ *
+ * For one row chunk hidden[N,H] (N = p->N rows), with W[V,H]:
+ *
+ * flce_chunk_logits:  logits[r][v] = sum_k hidden[r][k] W[v][k]
+ *   - Written in the input dtype, from fp32 accumulation. bf16 and fp16 use
+ *     the tcgen05 GEMM; fp32 uses the SIMT path.
+ *   - `logits` is device memory of N rows of ld_logits elements.
+ *     ld_logits >= V and ld_logits % 8 == 0. The tensor path may write up to
+ *     round_up(V, 8) elements of a row.
+ *   - The workspace holds the status word: FLCE_PASS_CHUNK_LOGITS bytes.
+ *   - Of p, only N, H, V and dtype matter here; the other fields must still
+ *     pass the usual checks.
+ *
+ * flce_chunk_grads:
+ *   grad_hidden[r][k]  = sum_v dlogits[r][v] W[v][k]        (the chunk's rows)
+ *   grad_weight[v][k] += sum_r dlogits[r][v] hidden[r][k]   (over all chunks)
+ *   - dlogits is device memory of N rows of ld_dlogits elements in the input
+ *     dtype (ld_dlogits >= V, ld_dlogits % 8 == 0), as the caller's loss
+ *     returned it.
+ *   - grad_hidden points to the chunk's rows. It is overwritten, or added to
+ *     when p->accumulate is 1. NULL skips it.
+ *   - grad_weight (V x H) is summed over the chunks of one loss, which the
+ *     caller numbers with `phase`:
+ *     - with p->grad_weight_accum = FLCE_ACCUM_FP32 (the default, "Chunked
+ *       Linear Loss", "Weight-gradient accumulation dtype") the sum runs in
+ *       an fp32 partial in the workspace. FIRST starts it (from grad_weight
+ *       when p->accumulate is 1), NEXT adds, and LAST adds and writes
+ *       grad_weight. With ONLY, grad_weight is written (or added to) directly;
+ *     - with FLCE_ACCUM_WEIGHT every chunk after the first adds into
+ *       grad_weight in the weight dtype.
+ *     NULL skips it.
+ *   - N must be at least 1.
+ *   - The workspace holds FLCE_PASS_CHUNK_GRADS bytes, queried with the
+ *     largest chunk's N. The same workspace must go to every chunk of one
+ *     loss, in order, on one stream.
+ *   - Errors: as for flce_backward.
+ */
+int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weight, void* logits,
+                      int64_t ld_logits, void* workspace, size_t ws_bytes, flce_stream_t stream);
+
+int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,
+                     const void* dlogits, int64_t ld_dlogits, int32_t phase, void* grad_hidden,
+                     void* grad_weight, void* workspace, size_t ws_bytes, flce_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns the device-detected status of the last

@@ -5,10 +5,12 @@ include/flce.h and ``_lib`` binds it with ctypes. ``functional`` wraps it for
 PyTorch tensors and autograd. Importing this package loads nothing: the
 library is loaded on the first call, and that call raises if it is missing.
 """
+from .chunked import autograd_loss_and_logits_grad, chunked_linear_loss  # noqa: F401
 from .functional import (  # noqa: F401
     flce_backward, flce_forward, flce_forward_combine, flce_forward_partial,
     fused_linear_cross_entropy,
 )
 
 __all__ = ["fused_linear_cross_entropy", "flce_forward", "flce_backward",
-           "flce_forward_partial", "flce_forward_combine"]
+           "flce_forward_partial", "flce_forward_combine", "chunked_linear_loss",
+           "autograd_loss_and_logits_grad"]

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
 
 FLCE_F32, FLCE_BF16, FLCE_F16 = 0, 1, 2
 FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
-FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD = 0, 1
+FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD, FLCE_PASS_CHUNK_LOGITS, FLCE_PASS_CHUNK_GRADS = 0, 1, 2, 3
+FLCE_CHUNK_ONLY, FLCE_CHUNK_FIRST, FLCE_CHUNK_NEXT, FLCE_CHUNK_LAST = 0, 1, 2, 3
 FLCE_ACCUM_FP32, FLCE_ACCUM_WEIGHT = 0, 1
 ACCUM_DTYPES = {"fp32": FLCE_ACCUM_FP32, "weight": FLCE_ACCUM_WEIGHT}
 REDUCTIONS = {"sum": FLCE_SUM, "mean": FLCE_MEAN, "none": FLCE_NONE}
@@ -30,7 +31,7 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_forward", "flce_backward", "flce_check_status",
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
-    "flce_forward_partial", "flce_forward_combine",
+    "flce_forward_partial", "flce_forward_combine", "flce_chunk_logits", "flce_chunk_grads",
 )
 
 
@@ -105,6 +106,11 @@ def load() -> ctypes.CDLL:
     lib.flce_forward_partial.restype = ctypes.c_int
     lib.flce_forward_combine.argtypes = [P, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_combine.restype = ctypes.c_int
+    lib.flce_chunk_logits.argtypes = [P, vp, vp, vp, ctypes.c_int64, vp, sz, vp]
+    lib.flce_chunk_logits.restype = ctypes.c_int
+    lib.flce_chunk_grads.argtypes = [P, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp, sz,
+                                     vp]
+    lib.flce_chunk_grads.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
     lib.flce_error_string.argtypes = [ctypes.c_int]
@@ -195,6 +201,19 @@ def backward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: in
                  ws_bytes: int, stream: int) -> int:
     return load().flce_backward(ctypes.byref(p), hidden, weight, bias, targets, lse, grad_loss,
                                 grad_hidden, grad_weight, grad_bias, ws, ws_bytes, stream)
+
+
+def chunk_logits_raw(p: FlceParams, hidden: int, weight: int, logits: int, ld_logits: int,
+                     ws: int, ws_bytes: int, stream: int) -> int:
+    return load().flce_chunk_logits(ctypes.byref(p), hidden, weight, logits, ld_logits, ws,
+                                    ws_bytes, stream)
+
+
+def chunk_grads_raw(p: FlceParams, hidden: int, weight: int, dlogits: int, ld_dlogits: int,
+                    phase: int, grad_hidden: int, grad_weight: int, ws: int, ws_bytes: int,
+                    stream: int) -> int:
+    return load().flce_chunk_grads(ctypes.byref(p), hidden, weight, dlogits, ld_dlogits, phase,
+                                   grad_hidden, grad_weight, ws, ws_bytes, stream)
 
 
 def check_status(ws: int, stream: int) -> int:

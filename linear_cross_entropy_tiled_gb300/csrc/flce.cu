@@ -457,6 +457,26 @@ CUtensorMapDataType map_type(const flce_params* p) {
   return p->dtype == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
+// Workspace of flce_chunk_grads: the status header, the fp32 grad_weight
+// partial that crosses row chunks, and the K-split partials of grad_hidden.
+// The two partials exist on the tensor path only; with
+// grad_weight_accum = weight the chunks accumulate in grad_weight itself.
+struct ChunkLayout {
+  size_t dw_part, dh_part, total;
+};
+
+ChunkLayout chunk_layout(const flce_params* p) {
+  ChunkLayout L{};
+  size_t o = kHeader;
+  L.dw_part = o;
+  if (tensor_path(p) && p->grad_weight_accum == FLCE_ACCUM_FP32)
+    o = align_up(o + size_t(p->V) * p->H * 4, 1024);
+  L.dh_part = o;
+  if (tensor_path(p)) o = align_up(o + size_t(kMaxKSplits) * p->N * p->H * 4, 1024);
+  L.total = o;
+  return L;
+}
+
 }  // namespace
 
 // ===================================================================== ABI
@@ -488,6 +508,10 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes) {
     *bytes = fwd_layout(p).total;
   } else if (pass == FLCE_PASS_BACKWARD) {
     *bytes = bwd_layout(p).total;
+  } else if (pass == FLCE_PASS_CHUNK_LOGITS) {
+    *bytes = kHeader;
+  } else if (pass == FLCE_PASS_CHUNK_GRADS) {
+    *bytes = chunk_layout(p).total;
   } else {
     return FLCE_ERR_INVALID_ARG;
   }
@@ -1070,6 +1094,226 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     ba.grad_bias = grad_bias;
     ba.accumulate = p->accumulate;
     v = launch("flce_bias_reduce", st, [&] { return launch_bias_reduce(ba, p->dtype, st); });
+    if (v != FLCE_OK) return v;
+  }
+  return FLCE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Generic chunked linear loss: the projection of one row chunk and the
+// folding of its dlogits into the gradients ("Chunked Linear Loss").
+int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weight, void* logits,
+                      int64_t ld_logits, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  if (weight == nullptr || (p->N > 0 && (hidden == nullptr || logits == nullptr)))
+    return FLCE_ERR_INVALID_ARG;
+  if (ld_logits < p->V || ld_logits % 8 != 0) return FLCE_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < kHeader) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits) || !aligned16(workspace))
+    return FLCE_ERR_ALIGNMENT;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  if (p->N == 0) return FLCE_OK;
+  const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  if (tensor_path(p)) {
+    // logits[N, V] = h[N, H] (K-major) x W[V, H]^T (K-major B)
+    const CUtensorMapDataType dt = map_type(p);
+    GemmOperand op_a, op_b;
+    GemmArgs ga{};
+    if ((v = make_k_operand(&op_a, hidden, H, N, uint64_t(H) * 2, kBM, dt)) != FLCE_OK) return v;
+    if ((v = make_k_operand(&op_b, weight, H, V, uint64_t(H) * 2, kBNHalf, dt)) != FLCE_OK) return v;
+    ga.M = N;
+    ga.N = V;
+    ga.K = H;
+    ga.m_tiles = static_cast<int>(ceil_div(N, kPairM));
+    ga.n_tiles = static_cast<int>(ceil_div(V, kBN));
+    ga.k_blocks = static_cast<int>(ceil_div(H, kBK));
+    ga.num_tiles = ga.m_tiles * ga.n_tiles;
+    ga.k_splits = 1;
+    ga.kb_per_split = ga.k_blocks;
+    ga.a_mn = 0;
+    ga.b_mn = 0;
+    ga.mode = kStoreOut;
+    ga.out = logits;
+    ga.ld_out = ld_logits;
+    ga.part = nullptr;
+    ga.ld_part = 0;
+    ga.status = reinterpret_cast<int*>(ws);
+    const bool f16 = p->dtype == FLCE_F16;
+    const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+    return launch("flce_chunk_logits_tc", st,
+                  [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+  }
+  SimtGemmArgs ga{};
+  ga.M = N;
+  ga.N = V;
+  ga.K = H;
+  ga.A = static_cast<const float*>(hidden);
+  ga.sam = H;
+  ga.sak = 1;
+  ga.B = static_cast<const float*>(weight);  // B(k, n) = W[n][k]
+  ga.sbk = 1;
+  ga.sbn = H;
+  ga.C = static_cast<float*>(logits);
+  ga.ldc = ld_logits;
+  ga.accumulate = 0;
+  return launch("flce_chunk_logits_simt", st, [&] { return launch_gemm_simt(ga, st); });
+}
+
+int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,
+                     const void* dlogits, int64_t ld_dlogits, int32_t phase, void* grad_hidden,
+                     void* grad_weight, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  if (p->N < 1 || phase < FLCE_CHUNK_ONLY || phase > FLCE_CHUNK_LAST) return FLCE_ERR_INVALID_ARG;
+  if (hidden == nullptr || weight == nullptr || dlogits == nullptr) return FLCE_ERR_INVALID_ARG;
+  if (ld_dlogits < p->V || ld_dlogits % 8 != 0) return FLCE_ERR_INVALID_ARG;
+  const ChunkLayout L = chunk_layout(p);
+  if (workspace == nullptr || ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(dlogits) || !aligned16(workspace) ||
+      (grad_hidden && !aligned16(grad_hidden)) || (grad_weight && !aligned16(grad_weight)))
+    return FLCE_ERR_ALIGNMENT;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  // grad_weight: the chunk's rows add dlogits^T h. Across chunks the fp32
+  // partial is started by the first chunk (from grad_weight when
+  // accumulating), added to by the next ones, and added and cast by the last.
+  // In the weight dtype every chunk after the first adds into grad_weight.
+  const bool later = phase == FLCE_CHUNK_NEXT || phase == FLCE_CHUNK_LAST;
+  if (!tensor_path(p)) {
+    const float* df = static_cast<const float*>(dlogits);
+    if (grad_hidden) {
+      SimtGemmArgs ga{};
+      ga.M = N;
+      ga.N = H;
+      ga.K = V;
+      ga.A = df;
+      ga.sam = ld_dlogits;
+      ga.sak = 1;
+      ga.B = static_cast<const float*>(weight);
+      ga.sbk = H;
+      ga.sbn = 1;
+      ga.C = static_cast<float*>(grad_hidden);
+      ga.ldc = H;
+      ga.accumulate = p->accumulate;
+      v = launch("flce_chunk_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
+      if (v != FLCE_OK) return v;
+    }
+    if (grad_weight) {
+      SimtGemmArgs ga{};
+      ga.M = V;
+      ga.N = H;
+      ga.K = N;
+      ga.A = df;  // A(m, k) = dlogits[k][m]
+      ga.sam = 1;
+      ga.sak = ld_dlogits;
+      ga.B = static_cast<const float*>(hidden);
+      ga.sbk = H;
+      ga.sbn = 1;
+      ga.C = static_cast<float*>(grad_weight);
+      ga.ldc = H;
+      ga.accumulate = (later || p->accumulate) ? 1 : 0;
+      v = launch("flce_chunk_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
+      if (v != FLCE_OK) return v;
+    }
+    return FLCE_OK;
+  }
+  const CUtensorMapDataType dt = map_type(p);
+  const bool f16 = p->dtype == FLCE_F16;
+  const uint64_t dl_row_bytes = uint64_t(ld_dlogits) * 2;
+  if (grad_hidden) {
+    // grad_hidden[N, H] (+)= dlogits[N, V] (K-major) x W[V, H] (MN-major)
+    GemmOperand op_a, op_b;
+    GemmArgs ga{};
+    if ((v = make_k_operand(&op_a, dlogits, V, N, dl_row_bytes, kBM, dt)) != FLCE_OK) return v;
+    if ((v = make_mn_operand(&op_b, &ga.b_atoms, weight, H, V, uint64_t(H) * 2, dt)) != FLCE_OK)
+      return v;
+    ga.M = N;
+    ga.N = H;
+    ga.K = V;
+    ga.m_tiles = static_cast<int>(ceil_div(N, kPairM));
+    ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+    ga.k_blocks = static_cast<int>(ceil_div(V, kBK));
+    ga.num_tiles = ga.m_tiles * ga.n_tiles;
+    ga.k_splits = choose_k_splits(ga.num_tiles, ga.k_blocks, d.pairs);
+    ga.kb_per_split = static_cast<int>(ceil_div(ga.k_blocks, ga.k_splits));
+    ga.a_mn = 0;
+    ga.b_mn = 1;
+    ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
+    ga.out = grad_hidden;
+    ga.ld_out = H;
+    ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+    ga.ld_part = H;
+    ga.split_stride = static_cast<long long>(N) * H;
+    ga.status = status;
+    const int units = ga.num_tiles * ga.k_splits;
+    const int g2 = units < d.pairs ? units : d.pairs;
+    v = launch("flce_chunk_grad_hidden_tc", st,
+               [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+    if (v != FLCE_OK) return v;
+    if (ga.k_splits > 1) {
+      SplitReduceArgs ra{};
+      ra.M = N;
+      ra.N = H;
+      ra.splits = ga.k_splits;
+      ra.accumulate = p->accumulate;
+      ra.f16 = f16 ? 1 : 0;
+      ra.part = ga.part;
+      ra.ld_part = H;
+      ra.split_stride = ga.split_stride;
+      ra.out = grad_hidden;
+      ra.ld_out = H;
+      v = launch("flce_split_reduce", st, [&] { return launch_split_reduce(ra, st); });
+      if (v != FLCE_OK) return v;
+    }
+  }
+  if (grad_weight) {
+    // grad_weight[V, H] (+)= dlogits^T[V, N] (MN-major) x h[N, H] (MN-major)
+    GemmOperand op_a, op_b;
+    GemmArgs ga{};
+    if ((v = make_mn_operand(&op_a, &ga.a_atoms, dlogits, V, N, dl_row_bytes, dt)) != FLCE_OK)
+      return v;
+    ga.a_atoms = 0;  // the A side loads through the 2-D map (the 3-D view does not help it)
+    if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt)) != FLCE_OK)
+      return v;
+    ga.M = V;
+    ga.N = H;
+    ga.K = N;
+    ga.m_tiles = static_cast<int>(ceil_div(V, kPairM));
+    ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
+    ga.k_blocks = static_cast<int>(ceil_div(N, kBK));
+    ga.num_tiles = ga.m_tiles * ga.n_tiles;
+    ga.k_splits = 1;
+    ga.kb_per_split = ga.k_blocks;
+    ga.a_mn = 1;
+    ga.b_mn = 1;
+    if (phase == FLCE_CHUNK_ONLY || p->grad_weight_accum == FLCE_ACCUM_WEIGHT)
+      ga.mode = (later || p->accumulate) ? kAddOutToOut : kStoreOut;
+    else if (phase == FLCE_CHUNK_FIRST)
+      ga.mode = p->accumulate ? kAddOutToPart : kStorePart;
+    else if (phase == FLCE_CHUNK_NEXT)
+      ga.mode = kAddPart;
+    else
+      ga.mode = kAddPartToOut;
+    ga.out = grad_weight;
+    ga.ld_out = H;
+    ga.part = reinterpret_cast<float*>(ws + L.dw_part);
+    ga.ld_part = H;
+    ga.status = status;
+    const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+    v = launch("flce_chunk_grad_weight_tc", st,
+               [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
     if (v != FLCE_OK) return v;
   }
   return FLCE_OK;

@@ -155,3 +155,30 @@ def test_null_and_misaligned_pointers_rejected_before_any_gpu_work(lib):
 
 def test_launch_counter_starts_at_zero_without_work(lib):
     assert _lib.launch_count() >= 0
+
+
+def test_chunked_linear_loss_entry_points_validate_before_any_gpu_work(lib):
+    """flce_chunk_logits / flce_chunk_grads ("Chunked Linear Loss"): sizes and argument checks."""
+    p = params(N=512, H=256, V=1000)
+    assert _lib.workspace_bytes(p, _lib.FLCE_PASS_CHUNK_LOGITS) == 256
+    # fp32 grad_weight partial [V, H] and two K-split partials of grad_hidden [N, H]
+    need = _lib.workspace_bytes(p, _lib.FLCE_PASS_CHUNK_GRADS)
+    assert 1000 * 256 * 4 + 2 * 512 * 256 * 4 < need < 1000 * 256 * 4 + 2 * 512 * 256 * 4 + 8192
+    pw = params(N=512, H=256, V=1000, grad_weight_accum="weight")
+    assert _lib.workspace_bytes(pw, _lib.FLCE_PASS_CHUNK_GRADS) < need - 1000 * 256 * 4 + 4096
+    pf = params(N=512, H=256, V=1000, dtype=_lib.FLCE_F32)
+    assert _lib.workspace_bytes(pf, _lib.FLCE_PASS_CHUNK_GRADS) == 256   # SIMT: no partials
+    fake = 1 << 20
+    # logits row stride below V, or not a multiple of 8
+    assert _lib.chunk_logits_raw(p, fake, fake, fake, 999, fake, 256, 0) == 1
+    assert _lib.chunk_logits_raw(p, fake, fake, fake, 1004, fake, 256, 0) == 1
+    # no workspace; misaligned logits
+    assert _lib.chunk_logits_raw(p, fake, fake, fake, 1000, 0, 256, 0) == 4
+    assert _lib.chunk_logits_raw(p, fake, fake, fake + 8, 1000, fake, 256, 0) == 3
+    # grads: zero rows, bad phase, NULL dlogits, short workspace, misaligned grad_hidden
+    p0 = params(N=0, H=256, V=1000)
+    assert _lib.chunk_grads_raw(p0, fake, fake, fake, 1000, 0, fake, fake, fake, need, 0) == 1
+    assert _lib.chunk_grads_raw(p, fake, fake, fake, 1000, 4, fake, fake, fake, need, 0) == 1
+    assert _lib.chunk_grads_raw(p, fake, fake, 0, 1000, 0, fake, fake, fake, need, 0) == 1
+    assert _lib.chunk_grads_raw(p, fake, fake, fake, 1000, 0, fake, fake, fake, need - 1, 0) == 4
+    assert _lib.chunk_grads_raw(p, fake, fake, fake, 1000, 0, fake + 4, fake, fake, need, 0) == 3

@@ -1,0 +1,116 @@
+"""GPU parity of the generic chunked linear loss ("Chunked Linear Loss") against the fp64 oracle.
+
+The projection of each chunk (flce_chunk_logits) and the folding of the
+caller's logits gradient into grad_input and grad_weight (flce_chunk_grads)
+run in the library's kernels. The loss callbacks below are the caller's code,
+written in torch as a user of the strategy would write them. They see the
+chunk's logits in the input dtype, so the bar is the 16-bit one from
+flce_check (fp32 for fp32 inputs).
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from linear_cross_entropy_tiled_gb300 import autograd_loss_and_logits_grad, chunked_linear_loss
+from linear_cross_entropy_tiled_gb300.workloads import round_to_16bit
+
+from flce_check import TOL, assert_grad_close
+
+pytestmark = pytest.mark.gpu
+
+TDT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+def stored(x, dtype):
+    """(values the GPU holds as float64, device tensor)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "f32":
+        return x.astype(np.float64), torch.from_numpy(x).cuda()
+    bits, vals = round_to_16bit(x, dtype)
+    return vals.astype(np.float64), torch.from_numpy(bits.view(np.int16)).cuda().view(TDT[dtype])
+
+
+def case(N, H, V, dtype, seed):
+    g = np.random.default_rng(seed)
+    X, Xd = stored(g.standard_normal((N, H)), dtype)
+    W, Wd = stored(g.standard_normal((V, H)) / np.sqrt(H), dtype)
+    Y = g.standard_normal((N, V)).astype(np.float32)
+    r = g.uniform(0.5, 1.5, N).astype(np.float32)
+    f = g.uniform(0.5, 1.5, V).astype(np.float32)
+    return X, W, Y, r, f, Xd, Wd
+
+
+def wmse_torch(z, y, rw, fw):
+    """The caller's weighted MSE: loss and logits gradient from one chunk of logits."""
+    err = z.float() - y
+    wgt = rw[:, None] * fw[None, :]
+    return (err * err * wgt).sum(), (2.0 * err * wgt).to(z.dtype)
+
+
+def run(Xd, Wd, Y, r, f, **kw):
+    x = Xd.clone().requires_grad_(True)
+    w = Wd.clone().requires_grad_(True)
+    loss = chunked_linear_loss(x, w, wmse_torch, torch.from_numpy(Y).cuda(),
+                               torch.from_numpy(r).cuda(), torch.from_numpy(f).cuda(), **kw)
+    loss.backward()
+    torch.cuda.synchronize()
+    return float(loss.item()), x.grad.double().cpu().numpy(), w.grad.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype,N,H,V,chunk_rows,accum", [
+    ("bf16", 1000, 264, 700, 256, "fp32"),    # 4 chunks, ragged rows, V and H
+    ("bf16", 300, 128, 520, None, "fp32"),    # one chunk
+    ("bf16", 700, 136, 900, 256, "weight"),   # grad_weight accumulated in bf16
+    ("f16", 600, 200, 640, 256, "fp32"),
+    ("f32", 300, 72, 500, 128, "fp32"),       # the SIMT path
+])
+def test_weighted_mse_matches_the_oracle(dtype, N, H, V, chunk_rows, accum):
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, dtype, seed=N + V)
+    loss, gx, gw = run(Xd, Wd, Y, r, f, chunk_rows=chunk_rows, grad_weight_accum_dtype=accum)
+    ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f,
+                                             chunk_rows=chunk_rows)
+    assert abs(loss - ref) <= TOL[dtype]["loss"] * abs(ref), (loss, ref)
+    assert_grad_close(gx, rx, dtype, "grad_inputs")
+    assert_grad_close(gw, rw, dtype, "grad_weight")
+
+
+def test_cross_entropy_through_the_autograd_adapter_matches_the_fused_oracle():
+    N, H, V = 700, 256, 1100
+    X, W, _, _, _, Xd, Wd = case(N, H, V, "bf16", seed=5)
+    t = np.random.default_rng(6).integers(0, V, N)
+    t[::7] = -100
+    fn = autograd_loss_and_logits_grad(
+        lambda z, tt: F.cross_entropy(z.float(), tt, ignore_index=-100, reduction="sum"))
+    x = Xd.clone().requires_grad_(True)
+    w = Wd.clone().requires_grad_(True)
+    loss = chunked_linear_loss(x, w, fn, torch.from_numpy(t).cuda(), chunk_rows=256)
+    loss.backward()
+    torch.cuda.synchronize()
+    ref = oracle.forward(X, W, t, reduction="sum")
+    rx, rw, _ = oracle.backward(X, W, t, reduction="sum")
+    assert abs(loss.item() - ref["loss"]) <= TOL["bf16"]["loss"] * abs(ref["loss"])
+    assert_grad_close(x.grad.double().cpu().numpy(), rx, "bf16", "grad_inputs")
+    assert_grad_close(w.grad.double().cpu().numpy(), rw, "bf16", "grad_weight")
+
+
+def test_strided_logits_gradient_and_scaled_backward():
+    """A callback gradient in column-major layout is staged; d(3 L) scales both gradients."""
+    N, H, V = 520, 96, 333
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, "bf16", seed=9)
+
+    def fn(z, y, rw, fw):
+        loss, g = wmse_torch(z, y, rw, fw)
+        return loss, g.t().contiguous().t()   # same values, column-major strides
+
+    x = Xd.clone().requires_grad_(True)
+    w = Wd.clone().requires_grad_(True)
+    loss = chunked_linear_loss(x, w, fn, torch.from_numpy(Y).cuda(), torch.from_numpy(r).cuda(),
+                               torch.from_numpy(f).cuda(), chunk_rows=256)
+    (3.0 * loss).backward()
+    torch.cuda.synchronize()
+    ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f, chunk_rows=256)
+    assert abs(loss.item() - ref) <= TOL["bf16"]["loss"] * abs(ref)
+    assert_grad_close(x.grad.double().cpu().numpy(), 3.0 * rx, "bf16", "grad_inputs")
+    assert_grad_close(w.grad.double().cpu().numpy(), 3.0 * rw, "bf16", "grad_weight")
