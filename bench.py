@@ -121,7 +121,8 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
     kernel's total time per step this is its throughput; with launches of equal
     shape it equals FLOPs per launch over the mean launch time.
     """
-    if name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
+    if name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc",
+                "flce_chunk_logits_tc", "flce_chunk_grad_hidden_tc", "flce_chunk_grad_weight_tc"):
         return 2.0 * w.N * w.H * w.V
     return 0.0
 
@@ -168,23 +169,30 @@ def cpu_oracle_rate(w: wl.Workload, inputs: dict, target_s: float = 15.0):
                         bias=inputs["bias"], **kw)
         return time.perf_counter() - t0
 
-    # Two-point calibration: every call has a fixed cost (the fp64 conversion of
-    # W) plus a per-row cost. Size the sample so that the timed call takes
-    # about target_s.
-    run(8)  # warm-up: thread pools and the first touch of the grad_weight buffer
+    n, t = calibrated_rows(run, w.N, target_s)
+    return n / t, n, t, os.cpu_count() or 1
+
+
+def calibrated_rows(run, n_max: int, target_s: float):
+    """Row count whose oracle call takes about target_s; returns (rows, seconds).
+
+    Two-point calibration: every call has a fixed cost (the fp64 conversion of
+    W) plus a per-row cost.
+    """
+    run(8)  # warm-up: thread pools and the first touch of the gradient buffers
     n0, n1 = 32, 128
     t0 = run(n0)
     t1 = run(n1)
     per_row = max((t1 - t0) / (n1 - n0), 1e-6)
     fixed = max(t0 - n0 * per_row, 0.0)
-    n = int(min(w.N, max(n1, (target_s - fixed) / per_row)))
+    n = int(min(n_max, max(n1, (target_s - fixed) / per_row)))
     t = run(n)
     for _ in range(2):  # the cost is not quite linear in the rows; refine twice at most
-        if t >= 0.6 * target_s or n >= w.N:
+        if t >= 0.6 * target_s or n >= n_max:
             break
-        n = int(min(w.N, n * target_s / max(t, 1e-3)))
+        n = int(min(n_max, n * target_s / max(t, 1e-3)))
         t = run(n)
-    return n / t, n, t, os.cpu_count() or 1
+    return n, t
 
 
 def workload_config(w: wl.Workload) -> dict:
@@ -477,12 +485,178 @@ def ours_main(args, w):
     return 0
 
 
+CHUNKED_METRIC = "chunked linear loss (weighted MSE) fwd+bwd tokens/s and TFLOP/s (6NHV)"
+
+
+def regression_config(w) -> dict:
+    return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "chunk_rows": w.chunk_rows,
+            "loss": "row- and feature-weighted squared error, the caller's torch callback",
+            "l2": "inputs larger than L2 (the fp32 target alone is 2.1 GB); no flush"}
+
+
+def chunked_main(args, w):
+    """The generic chunked linear loss on a regression head ("Chunked Linear Loss").
+
+    One step is chunked_linear_loss forward + backward: per row chunk the
+    library's projection, the caller's weighted-MSE callback (torch), and the
+    library's two gradient contractions.
+    """
+    import torch
+    import torch.distributed as dist
+
+    from linear_cross_entropy_tiled_gb300 import _lib, chunked_linear_loss
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.dtype:
+        w = w.replace(dtype=args.dtype)
+    inputs = wl.generate_regression(w.replace(seed=w.seed + 7919 * rank))
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+
+    def mat(name):
+        return torch.from_numpy(inputs[name + "_bits"].view(np.int16)).to(dev).view(tdt)
+
+    x = mat("hidden").requires_grad_(True)
+    Wt = mat("weight").requires_grad_(True)
+    Y = torch.from_numpy(inputs["target"]).to(dev)
+    rw = torch.from_numpy(inputs["row_weight"]).to(dev)
+    fw = torch.from_numpy(inputs["feature_weight"]).to(dev)
+
+    def wmse(z, y, rw_, fw_):
+        # the caller's loss: weighted squared error and its logits gradient
+        err = z.float() - y
+        werr = err * (rw_[:, None] * fw_[None, :])
+        return (werr * err).sum(), (2.0 * werr).to(z.dtype)
+
+    def step(xl, Wl, Yd, rwd, fwd):
+        xl.grad = None
+        Wl.grad = None
+        loss = chunked_linear_loss(xl, Wl, wmse, Yd, rwd, fwd, chunk_rows=w.chunk_rows,
+                                   grad_weight_accum_dtype=args.grad_weight_accum)
+        loss.backward()
+        return loss
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(x, Wt, Y, rw, fw)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    barrier()
+    n_launch0 = _lib.launch_count()
+    _lib.profiling_enable(True)
+    _lib.profiling_read()
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(x, Wt, Y, rw, fw)
+    e1.record(stream)
+    barrier()
+    _lib.profiling_enable(False)
+    launches = _lib.launch_count() - n_launch0
+    kernels = _lib.profiling_read()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    e2e = None
+    if not args.no_e2e:
+        host = [t.detach().cpu().pin_memory() for t in (x, Wt, Y, rw, fw)]
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            xd, Wd, Yd, rwd, fwd = [t.to(dev, non_blocking=True) for t in host]
+            loss = step(xd.requires_grad_(True), Wd.requires_grad_(True), Yd, rwd, fwd)
+            loss_host.copy_(loss.detach().reshape(1), non_blocking=True)
+
+        e2e_steps = max(3, args.steps // 2)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        barrier()
+        ems = f0.elapsed_time(f1) / e2e_steps
+        e2e = {"value": world * w.N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ms_per_step": ems, "steps": e2e_steps,
+               "api": "chunked_linear_loss + backward"}
+
+    if rank == 0:
+        peaks = load_peaks()
+        tflops = w.flops_fwd_bwd / (ms * 1e-3) / 1e12
+        kern = []
+        for name, n, tot in kernels:
+            f = kernel_flops(name, w)
+            kern.append({"name": name, "launches": n, "ms_per_launch": tot / n if n else 0.0,
+                         "share": tot / max(sum(k[2] for k in kernels), 1e-9),
+                         "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
+        kern.sort(key=lambda k: -k["share"])
+        dom = kern[0] if kern else None
+        roof = None
+        if dom is not None and dom["tflops"] is not None:
+            roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
+                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": dom["tflops"] / peaks["bf16_sustained"],
+                    "peak_kind": f"bf16 sustained ({peaks['source']})", "traffic": None}
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            import oracle
+
+            def run(n):
+                t0 = time.perf_counter()
+                oracle.chunked_linear_loss(inputs["hidden"][:n], inputs["weight"],
+                                           oracle.weighted_mse, inputs["target"][:n],
+                                           inputs["row_weight"][:n], inputs["feature_weight"])
+                return time.perf_counter() - t0
+
+            n, tcpu = calibrated_rows(run, w.N, 15.0)
+            cpu = {"value": n / tcpu, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+                   "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64 ({tcpu:.1f} s)"}
+        line = {
+            "metric": CHUNKED_METRIC, "value": world * w.N / (ms * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded; inputs generated on the host)",
+            "config": regression_config(w), "tflops": tflops,
+            "frac_of_peak": {"bf16_burst": tflops / peaks["bf16_burst"],
+                             "bf16_sustained": tflops / peaks["bf16_sustained"],
+                             "source": peaks["source"]},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "kernels": kern,
+            "logits_bytes_avoided": w.logits_bytes_avoided,
+            "peak_device_bytes": int(torch.cuda.max_memory_allocated(dev)),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default=wl.HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default=wl.HEADLINE,
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.REGRESSION_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -494,6 +668,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in wl.REGRESSION_WORKLOADS:
+        if args.impl == "reference" or args.vocab_shards != 1:
+            ap.error("the regression workload runs only --impl ours without --vocab-shards")
+        return chunked_main(args, wl.REGRESSION_WORKLOADS[args.workload])
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_main(args, w)

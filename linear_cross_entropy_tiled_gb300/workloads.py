@@ -209,3 +209,60 @@ def small_case(N: int, H: int, V: int, seed: int, dtype: str = "bf16", bias: boo
         else:
             d["hidden"] = x
     return d
+
+
+@dataclasses.dataclass(frozen=True)
+class RegressionWorkload:
+    """Inputs of the generic chunked linear loss with a row- and feature-weighted MSE.
+
+    "Chunked Linear Loss" ("Direct logits gradients") uses such a loss as its
+    example of a caller-supplied loss and logits gradient. hidden ~ N(0, 1),
+    weight ~ N(0, 1/H) in the 16-bit dtype; target ~ N(0, 1) in fp32, [N, V];
+    row and feature weights ~ U(0.5, 1.5) in fp32.
+    """
+    name: str
+    N: int
+    H: int
+    V: int
+    chunk_rows: int
+    dtype: str = "bf16"
+    seed: int = 0
+
+    def replace(self, **kw) -> "RegressionWorkload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def flops_fwd_bwd(self) -> float:
+        """6*N*H*V: the projection and the two gradient contractions."""
+        return 6.0 * self.N * self.H * self.V
+
+    @property
+    def sixteen_bit(self) -> bool:
+        return self.dtype in ("bf16", "f16")
+
+    @property
+    def logits_bytes_avoided(self) -> int:
+        return self.N * self.V * (4 if self.dtype == "f32" else 2)
+
+
+REGRESSION_WORKLOADS = {
+    "mse_v32768": RegressionWorkload("mse_v32768", N=16384, H=4096, V=32768, chunk_rows=4096,
+                                     seed=2001),
+}
+
+
+def generate_regression(w: RegressionWorkload, threads: Optional[int] = None) -> dict:
+    """hidden / weight (values and 16-bit bits), target [N, V], row_weight [N], feature_weight [V]."""
+    threads = threads or min(16, os.cpu_count() or 1)
+    root = np.random.SeedSequence(w.seed)
+    s_hidden, s_weight, s_target, s_rw, s_fw = root.spawn(5)
+    hidden, hidden_bits = _normal_matrix(s_hidden, w.N, w.H, 1.0, w.dtype, threads)
+    weight, weight_bits = _normal_matrix(s_weight, w.V, w.H, float(1.0 / np.sqrt(w.H)), w.dtype,
+                                         threads)
+    target, _ = _normal_matrix(s_target, w.N, w.V, 1.0, "f32", threads)
+    rw = np.random.Generator(np.random.PCG64(s_rw)).uniform(0.5, 1.5, w.N).astype(np.float32)
+    fw = np.random.Generator(np.random.PCG64(s_fw)).uniform(0.5, 1.5, w.V).astype(np.float32)
+    out = dict(hidden=hidden, weight=weight, target=target, row_weight=rw, feature_weight=fw)
+    if w.sixteen_bit:
+        out.update(hidden_bits=hidden_bits, weight_bits=weight_bits)
+    return out
