@@ -122,7 +122,8 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
     shape it equals FLOPs per launch over the mean launch time.
     """
     if name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc",
-                "flce_chunk_logits_tc", "flce_chunk_grad_hidden_tc", "flce_chunk_grad_weight_tc"):
+                "flce_chunk_logits_tc", "flce_chunk_mse_tc", "flce_chunk_grad_hidden_tc",
+                "flce_chunk_grad_weight_tc"):
         return 2.0 * w.N * w.H * w.V
     return 0.0
 
@@ -488,9 +489,11 @@ def ours_main(args, w):
 CHUNKED_METRIC = "chunked linear loss (weighted MSE) fwd+bwd tokens/s and TFLOP/s (6NHV)"
 
 
-def regression_config(w) -> dict:
+def regression_config(w, torch_loss: bool) -> dict:
+    loss = ("row- and feature-weighted squared error, the caller's torch callback" if torch_loss
+            else "row- and feature-weighted squared error in the projection's epilogue")
     return {"workload": w.name, "N": w.N, "H": w.H, "V": w.V, "chunk_rows": w.chunk_rows,
-            "loss": "row- and feature-weighted squared error, the caller's torch callback",
+            "loss": loss,
             "l2": "inputs larger than L2 (the fp32 target alone is 2.1 GB); no flush"}
 
 
@@ -504,7 +507,7 @@ def chunked_main(args, w):
     import torch
     import torch.distributed as dist
 
-    from linear_cross_entropy_tiled_gb300 import _lib, chunked_linear_loss
+    from linear_cross_entropy_tiled_gb300 import _lib, chunked_linear_loss, weighted_mse_loss
 
     rank, world, local = dist_env()
     if world > 1:
@@ -534,8 +537,14 @@ def chunked_main(args, w):
     def step(xl, Wl, Yd, rwd, fwd):
         xl.grad = None
         Wl.grad = None
-        loss = chunked_linear_loss(xl, Wl, wmse, Yd, rwd, fwd, chunk_rows=w.chunk_rows,
-                                   grad_weight_accum_dtype=args.grad_weight_accum)
+        if args.torch_loss:
+            loss = chunked_linear_loss(xl, Wl, wmse, Yd, rwd, fwd, chunk_rows=w.chunk_rows,
+                                       grad_weight_accum_dtype=args.grad_weight_accum)
+        else:
+            # the same loss inside the projection's epilogue
+            loss = chunked_linear_loss(xl, Wl, weighted_mse_loss(Yd, rwd, fwd),
+                                       chunk_rows=w.chunk_rows,
+                                       grad_weight_accum_dtype=args.grad_weight_accum)
         loss.backward()
         return loss
 
@@ -634,7 +643,7 @@ def chunked_main(args, w):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded; inputs generated on the host)",
-            "config": regression_config(w), "tflops": tflops,
+            "config": regression_config(w, args.torch_loss), "tflops": tflops,
             "frac_of_peak": {"bf16_burst": tflops / peaks["bf16_burst"],
                              "bf16_sustained": tflops / peaks["bf16_sustained"],
                              "source": peaks["source"]},
@@ -665,6 +674,8 @@ def main():
     ap.add_argument("--grad-weight-accum", choices=("fp32", "weight"), default="fp32")
     ap.add_argument("--vocab-shards", type=int, default=1,
                     help="run the vocabulary-parallel flow with this many shards on one GPU")
+    ap.add_argument("--torch-loss", action="store_true",
+                    help="regression workload: the loss as a torch callback instead of on the device")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

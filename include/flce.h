@@ -79,10 +79,11 @@ typedef enum {
   FLCE_PASS_FORWARD = 0,      /* flce_forward, flce_forward_partial, flce_forward_combine */
   FLCE_PASS_BACKWARD = 1,     /* flce_backward                                           */
   FLCE_PASS_CHUNK_LOGITS = 2, /* flce_chunk_logits (the status word only)                */
-  FLCE_PASS_CHUNK_GRADS = 3   /* flce_chunk_grads; N is the largest chunk's row count;
+  FLCE_PASS_CHUNK_GRADS = 3,  /* flce_chunk_grads; N is the largest chunk's row count;
                                  the same workspace must be passed to every chunk of
                                  one loss, because it carries the fp32 grad_weight
                                  partial from chunk to chunk                            */
+  FLCE_PASS_CHUNK_MSE = 4     /* flce_chunk_weighted_mse; N is the largest chunk's rows */
 } flce_pass;
 
 /* Position of a row chunk in flce_chunk_grads' accumulation of grad_weight. */
@@ -331,6 +332,35 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
 int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,
                      const void* dlogits, int64_t ld_dlogits, int32_t phase, void* grad_hidden,
                      void* grad_weight, void* workspace, size_t ws_bytes, flce_stream_t stream);
+
+/*
+ * A loss computed on the device for the chunked linear loss: the row- and
+ * feature-weighted squared error that "Chunked Linear Loss" ("Direct logits
+ * gradients") writes as a caller's callback,
+ *
+ *   L       = sum_rv r_r f_v (z_rv - y_rv)^2,   z = hidden W^T (this chunk)
+ *   dlogits = 2 r_r f_v (z_rv - y_rv)
+ *
+ * It replaces flce_chunk_logits plus the callback for one chunk. The logits
+ * stay in the GEMM's fp32 accumulator: the epilogue reads the target and the
+ * weights, writes dlogits (input dtype) and per-tile row sums of the loss.
+ * A fixed-order reduction then sets *loss (fp64, device) to the chunk's loss,
+ * or adds it when accumulate_loss is 1. Pass dlogits to flce_chunk_grads.
+ *
+ * - bf16 / fp16 only (FLCE_ERR_UNSUPPORTED for fp32 inputs).
+ * - target: fp32 [N][ld_target], ld_target >= V and a multiple of 4.
+ * - row_weight: fp32 [N], 4-byte aligned; feature_weight: fp32 [V], 16-byte
+ *   aligned; target 16-byte aligned.
+ * - dlogits: [N][ld_dlogits] in the input dtype, ld_dlogits >= V and a
+ *   multiple of 8; up to round_up(V, 8) elements of a row may be written.
+ * - loss: one device double, 8-byte aligned.
+ * - workspace: FLCE_PASS_CHUNK_MSE bytes (the status word and the partials).
+ */
+int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void* weight,
+                            const float* target, int64_t ld_target, const float* row_weight,
+                            const float* feature_weight, void* dlogits, int64_t ld_dlogits,
+                            double* loss, int32_t accumulate_loss, void* workspace,
+                            size_t ws_bytes, flce_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns the device-detected status of the last

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
 FLCE_F32, FLCE_BF16, FLCE_F16 = 0, 1, 2
 FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
 FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD, FLCE_PASS_CHUNK_LOGITS, FLCE_PASS_CHUNK_GRADS = 0, 1, 2, 3
+FLCE_PASS_CHUNK_MSE = 4
 FLCE_CHUNK_ONLY, FLCE_CHUNK_FIRST, FLCE_CHUNK_NEXT, FLCE_CHUNK_LAST = 0, 1, 2, 3
 FLCE_ACCUM_FP32, FLCE_ACCUM_WEIGHT = 0, 1
 ACCUM_DTYPES = {"fp32": FLCE_ACCUM_FP32, "weight": FLCE_ACCUM_WEIGHT}
@@ -32,6 +33,7 @@ EXPORTS = (
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
     "flce_forward_partial", "flce_forward_combine", "flce_chunk_logits", "flce_chunk_grads",
+    "flce_chunk_weighted_mse",
 )
 
 
@@ -111,6 +113,9 @@ def load() -> ctypes.CDLL:
     lib.flce_chunk_grads.argtypes = [P, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp, sz,
                                      vp]
     lib.flce_chunk_grads.restype = ctypes.c_int
+    lib.flce_chunk_weighted_mse.argtypes = [P, vp, vp, vp, ctypes.c_int64, vp, vp, vp,
+                                            ctypes.c_int64, vp, ctypes.c_int32, vp, sz, vp]
+    lib.flce_chunk_weighted_mse.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
     lib.flce_error_string.argtypes = [ctypes.c_int]
@@ -214,6 +219,15 @@ def chunk_grads_raw(p: FlceParams, hidden: int, weight: int, dlogits: int, ld_dl
                     stream: int) -> int:
     return load().flce_chunk_grads(ctypes.byref(p), hidden, weight, dlogits, ld_dlogits, phase,
                                    grad_hidden, grad_weight, ws, ws_bytes, stream)
+
+
+def chunk_weighted_mse_raw(p: FlceParams, hidden: int, weight: int, target: int, ld_target: int,
+                           row_weight: int, feature_weight: int, dlogits: int, ld_dlogits: int,
+                           loss: int, accumulate_loss: int, ws: int, ws_bytes: int,
+                           stream: int) -> int:
+    return load().flce_chunk_weighted_mse(ctypes.byref(p), hidden, weight, target, ld_target,
+                                          row_weight, feature_weight, dlogits, ld_dlogits, loss,
+                                          accumulate_loss, ws, ws_bytes, stream)
 
 
 def check_status(ws: int, stream: int) -> int:

@@ -22,6 +22,12 @@ on the chunk's device tensors. Tensor arguments whose first dimension equals
 the number of rows of ``inputs`` are sliced to the chunk's rows; all other
 arguments are passed unchanged. The chunk losses are summed, so the loss must
 be additive over rows ("Reduction semantics").
+
+``weighted_mse_loss(target, row_weight, feature_weight)`` can stand in for a
+callback. It is the page's weighted squared error ("Direct logits
+gradients") computed on the device: steps 1 and 2 become one kernel
+(``flce_chunk_weighted_mse``) whose epilogue applies the loss to the fp32
+accumulator, so the chunk's logits are never written.
 """
 from __future__ import annotations
 
@@ -50,6 +56,32 @@ def _slice_arg(a, n_rows: int, r0: int, r1: int):
     if isinstance(a, torch.Tensor) and a.dim() >= 1 and a.shape[0] == n_rows:
         return a[r0:r1]
     return a
+
+
+class _WeightedMSE:
+    """sum_rv r_r f_v (z_rv - y_rv)^2 over the rows, evaluated inside the projection's epilogue."""
+
+    def __init__(self, target: torch.Tensor, row_weight: torch.Tensor,
+                 feature_weight: torch.Tensor):
+        if target.dim() != 2 or row_weight.dim() != 1 or feature_weight.dim() != 1:
+            raise ValueError("target must be [N, V], row_weight [N] and feature_weight [V]")
+        self.target = target.float()
+        if self.target.stride(1) != 1 or self.target.stride(0) % 4 != 0 \
+                or self.target.data_ptr() % 16 != 0:
+            # the kernel reads rows of a 4-float-multiple stride, 16-byte aligned
+            N, V = self.target.shape
+            padded = torch.empty((N, (V + 3) // 4 * 4), dtype=torch.float32,
+                                 device=self.target.device)
+            padded[:, :V].copy_(self.target)
+            self.target = padded[:, :V]
+        self.row_weight = row_weight.float().contiguous()
+        self.feature_weight = feature_weight.float().contiguous()
+
+
+def weighted_mse_loss(target: torch.Tensor, row_weight: torch.Tensor,
+                      feature_weight: torch.Tensor) -> _WeightedMSE:
+    """The weighted squared error as a device-side loss for ``chunked_linear_loss``."""
+    return _WeightedMSE(target, row_weight, feature_weight)
 
 
 class _ChunkedLinearLoss(torch.autograd.Function):
@@ -92,26 +124,49 @@ class _ChunkedLinearLoss(torch.autograd.Function):
                            dtype=torch.uint8, device=dev)
         staged = None
         stream = _stream(dev)
+        device_loss = isinstance(fn, _WeightedMSE)
+        if device_loss:
+            if fn.target.shape != (N, V) or fn.row_weight.shape != (N,) or \
+                    fn.feature_weight.shape != (V,):
+                raise ValueError("weighted_mse_loss: target [N, V], row_weight [N], "
+                                 "feature_weight [V] must match inputs and weight")
+            loss64 = torch.zeros(1, dtype=torch.float64, device=dev)
+            ws_m = torch.empty(max(256, _lib.workspace_bytes(p_max, _lib.FLCE_PASS_CHUNK_MSE)),
+                               dtype=torch.uint8, device=dev)
         for c in range(nchunks):
             r0, r1 = c * rows, min(N, (c + 1) * rows)
             p = _lib.make_params(N=r1 - r0, **kw)
             xc = x[r0:r1]
-            _lib.check(_lib.chunk_logits_raw(p, _ptr(xc), _ptr(w), _ptr(logits), ld, _ptr(ws_l),
-                                             ws_l.numel(), stream), "flce_chunk_logits")
-            _maybe_check(ws_l, "flce_chunk_logits")
-            args = [_slice_arg(a, N, r0, r1) for a in loss_args]
-            kwargs = {k: _slice_arg(a, N, r0, r1) for k, a in loss_kwargs.items()}
-            loss_c, g = fn(logits[: r1 - r0, :V], *args, **kwargs)
-            if loss_c.dim() != 0:
-                raise ValueError("loss_and_grad_fn must return a scalar loss")
-            total += loss_c.float()
+            if device_loss:
+                # steps 1 and 2 in one kernel: the logits never leave the accumulator
+                tgt = fn.target[r0:r1]
+                rc = _lib.chunk_weighted_mse_raw(
+                    p, _ptr(xc), _ptr(w), _ptr(tgt), tgt.stride(0), _ptr(fn.row_weight[r0:r1]),
+                    _ptr(fn.feature_weight), _ptr(logits), ld, _ptr(loss64), 1 if c > 0 else 0,
+                    _ptr(ws_m), ws_m.numel(), stream)
+                _lib.check(rc, "flce_chunk_weighted_mse")
+                _maybe_check(ws_m, "flce_chunk_weighted_mse")
+                g = logits[: r1 - r0]
+            else:
+                _lib.check(_lib.chunk_logits_raw(p, _ptr(xc), _ptr(w), _ptr(logits), ld,
+                                                 _ptr(ws_l), ws_l.numel(), stream),
+                           "flce_chunk_logits")
+                _maybe_check(ws_l, "flce_chunk_logits")
+                args = [_slice_arg(a, N, r0, r1) for a in loss_args]
+                kwargs = {k: _slice_arg(a, N, r0, r1) for k, a in loss_kwargs.items()}
+                loss_c, g = fn(logits[: r1 - r0, :V], *args, **kwargs)
+                if loss_c.dim() != 0:
+                    raise ValueError("loss_and_grad_fn must return a scalar loss")
+                total += loss_c.float()
             if not (need_x or need_w):
                 continue
-            if g.shape != (r1 - r0, V):
+            if device_loss:
+                pass   # g is the kernel's own [rows][ld] buffer
+            elif g.shape != (r1 - r0, V):
                 raise ValueError(f"the logits gradient must be [{r1 - r0}, {V}], got {tuple(g.shape)}")
             g = g.to(x.dtype)
             ok = (g.stride(1) == 1 and g.stride(0) >= V and g.stride(0) % 8 == 0
-                  and g.data_ptr() % 16 == 0)
+                  and g.data_ptr() % 16 == 0) or device_loss
             if not ok:
                 # The kernels read rows of 16-byte-aligned, 8-element-multiple
                 # stride; anything else is copied into a buffer of that layout.
@@ -126,6 +181,8 @@ class _ChunkedLinearLoss(torch.autograd.Function):
                                       _ptr(ws_g), ws_g.numel(), stream)
             _lib.check(rc, "flce_chunk_grads")
             _maybe_check(ws_g, "flce_chunk_grads")
+        if device_loss:
+            total = loss64[0].float()
         ctx.save_for_backward(gx, gw)
         ctx.shape = inputs.shape
         return total

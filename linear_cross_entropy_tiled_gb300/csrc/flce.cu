@@ -512,6 +512,8 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes) {
     *bytes = kHeader;
   } else if (pass == FLCE_PASS_CHUNK_GRADS) {
     *bytes = chunk_layout(p).total;
+  } else if (pass == FLCE_PASS_CHUNK_MSE) {
+    *bytes = align_up(kHeader + size_t(ceil_div(p->V, kBN)) * ceil_div(p->N, 32) * 4, 256);
   } else {
     return FLCE_ERR_INVALID_ARG;
   }
@@ -1163,6 +1165,73 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
   ga.ldc = ld_logits;
   ga.accumulate = 0;
   return launch("flce_chunk_logits_simt", st, [&] { return launch_gemm_simt(ga, st); });
+}
+
+int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void* weight,
+                            const float* target, int64_t ld_target, const float* row_weight,
+                            const float* feature_weight, void* dlogits, int64_t ld_dlogits,
+                            double* loss, int32_t accumulate_loss, void* workspace,
+                            size_t ws_bytes, flce_stream_t stream) {
+  int v = validate(p);
+  if (v != FLCE_OK) return v;
+  if (!tensor_path(p)) return FLCE_ERR_UNSUPPORTED;
+  if (p->N < 1 || hidden == nullptr || weight == nullptr || target == nullptr ||
+      row_weight == nullptr || feature_weight == nullptr || dlogits == nullptr || loss == nullptr)
+    return FLCE_ERR_INVALID_ARG;
+  if (accumulate_loss != 0 && accumulate_loss != 1) return FLCE_ERR_INVALID_ARG;
+  if (ld_target < p->V || ld_target % 4 != 0 || ld_dlogits < p->V || ld_dlogits % 8 != 0)
+    return FLCE_ERR_INVALID_ARG;
+  const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  const int n_tiles = static_cast<int>(ceil_div(V, kBN));
+  const size_t need = align_up(kHeader + size_t(n_tiles) * ceil_div(N, 32) * 4, 256);
+  if (workspace == nullptr || ws_bytes < need) return FLCE_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(target) ||
+      (reinterpret_cast<uintptr_t>(row_weight) & 3u) != 0 || !aligned16(feature_weight) ||
+      !aligned16(dlogits) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(loss) & 7u) != 0)
+    return FLCE_ERR_ALIGNMENT;
+  DeviceInfo d;
+  if ((v = device_info(&d)) != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  // dlogits[N, V] = 2 r f (h W^T - y): the GEMM of flce_chunk_logits, with the
+  // loss applied to the fp32 accumulator in the epilogue.
+  const CUtensorMapDataType dt = map_type(p);
+  GemmOperand op_a, op_b;
+  GemmArgs ga{};
+  if ((v = make_k_operand(&op_a, hidden, H, N, uint64_t(H) * 2, kBM, dt)) != FLCE_OK) return v;
+  if ((v = make_k_operand(&op_b, weight, H, V, uint64_t(H) * 2, kBNHalf, dt)) != FLCE_OK) return v;
+  ga.M = N;
+  ga.N = V;
+  ga.K = H;
+  ga.m_tiles = static_cast<int>(ceil_div(N, kPairM));
+  ga.n_tiles = n_tiles;
+  ga.k_blocks = static_cast<int>(ceil_div(H, kBK));
+  ga.num_tiles = ga.m_tiles * ga.n_tiles;
+  ga.k_splits = 1;
+  ga.kb_per_split = ga.k_blocks;
+  ga.a_mn = 0;
+  ga.b_mn = 0;
+  ga.mode = kWeightedMse;
+  ga.out = dlogits;
+  ga.ld_out = ld_dlogits;
+  ga.status = reinterpret_cast<int*>(ws);
+  ga.target = target;
+  ga.ld_target = ld_target;
+  ga.row_w = row_weight;
+  ga.feat_w = feature_weight;
+  ga.loss_part = reinterpret_cast<float*>(ws + kHeader);
+  const bool f16 = p->dtype == FLCE_F16;
+  const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+  v = launch("flce_chunk_mse_tc", st, [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+  if (v != FLCE_OK) return v;
+  LossReduceArgs la{};
+  la.part = ga.loss_part;
+  la.count = static_cast<long long>(n_tiles) * ceil_div(N, 32);
+  la.loss = loss;
+  la.accumulate = accumulate_loss;
+  return launch("flce_loss_reduce", st, [&] { return launch_loss_reduce(la, st); });
 }
 
 int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,

@@ -179,7 +179,12 @@ enum GemmMode : int {
   kAddPart = 2,       // part = part + acc
   kAddPartToOut = 3,  // out  = part + acc
   kAddOutToOut = 4,   // out  = out + acc (read-modify-write in the output dtype)
-  kAddOutToPart = 5   // part = out + acc
+  kAddOutToPart = 5,  // part = out + acc
+  // A row- and feature-weighted squared error on the accumulator, whose
+  // logits are never stored: out = 2 r_m f_n (acc - y_mn) in the output dtype,
+  // and loss_part[n_tile][m / 32] = sum over the tile's columns and the 32
+  // rows m / 32 of r_m f_n (acc - y_mn)^2 (fp32). Needs k_splits == 1.
+  kWeightedMse = 6
 };
 
 // One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With
@@ -202,6 +207,20 @@ struct GemmArgs {
   long long split_stride;      // elements between split partial buffers
   const float* acc_scale;      // nullable: the accumulator is multiplied by *acc_scale first
   int* status;
+  // kWeightedMse only
+  const float* target;         // y [M][ld_target], fp32
+  long long ld_target;         // multiple of 4
+  const float* row_w;          // r [M]
+  const float* feat_w;         // f [N]
+  float* loss_part;            // [n_tiles][ceil(M / 32)]
+};
+
+// loss = (accumulate ? loss : 0) + sum of part[0 .. count), in a fixed order.
+struct LossReduceArgs {
+  const float* part;
+  long long count;
+  double* loss;
+  int accumulate;
 };
 
 // out[m, n] (bf16) = sum over s of part[s][m, n], in split order.
@@ -270,6 +289,7 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s);
+cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s);
 
 constexpr int kMergeThreads = 256;
 

@@ -366,6 +366,21 @@ cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// One block: every thread sums a fixed strided subset in fp64, then a fixed
+// tree sums the threads. The result does not depend on timing.
+__global__ void __launch_bounds__(1024) loss_reduce_kernel(const LossReduceArgs a) {
+  __shared__ double sh[32];
+  double s = 0.0;
+  for (long long i = threadIdx.x; i < a.count; i += blockDim.x) s += a.part[i];
+  s = block_sum(s, sh);
+  if (threadIdx.x == 0) a.loss[0] = (a.accumulate ? a.loss[0] : 0.0) + s;
+}
+
+cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s) {
+  loss_reduce_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s) {
   const int grid = (a.V + 255) / 256;
   if (dtype == 1)

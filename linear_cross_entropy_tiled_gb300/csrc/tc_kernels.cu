@@ -675,7 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
 // neighbouring tiles of the same K range, which share an operand strip in L2.
 // The arguments are copied into registers up front; the role loops read no
 // kernel parameters.
-template <typename T>
+template <typename T, bool kMse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_a3,
@@ -762,6 +762,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
     const bool add_out = mode0 == kAddOutToOut || mode0 == kAddOutToPart;
     const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
+    constexpr bool mse = kMse;  // the kWeightedMse epilogue is its own instantiation
+    const float* const tgt = a.target;
+    const float* const feat = a.feat_w;
+    const long long ld_target = a.ld_target;
     float* const part0 = a.part;
     const long long ld_part = a.ld_part, split_stride = a.split_stride, ld_out = a.ld_out;
     T* const out = static_cast<T*>(a.out);
@@ -777,6 +781,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       if (!dead) {
         const int m = mt * kPairM + static_cast<int>(rank) * kBM + r;
         const bool row_ok = m < M;
+        const float rm = (mse && row_ok) ? a.row_w[m] : 0.f;
+        float lsum = 0.f;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -789,6 +795,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           float d[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
+          if (mse) {
+            // d holds the logits z of this row's 32 columns; they become
+            // 2 r f (z - y), and r f (z - y)^2 goes into the row's loss.
+            float y[32], f[32];
+            const float* yrow = tgt + static_cast<size_t>(m) * ld_target + col0;
+            if (col0 + 32 <= N) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 y4 = reinterpret_cast<const float4*>(yrow)[i];
+                const float4 f4 = __ldg(reinterpret_cast<const float4*>(feat + col0) + i);
+                y[4 * i] = y4.x; y[4 * i + 1] = y4.y; y[4 * i + 2] = y4.z; y[4 * i + 3] = y4.w;
+                f[4 * i] = f4.x; f[4 * i + 1] = f4.y; f[4 * i + 2] = f4.z; f[4 * i + 3] = f4.w;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const bool in = col0 + j < N;
+                y[j] = in ? yrow[j] : 0.f;
+                f[j] = in ? feat[col0 + j] : 0.f;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float e = d[j] - y[j];
+              const float we = rm * f[j] * e;
+              lsum = fmaf(we, e, lsum);
+              d[j] = 2.f * we;
+            }
+          }
           if (add_part) {
             const float4* src =
                 reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * ld_part + col0);
@@ -838,6 +873,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
               }
             }
           }
+        }
+        if (mse) {
+          // the warp's 32 rows summed by a fixed shuffle tree: one partial per
+          // (column tile, 32-row group)
+          float t = row_ok ? lsum : 0.f;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+          const int m_base = m - lane;
+          if (lane == 0 && m_base < M)
+            a.loss_part[static_cast<size_t>(nt) * ((M + 31) / 32) + (m_base >> 5)] = t;
         }
         epi_release(s, acc, lane);
       }
@@ -896,10 +941,10 @@ cudaError_t launch_ds_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const 
 template <typename T>
 cudaError_t launch_gemm_t(const GemmOperand& op_a, const GemmOperand& op_b, const GemmArgs& a,
                           int grid, cudaStream_t st) {
-  cudaError_t e = set_smem_attr(gemm_tc_kernel<T>);
+  auto k = a.mode == kWeightedMse ? gemm_tc_kernel<T, true> : gemm_tc_kernel<T, false>;
+  cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<T><<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(op_a.map, op_b.map, op_a.map3,
-                                                                 op_b.map3, a);
+  k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(op_a.map, op_b.map, op_a.map3, op_b.map3, a);
   return cudaGetLastError();
 }
 }  // namespace

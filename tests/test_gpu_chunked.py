@@ -114,3 +114,40 @@ def test_strided_logits_gradient_and_scaled_backward():
     assert abs(loss.item() - ref) <= TOL["bf16"]["loss"] * abs(ref)
     assert_grad_close(x.grad.double().cpu().numpy(), 3.0 * rx, "bf16", "grad_inputs")
     assert_grad_close(w.grad.double().cpu().numpy(), 3.0 * rw, "bf16", "grad_weight")
+
+
+@pytest.mark.parametrize("dtype,N,H,V,chunk_rows", [
+    ("bf16", 1000, 264, 700, 256),   # 4 chunks; 700 is not a multiple of 8
+    ("bf16", 600, 128, 701, 256),    # V not a multiple of 4: the target is padded
+    ("f16", 520, 200, 512, None),    # one chunk
+])
+def test_device_weighted_mse_matches_the_oracle(dtype, N, H, V, chunk_rows):
+    """weighted_mse_loss: the loss inside the projection's epilogue (flce_chunk_weighted_mse)."""
+    from linear_cross_entropy_tiled_gb300 import weighted_mse_loss
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, dtype, seed=3 * N + V)
+    x = Xd.clone().requires_grad_(True)
+    w = Wd.clone().requires_grad_(True)
+    loss_fn = weighted_mse_loss(torch.from_numpy(Y).cuda(), torch.from_numpy(r).cuda(),
+                                torch.from_numpy(f).cuda())
+    loss = chunked_linear_loss(x, w, loss_fn, chunk_rows=chunk_rows)
+    loss.backward()
+    torch.cuda.synchronize()
+    ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f,
+                                             chunk_rows=chunk_rows)
+    # the loss is taken from the fp32 accumulator, so it is closer than the 16-bit bar
+    assert abs(loss.item() - ref) <= 1e-4 * abs(ref), (loss.item(), ref)
+    assert_grad_close(x.grad.double().cpu().numpy(), rx, dtype, "grad_inputs")
+    assert_grad_close(w.grad.double().cpu().numpy(), rw, dtype, "grad_weight")
+    # the same loss through the torch callback path
+    loss2, gx2, gw2 = run(Xd, Wd, Y, r, f, chunk_rows=chunk_rows)
+    assert abs(loss2 - loss.item()) <= TOL[dtype]["loss"] * abs(ref)
+    assert_grad_close(x.grad.double().cpu().numpy(), gx2, dtype, "device vs callback grad_inputs")
+
+
+def test_device_weighted_mse_refuses_fp32_inputs():
+    from linear_cross_entropy_tiled_gb300 import weighted_mse_loss
+    X, W, Y, r, f, Xd, Wd = case(64, 32, 48, "f32", seed=1)
+    loss_fn = weighted_mse_loss(torch.from_numpy(Y).cuda(), torch.from_numpy(r).cuda(),
+                                torch.from_numpy(f).cuda())
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        chunked_linear_loss(Xd.requires_grad_(True), Wd.requires_grad_(True), loss_fn)
