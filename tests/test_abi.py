@@ -182,3 +182,30 @@ def test_chunked_linear_loss_entry_points_validate_before_any_gpu_work(lib):
     assert _lib.chunk_grads_raw(p, fake, fake, 0, 1000, 0, fake, fake, fake, need, 0) == 1
     assert _lib.chunk_grads_raw(p, fake, fake, fake, 1000, 0, fake, fake, fake, need - 1, 0) == 4
     assert _lib.chunk_grads_raw(p, fake, fake, fake, 1000, 0, fake + 4, fake, fake, need, 0) == 3
+
+
+def test_device_weighted_mse_entry_point_validates_before_any_gpu_work(lib):
+    p = params(N=512, H=256, V=1000)
+    need = _lib.workspace_bytes(p, _lib.FLCE_PASS_CHUNK_MSE)
+    # the status word plus one fp32 partial per (256-column tile, 32-row group):
+    # 4 tiles x 16 groups x 4 bytes
+    assert need == 256 + 4 * 16 * 4
+    fake = 1 << 20
+    args = dict(target=fake, ld_target=1000, row_weight=fake, feature_weight=fake, dlogits=fake,
+                ld_dlogits=1000, loss=fake, accumulate_loss=0, ws=fake, ws_bytes=need, stream=0)
+
+    def call(pp, **kw):
+        a = dict(args, **kw)
+        return _lib.chunk_weighted_mse_raw(pp, fake, fake, a["target"], a["ld_target"],
+                                           a["row_weight"], a["feature_weight"], a["dlogits"],
+                                           a["ld_dlogits"], a["loss"], a["accumulate_loss"],
+                                           a["ws"], a["ws_bytes"], a["stream"])
+
+    assert call(params(N=512, H=256, V=1000, dtype=_lib.FLCE_F32)) == 2   # fp32: unsupported
+    assert call(p, ld_target=1002) == 1                                   # not a multiple of 4
+    assert call(p, ld_dlogits=996) == 1                                   # below V
+    assert call(p, accumulate_loss=2) == 1
+    assert call(p, loss=0) == 1
+    assert call(p, ws_bytes=need - 4) == 4
+    assert call(p, loss=fake + 4) == 3                                    # fp64 needs 8 bytes
+    assert call(p, row_weight=fake + 2) == 3                              # fp32 needs 4 bytes
