@@ -357,6 +357,27 @@ def ours_main(args, w):
         ms = float(tt.item())
     _lib.check(_lib.check_status(bws.data_ptr(), stream.cuda_stream), "timed backward")
 
+    # ---------------- forward only (2NHV), timed the same way ----------------
+    fwd_ms = None
+    if args.vocab_shards == 1:
+        for _ in range(2):
+            flce_forward(p, h, W, t, b, return_metrics=w.metrics, workspace=fws)
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            flce_forward(p, h, W, t, b, return_metrics=w.metrics, workspace=fws)
+        g1.record(stream)
+        barrier()
+        fwd_ms = g0.elapsed_time(g1) / args.steps
+    # No single buffer of the default schedule may reach the size of the N x V
+    # logits in bf16. (Forcing row chunks at N < V adds the fp32 [V, H]
+    # grad_weight partial to the workspace, which can.)
+    largest = max(fws.numel(), bws.numel())
+    if not os.environ.get("FLCE_BWD_CHUNKS"):
+        assert largest < w.N * w.V * 2, f"a {largest}-byte workspace reaches N*V*2 bytes"
+
     # ---------------- end to end, host buffers ----------------
     e2e = None
     if not args.no_e2e and args.vocab_shards == 1:
@@ -476,6 +497,10 @@ def ours_main(args, w):
             "clocks": clk, "kernels": kern,
             "variant": {"dtype": w.dtype, "grad_weight_accum": args.grad_weight_accum,
                         "vocab_shards": args.vocab_shards},
+            "forward": None if fwd_ms is None else {
+                "ms_per_step": fwd_ms, "tokens_per_s": world * w.N / (fwd_ms * 1e-3),
+                "tflops": 2.0 * w.N * w.H * w.V / (fwd_ms * 1e-3) / 1e12},
+            "largest_workspace_bytes": int(largest),
             "logits_bytes_avoided": w.logits_bytes_avoided,
             "peak_device_bytes": int(torch.cuda.max_memory_allocated(dev)),
         }
