@@ -1,0 +1,45 @@
+"""bench.py's JSON contract, checked on the CPU through its reference leg.
+
+``--impl reference`` times the fp64 oracle on the host cores and needs no GPU.
+The line must carry the contract's keys, with the same metric and config as
+the CUDA leg, so that the driver can divide the two.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+from linear_cross_entropy_tiled_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_leg_prints_one_contract_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_f32",
+                          "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True,
+                         text=True, timeout=600, env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["config"] == bench.workload_config(wl.WORKLOADS["tiny_f32"])
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+
+
+def test_kernel_flops_count_each_contraction_once_per_step():
+    w = wl.WORKLOADS[wl.HEADLINE]
+    names = ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc")
+    assert sum(bench.kernel_flops(n, w) for n in names) == w.flops_fwd_bwd
+    assert bench.kernel_flops("flce_merge", w) == 0.0
+    r = wl.REGRESSION_WORKLOADS["mse_v32768"]
+    names = ("flce_chunk_mse_tc", "flce_chunk_grad_hidden_tc", "flce_chunk_grad_weight_tc")
+    assert sum(bench.kernel_flops(n, r) for n in names) == r.flops_fwd_bwd
