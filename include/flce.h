@@ -299,6 +299,9 @@ int flce_forward_noalloc(const flce_params* p, const void* hidden, const void* w
  *     ld_logits >= V and ld_logits % 8 == 0. The tensor path may write up to
  *     round_up(V, 8) elements of a row.
  *   - The workspace holds the status word: FLCE_PASS_CHUNK_LOGITS bytes.
+ *   - Alignment: 16 bytes for bf16 / fp16. For fp32 inputs hidden, weight,
+ *     logits, dlogits and the gradients need only 4-byte alignment, so a
+ *     chunk may start at any row. Workspaces are always 16-byte aligned.
  *   - Of p, only N, H, V and dtype matter here; the other fields must still
  *     pass the usual checks.
  *

@@ -163,6 +163,13 @@ bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) ==
 // bf16 and fp16 run on the tensor cores; fp32 on the SIMT path.
 bool tensor_path(const flce_params* p) { return p->dtype != FLCE_F32; }
 
+// The tensor path moves 16-byte vectors and TMA boxes; the fp32 SIMT path
+// reads single elements, so a row chunk of fp32 data may start anywhere on
+// a 4-byte boundary.
+bool aligned_for(const flce_params* p, const void* q) {
+  return tensor_path(p) ? aligned16(q) : (reinterpret_cast<uintptr_t>(q) & 3u) == 0;
+}
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -1112,7 +1119,8 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
     return FLCE_ERR_INVALID_ARG;
   if (ld_logits < p->V || ld_logits % 8 != 0) return FLCE_ERR_INVALID_ARG;
   if (workspace == nullptr || ws_bytes < kHeader) return FLCE_ERR_WORKSPACE;
-  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits) || !aligned16(workspace))
+  if (!aligned_for(p, hidden) || !aligned_for(p, weight) || !aligned_for(p, logits) ||
+      !aligned16(workspace))
     return FLCE_ERR_ALIGNMENT;
   DeviceInfo d;
   if ((v = device_info(&d)) != FLCE_OK) return v;
@@ -1244,8 +1252,9 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
   if (ld_dlogits < p->V || ld_dlogits % 8 != 0) return FLCE_ERR_INVALID_ARG;
   const ChunkLayout L = chunk_layout(p);
   if (workspace == nullptr || ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
-  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(dlogits) || !aligned16(workspace) ||
-      (grad_hidden && !aligned16(grad_hidden)) || (grad_weight && !aligned16(grad_weight)))
+  if (!aligned_for(p, hidden) || !aligned_for(p, weight) || !aligned_for(p, dlogits) ||
+      !aligned16(workspace) || (grad_hidden && !aligned_for(p, grad_hidden)) ||
+      (grad_weight && !aligned_for(p, grad_weight)))
     return FLCE_ERR_ALIGNMENT;
   DeviceInfo d;
   if ((v = device_info(&d)) != FLCE_OK) return v;

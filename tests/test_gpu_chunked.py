@@ -151,3 +151,38 @@ def test_device_weighted_mse_refuses_fp32_inputs():
                                 torch.from_numpy(f).cuda())
     with pytest.raises(RuntimeError, match="UNSUPPORTED"):
         chunked_linear_loss(Xd.requires_grad_(True), Wd.requires_grad_(True), loss_fn)
+
+
+@pytest.mark.parametrize("dtype,N,H,V,chunk_rows", [
+    ("bf16", 3, 8, 5, None),      # every tile ragged; no 3-D view (fewer than two 64-column atoms)
+    ("bf16", 7, 72, 130, 1),      # one-row chunks: FIRST, six NEXT, LAST
+    ("f32", 5, 3, 7, 2),          # the SIMT path with odd sizes
+])
+def test_tiny_and_ragged_chunks(dtype, N, H, V, chunk_rows):
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, dtype, seed=N * 31 + V)
+    loss, gx, gw = run(Xd, Wd, Y, r, f, chunk_rows=chunk_rows)
+    ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f,
+                                             chunk_rows=chunk_rows)
+    assert abs(loss - ref) <= TOL[dtype]["loss"] * abs(ref) + 1e-6, (loss, ref)
+    assert_grad_close(gx, rx, dtype, "grad_inputs")
+    assert_grad_close(gw, rw, dtype, "grad_weight")
+
+
+@pytest.mark.parametrize("which", ["inputs", "weight"])
+def test_gradient_of_one_argument_only(which):
+    N, H, V = 400, 128, 600
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, "bf16", seed=21)
+    x = Xd.clone().requires_grad_(which == "inputs")
+    w = Wd.clone().requires_grad_(which == "weight")
+    loss = chunked_linear_loss(x, w, wmse_torch, torch.from_numpy(Y).cuda(),
+                               torch.from_numpy(r).cuda(), torch.from_numpy(f).cuda(),
+                               chunk_rows=256)
+    loss.backward()
+    torch.cuda.synchronize()
+    ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f, chunk_rows=256)
+    if which == "inputs":
+        assert w.grad is None
+        assert_grad_close(x.grad.double().cpu().numpy(), rx, "bf16", "grad_inputs")
+    else:
+        assert x.grad is None
+        assert_grad_close(w.grad.double().cpu().numpy(), rw, "bf16", "grad_weight")
