@@ -110,11 +110,12 @@ def load() -> ctypes.CDLL:
     lib.flce_forward_combine.restype = ctypes.c_int
     lib.flce_chunk_logits.argtypes = [P, vp, vp, vp, ctypes.c_int64, vp, sz, vp]
     lib.flce_chunk_logits.restype = ctypes.c_int
-    lib.flce_chunk_grads.argtypes = [P, vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp, sz,
-                                     vp]
+    lib.flce_chunk_grads.argtypes = [P, vp, vp, vp, ctypes.c_int64, vp, ctypes.c_int64,
+                                     ctypes.c_int32, vp, vp, vp, sz, vp]
     lib.flce_chunk_grads.restype = ctypes.c_int
     lib.flce_chunk_weighted_mse.argtypes = [P, vp, vp, vp, ctypes.c_int64, vp, vp, vp,
-                                            ctypes.c_int64, vp, ctypes.c_int32, vp, sz, vp]
+                                            ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                            ctypes.c_int32, vp, sz, vp]
     lib.flce_chunk_weighted_mse.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
@@ -216,18 +217,20 @@ def chunk_logits_raw(p: FlceParams, hidden: int, weight: int, logits: int, ld_lo
 
 def chunk_grads_raw(p: FlceParams, hidden: int, weight: int, dlogits: int, ld_dlogits: int,
                     phase: int, grad_hidden: int, grad_weight: int, ws: int, ws_bytes: int,
-                    stream: int) -> int:
-    return load().flce_chunk_grads(ctypes.byref(p), hidden, weight, dlogits, ld_dlogits, phase,
-                                   grad_hidden, grad_weight, ws, ws_bytes, stream)
+                    stream: int, dlogits_t: int = 0, ld_dlogits_t: int = 0) -> int:
+    return load().flce_chunk_grads(ctypes.byref(p), hidden, weight, dlogits, ld_dlogits, dlogits_t,
+                                   ld_dlogits_t, phase, grad_hidden, grad_weight, ws, ws_bytes,
+                                   stream)
 
 
 def chunk_weighted_mse_raw(p: FlceParams, hidden: int, weight: int, target: int, ld_target: int,
                            row_weight: int, feature_weight: int, dlogits: int, ld_dlogits: int,
                            loss: int, accumulate_loss: int, ws: int, ws_bytes: int,
-                           stream: int) -> int:
+                           stream: int, dlogits_t: int = 0, ld_dlogits_t: int = 0) -> int:
     return load().flce_chunk_weighted_mse(ctypes.byref(p), hidden, weight, target, ld_target,
-                                          row_weight, feature_weight, dlogits, ld_dlogits, loss,
-                                          accumulate_loss, ws, ws_bytes, stream)
+                                          row_weight, feature_weight, dlogits, ld_dlogits,
+                                          dlogits_t, ld_dlogits_t, loss, accumulate_loss, ws,
+                                          ws_bytes, stream)
 
 
 def check_status(ws: int, stream: int) -> int:

@@ -1178,8 +1178,9 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
 int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void* weight,
                             const float* target, int64_t ld_target, const float* row_weight,
                             const float* feature_weight, void* dlogits, int64_t ld_dlogits,
-                            double* loss, int32_t accumulate_loss, void* workspace,
-                            size_t ws_bytes, flce_stream_t stream) {
+                            void* dlogits_t, int64_t ld_dlogits_t, double* loss,
+                            int32_t accumulate_loss, void* workspace, size_t ws_bytes,
+                            flce_stream_t stream) {
   int v = validate(p);
   if (v != FLCE_OK) return v;
   if (!tensor_path(p)) return FLCE_ERR_UNSUPPORTED;
@@ -1189,6 +1190,9 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   if (accumulate_loss != 0 && accumulate_loss != 1) return FLCE_ERR_INVALID_ARG;
   if (ld_target < p->V || ld_target % 4 != 0 || ld_dlogits < p->V || ld_dlogits % 8 != 0)
     return FLCE_ERR_INVALID_ARG;
+  if (dlogits_t != nullptr && (ld_dlogits_t < p->N || ld_dlogits_t % 8 != 0))
+    return FLCE_ERR_INVALID_ARG;
+  if (dlogits_t != nullptr && !aligned16(dlogits_t)) return FLCE_ERR_ALIGNMENT;
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const int n_tiles = static_cast<int>(ceil_div(V, kBN));
   const size_t need = align_up(kHeader + size_t(n_tiles) * ceil_div(N, 32) * 4, 256);
@@ -1230,6 +1234,8 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   ga.row_w = row_weight;
   ga.feat_w = feature_weight;
   ga.loss_part = reinterpret_cast<float*>(ws + kHeader);
+  ga.out_t = dlogits_t;
+  ga.ld_out_t = ld_dlogits_t;
   const bool f16 = p->dtype == FLCE_F16;
   const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
   v = launch("flce_chunk_mse_tc", st, [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
@@ -1243,13 +1249,17 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
 }
 
 int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,
-                     const void* dlogits, int64_t ld_dlogits, int32_t phase, void* grad_hidden,
-                     void* grad_weight, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+                     const void* dlogits, int64_t ld_dlogits, const void* dlogits_t,
+                     int64_t ld_dlogits_t, int32_t phase, void* grad_hidden, void* grad_weight,
+                     void* workspace, size_t ws_bytes, flce_stream_t stream) {
   int v = validate(p);
   if (v != FLCE_OK) return v;
   if (p->N < 1 || phase < FLCE_CHUNK_ONLY || phase > FLCE_CHUNK_LAST) return FLCE_ERR_INVALID_ARG;
   if (hidden == nullptr || weight == nullptr || dlogits == nullptr) return FLCE_ERR_INVALID_ARG;
   if (ld_dlogits < p->V || ld_dlogits % 8 != 0) return FLCE_ERR_INVALID_ARG;
+  if (dlogits_t != nullptr && (!tensor_path(p) || ld_dlogits_t < p->N || ld_dlogits_t % 8 != 0))
+    return FLCE_ERR_INVALID_ARG;
+  if (dlogits_t != nullptr && !aligned16(dlogits_t)) return FLCE_ERR_ALIGNMENT;
   const ChunkLayout L = chunk_layout(p);
   if (workspace == nullptr || ws_bytes < L.total) return FLCE_ERR_WORKSPACE;
   if (!aligned_for(p, hidden) || !aligned_for(p, weight) || !aligned_for(p, dlogits) ||
@@ -1357,12 +1367,20 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     }
   }
   if (grad_weight) {
-    // grad_weight[V, H] (+)= dlogits^T[V, N] (MN-major) x h[N, H] (MN-major)
+    // grad_weight[V, H] (+)= dlogits^T[V, N] x h[N, H] (MN-major). dlogits^T is
+    // read K-major from the transposed copy when the caller has one, else
+    // MN-major from dlogits (about 20 % slower).
     GemmOperand op_a, op_b;
     GemmArgs ga{};
-    if ((v = make_mn_operand(&op_a, &ga.a_atoms, dlogits, V, N, dl_row_bytes, dt)) != FLCE_OK)
-      return v;
-    ga.a_atoms = 0;  // the A side loads through the 2-D map (the 3-D view does not help it)
+    if (dlogits_t != nullptr) {
+      if ((v = make_k_operand(&op_a, dlogits_t, N, V, uint64_t(ld_dlogits_t) * 2, kBM, dt)) !=
+          FLCE_OK)
+        return v;
+    } else {
+      if ((v = make_mn_operand(&op_a, &ga.a_atoms, dlogits, V, N, dl_row_bytes, dt)) != FLCE_OK)
+        return v;
+      ga.a_atoms = 0;  // the A side loads through the 2-D map (the 3-D view does not help it)
+    }
     if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt)) != FLCE_OK)
       return v;
     ga.M = V;
@@ -1374,7 +1392,7 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     ga.num_tiles = ga.m_tiles * ga.n_tiles;
     ga.k_splits = 1;
     ga.kb_per_split = ga.k_blocks;
-    ga.a_mn = 1;
+    ga.a_mn = dlogits_t != nullptr ? 0 : 1;
     ga.b_mn = 1;
     if (phase == FLCE_CHUNK_ONLY || p->grad_weight_accum == FLCE_ACCUM_WEIGHT)
       ga.mode = (later || p->accumulate) ? kAddOutToOut : kStoreOut;

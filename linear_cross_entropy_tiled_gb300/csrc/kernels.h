@@ -213,6 +213,8 @@ struct GemmArgs {
   const float* row_w;          // r [M]
   const float* feat_w;         // f [N]
   float* loss_part;            // [n_tiles][ceil(M / 32)]
+  void* out_t;                 // nullable: out transposed as well, [N][ld_out_t]
+  long long ld_out_t;
 };
 
 // loss = (accumulate ? loss : 0) + sum of part[0 .. count), in a fixed order.

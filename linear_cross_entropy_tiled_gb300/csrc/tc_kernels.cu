@@ -530,27 +530,38 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
   }
 }
 
-// Stores a warp's 32 rows x 32 columns of dlogits transposed: row v of ds_t
-// holds column v for every row of the chunk. Each lane pair swaps one value,
-// so that every lane writes two neighbouring rows of one column as one 32-bit
-// word and a warp store covers 64 contiguous bytes of two ds_t rows. All 32
-// lanes must call it (it shuffles).
+// Stores a warp's 32 rows x 32 columns of g (times mul) transposed: row c
+// of dst_t holds column c for every row. Each lane pair swaps one value, so
+// that every lane writes two neighbouring rows of one column as one 32-bit
+// word and a warp store covers 64 contiguous bytes of two dst_t rows. `row_w`
+// is the warp's first row; rows >= rows and columns >= cols are not written.
+// ld_t must be even. All 32 lanes must call it (it shuffles).
 template <typename T>
-__device__ __forceinline__ void store_ds_t(const float (&g)[32], const DsArgs& a, int col0,
-                                          int row_w, int lane, float ds_mul, bool live) {
+__device__ __forceinline__ void store_transposed32(const float (&g)[32], T* dst_t, long long ld_t,
+                                                   int col0, int row_w, int lane, int rows,
+                                                   int cols, float mul, bool live) {
   const bool odd = (lane & 1) != 0;
   const int row_pair = row_w + (lane & ~1);  // the first of this lane's two rows
-  T* const base = static_cast<T*>(a.ds_t) + row_pair;
+  T* const base = dst_t + row_pair;
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
     const float recv = __shfl_xor_sync(kFull, odd ? g[2 * jj] : g[2 * jj + 1], 1);
     const float lo = odd ? recv : g[2 * jj];
     const float hi = odd ? g[2 * jj + 1] : recv;
     const int col = col0 + 2 * jj + (odd ? 1 : 0);
-    if (live && row_pair < a.rows && col < a.V)
-      *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(col) * a.ld_t) =
-          Elem<T>::pack(lo * ds_mul, hi * ds_mul);
+    if (live && row_pair < rows && col < cols)
+      *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(col) * ld_t) =
+          Elem<T>::pack(lo * mul, hi * mul);
   }
+}
+
+// dlogits transposed for grad_weight: row v of ds_t holds column v for every
+// row of the chunk.
+template <typename T>
+__device__ __forceinline__ void store_ds_t(const float (&g)[32], const DsArgs& a, int col0,
+                                          int row_w, int lane, float ds_mul, bool live) {
+  store_transposed32<T>(g, static_cast<T*>(a.ds_t), a.ld_t, col0, row_w, lane, a.rows, a.V,
+                        ds_mul, live);
 }
 
 template <typename T, bool kBias, bool kSoftcap>
@@ -791,7 +802,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     v);
           tmem_ld_wait(v);
           const int col0 = nt * kBN + c * 32;
-          if (!row_ok || col0 >= N) continue;
+          // The loss epilogue keeps every lane of a warp (the transposed store
+          // shuffles); a row past M has zero logits and zero weight there.
+          if (mse ? col0 >= N : (!row_ok || col0 >= N)) continue;
           float d[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
@@ -799,11 +812,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             // d holds the logits z of this row's 32 columns; they become
             // 2 r f (z - y), and r f (z - y)^2 goes into the row's loss.
             float y[32], f[32];
-            const float* yrow = tgt + static_cast<size_t>(m) * ld_target + col0;
+            const float* yrow = tgt + static_cast<size_t>(row_ok ? m : 0) * ld_target + col0;
             if (col0 + 32 <= N) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float4 y4 = reinterpret_cast<const float4*>(yrow)[i];
+                const float4 y4 = row_ok ? reinterpret_cast<const float4*>(yrow)[i]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float4 f4 = __ldg(reinterpret_cast<const float4*>(feat + col0) + i);
                 y[4 * i] = y4.x; y[4 * i + 1] = y4.y; y[4 * i + 2] = y4.z; y[4 * i + 3] = y4.w;
                 f[4 * i] = f4.x; f[4 * i + 1] = f4.y; f[4 * i + 2] = f4.z; f[4 * i + 3] = f4.w;
@@ -812,7 +826,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const bool in = col0 + j < N;
-                y[j] = in ? yrow[j] : 0.f;
+                y[j] = (in && row_ok) ? yrow[j] : 0.f;
                 f[j] = in ? feat[col0 + j] : 0.f;
               }
             }
@@ -823,6 +837,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
               lsum = fmaf(we, e, lsum);
               d[j] = 2.f * we;
             }
+            if (a.out_t != nullptr)
+              store_transposed32<T>(d, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane, lane,
+                                    M, N, 1.f, true);
+            if (!row_ok) continue;
           }
           if (add_part) {
             const float4* src =
