@@ -228,7 +228,7 @@ struct BwdLayout {
 // half of the N x V logits, and at most 4 GiB. Whatever crosses chunks is
 // summed in an fp32 partial: grad_weight [V, H] when the chunks are row
 // ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
-// chunks the vocabulary when N < V, where that partial is the smaller one:
+// chunks the vocabulary whenever N < V, where that partial is the smaller one:
 // each chunk's grad_weight rows are then complete after one GEMM over all N
 // rows. FLCE_BWD_CHUNKS=rows or =vocab fixes the axis, so that tests reach
 // both schedules at any size; the result is the same either way.
@@ -238,7 +238,7 @@ bool vocab_chunked(const flce_params* p) {
     if (strcmp(env, "rows") == 0) return false;
     if (strcmp(env, "vocab") == 0) return true;
   }
-  return p->N > kPairM && p->N < p->V;
+  return p->N < p->V;
 }
 
 BwdLayout bwd_layout(const flce_params* p) {
@@ -284,25 +284,26 @@ BwdLayout bwd_layout(const flce_params* p) {
     return L;
   }
   L.ds_ld = L.V_pad;
+  // Row chunks of a quarter of the rows: two 16-bit copies (tensor path) or
+  // one fp32 copy (SIMT path) then hold about N x V bytes, half of the logits
+  // in bf16. Chunk boundaries fall on 256-row pair blocks (tensor path) or
+  // 64-row SIMT tiles.
   const int copies = tensor_path(p) ? 2 : 1;
-  if (N <= kPairM) {
-    L.chunk = N;
-  } else {
-    // chunk boundaries fall on 256-row pair blocks; each copy of dlogits
-    // holds a quarter of the rows (half of them on the fp32 path, which keeps
-    // one copy)
-    const int64_t half = ceil_div(ceil_div(N, 2 * copies), kPairM) * kPairM;
+  const int64_t gran = tensor_path(p) ? kPairM : kSimtTile;
+  {
+    const int64_t quarter = ceil_div(ceil_div(N, 4), gran) * gran;
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem * copies)) /
-                  kPairM * kPairM;
-    if (cap < kPairM) cap = kPairM;
-    // FLCE_MAX_CHUNK_ROWS (a multiple of 256) lowers the row-chunk cap. The
-    // work and the result are the same; it is there so tests can reach the
-    // three-or-more-chunk schedule at small sizes.
+                  gran * gran;
+    if (cap < gran) cap = gran;
+    // FLCE_MAX_CHUNK_ROWS (a multiple of the granule) lowers the row-chunk
+    // cap. The work and the result are the same; it is there so tests can
+    // reach the three-or-more-chunk schedule at small sizes.
     if (const char* env = getenv("FLCE_MAX_CHUNK_ROWS")) {
-      const long long r = atoll(env) / kPairM * kPairM;
-      if (r >= kPairM && r < cap) cap = r;
+      const long long r = atoll(env) / gran * gran;
+      if (r >= gran && r < cap) cap = r;
     }
-    L.chunk = half < cap ? half : cap;
+    L.chunk = quarter < cap ? quarter : cap;
+    if (L.chunk > N && N > 0) L.chunk = N;
   }
   L.nchunks = N > 0 ? static_cast<int>(ceil_div(N, L.chunk)) : 0;
   L.rowblk = tensor_path(p) ? kBM : kSimtTile;

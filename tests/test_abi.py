@@ -73,10 +73,16 @@ def test_workspace_sizes(lib, monkeypatch):
     chunk = 2 * 16384 * 32000 * 2
     dw = 32000 * 1024 * 4
     assert chunk + dw < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < chunk + dw + (300 << 20)
-    # the fp32 path keeps one copy of half of the rows
+    # the fp32 path keeps one copy of a quarter of the rows: together with the
+    # 16-bit paths' two copies of a quarter, about N x V bytes
     f = params(N=4096, H=1024, V=3000, dtype=_lib.FLCE_F32)
-    chunk = 2048 * 3000 * 4
+    chunk = 1024 * 3000 * 4
     assert chunk < _lib.workspace_bytes(f, _lib.FLCE_PASS_BACKWARD) < chunk + (64 << 20)
+    # no dlogits buffer reaches N x V x 2 bytes, also for a single 256-row block
+    for N, V, dt in ((256, 8192, _lib.FLCE_F32), (256, 8192, _lib.FLCE_BF16),
+                     (8192, 128256, _lib.FLCE_BF16), (16384, 151936, _lib.FLCE_BF16)):
+        w = _lib.workspace_bytes(params(N=N, H=512, V=V, dtype=dt), _lib.FLCE_PASS_BACKWARD)
+        assert w < N * V * 2, (N, V, dt, w)
     small = params(N=100, H=64, V=50)
     assert _lib.workspace_bytes(small, _lib.FLCE_PASS_BACKWARD) > 0
 
