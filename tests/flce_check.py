@@ -1,8 +1,10 @@
 """Helpers for the GPU parity tests: run the CUDA path through the C ABI and compare it with the oracle.
 
 Tolerances. The bf16 ones are the stated bar, applied to fp16 as well (fp16
-carries more mantissa than bf16). The fp32 ones are derived in the design doc from
-fp32 accumulation:
+carries more mantissa than bf16). The fp32 gradient bar follows from fp32
+accumulation over K <= V terms: the error grows like sqrt(K) * 2^-24 relative
+to the terms, about 1e-5 at K = 8192, so 1e-4 of the largest gradient. The lse
+bar covers fp32 arithmetic with ex2.approx (relative error near 2^-22):
   loss          relative error <= 2e-3 (bf16 inputs), <= 1e-5 (fp32 inputs)
   lse           |err| <= 1e-4 * max(1, |lse|)  (fp32 arithmetic on both dtypes)
   gradients     max|err| <= 2e-2 * max|ref| and cosine >= 0.9999 (bf16);

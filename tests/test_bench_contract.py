@@ -2,7 +2,7 @@
 
 ``--impl reference`` times the fp64 oracle on the host cores and needs no GPU.
 The line must carry the contract's keys, with the same metric and config as
-the CUDA leg, so that the driver can divide the two.
+the CUDA leg, so that the two lines can be compared.
 """
 import json
 import os
