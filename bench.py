@@ -554,10 +554,11 @@ def chunked_main(args, w):
     fw = torch.from_numpy(inputs["feature_weight"]).to(dev)
 
     def wmse(z, y, rw_, fw_):
-        # the caller's loss: weighted squared error and its logits gradient
-        err = z.float() - y
-        werr = err * (rw_[:, None] * fw_[None, :])
-        return (werr * err).sum(), (2.0 * werr).to(z.dtype)
+        # the caller's loss: weighted squared error and its logits gradient,
+        # grad = 2 r f (z - y), loss = half the dot product of grad and z - y
+        d = torch.sub(z.float(), y)
+        grad = torch.outer(rw_, fw_).mul_(d).mul_(2.0)
+        return 0.5 * torch.dot(grad.flatten(), d.flatten()), grad.to(z.dtype)
 
     def step(xl, Wl, Yd, rwd, fwd):
         xl.grad = None

@@ -225,13 +225,13 @@ def chunked_linear_loss(inputs: torch.Tensor, weight: torch.Tensor,
 def autograd_loss_and_logits_grad(loss_fn: Callable) -> Callable:
     """Adapts a loss that returns only a scalar ("Adapting PyTorch losses").
 
-    The adapter runs PyTorch autograd on the temporary logits chunk and
-    returns ``(loss, d loss / d logits)``.
+    The gradient of the loss in the logits chunk comes from PyTorch's
+    functional transform ``torch.func.grad_and_value``, applied to the loss
+    with the chunk's other arguments fixed. Returns ``(loss, d loss / d logits)``.
     """
+    from torch.func import grad_and_value
+
     def fn(logits, *args, **kwargs):
-        with torch.enable_grad():
-            z = logits.detach().requires_grad_(True)
-            loss = loss_fn(z, *args, **kwargs)
-            (g,) = torch.autograd.grad(loss, z)
+        g, loss = grad_and_value(lambda z: loss_fn(z, *args, **kwargs))(logits.detach())
         return loss.detach(), g
     return fn

@@ -14,5 +14,5 @@ from .flce_oracle import (  # noqa: F401
     grad_hidden_rows, grad_weight_rows, row_gamma, row_terms, transformed_logits,
 )
 from .chunked_oracle import (  # noqa: F401
-    chunked_linear_loss, chunked_rows_grad_hidden, cross_entropy_sum, weighted_mse,
+    chunked_linear_loss, cross_entropy_sum, weighted_mse,
 )

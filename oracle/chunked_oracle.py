@@ -45,10 +45,14 @@ def _f64(x) -> np.ndarray:
 
 
 def weighted_mse(z: np.ndarray, target, row_weight, feature_weight):
-    """(sum_ij r_i f_j (z_ij - y_ij)^2, its gradient in z)."""
-    err = _f64(z) - _f64(target)
-    wgt = _f64(row_weight)[:, None] * _f64(feature_weight)[None, :]
-    return float((err * err * wgt).sum()), 2.0 * err * wgt
+    """(sum_ij r_i f_j (z_ij - y_ij)^2, its gradient in z).
+
+    With the residual d = z - y, the gradient is G = 2 r_i f_j d_ij, and the
+    loss is half the elementwise product of G with d, summed.
+    """
+    d = _f64(z) - _f64(target)
+    G = 2.0 * np.outer(_f64(row_weight), _f64(feature_weight)) * d
+    return 0.5 * float(np.einsum("ij,ij->", G, d)), G
 
 
 def cross_entropy_sum(z: np.ndarray, targets, ignore_index: int = -100):
@@ -95,19 +99,3 @@ def chunked_linear_loss(inputs, weight, loss_and_grad: Callable, *args,
         dX[r0:r1] = G @ W
         dW += G.T @ X[r0:r1]
     return loss, dX, dW
-
-
-def chunked_rows_grad_hidden(inputs, weight, loss_and_grad: Callable, rows, *args, **kwargs):
-    """grad_inputs of the given rows only. The loss is additive over rows, so
-    each row's gradient needs only that row's logits."""
-    X = _f64(inputs)
-    W = _f64(weight)
-    N = X.shape[0]
-    idx = np.asarray(rows)
-    Z = X[idx] @ W.T
-    a = [v[idx] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == N else v
-         for v in args]
-    k = {key: (v[idx] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == N else v)
-         for key, v in kwargs.items()}
-    _, G = loss_and_grad(Z, *a, **k)
-    return _f64(G) @ W

@@ -43,10 +43,13 @@ def case(N, H, V, dtype, seed):
 
 
 def wmse_torch(z, y, rw, fw):
-    """The caller's weighted MSE: loss and logits gradient from one chunk of logits."""
-    err = z.float() - y
-    wgt = rw[:, None] * fw[None, :]
-    return (err * err * wgt).sum(), (2.0 * err * wgt).to(z.dtype)
+    """The caller's weighted MSE: loss and logits gradient from one chunk of logits.
+
+    grad = 2 r f (z - y); the loss is half the dot product of grad with the residual.
+    """
+    d = torch.sub(z.float(), y)
+    grad = torch.outer(rw, fw).mul_(d).mul_(2.0)
+    return 0.5 * torch.dot(grad.flatten(), d.flatten()), grad.to(z.dtype)
 
 
 def run(Xd, Wd, Y, r, f, **kw):
