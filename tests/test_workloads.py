@@ -65,3 +65,18 @@ def test_fp16_rounding_matches_torch():
     ref = torch.from_numpy(x).to(torch.float16)
     np.testing.assert_array_equal(bits, ref.view(torch.int16).numpy().view(np.uint16))
     np.testing.assert_array_equal(vals, ref.float().numpy())
+
+
+def test_regression_workload_generator():
+    """The generic chunked linear loss's workload: seeded, shapes and distributions."""
+    w = wl.REGRESSION_WORKLOADS["mse_v32768"].replace(N=600, H=64, V=900)
+    a = wl.generate_regression(w, threads=1)
+    b = wl.generate_regression(w, threads=5)
+    for k in ("hidden", "weight", "target", "row_weight", "feature_weight", "hidden_bits"):
+        np.testing.assert_array_equal(a[k], b[k])
+    assert a["target"].shape == (600, 900) and a["target"].dtype == np.float32
+    assert a["row_weight"].shape == (600,) and a["feature_weight"].shape == (900,)
+    assert 0.5 <= a["row_weight"].min() and a["row_weight"].max() <= 1.5
+    np.testing.assert_array_equal(wl.bf16_bits_to_f32(a["weight_bits"]), a["weight"])
+    assert abs(a["target"].std() - 1.0) < 0.02
+    assert w.flops_fwd_bwd == 6 * 600 * 64 * 900
