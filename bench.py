@@ -64,8 +64,9 @@ def load_peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return dict(bf16_burst=d.get("bf16_tflops"), bf16_sustained=d.get("bf16_tflops_sustained"),
-                    hbm=d.get("hbm_gbs"), source="measured")
-    return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+                    hbm=d.get("hbm_gbs"), sm_max_mhz=d.get("sm_max_mhz"), source="measured")
+    return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm=6800.0, sm_max_mhz=2070.0,
+                source="fallback")
 
 
 class ClockSampler:
@@ -123,9 +124,15 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
     """
     if name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc",
                 "flce_chunk_logits_tc", "flce_chunk_mse_tc", "flce_chunk_grad_hidden_tc",
-                "flce_chunk_grad_weight_tc"):
+                "flce_chunk_grad_weight_tc", "flce_fwd_simt", "flce_dlogits_simt",
+                "flce_grad_hidden_simt", "flce_grad_weight_simt"):
         return 2.0 * w.N * w.H * w.V
     return 0.0
+
+
+def fp32_alu_peak(sms: int, sm_max_mhz: float) -> float:
+    """fp32 FFMA peak in TFLOP/s: SMs x 128 fp32 lanes x 2 FLOP x the maximum SM clock."""
+    return sms * 128 * 2 * sm_max_mhz * 1e6 / 1e12
 
 
 def sources_digest() -> str:
@@ -472,7 +479,15 @@ def ours_main(args, w):
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None
         roof = None
-        if dom is not None and dom["tflops"] is not None:
+        if dom is not None and dom["tflops"] is not None and dom["name"].endswith("_simt"):
+            # fp32 inputs run on FFMA: the bound is the fp32 ALU, not the tensor cores
+            props = torch.cuda.get_device_properties(dev)
+            peak = fp32_alu_peak(props.multi_processor_count, peaks.get("sm_max_mhz") or 2070.0)
+            roof = {"bound": "alu", "kernel": dom["name"], "achieved": dom["tflops"],
+                    "peak": peak, "unit": "TFLOP/s", "frac": dom["tflops"] / peak,
+                    "peak_kind": "fp32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock",
+                    "traffic": None}
+        elif dom is not None and dom["tflops"] is not None:
             roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                     "frac": dom["tflops"] / peaks["bf16_sustained"],

@@ -181,6 +181,20 @@ constexpr size_t kScaleOffset = 64;
 constexpr size_t kChunkByteCap = size_t(4) << 30;
 constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_splits)
 
+// K splits of a SIMT (fp32) GEMM: enough 64 x 64 output tiles times splits to
+// fill the GPU (about 256 blocks), at least 512 of K per split, at most 16,
+// and at most K / (2 N), so that the split partials (s x M x N) hold no more
+// than half of the A operand (M x K, the dlogits chunk). A function of the
+// shape only, so the workspace query and the launch agree.
+int simt_k_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
+  int64_t s = (256 + tiles - 1) / tiles;
+  if (s > K / 512) s = K / 512;
+  if (s > K / (2 * N)) s = K / (2 * N);
+  if (s > 16) s = 16;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
 struct FwdLayout {
   int num_panels_max;
   int nblk;
@@ -320,7 +334,12 @@ BwdLayout bwd_layout(const flce_params* p) {
   if (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
     o = align_up(o + size_t(V) * H * 4, 1024);
   L.dh_part = o;
-  if (tensor_path(p)) o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
+  if (tensor_path(p)) {
+    o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
+  } else if (N > 0) {
+    const int s = simt_k_splits(L.chunk, H, V);   // fp32 grad_hidden split partials
+    if (s > 1) o = align_up(o + size_t(s) * L.chunk * H * 4, 1024);
+  }
   L.bias_part = o;
   if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
   L.total = o;
@@ -480,7 +499,12 @@ ChunkLayout chunk_layout(const flce_params* p) {
   if (tensor_path(p) && p->grad_weight_accum == FLCE_ACCUM_FP32)
     o = align_up(o + size_t(p->V) * p->H * 4, 1024);
   L.dh_part = o;
-  if (tensor_path(p)) o = align_up(o + size_t(kMaxKSplits) * p->N * p->H * 4, 1024);
+  if (tensor_path(p)) {
+    o = align_up(o + size_t(kMaxKSplits) * p->N * p->H * 4, 1024);
+  } else {
+    const int s = simt_k_splits(p->N, p->H, p->V);
+    if (s > 1) o = align_up(o + size_t(s) * p->N * p->H * 4, 1024);
+  }
   L.total = o;
   return L;
 }
@@ -1073,6 +1097,10 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.C = static_cast<float*>(grad_hidden) + size_t(row0) * H;
         ga.ldc = H;
         ga.accumulate = p->accumulate;
+        // K = V is long and the chunk's output is small: split K, sized for
+        // the full chunk so that the workspace holds every chunk's partials
+        ga.k_splits = simt_k_splits(L.chunk, H, V);
+        ga.part = reinterpret_cast<float*>(ws + L.dh_part);
         v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
@@ -1296,6 +1324,8 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
       ga.C = static_cast<float*>(grad_hidden);
       ga.ldc = H;
       ga.accumulate = p->accumulate;
+      ga.k_splits = simt_k_splits(N, H, V);
+      ga.part = reinterpret_cast<float*>(ws + L.dh_part);
       v = launch("flce_chunk_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
       if (v != FLCE_OK) return v;
     }

@@ -38,7 +38,7 @@ constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;
 
 // ---- fp32 SIMT path tile shape -------------------------------------------
 constexpr int kSimtTile = 64;        // 64 x 64 logit tiles
-constexpr int kSimtPanelCols = 512;  // columns per partial-state panel
+constexpr int kSimtPanelCols = 256;  // columns per partial-state panel (fp32 forward)
 constexpr int kSimtThreads = 256;
 
 // Per (panel, row) partial state of the online log-sum-exp:
@@ -245,6 +245,12 @@ struct SimtGemmArgs {
   float* C;                    // C[m*ldc + n]
   long long ldc;
   int accumulate;              // 1: C += A B, 0: C = A B
+  // k_splits > 1: split s of the K range stores its fp32 product to
+  // part + s * M * N ([M][N], row-major), and a second kernel sums the splits
+  // in order into C (adding C when accumulate). For outputs with few 64 x 64
+  // tiles and a long K.
+  int k_splits;
+  float* part;
 };
 
 struct BiasReduceArgs {

@@ -173,17 +173,21 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
   __shared__ float Bs[GK][T + 4];
   const int m0 = blockIdx.y * T, n0 = blockIdx.x * T;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  // this block's K range: all of K, or split blockIdx.z of k_splits
+  const int kc = a.k_splits > 1 ? (a.K + a.k_splits - 1) / a.k_splits : a.K;
+  const int kb = static_cast<int>(blockIdx.z) * kc;
+  const int ke = min(a.K, kb + kc);
   float acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < a.K; k0 += GK) {
+  for (int k0 = kb; k0 < ke; k0 += GK) {
     for (int e = tid; e < T * GK; e += kSimtThreads) {
       const int kk = e / T, mm = e % T;
       const int k = k0 + kk;
-      As[kk][mm] = (m0 + mm < a.M && k < a.K) ? a.A[(m0 + mm) * a.sam + k * a.sak] : 0.f;
-      Bs[kk][mm] = (n0 + mm < a.N && k < a.K) ? a.B[k * a.sbk + (n0 + mm) * a.sbn] : 0.f;
+      As[kk][mm] = (m0 + mm < a.M && k < ke) ? a.A[(m0 + mm) * a.sam + k * a.sak] : 0.f;
+      Bs[kk][mm] = (n0 + mm < a.N && k < ke) ? a.B[k * a.sbk + (n0 + mm) * a.sbn] : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -208,9 +212,25 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= a.N) continue;
-      float* c = a.C + m * a.ldc + n;
-      *c = a.accumulate ? *c + acc[i][j] : acc[i][j];
+      if (a.k_splits > 1) {
+        a.part[(static_cast<size_t>(blockIdx.z) * a.M + m) * a.N + n] = acc[i][j];
+      } else {
+        float* c = a.C + m * a.ldc + n;
+        *c = a.accumulate ? *c + acc[i][j] : acc[i][j];
+      }
     }
+  }
+}
+
+// C[m][n] (+)= sum over s of part[s][m][n], in split order.
+__global__ void __launch_bounds__(256) simt_split_reduce_kernel(const SimtGemmArgs a) {
+  const long long total = static_cast<long long>(a.M) * a.N;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += 256ll * gridDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < a.k_splits; ++z) s += a.part[z * total + i];
+    const int m = static_cast<int>(i / a.N), n = static_cast<int>(i - static_cast<long long>(m) * a.N);
+    float* c = a.C + m * a.ldc + n;
+    *c = a.accumulate ? *c + s : s;
   }
 }
 
@@ -228,8 +248,14 @@ cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cuda
 }
 
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s) {
-  dim3 grid((a.N + T - 1) / T, (a.M + T - 1) / T);
+  const int splits = a.k_splits > 1 ? a.k_splits : 1;
+  dim3 grid((a.N + T - 1) / T, (a.M + T - 1) / T, splits);
   gemm_simt_kernel<<<grid, kSimtThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  const long long total = static_cast<long long>(a.M) * a.N;
+  const int blocks = static_cast<int>(min(4096ll, (total + 255) / 256));
+  simt_split_reduce_kernel<<<blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
