@@ -6,8 +6,9 @@
 // operands to 10 mantissa bits, which is not enough. The schedule is the same
 // as the bf16 path: vocabulary panels with an online log-sum-exp (forward),
 // and a recompute -> dlogits -> two contractions backward. Only the tile
-// arithmetic differs. Speed is not a goal here. The fp32 workload is the small
-// 256 x 512 x 8192 case.
+// arithmetic differs. Speed is secondary to the 1e-5 accuracy bar; the work is
+// spread over enough blocks for small problems (256-column forward panels,
+// and a fixed-order K split for grad_hidden, whose output is small).
 #include <math.h>
 
 #include "kernels.h"
