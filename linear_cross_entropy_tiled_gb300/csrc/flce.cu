@@ -402,6 +402,28 @@ int choose_panel_tiles(int n_blocks, int group, int v_tiles, int pairs, int* gri
   return best;
 }
 
+// Row tiles per raster group of a plain GEMM (decode_unit). When a wave of
+// `pairs` tiles spans fewer than all column tiles, row-after-row order reads
+// every B strip once per row tile: the projection of a row chunk (K = H,
+// thousands of vocabulary columns) streamed all of W once per 256 rows.
+// Groups of row tiles whose A strips (256 x K x 2 bytes each) total about
+// 32 MB stay in L2 while the columns sweep past, so each B strip is read
+// once per group. Otherwise a wave already covers whole rows of tiles, and
+// the order stays row after row (a group of 1).
+int gemm_group_m(const GemmArgs& ga, int pairs) {
+  if (ga.n_tiles <= pairs) return 1;
+  const long long strip = static_cast<long long>(kPairM) * ga.kb_per_split * kBK * 2;
+  long long g = (32ll << 20) / strip;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < ga.m_tiles ? g : ga.m_tiles);
+}
+
+cudaError_t launch_gemm(const GemmOperand& op_a, const GemmOperand& op_b, GemmArgs ga, bool f16,
+                        int pairs, cudaStream_t st) {
+  ga.group_m = gemm_group_m(ga, pairs);
+  return launch_gemm_tc(op_a, op_b, ga, f16, pairs, st);
+}
+
 // K splits of the grad_hidden GEMM. Its long tiles (K = V) number only
 // rows/256 x H/256 (256 at the headline size), which is 3.37 waves on 76
 // pairs: the last wave runs a third full. Two K halves give 6.74 waves
@@ -922,7 +944,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.status = status;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_hidden_tc", st,
-                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
       if (grad_weight) {
@@ -955,7 +977,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.status = status;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
-                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
     }
@@ -1008,7 +1030,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         const int units = ga.num_tiles * ga.k_splits;
         const int g2 = units < d.pairs ? units : d.pairs;
         v = launch("flce_grad_hidden_tc", st,
-                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
         if (ga.k_splits > 1) {
           SplitReduceArgs ra2{};
@@ -1067,7 +1089,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.status = status;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
-                   [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
     }
@@ -1186,7 +1208,7 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
     const bool f16 = p->dtype == FLCE_F16;
     const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
     return launch("flce_chunk_logits_tc", st,
-                  [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+                  [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
   }
   SimtGemmArgs ga{};
   ga.M = N;
@@ -1267,7 +1289,7 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   ga.ld_out_t = ld_dlogits_t;
   const bool f16 = p->dtype == FLCE_F16;
   const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
-  v = launch("flce_chunk_mse_tc", st, [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+  v = launch("flce_chunk_mse_tc", st, [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
   if (v != FLCE_OK) return v;
   LossReduceArgs la{};
   la.part = ga.loss_part;
@@ -1379,7 +1401,7 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     const int units = ga.num_tiles * ga.k_splits;
     const int g2 = units < d.pairs ? units : d.pairs;
     v = launch("flce_chunk_grad_hidden_tc", st,
-               [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+               [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
     if (v != FLCE_OK) return v;
     if (ga.k_splits > 1) {
       SplitReduceArgs ra{};
@@ -1440,7 +1462,7 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     ga.status = status;
     const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
     v = launch("flce_chunk_grad_weight_tc", st,
-               [&] { return launch_gemm_tc(op_a, op_b, ga, f16, g2, st); });
+               [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
     if (v != FLCE_OK) return v;
   }
   return FLCE_OK;

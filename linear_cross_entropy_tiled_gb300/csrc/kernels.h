@@ -197,6 +197,7 @@ struct GemmArgs {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks, num_tiles;
   int k_splits, kb_per_split;
+  int group_m;                 // row tiles per raster group (decode_unit; 1: row after row)
   int a_mn, b_mn;              // 1: operand is MN-major in memory
   int a_atoms, b_atoms;        // full 64-column atoms in the operand's 3-D view (0: none)
   int mode;                    // GemmMode (kStorePart when k_splits > 1)

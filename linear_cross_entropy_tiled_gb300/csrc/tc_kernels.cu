@@ -684,6 +684,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
 // D = A B with fp32 accumulation; the two gradient contractions. Units
 // (split, tile) go round-robin over the pairs: consecutive units are
 // neighbouring tiles of the same K range, which share an operand strip in L2.
+// Tiles are rastered in groups of `group_m` row tiles, column after column
+// within a group (decode_unit), so that with many column tiles the group's
+// A strips stay in L2 while each B strip is read once per group.
 // The arguments are copied into registers up front; the role loops read no
 // kernel parameters.
 template <typename T, bool kMse>
@@ -699,19 +702,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
   const int M = a.M, N = a.N, n_tiles = a.n_tiles, num_tiles = a.num_tiles;
+  const int m_tiles = a.m_tiles, group_m = a.group_m;
   const int k_blocks = a.k_blocks, kb_per_split = a.kb_per_split;
   const int units = num_tiles * a.k_splits;
   const bool a_mn = a.a_mn != 0, b_mn = a.b_mn != 0;
   const int a_atoms = a.a_atoms, b_atoms = a.b_atoms;
 
-  // (split, tile) of every unit of this pair
+  // Every unit of this pair as (row tile << 8 | split, column tile), decoded
+  // once per tile: the per-stage work of the single producer thread stays
+  // free of divisions. Splits number at most 255 (the host uses at most 2).
   auto for_each_tile = [&](auto&& f) {
     for (int u = pair; u < units; u += npairs) {
       const int sp = u / num_tiles;
-      f(sp, u - sp * num_tiles);
+      int mt, nt;
+      decode_unit(u - sp * num_tiles, m_tiles, group_m, n_tiles, nt, mt);
+      f((mt << 8) | sp, nt);
     }
   };
-  auto kblocks_of = [&](int sp, int) {
+  auto kblocks_of = [&](int ta, int) {
+    const int sp = ta & 255;
     return min(k_blocks, (sp + 1) * kb_per_split) - sp * kb_per_split;
   };
 
@@ -724,8 +733,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       const uint64_t pol = l2_policy_evict_normal();
       const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
       producer_role(s, g, kblocks_of, rank == 0, for_each_tile,
-                    [&](int sp, int t, int kb_rel, uint8_t* da, uint8_t* db, uint32_t bar) {
-                      const int mt = t / n_tiles, nt = t - mt * n_tiles;
+                    [&](int ta, int nt, int kb_rel, uint8_t* da, uint8_t* db, uint32_t bar) {
+                      const int sp = ta & 255, mt = ta >> 8;
                       const int m0 = mt * kPairM + m_off, n0 = nt * kBN + n_off;
                       const int k0 = (sp * kb_per_split + kb_rel) * kBK;
                       if (a_mn) {
@@ -786,7 +795,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     bool dead = false;
     for (int u = pair; u < units; u += npairs) {
       const int sp = u / num_tiles, t = u - sp * num_tiles;
-      const int mt = t / n_tiles, nt = t - mt * n_tiles;
+      int mt, nt;
+      decode_unit(t, m_tiles, group_m, n_tiles, nt, mt);
       float* const part = part0 + static_cast<size_t>(sp) * split_stride;
       dead = !epi_wait_full(s, acc, acc_phase, g, dead);
       if (!dead) {
@@ -982,6 +992,9 @@ cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const
 
 cudaError_t launch_gemm_tc(const GemmOperand& op_a, const GemmOperand& op_b, const GemmArgs& a,
                            bool f16, int grid, cudaStream_t st) {
+  if (a.group_m < 1 || a.m_tiles < 1 || a.n_tiles < 1 || a.k_splits < 1 || a.k_splits > 255 ||
+      a.m_tiles > (1 << 22))
+    return cudaErrorInvalidValue;
   return f16 ? launch_gemm_t<__half>(op_a, op_b, a, grid, st)
              : launch_gemm_t<__nv_bfloat16>(op_a, op_b, a, grid, st);
 }
