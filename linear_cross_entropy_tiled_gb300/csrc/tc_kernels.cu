@@ -493,8 +493,7 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&x)[32], int lane) 
 
 template <typename T, bool kRagged, bool kBias, bool kSoftcap>
 __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& a, int col0,
-                                         float4 cf, bool row_ok, int row_local, float ds_mul,
-                                         float (&gout)[32]) {
+                                         float4 cf, bool row_ok, float (&gout)[32]) {
   float bs[32];
   if (kBias) load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
   const int tgt = __float_as_int(cf.w) - a.tgt_base;  // no target (-1) stays negative
@@ -513,55 +512,58 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&v)[32], const DsArgs& 
     if (kRagged && col0 + j >= a.V) gj = 0.f;
     gout[j] = row_ok ? gj : 0.f;
   }
-  if (row_ok) {
-    // fp16 stores dlogits times a power of two (ds_mul), which keeps the small
-    // probabilities out of the fp16 subnormal range; the GEMMs undo it exactly.
-    T* dst = static_cast<T*>(a.ds) + static_cast<size_t>(row_local) * a.V_pad + col0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (kRagged && col0 + q * 8 >= a.V) break;
-      uint4 w;
-      w.x = Elem<T>::pack(gout[q * 8 + 0] * ds_mul, gout[q * 8 + 1] * ds_mul);
-      w.y = Elem<T>::pack(gout[q * 8 + 2] * ds_mul, gout[q * 8 + 3] * ds_mul);
-      w.z = Elem<T>::pack(gout[q * 8 + 4] * ds_mul, gout[q * 8 + 5] * ds_mul);
-      w.w = Elem<T>::pack(gout[q * 8 + 6] * ds_mul, gout[q * 8 + 7] * ds_mul);
-      *reinterpret_cast<uint4*>(dst + q * 8) = w;
-    }
-  }
 }
 
-// Stores a warp's 32 rows x 32 columns of g (times mul) transposed: row c
-// of dst_t holds column c for every row. Each lane pair swaps one value, so
-// that every lane writes two neighbouring rows of one column as one 32-bit
-// word and a warp store covers 64 contiguous bytes of two dst_t rows. `row_w`
-// is the warp's first row; rows >= rows and columns >= cols are not written.
-// ld_t must be even. All 32 lanes must call it (it shuffles).
+// 32 values of one row times mul, as 16 words of two neighbouring columns
+// in the element type: word i holds columns 2i (low half) and 2i + 1.
 template <typename T>
-__device__ __forceinline__ void store_transposed32(const float (&g)[32], T* dst_t, long long ld_t,
-                                                   int col0, int row_w, int lane, int rows,
-                                                   int cols, float mul, bool live) {
+__device__ __forceinline__ void pack32(const float (&g)[32], float mul, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = Elem<T>::pack(g[2 * i] * mul, g[2 * i + 1] * mul);
+}
+
+// One row's 32 packed columns, row-major, as four 16-byte pieces; a piece is
+// written if its first column is below `cols` (the padding up to the next
+// multiple of 8 columns receives the packed zeros).
+template <typename T>
+__device__ __forceinline__ void store_row_packed(const uint32_t (&w)[16], T* dst, int col0,
+                                                 int cols) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (col0 + q * 8 < cols)
+      *reinterpret_cast<uint4*>(dst + q * 8) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Stores a warp's 32 rows x 32 columns, packed by pack32, transposed: row c
+// of dst_t holds column c for every row. Lanes 2k and 2k + 1 (rows row_w + 2k
+// and row_w + 2k + 1) swap their word of columns (2i, 2i + 1); a byte
+// permute then gives the even lane the word of column 2i for both rows and
+// the odd lane that of column 2i + 1, so a warp store covers 64 contiguous
+// bytes of two dst_t rows. Rows >= rows and columns >= cols are not written
+// (a pair whose first row is below `rows` is written whole; ld_t must be
+// even). All 32 lanes must call it (it shuffles).
+template <typename T>
+__device__ __forceinline__ void store_transposed_packed(const uint32_t (&w)[16], T* dst_t,
+                                                        long long ld_t, int col0, int row_w,
+                                                        int lane, int rows, int cols, bool live) {
   const bool odd = (lane & 1) != 0;
   const int row_pair = row_w + (lane & ~1);  // the first of this lane's two rows
-  T* const base = dst_t + row_pair;
+  // even lane: (own low half, partner's low half); odd: (partner's high, own high)
+  const uint32_t sel = odd ? 0x3276u : 0x5410u;
+  const int c_first = col0 + (odd ? 1 : 0);
+  T* const base = dst_t + static_cast<size_t>(c_first) * ld_t + row_pair;
+  const size_t step = 2 * static_cast<size_t>(ld_t);
+  // warp-uniform: the whole 32 x 32 block is inside
+  const bool inside = live && row_w + 32 <= rows && col0 + 32 <= cols;
+  const bool row_in = live && row_pair < rows;
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    const float recv = __shfl_xor_sync(kFull, odd ? g[2 * jj] : g[2 * jj + 1], 1);
-    const float lo = odd ? recv : g[2 * jj];
-    const float hi = odd ? g[2 * jj + 1] : recv;
-    const int col = col0 + 2 * jj + (odd ? 1 : 0);
-    if (live && row_pair < rows && col < cols)
-      *reinterpret_cast<uint32_t*>(base + static_cast<size_t>(col) * ld_t) =
-          Elem<T>::pack(lo * mul, hi * mul);
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t recv = __shfl_xor_sync(kFull, w[i], 1);
+    const uint32_t out = __byte_perm(w[i], recv, sel);
+    if (inside || (row_in && c_first + 2 * i < cols))
+      *reinterpret_cast<uint32_t*>(base + i * step) = out;
   }
-}
-
-// dlogits transposed for grad_weight: row v of ds_t holds column v for every
-// row of the chunk.
-template <typename T>
-__device__ __forceinline__ void store_ds_t(const float (&g)[32], const DsArgs& a, int col0,
-                                          int row_w, int lane, float ds_mul, bool live) {
-  store_transposed32<T>(g, static_cast<T*>(a.ds_t), a.ld_t, col0, row_w, lane, a.rows, a.V,
-                        ds_mul, live);
 }
 
 template <typename T, bool kBias, bool kSoftcap>
@@ -640,9 +642,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
                       v);
             tmem_ld_wait(v);
             if (!ragged) {
-              ds_chunk<T, false, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, ds_mul, gv);
+              ds_chunk<T, false, kBias, kSoftcap>(v, a, col0, cf, row_ok, gv);
             } else if (col0 < a.V) {
-              ds_chunk<T, true, kBias, kSoftcap>(v, a, col0, cf, row_ok, row_local, ds_mul, gv);
+              ds_chunk<T, true, kBias, kSoftcap>(v, a, col0, cf, row_ok, gv);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) gv[j] = 0.f;
@@ -651,8 +653,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) gv[j] = 0.f;
           }
+          // dlogits in the input type, packed once for both layouts. fp16
+          // stores dlogits times a power of two (ds_mul), which keeps the
+          // small probabilities out of the fp16 subnormal range; the GEMMs
+          // undo it exactly. bf16 is stored unscaled.
+          uint32_t w[16];
+          pack32<T>(gv, Elem<T>::kBf16 ? 1.f : ds_mul, w);
+          if (!dead && row_ok && col0 < a.V) {
+            T* const row = static_cast<T*>(a.ds) + static_cast<size_t>(row_local) * a.V_pad;
+            store_row_packed<T>(w, row + col0, col0, a.V);
+          }
           if (a.ds_t != nullptr)
-            store_ds_t<T>(gv, a, col0, row_local - lane, lane, ds_mul, !dead);
+            store_transposed_packed<T>(w, static_cast<T*>(a.ds_t), a.ld_t, col0, row_local - lane,
+                                       lane, a.rows, a.V, !dead);
           if (a.bias_part != nullptr) {
             const float cs = warp_transpose_sum32(gv, lane);
             colsum[q * kBN + c * 32 + lane] = cs;
@@ -847,10 +860,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
               lsum = fmaf(we, e, lsum);
               d[j] = 2.f * we;
             }
+            uint32_t w[16];
+            pack32<T>(d, 1.f, w);
             if (a.out_t != nullptr)
-              store_transposed32<T>(d, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane, lane,
-                                    M, N, 1.f, true);
-            if (!row_ok) continue;
+              store_transposed_packed<T>(w, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane,
+                                         lane, M, N, true);
+            if (row_ok) store_row_packed<T>(w, out + static_cast<size_t>(m) * ld_out + col0, col0, N);
+            continue;
           }
           if (add_part) {
             const float4* src =
