@@ -43,3 +43,22 @@ def test_kernel_flops_count_each_contraction_once_per_step():
     r = wl.REGRESSION_WORKLOADS["mse_v32768"]
     names = ("flce_chunk_mse_tc", "flce_chunk_grad_hidden_tc", "flce_chunk_grad_weight_tc")
     assert sum(bench.kernel_flops(n, r) for n in names) == r.flops_fwd_bwd
+
+
+def test_reference_leg_under_torchrun_prints_once_from_rank_0():
+    """With two ranks the reference leg runs on rank 0 alone; rank 1 exits 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), "bench.py", "--impl", "reference",
+                          "--gpus", "2", "--workload", "tiny_f32", "--steps", "1", "--warmup", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600,
+                         env=dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="4"))
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
