@@ -59,6 +59,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: each rank's value all-reduced with MAX (no-op for one rank)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(world: int, rows_per_rank: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's rows over the slowest rank's step time."""
+    return world * rows_per_rank / (ms * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -358,10 +374,7 @@ def ours_main(args, w):
     kernels = _lib.profiling_read()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     _lib.check(_lib.check_status(bws.data_ptr(), stream.cuda_stream), "timed backward")
 
     # ---------------- forward only (2NHV), timed the same way ----------------
@@ -377,7 +390,7 @@ def ours_main(args, w):
             flce_forward(p, h, W, t, b, return_metrics=w.metrics, workspace=fws)
         g1.record(stream)
         barrier()
-        fwd_ms = g0.elapsed_time(g1) / args.steps
+        fwd_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world, dev)
     # No single buffer of the default schedule may reach the size of the N x V
     # logits in bf16. (Forcing row chunks at N < V adds the fp32 [V, H]
     # grad_weight partial to the workspace, which can.)
@@ -451,11 +464,8 @@ def ours_main(args, w):
         f1.record(stream)
         barrier()
         ems = f0.elapsed_time(f1) / e2e_steps
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
-        e2e = {"value": world * w.N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        ems = max_over_ranks(ems, world, dev)
+        e2e = {"value": job_rate(world, w.N, ems), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(loss_host.numel() * 4), "ms_per_step": ems,
                "steps": e2e_steps, "api": "fused_linear_cross_entropy + backward",
                "copies": "pinned host -> device on a side stream, next step's inputs during this step's compute"}
@@ -499,7 +509,7 @@ def ours_main(args, w):
             cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                    "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64 ({tcpu:.1f} s)"}
         line = {
-            "metric": METRIC, "value": world * w.N / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": job_rate(world, w.N, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; inputs generated on the host)",
@@ -513,7 +523,7 @@ def ours_main(args, w):
             "variant": {"dtype": w.dtype, "grad_weight_accum": args.grad_weight_accum,
                         "vocab_shards": args.vocab_shards},
             "forward": None if fwd_ms is None else {
-                "ms_per_step": fwd_ms, "tokens_per_s": world * w.N / (fwd_ms * 1e-3),
+                "ms_per_step": fwd_ms, "tokens_per_s": job_rate(world, w.N, fwd_ms),
                 "tflops": 2.0 * w.N * w.H * w.V / (fwd_ms * 1e-3) / 1e12},
             "largest_workspace_bytes": int(largest),
             "logits_bytes_avoided": w.logits_bytes_avoided,
@@ -616,10 +626,7 @@ def chunked_main(args, w):
     kernels = _lib.profiling_read()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
 
     e2e = None
     if not args.no_e2e:
@@ -643,8 +650,8 @@ def chunked_main(args, w):
             e2e_step()
         f1.record(stream)
         barrier()
-        ems = f0.elapsed_time(f1) / e2e_steps
-        e2e = {"value": world * w.N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        ems = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, dev)
+        e2e = {"value": job_rate(world, w.N, ems), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ms_per_step": ems, "steps": e2e_steps,
                "api": "chunked_linear_loss + backward"}
 
@@ -680,7 +687,7 @@ def chunked_main(args, w):
             cpu = {"value": n / tcpu, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
                    "sample": f"{n} of {w.N} rows, full V and H, fwd+bwd in fp64 ({tcpu:.1f} s)"}
         line = {
-            "metric": CHUNKED_METRIC, "value": world * w.N / (ms * 1e-3), "unit": UNIT,
+            "metric": CHUNKED_METRIC, "value": job_rate(world, w.N, ms), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded; inputs generated on the host)",

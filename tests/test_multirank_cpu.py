@@ -177,3 +177,30 @@ def test_two_rank_vocabulary_parallel_head_matches_the_oracle():
     np.testing.assert_allclose(lse, ref["lse"], rtol=1e-13)
     np.testing.assert_allclose(gh, rh, rtol=1e-11, atol=1e-14)
     np.testing.assert_allclose(gw, rw, rtol=1e-11, atol=1e-14)
+
+
+def _timing_rank_main(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = bench.max_over_ranks(10.0 + 7.5 * rank, world, torch.device("cpu"))
+    q.put((rank, ms, bench.job_rate(world, 8192, ms)))
+    dist.destroy_process_group()
+
+
+def test_bench_reports_the_slowest_rank_and_every_ranks_tokens():
+    """bench.py's timing: the max over ranks of the step time, and all ranks' rows over it."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_timing_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, rate in res:
+        assert ms == 17.5                       # rank 1's 17.5 ms, seen by both ranks
+        assert rate == pytest.approx(2 * 8192 / 17.5e-3)
