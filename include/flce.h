@@ -37,7 +37,8 @@
  * Conventions common to every entry point:
  * - Pointers named "device" must point to device memory of the current CUDA
  *   device. All tensors are dense and row-major (the last index moves
- *   fastest) and 16-byte aligned.
+ *   fastest) and 16-byte aligned, unless an entry point below states a
+ *   smaller alignment for one of its arguments.
  * - The caller owns every buffer. The library allocates no device memory. It
  *   keeps only small per-device host state: attributes, tensor-map encoder,
  *   profiling events.
@@ -103,7 +104,8 @@ typedef enum { FLCE_ACCUM_FP32 = 0, FLCE_ACCUM_WEIGHT = 1 } flce_accum;
 enum {
   FLCE_OK = 0,
   FLCE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, dtype, reduction or scalar   */
-  FLCE_ERR_UNSUPPORTED = 2,  /* the current device is not sm_103 (GB300)            */
+  FLCE_ERR_UNSUPPORTED = 2,  /* the current device is not sm_103 (GB300), or the
+                                entry point does not take this dtype                */
   FLCE_ERR_ALIGNMENT = 3,    /* a pointer is not 16-B aligned, or H % 8 != 0       */
   FLCE_ERR_WORKSPACE = 4,    /* NULL workspace or ws_bytes below the required size */
   FLCE_ERR_CUDA = 5,         /* a CUDA runtime call failed                          */
@@ -139,11 +141,15 @@ typedef struct {
  * Device bytes the caller must provide as `workspace` for one pass. The
  * forward and backward need different amounts, and one workspace may serve
  * both passes in turn. For the headline size (N=8192, H=4096, V=128256,
- * bf16) the forward needs a few MB. The backward needs about 3.3 GB:
- * - a 4096-row bf16 dlogits chunk (1.05 GB);
- * - an fp32 grad_weight partial (2.1 GB);
- * - two fp32 K-split partials of the grad_hidden chunk (134 MB);
- * - per-128-row bias partial sums.
+ * bf16, with bias) the forward needs 16.5 MB and the backward 1.22 GB:
+ * - N < V, so the backward chunks the vocabulary: a quarter of V (32256
+ *   columns) of dlogits for all rows, row-major and transposed
+ *   (2 x 528 MB);
+ * - the fp32 grad_hidden partial carried across the chunks (134 MB);
+ * - per-128-row bias partial sums (33 MB).
+ * With N >= V it chunks rows instead and holds the fp32 grad_weight partial
+ * (V x H x 4 bytes) with FLCE_ACCUM_FP32. No workspace of either layout
+ * reaches the N x V x 2 bytes of the logits in 16 bits.
  * Returns FLCE_OK and sets *bytes, or an argument error.
  */
 int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
@@ -185,10 +191,15 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight,
  *   grad_weight device [V,H] dtype, or NULL to skip it
  *   grad_bias   device [V] dtype, or NULL to skip it (requires has_bias == 1
  *               when given)
- * dlogits is rounded to bf16 before the two bf16 contractions. grad_weight is
- * accumulated in fp32 across row chunks, in chunk order, and cast once
- * ("Chunked Linear Loss", section "Weight-gradient accumulation dtype", the
- * "fp32" default).
+ * dlogits is rounded to the input dtype (fp16: times an exact power of two)
+ * before the two contractions.
+ * - N < V (vocabulary chunks): grad_hidden is accumulated in fp32 across the
+ *   chunks, in chunk order, and cast once. Each grad_weight row is complete
+ *   after one contraction over all N rows.
+ * - N >= V (row chunks): grad_weight is accumulated across the chunks, in
+ *   chunk order, in fp32 and cast once ("Chunked Linear Loss", section
+ *   "Weight-gradient accumulation dtype", the "fp32" default), or in the
+ *   weight dtype with FLCE_ACCUM_WEIGHT.
  *   workspace   device, >= flce_workspace_bytes(p, FLCE_PASS_BACKWARD) bytes
  * With N == 0, the row-indexed pointers may be NULL. grad_weight and grad_bias
  * are then zero-filled.
