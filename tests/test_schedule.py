@@ -25,12 +25,14 @@ def _cuda_include():
     return None
 
 
-def test_decode_unit_visits_every_tile_once(tmp_path):
+def test_decode_unit_visits_every_tile_once():
     cxx = shutil.which("g++") or shutil.which("c++")
     inc = _cuda_include()
     if cxx is None or inc is None:
         pytest.skip("needs a host C++ compiler and the CUDA headers")
-    exe = str(tmp_path / "sched_check")
+    out_dir = os.path.join(os.path.dirname(HERE), "_build")   # git-ignored build folder
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "sched_check")
     build = subprocess.run([cxx, "-std=c++17", "-O1", "-I", inc, "-I", CSRC,
                             os.path.join(HERE, "sched_check.cc"), "-o", exe],
                            capture_output=True, text=True, timeout=300)
