@@ -215,13 +215,18 @@ def test_two_classes_softplus_and_one_class_zero():
     assert np.abs(gh).max() == 0 and np.abs(gw).max() == 0 and np.abs(gb).max() == 0
 
 
-def test_bias_shift_invariance():
+@pytest.mark.parametrize("shift", [3.25, 1000.0])
+def test_bias_shift_invariance(shift):
+    """A constant added to every logit changes nothing. At a shift of 1000 the
+    logits are far past exp's fp64 overflow (about 709), so this also pins the
+    max subtraction; the shift cancels in fp64 to about shift x 2^-52."""
     h, W, b, t = rnd(8, 7, 4, 11, ignore=(3,))
     a = oracle.forward(h, W, t, bias=b, reduction="mean", logit_scale=1.7)
-    c = oracle.forward(h, W, t, bias=b + 3.25, reduction="mean", logit_scale=1.7)
+    c = oracle.forward(h, W, t, bias=b + shift / 1.7, reduction="mean", logit_scale=1.7)
+    assert np.isfinite(c["loss"])
     assert a["loss"] == pytest.approx(c["loss"], rel=1e-12)
     ga = oracle.backward(h, W, t, bias=b, reduction="mean", logit_scale=1.7)
-    gc = oracle.backward(h, W, t, bias=b + 3.25, reduction="mean", logit_scale=1.7)
+    gc = oracle.backward(h, W, t, bias=b + shift / 1.7, reduction="mean", logit_scale=1.7)
     for x, y in zip(ga, gc):
         np.testing.assert_allclose(x, y, rtol=1e-10, atol=1e-13)
 
