@@ -115,3 +115,18 @@ def test_sliced_and_passed_through_arguments():
     assert seen == [(4, 4, 4, 9, 2.0), (2, 2, 2, 9, 2.0)]
     ref = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f)
     assert got[0] == pytest.approx(2 * ref[0], rel=1e-13)
+
+
+def test_cross_entropy_is_shift_invariant_past_exp_overflow():
+    """Adding 1000 to every logit (past exp's fp64 overflow near 709) changes
+    neither the summed cross-entropy nor its gradient: the log-sum-exp must
+    subtract the row maximum."""
+    g = np.random.default_rng(17)
+    z = g.standard_normal((9, 13))
+    t = g.integers(0, 13, 9)
+    t[2] = -100
+    l0, g0 = oracle.cross_entropy_sum(z, t)
+    l1, g1 = oracle.cross_entropy_sum(z + 1000.0, t)
+    assert np.isfinite(l1)
+    assert l1 == pytest.approx(l0, rel=1e-11)
+    np.testing.assert_allclose(g1, g0, rtol=1e-9, atol=1e-12)
