@@ -62,3 +62,17 @@ def test_reference_leg_under_torchrun_prints_once_from_rank_0():
     assert len(lines) == 1, out.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
+    """roofline.traffic comes from the committed DRAM capture, and only while
+    the kernel sources still match the digest recorded with it."""
+    d = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    wl_name = d["workload"]
+    kernel = next(iter(d["kernels"]))
+    assert d["sources_digest"] == bench.sources_digest()   # the capture is current
+    assert bench.traffic_for(kernel, wl_name) == d["kernels"][kernel]["bytes_per_launch"]
+    assert bench.traffic_for(kernel, "some_other_workload") is None
+    assert bench.traffic_for("no_such_kernel", wl_name) is None
+    monkeypatch.setattr(bench, "sources_digest", lambda: "changed")
+    assert bench.traffic_for(kernel, wl_name) is None
