@@ -8,9 +8,10 @@ bf16_v128256_bias_zloss: N=8192 tokens, H=4096, V=128256, bias, Zipf targets,
 5% ignored, z-loss 1e-4, mean reduction.
 
 Timing:
-- ``value`` is tokens/s with the inputs already resident in HBM. It is
-  measured with CUDA events over K steps on the launching stream, with a
-  barrier and a device synchronize on both sides, max over ranks.
+- ``value`` is tokens/s with the inputs already resident in HBM, from the
+  median step time. Each of the K steps is bracketed by CUDA events on the
+  launching stream; the K steps as a whole have a barrier and a device
+  synchronize on both sides. The slowest rank's median counts.
 - ``e2e`` is the same metric through the public PyTorch API with host
   buffers. Each step copies the step's inputs from pinned host memory and
   reads the loss back. The copy for the next step runs on a side stream,
@@ -18,9 +19,10 @@ Timing:
 - The inputs are larger than L2 (W alone is 1.05 GB), so no L2 flush is
   needed between steps.
 
-For N > 1 ranks (torchrun) every rank runs its own batch (weak scaling) and
-there is no collective on the data path. The only collective is the timing
-reduction.
+For N > 1 ranks every rank runs its own batch (weak scaling) and there is no
+collective on the data path. The only collective is the timing reduction.
+``--gpus N`` run without torchrun starts the N local ranks itself, through
+torch.distributed.run on 127.0.0.1.
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
 same workload. The oracle is the only reference implementation in this
@@ -57,6 +59,30 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def relaunch_ranks(n: int) -> int:
+    """Starts this command again as n local ranks under torch.distributed.run; returns its status."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def timed_region_peak(peaks: dict, region_ms: float) -> tuple[float, str]:
+    """The bf16 peak that matches the timed region's length.
+
+    The sustained figure is a cuBLAS loop run for seconds under the power cap;
+    the burst figure is a short run before the cap pulls the clock down. A
+    timed region shorter than two seconds is compared with the burst peak.
+    """
+    if region_ms >= 2000.0:
+        return peaks["bf16_sustained"], f"bf16 sustained ({peaks['source']}; timed region {region_ms / 1e3:.2f} s)"
+    return peaks["bf16_burst"], f"bf16 burst ({peaks['source']}; timed region {region_ms / 1e3:.2f} s)"
 
 
 def max_over_ranks(ms: float, world: int, device) -> float:
@@ -248,7 +274,7 @@ def reference_main(args, w):
                         bias=inputs["bias"], **kw)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    step_s = max(times) if times else t
+    step_s = statistics.median(times) if times else t
     value = n / step_s
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -301,7 +327,8 @@ def ours_main(args, w):
                          reduction=w.reduction, ignore_index=wl.IGNORE_INDEX,
                          logit_scale=w.logit_scale, softcap=w.softcap,
                          z_loss_multiplier=w.z_loss_multiplier, has_bias=w.bias,
-                         deterministic=w.deterministic, grad_weight_accum=args.grad_weight_accum)
+                         deterministic=w.deterministic, grad_weight_accum=args.grad_weight_accum,
+                         bwd_chunk_axis=args.bwd_chunk_axis)
     fws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD), dtype=torch.uint8, device=dev)
     bws = torch.empty(_lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD), dtype=torch.uint8, device=dev)
     gh, gw = torch.empty_like(h), torch.empty_like(W)
@@ -362,19 +389,20 @@ def ours_main(args, w):
     _lib.profiling_enable(True)
     _lib.profiling_read()  # clear
     stream = torch.cuda.current_stream(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
         step()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     barrier()
     _lib.profiling_enable(False)
     launches = _lib.launch_count() - n_launch0
     kernels = _lib.profiling_read()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, world, dev)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    region_ms = ev[0].elapsed_time(ev[-1])
+    ms = max_over_ranks(statistics.median(step_ms), world, dev)
+    mean_ms = max_over_ranks(region_ms / args.steps, world, dev)
     _lib.check(_lib.check_status(bws.data_ptr(), stream.cuda_stream), "timed backward")
 
     # ---------------- forward only (2NHV), timed the same way ----------------
@@ -395,7 +423,7 @@ def ours_main(args, w):
     # logits in bf16. (Forcing row chunks at N < V adds the fp32 [V, H]
     # grad_weight partial to the workspace, which can.)
     largest = max(fws.numel(), bws.numel())
-    if not os.environ.get("FLCE_BWD_CHUNKS"):
+    if args.bwd_chunk_axis == "auto":
         assert largest < w.N * w.V * 2, f"a {largest}-byte workspace reaches N*V*2 bytes"
 
     # ---------------- end to end, host buffers ----------------
@@ -468,7 +496,8 @@ def ours_main(args, w):
         e2e = {"value": job_rate(world, w.N, ems), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(loss_host.numel() * 4), "ms_per_step": ems,
                "steps": e2e_steps, "api": "fused_linear_cross_entropy + backward",
-               "copies": "pinned host -> device on a side stream, next step's inputs during this step's compute"}
+               "copies": "pinned host -> device on a side stream, next step's inputs during this step's compute",
+               "results_on_host": "the loss; the three gradients stay on the device, as in training"}
 
     if rank == 0:
         peaks = load_peaks()
@@ -483,9 +512,7 @@ def ours_main(args, w):
                          "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
         # the committed DRAM counts hold for the default schedule only
         default_variant = args.grad_weight_accum == "fp32" and args.vocab_shards == 1 and \
-            w.dtype == wl.WORKLOADS[w.name].dtype and not any(
-                os.environ.get(k) for k in ("FLCE_BWD_CHUNKS", "FLCE_MAX_CHUNK_ROWS",
-                                            "FLCE_MAX_CHUNK_COLS"))
+            w.dtype == wl.WORKLOADS[w.name].dtype and args.bwd_chunk_axis == "auto"
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None
         roof = None
@@ -498,10 +525,12 @@ def ours_main(args, w):
                     "peak_kind": "fp32 FFMA: SMs x 128 lanes x 2 FLOP x max SM clock",
                     "traffic": None}
         elif dom is not None and dom["tflops"] is not None:
+            peak, kind = timed_region_peak(peaks, region_ms)
             roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
-                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": dom["tflops"] / peaks["bf16_sustained"],
-                    "peak_kind": f"bf16 sustained ({peaks['source']})",
+                    "peak": peak, "unit": "TFLOP/s", "frac": dom["tflops"] / peak,
+                    "peak_kind": kind,
+                    "frac_of_burst": dom["tflops"] / peaks["bf16_burst"],
+                    "frac_of_sustained": dom["tflops"] / peaks["bf16_sustained"],
                     "traffic": traffic_for(dom["name"], w.name) if default_variant else None}
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -511,6 +540,7 @@ def ours_main(args, w):
         line = {
             "metric": METRIC, "value": job_rate(world, w.N, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_mean": mean_ms, "timing": "median of per-step CUDA events",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; inputs generated on the host)",
             "config": workload_config(w),
@@ -521,7 +551,7 @@ def ours_main(args, w):
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "kernels": kern,
             "variant": {"dtype": w.dtype, "grad_weight_accum": args.grad_weight_accum,
-                        "vocab_shards": args.vocab_shards},
+                        "vocab_shards": args.vocab_shards, "bwd_chunk_axis": args.bwd_chunk_axis},
             "forward": None if fwd_ms is None else {
                 "ms_per_step": fwd_ms, "tokens_per_s": job_rate(world, w.N, fwd_ms),
                 "tflops": 2.0 * w.N * w.H * w.V / (fwd_ms * 1e-3) / 1e12},
@@ -614,19 +644,20 @@ def chunked_main(args, w):
     _lib.profiling_enable(True)
     _lib.profiling_read()
     stream = torch.cuda.current_stream(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
         step(x, Wt, Y, rw, fw)
-    e1.record(stream)
+        ev[i + 1].record(stream)
     barrier()
     _lib.profiling_enable(False)
     launches = _lib.launch_count() - n_launch0
     kernels = _lib.profiling_read()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, world, dev)
+    region_ms = ev[0].elapsed_time(ev[-1])
+    ms = max_over_ranks(statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)),
+                        world, dev)
+    mean_ms = max_over_ranks(region_ms / args.steps, world, dev)
 
     e2e = None
     if not args.no_e2e:
@@ -653,7 +684,8 @@ def chunked_main(args, w):
         ems = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, world, dev)
         e2e = {"value": job_rate(world, w.N, ems), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ms_per_step": ems, "steps": e2e_steps,
-               "api": "chunked_linear_loss + backward"}
+               "api": "chunked_linear_loss + backward",
+               "results_on_host": "the loss; the gradients stay on the device, as in training"}
 
     if rank == 0:
         peaks = load_peaks()
@@ -668,10 +700,11 @@ def chunked_main(args, w):
         dom = kern[0] if kern else None
         roof = None
         if dom is not None and dom["tflops"] is not None:
+            peak, kind = timed_region_peak(peaks, region_ms)
             roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
-                    "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": dom["tflops"] / peaks["bf16_sustained"],
-                    "peak_kind": f"bf16 sustained ({peaks['source']})", "traffic": None}
+                    "peak": peak, "unit": "TFLOP/s", "frac": dom["tflops"] / peak,
+                    "peak_kind": kind, "frac_of_burst": dom["tflops"] / peaks["bf16_burst"],
+                    "frac_of_sustained": dom["tflops"] / peaks["bf16_sustained"], "traffic": None}
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             import oracle
@@ -689,6 +722,7 @@ def chunked_main(args, w):
         line = {
             "metric": CHUNKED_METRIC, "value": job_rate(world, w.N, ms), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_mean": mean_ms, "timing": "median of per-step CUDA events",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic (seeded; inputs generated on the host)",
             "config": regression_config(w, args.torch_loss), "tflops": tflops,
@@ -724,9 +758,19 @@ def main():
                     help="run the vocabulary-parallel flow with this many shards on one GPU")
     ap.add_argument("--torch-loss", action="store_true",
                     help="regression workload: the loss as a torch callback instead of on the device")
+    ap.add_argument("--bwd-chunk-axis", choices=("auto", "rows", "vocab"), default="auto",
+                    help="axis of the backward's chunks (flce_params.bwd_chunk_axis)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return relaunch_ranks(args.gpus)       # one rank per GPU, like torchrun
+    rank, world, _ = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but this is one of WORLD_SIZE={world} ranks")
+    print(f"bench.py: rank {rank} of {world} ({args.impl})", file=sys.stderr, flush=True)
     if args.workload in wl.REGRESSION_WORKLOADS:
         if args.impl == "reference" or args.vocab_shards != 1:
             ap.error("the regression workload runs only --impl ours without --vocab-shards")

@@ -48,6 +48,10 @@
  *   before any work is enqueued. Errors the device detects (a target out of
  *   range, an expired bounded wait) are written to a status word at the start
  *   of the workspace. flce_check_status reads it.
+ * - A forward whose bounded wait expired leaves no output that looks like a
+ *   result: its loss, lse and entropy_sum are NaN and num_correct is -1 (the
+ *   shard states of flce_forward_partial are NaN). A backward whose wait
+ *   expired leaves its gradients undefined; only the status word tells.
  * - Outputs are overwritten, unless flce_params.accumulate asks the backward
  *   to add its gradients into the buffers it is given.
  * - Results do not depend on launch timing. Every reduction runs in a fixed
@@ -101,6 +105,16 @@ typedef enum {
  * rounds between chunks but needs no fp32 [V,H] partial. */
 typedef enum { FLCE_ACCUM_FP32 = 0, FLCE_ACCUM_WEIGHT = 1 } flce_accum;
 
+/* Axis along which flce_backward cuts its work into chunks (see
+ * flce_workspace_bytes). AUTO takes vocabulary chunks when N < V on the 16-bit
+ * path and row chunks otherwise. The results are the same either way; the
+ * workspace size and the speed differ. The fp32 path always chunks rows. */
+typedef enum {
+  FLCE_CHUNK_AXIS_AUTO = 0,
+  FLCE_CHUNK_AXIS_ROWS = 1,
+  FLCE_CHUNK_AXIS_VOCAB = 2
+} flce_chunk_axis;
+
 enum {
   FLCE_OK = 0,
   FLCE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, dtype, reduction or scalar   */
@@ -135,6 +149,13 @@ typedef struct {
                                 vocab_start .. vocab_start+V-1 of vocab_total. targets
                                 are global ids. 0 when not sharded                     */
   int64_t vocab_total;       /* global vocabulary size; 0 means V (not sharded)       */
+  int32_t bwd_chunk_axis;    /* flce_chunk_axis of the backward; 0 = AUTO             */
+  int32_t max_chunk;         /* >= 0. If > 0, an upper bound on the rows or vocabulary
+                                columns of one backward chunk, rounded down to whole
+                                tiles (256 rows or columns on the 16-bit path, 64 rows
+                                on the fp32 path; at least one tile). It lowers the
+                                workspace at the cost of more launches. 0 = only the
+                                4 GiB bound on the dlogits copies                     */
 } flce_params;
 
 /*
@@ -285,8 +306,11 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
  *   scratch byte is written before it is read. Calls that overlap on the GPU
  *   (different streams, or several host threads) race on the array, so
  *   serialise them.
- * - flce_check_status cannot reach the array. Device-detected errors of this
- *   entry point show up as NaN losses only.
+ * - flce_check_status cannot reach the array, so the outputs carry the
+ *   device-detected errors: a target out of range makes that row's loss NaN
+ *   (and so a SUM or MEAN loss), and an expired bounded wait makes the loss,
+ *   every lse and entropy_sum NaN and num_correct -1, whatever the array held
+ *   from an earlier call.
  */
 int flce_forward_noalloc(const flce_params* p, const void* hidden, const void* weight,
                          const void* bias, const int64_t* targets, float* loss, float* lse,
@@ -399,6 +423,21 @@ const char* flce_error_string(int code);
  * thread (empty if none). It is meant for diagnostics after FLCE_ERR_CUDA or
  * FLCE_ERR_UNSUPPORTED. Never NULL. */
 const char* flce_last_error_detail(void);
+
+/*
+ * Test hook for the bounded waits; not for production use. From this call on,
+ * every forward pass launched from the calling host thread starves one TMA
+ * pipeline stage: the even CTA of the first CTA pair arms the stage of K slice
+ * `drop_kblock` of its first tile but never issues its loads, so the MMA's
+ * wait on it must expire. wait_ms > 0 shortens every wait of those launches
+ * to that many milliseconds (0 keeps the default of 4 s). The kernel then
+ * records FLCE_ERR_TIMEOUT in the status word, stops its other roles, drains
+ * its copies in flight, frees its tensor memory and returns; the forward's
+ * outputs are NaN as described above. drop_kblock = -1 (with wait_ms = 0)
+ * turns the hook off again. Other host threads are not affected. Returns
+ * FLCE_ERR_INVALID_ARG for drop_kblock < -1 or wait_ms < 0.
+ */
+int flce_test_fault(int32_t drop_kblock, int32_t wait_ms);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t flce_launch_count(void);

@@ -19,6 +19,9 @@ FLCE_PASS_FORWARD, FLCE_PASS_BACKWARD, FLCE_PASS_CHUNK_LOGITS, FLCE_PASS_CHUNK_G
 FLCE_PASS_CHUNK_MSE = 4
 FLCE_CHUNK_ONLY, FLCE_CHUNK_FIRST, FLCE_CHUNK_NEXT, FLCE_CHUNK_LAST = 0, 1, 2, 3
 FLCE_ACCUM_FP32, FLCE_ACCUM_WEIGHT = 0, 1
+FLCE_CHUNK_AXIS_AUTO, FLCE_CHUNK_AXIS_ROWS, FLCE_CHUNK_AXIS_VOCAB = 0, 1, 2
+CHUNK_AXES = {"auto": FLCE_CHUNK_AXIS_AUTO, "rows": FLCE_CHUNK_AXIS_ROWS,
+              "vocab": FLCE_CHUNK_AXIS_VOCAB}
 ACCUM_DTYPES = {"fp32": FLCE_ACCUM_FP32, "weight": FLCE_ACCUM_WEIGHT}
 REDUCTIONS = {"sum": FLCE_SUM, "mean": FLCE_MEAN, "none": FLCE_NONE}
 
@@ -33,7 +36,7 @@ EXPORTS = (
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
     "flce_forward_partial", "flce_forward_combine", "flce_chunk_logits", "flce_chunk_grads",
-    "flce_chunk_weighted_mse",
+    "flce_chunk_weighted_mse", "flce_test_fault",
 )
 
 
@@ -54,6 +57,8 @@ class FlceParams(ctypes.Structure):
         ("grad_weight_accum", ctypes.c_int32),
         ("vocab_start", ctypes.c_int64),
         ("vocab_total", ctypes.c_int64),
+        ("bwd_chunk_axis", ctypes.c_int32),
+        ("max_chunk", ctypes.c_int32),
     ]
 
 
@@ -117,6 +122,8 @@ def load() -> ctypes.CDLL:
                                             ctypes.c_int64, vp, ctypes.c_int64, vp,
                                             ctypes.c_int32, vp, sz, vp]
     lib.flce_chunk_weighted_mse.restype = ctypes.c_int
+    lib.flce_test_fault.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    lib.flce_test_fault.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
     lib.flce_check_status.restype = ctypes.c_int
     lib.flce_error_string.argtypes = [ctypes.c_int]
@@ -152,11 +159,14 @@ def make_params(N: int, H: int, V: int, dtype: int, reduction: str = "mean",
                 softcap: Optional[float] = None, z_loss_multiplier: float = 0.0,
                 has_bias: bool = False, deterministic: bool = False, accumulate: bool = False,
                 grad_weight_accum: str = "fp32", vocab_start: int = 0,
-                vocab_total: int = 0) -> FlceParams:
+                vocab_total: int = 0, bwd_chunk_axis: str = "auto",
+                max_chunk: int = 0) -> FlceParams:
     if reduction not in REDUCTIONS:
         raise ValueError(f"reduction must be one of {tuple(REDUCTIONS)}, got {reduction!r}")
     if grad_weight_accum not in ACCUM_DTYPES:
         raise ValueError(f"grad_weight_accum must be one of {tuple(ACCUM_DTYPES)}")
+    if bwd_chunk_axis not in CHUNK_AXES:
+        raise ValueError(f"bwd_chunk_axis must be one of {tuple(CHUNK_AXES)}")
     return FlceParams(N=N, H=H, V=V, dtype=dtype, reduction=REDUCTIONS[reduction],
                       ignore_index=ignore_index, logit_scale=logit_scale,
                       softcap=softcap if softcap else 0.0,
@@ -164,7 +174,8 @@ def make_params(N: int, H: int, V: int, dtype: int, reduction: str = "mean",
                       deterministic=1 if deterministic else 0,
                       accumulate=1 if accumulate else 0,
                       grad_weight_accum=ACCUM_DTYPES[grad_weight_accum],
-                      vocab_start=vocab_start, vocab_total=vocab_total)
+                      vocab_start=vocab_start, vocab_total=vocab_total,
+                      bwd_chunk_axis=CHUNK_AXES[bwd_chunk_axis], max_chunk=max_chunk)
 
 
 def workspace_bytes(p: FlceParams, pass_: int) -> int:
@@ -231,6 +242,11 @@ def chunk_weighted_mse_raw(p: FlceParams, hidden: int, weight: int, target: int,
                                           row_weight, feature_weight, dlogits, ld_dlogits,
                                           dlogits_t, ld_dlogits_t, loss, accumulate_loss, ws,
                                           ws_bytes, stream)
+
+
+def test_fault(drop_kblock: int, wait_ms: int) -> None:
+    """flce_test_fault: starve one stage of this thread's forward launches (-1, 0: off)."""
+    check(load().flce_test_fault(drop_kblock, wait_ms), "flce_test_fault")
 
 
 def check_status(ws: int, stream: int) -> int:

@@ -37,6 +37,11 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_launches{0};
 thread_local char g_detail[256] = "";
 
+// Test hook for the bounded waits (flce_test_fault): the forward launches of
+// this host thread starve one pipeline stage and shorten every wait.
+thread_local int g_test_drop_kb = -1;
+thread_local unsigned long long g_test_wait_ns = 0;
+
 int cuda_fail(cudaError_t e, const char* what) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s", what, cudaGetErrorString(e));
   return FLCE_ERR_CUDA;
@@ -154,6 +159,9 @@ int validate(const flce_params* p) {
   } else if (p->vocab_start < 0 || p->vocab_total > lim || p->vocab_start + p->V > p->vocab_total) {
     return FLCE_ERR_INVALID_ARG;
   }
+  if (p->bwd_chunk_axis < FLCE_CHUNK_AXIS_AUTO || p->bwd_chunk_axis > FLCE_CHUNK_AXIS_VOCAB ||
+      p->max_chunk < 0)
+    return FLCE_ERR_INVALID_ARG;
   if (p->dtype != FLCE_F32 && (p->H % 8) != 0) return FLCE_ERR_ALIGNMENT;
   return FLCE_OK;
 }
@@ -244,14 +252,12 @@ struct BwdLayout {
 // ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
 // chunks the vocabulary whenever N < V, where that partial is the smaller one:
 // each chunk's grad_weight rows are then complete after one GEMM over all N
-// rows. FLCE_BWD_CHUNKS=rows or =vocab fixes the axis, so that tests reach
-// both schedules at any size; the result is the same either way.
+// rows. flce_params.bwd_chunk_axis fixes the axis, so that callers and tests
+// can reach both schedules at any size; the result is the same either way.
 bool vocab_chunked(const flce_params* p) {
   if (!tensor_path(p) || p->N == 0) return false;
-  if (const char* env = getenv("FLCE_BWD_CHUNKS")) {
-    if (strcmp(env, "rows") == 0) return false;
-    if (strcmp(env, "vocab") == 0) return true;
-  }
+  if (p->bwd_chunk_axis == FLCE_CHUNK_AXIS_ROWS) return false;
+  if (p->bwd_chunk_axis == FLCE_CHUNK_AXIS_VOCAB) return true;
   return p->N < p->V;
 }
 
@@ -265,13 +271,12 @@ BwdLayout bwd_layout(const flce_params* p) {
     // Four column chunks of whole 256-column tiles (two copies of a quarter
     // of the columns), fewer columns per chunk if N rows of them would pass
     // the 4 GiB cap; then the columns are spread evenly over the chunks.
-    // FLCE_MAX_CHUNK_COLS (a multiple of 256) lowers the cap, like
-    // FLCE_MAX_CHUNK_ROWS for row chunks.
+    // flce_params.max_chunk (rounded down to whole tiles) lowers the cap.
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * 2)) / kBN * kBN;
     if (cap < kBN) cap = kBN;
-    if (const char* env = getenv("FLCE_MAX_CHUNK_COLS")) {
-      const long long c = atoll(env) / kBN * kBN;
-      if (c >= kBN && c < cap) cap = c;
+    if (p->max_chunk > 0) {
+      const int64_t c = p->max_chunk < kBN ? kBN : p->max_chunk / kBN * kBN;
+      if (c < cap) cap = c;
     }
     int64_t w = ceil_div(ceil_div(V, 4), kBN) * kBN;
     if (w > cap) w = cap;
@@ -309,12 +314,11 @@ BwdLayout bwd_layout(const flce_params* p) {
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem * copies)) /
                   gran * gran;
     if (cap < gran) cap = gran;
-    // FLCE_MAX_CHUNK_ROWS (a multiple of the granule) lowers the row-chunk
-    // cap. The work and the result are the same; it is there so tests can
-    // reach the three-or-more-chunk schedule at small sizes.
-    if (const char* env = getenv("FLCE_MAX_CHUNK_ROWS")) {
-      const long long r = atoll(env) / gran * gran;
-      if (r >= gran && r < cap) cap = r;
+    // flce_params.max_chunk (rounded down to the granule) lowers the cap. The
+    // work and the result are the same, in less workspace.
+    if (p->max_chunk > 0) {
+      const int64_t r = p->max_chunk < gran ? gran : p->max_chunk / gran * gran;
+      if (r < cap) cap = r;
     }
     L.chunk = quarter < cap ? quarter : cap;
     if (L.chunk > N && N > 0) L.chunk = N;
@@ -533,6 +537,10 @@ ChunkLayout chunk_layout(const flce_params* p) {
 
 }  // namespace
 
+void flce::set_error_detail(const char* msg) {
+  snprintf(g_detail, sizeof(g_detail), "%s", msg);
+}
+
 // ===================================================================== ABI
 extern "C" {
 
@@ -551,6 +559,13 @@ const char* flce_error_string(int code) {
 }
 
 const char* flce_last_error_detail(void) { return g_detail; }
+
+int flce_test_fault(int32_t drop_kblock, int32_t wait_ms) {
+  if (drop_kblock < -1 || wait_ms < 0) return FLCE_ERR_INVALID_ARG;
+  g_test_drop_kb = drop_kblock;
+  g_test_wait_ns = static_cast<unsigned long long>(wait_ms) * 1000000ull;
+  return FLCE_OK;
+}
 
 uint64_t flce_launch_count(void) { return g_launches.load(); }
 
@@ -614,16 +629,10 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   fa.partials = reinterpret_cast<float4*>(ws + L.partials);
   fa.zt = reinterpret_cast<float*>(ws + L.zt);
   fa.status = reinterpret_cast<int*>(ws);
-  fa.wait_ns = kWaitLimitNs;
-  fa.drop_kb = -1;
-  // Fault injection for the bounded-wait test (tests/test_gpu_faults.py):
-  // FLCE_TEST_DROP_KBLOCK names a K slice whose loads the forward never issues,
-  // and FLCE_TEST_WAIT_MS shortens every wait of that launch.
-  if (const char* e = getenv("FLCE_TEST_DROP_KBLOCK")) fa.drop_kb = atoi(e);
-  if (const char* e = getenv("FLCE_TEST_WAIT_MS")) {
-    const long long ms = atoll(e);
-    if (ms > 0) fa.wait_ns = static_cast<unsigned long long>(ms) * 1000000ull;
-  }
+  // flce_test_fault arms these for the calling thread only; otherwise no
+  // stage is starved and every wait has the default limit.
+  fa.wait_ns = g_test_wait_ns > 0 ? g_test_wait_ns : kWaitLimitNs;
+  fa.drop_kb = g_test_drop_kb;
   int v;
   if (tensor_path(p)) {
     const CUtensorMapDataType dt = map_type(p);
@@ -659,6 +668,7 @@ static int forward_finalize(const flce_params* p, uint8_t* ws, const FwdLayout& 
                             cudaStream_t st) {
   FinalizeArgs fz{};
   fz.nblk = nblk;
+  fz.status = reinterpret_cast<const int*>(ws);
   fz.reduction = p->reduction;
   fz.blk_loss = reinterpret_cast<const double*>(ws + L.blk_loss);
   fz.blk_ent = reinterpret_cast<const double*>(ws + L.blk_ent);
@@ -740,6 +750,7 @@ int flce_forward_partial(const flce_params* p, const void* hidden, const void* w
   sa.N = static_cast<int>(p->N);
   sa.V = static_cast<int>(p->V);
   sa.num_panels = fa.num_panels;
+  sa.status = reinterpret_cast<const int*>(ws);
   sa.vocab_start = p->vocab_start;
   sa.ignore_index = p->ignore_index;
   sa.partials = fa.partials;

@@ -76,6 +76,10 @@ struct FwdArgs {
   int* status;
 };
 
+// A forward whose bounded wait expired skipped some partial-state stores, so
+// the merge would combine whatever the workspace held before. merge_kernel
+// reads the status word first (the stream orders it after the forward) and
+// then writes NaN to every lse and loss instead.
 struct MergeArgs {
   int N, V, num_panels, reduction;
   long long vocab_start, vocab_total;   // shard placement; vocab_total = V when not sharded
@@ -104,6 +108,7 @@ struct ShardState {
 
 struct ShardStateArgs {
   int N, V, num_panels;
+  const int* status;           // kDevErrTimeout set: every state is NaN (the partials are incomplete)
   long long vocab_start;
   long long ignore_index;
   const float4* partials;
@@ -131,6 +136,7 @@ struct CombineArgs {
 
 struct FinalizeArgs {
   int nblk, reduction;
+  const int* status;           // kDevErrTimeout set: loss and entropy NaN, num_correct -1
   const double* blk_loss;
   const double* blk_ent;
   const long long* blk_correct;
@@ -301,5 +307,8 @@ cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s);
 cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s);
 
 constexpr int kMergeThreads = 256;
+
+// Host side: sets the text flce_last_error_detail returns on this thread.
+void set_error_detail(const char* msg);
 
 }  // namespace flce

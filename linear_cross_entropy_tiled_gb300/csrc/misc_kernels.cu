@@ -47,7 +47,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   double loss_i = 0.0, ent_i = 0.0;
   long long corr = 0, valid = 0;
-  if (i < a.N) {
+  const bool timed_out = (*a.status & kDevErrTimeout) != 0;
+  if (i < a.N && timed_out) {
+    // The forward gave up before storing all of its partial states: no
+    // output of this call may look like a result.
+    a.lse[i] = NAN;
+    loss_i = NAN;
+    ent_i = NAN;
+    if (a.loss_rows != nullptr) a.loss_rows[i] = NAN;
+  } else if (i < a.N) {
     float M = -INFINITY, S = 0.f, Tt = 0.f;
     int A = 0;
     for (int p = 0; p < a.num_panels; ++p) {
@@ -100,6 +108,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
 __global__ void __launch_bounds__(256) shard_state_kernel(const ShardStateArgs a) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= a.N) return;
+  if ((*a.status & kDevErrTimeout) != 0) {
+    // the forward gave up before storing all of its partial states
+    a.out[i] = ShardState{NAN, NAN, NAN, -1, NAN};
+    return;
+  }
   float M = -INFINITY, S = 0.f, Tt = 0.f;
   int A = 0;
   for (int p = 0; p < a.num_panels; ++p) {
@@ -203,7 +216,11 @@ __global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
   e = block_sum(e, sh_d);
   c = block_sum(c, sh_i);
   v = block_sum(v, sh_i);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && a.status != nullptr && (*a.status & kDevErrTimeout) != 0) {
+    if (a.loss != nullptr) *a.loss = NAN;
+    if (a.num_correct != nullptr) *a.num_correct = -1;
+    if (a.entropy_sum != nullptr) *a.entropy_sum = NAN;
+  } else if (threadIdx.x == 0) {
     if (a.loss != nullptr) {
       if (a.reduction == 0) {
         *a.loss = static_cast<float>(l);

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "flce.h"
+#include "kernels.h"
 
 namespace {
 
@@ -29,7 +30,6 @@ static __device__ __align__(256) unsigned char g_forward_scratch[kNoAllocScratch
 
 std::mutex g_mu;
 void* g_scratch_addr[64] = {};
-thread_local char g_msg[160];
 
 // Device address of g_forward_scratch on the current device. In host code
 // the array's name is only a host-side stand-in, so the address has to be
@@ -59,17 +59,22 @@ extern "C" int flce_forward_noalloc(const flce_params* p, const void* hidden, co
   int rc = flce_workspace_bytes(p, FLCE_PASS_FORWARD, &need);
   if (rc != FLCE_OK) return rc;
   if (need > kNoAllocScratchBytes) {
-    snprintf(g_msg, sizeof(g_msg),
+    char msg[160];
+    snprintf(msg, sizeof(msg),
              "flce_forward_noalloc: this size needs %zu bytes of scratch, above the "
              "fixed maximum of %zu",
              need, kNoAllocScratchBytes);
-    fprintf(stderr, "%s\n", g_msg);
+    flce::set_error_detail(msg);
+    fprintf(stderr, "%s\n", msg);
     return FLCE_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
   if ((rc = scratch_address(&scratch)) != FLCE_OK) return rc;
   // flce_forward zeroes the status word at the start of the scratch before
-  // any kernel runs. Every other scratch byte is written before it is read.
+  // any kernel runs. Every other scratch byte is written before it is read,
+  // except after an expired bounded wait: the forward then skips stores, and
+  // the merge, seeing the timeout in the status word, writes NaN outputs
+  // instead of combining what an earlier call left in the array.
   return flce_forward(p, hidden, weight, bias, targets, loss, lse, num_correct, entropy_sum,
                       scratch, kNoAllocScratchBytes, stream);
 }

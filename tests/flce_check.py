@@ -44,12 +44,16 @@ def to_device(d: dict, dtype: str, dev="cuda"):
 
 
 def run_gpu(d: dict, dtype: str, kw: dict, grad_loss=1.0, return_metrics=True,
-            need=(True, True, True)):
-    """Forward + backward through the C ABI. Returns numpy outputs."""
+            need=(True, True, True), schedule=None):
+    """Forward + backward through the C ABI. Returns numpy outputs.
+
+    ``schedule`` holds flce_params fields that change only how the backward is
+    cut into chunks (bwd_chunk_axis, max_chunk), never the result.
+    """
     h, w, b, t = to_device(d, dtype)
     dt = {"bf16": _lib.FLCE_BF16, "f16": _lib.FLCE_F16, "f32": _lib.FLCE_F32}[dtype]
     p = _lib.make_params(N=h.shape[0], H=h.shape[1], V=w.shape[0], dtype=dt,
-                         has_bias=b is not None, **kw)
+                         has_bias=b is not None, **kw, **(schedule or {}))
     loss, lse, nc, ent, fws = flce_forward(p, h, w, t, b, return_metrics=return_metrics)
     st = _lib.check_status(fws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     gl = torch.as_tensor(np.asarray(grad_loss, dtype=np.float32).reshape(-1), device=h.device)

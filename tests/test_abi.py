@@ -45,7 +45,7 @@ def params(**kw):
     return _lib.make_params(**base)
 
 
-def test_workspace_sizes(lib, monkeypatch):
+def test_workspace_sizes(lib):
     p = params(N=8192, H=4096, V=128256, has_bias=True)
     fwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
     assert fwd < 64 << 20                       # a few MB of partial states
@@ -60,14 +60,14 @@ def test_workspace_sizes(lib, monkeypatch):
     assert bwd < 8192 * 128256 * 2              # less than one N x V buffer
     # row chunks: two copies of a quarter of the rows, the fp32 grad_weight
     # partial and two fp32 K-split partials of grad_hidden
-    monkeypatch.setenv("FLCE_BWD_CHUNKS", "rows")
-    bwd_rows = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
+    pr = _lib.FlceParams.from_buffer_copy(p)
+    pr.bwd_chunk_axis = _lib.FLCE_CHUNK_AXIS_ROWS
+    bwd_rows = _lib.workspace_bytes(pr, _lib.FLCE_PASS_BACKWARD)
     chunk = 2 * 2048 * 128256 * 2
     dw = 128256 * 4096 * 4
     dh = 2 * 2048 * 4096 * 4
     assert chunk + dw + dh < bwd_rows < chunk + dw + dh + (64 << 20)
     assert bwd_rows < 8192 * 128256 * 2 + dw
-    monkeypatch.delenv("FLCE_BWD_CHUNKS")
     # N > V: row chunks by default
     q = params(N=65536, H=1024, V=32000)
     chunk = 2 * 16384 * 32000 * 2
@@ -215,3 +215,46 @@ def test_device_weighted_mse_entry_point_validates_before_any_gpu_work(lib):
     assert call(p, ws_bytes=need - 4) == 4
     assert call(p, loss=fake + 4) == 3                                    # fp64 needs 8 bytes
     assert call(p, row_weight=fake + 2) == 3                              # fp32 needs 4 bytes
+
+
+def test_schedule_fields(lib):
+    """bwd_chunk_axis and max_chunk change only the chunking, so only the workspace size."""
+    n = ctypes.c_size_t(0)
+    for bad in (dict(bwd_chunk_axis=3), dict(bwd_chunk_axis=-1), dict(max_chunk=-256)):
+        p = params()
+        for k, v in bad.items():
+            setattr(p, k, v)
+        assert lib.flce_workspace_bytes(ctypes.byref(p), 1, ctypes.byref(n)) == 1, bad
+    base = params(N=8192, H=4096, V=128256)
+    full = _lib.workspace_bytes(base, _lib.FLCE_PASS_BACKWARD)
+    capped = params(N=8192, H=4096, V=128256, max_chunk=8192)
+    small = _lib.workspace_bytes(capped, _lib.FLCE_PASS_BACKWARD)
+    # vocabulary chunks of 8192 columns instead of 32256: two copies of N x chunk shrink
+    assert full - small == pytest.approx(2 * 8192 * (32256 - 8192) * 2, rel=1e-3)
+    # below one tile it is one tile (256 columns), not an error
+    tiny = params(N=8192, H=4096, V=128256, max_chunk=1)
+    assert _lib.workspace_bytes(tiny, _lib.FLCE_PASS_BACKWARD) < small
+    rows = params(N=8192, H=4096, V=128256, bwd_chunk_axis="rows")
+    assert _lib.workspace_bytes(rows, _lib.FLCE_PASS_BACKWARD) > full   # + fp32 grad_weight partial
+    # the forward does not chunk
+    assert _lib.workspace_bytes(capped, 0) == _lib.workspace_bytes(base, 0)
+
+
+def test_params_struct_layout(lib):
+    """The ctypes mirror of flce_params has the C layout: 96 bytes, new fields last."""
+    assert ctypes.sizeof(_lib.FlceParams) == 96
+    assert _lib.FlceParams.bwd_chunk_axis.offset == 88
+    assert _lib.FlceParams.max_chunk.offset == 92
+
+
+def test_test_fault_argument_checks(lib):
+    assert lib.flce_test_fault(-2, 0) == 1
+    assert lib.flce_test_fault(0, -1) == 1
+    assert lib.flce_test_fault(-1, 0) == 0     # off
+
+
+def test_no_environment_reads_in_the_library():
+    """Schedules and test hooks are explicit arguments; the library reads no environment."""
+    csrc = os.path.join(ROOT, "linear_cross_entropy_tiled_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert "getenv" not in open(os.path.join(csrc, f)).read(), f

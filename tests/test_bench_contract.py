@@ -78,3 +78,34 @@ def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
     assert bench.traffic_for("no_such_kernel", wl_name) is None
     monkeypatch.setattr(bench, "sources_digest", lambda: "changed")
     assert bench.traffic_for(kernel, wl_name) is None
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """``--gpus 2`` without a launcher starts two local ranks itself; the line says n_gpus 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env.update(CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="4")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                          "--workload", "tiny_f32", "--steps", "1", "--warmup", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert "rank 0 of 2" in out.stderr and "rank 1 of 2" in out.stderr, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """Under a launcher of one rank, ``--gpus 2`` is an error, not a one-GPU line labelled 2."""
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                          "--workload", "tiny_f32", "--steps", "1", "--warmup", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=120, env=env)
+    assert out.returncode != 0 and "WORLD_SIZE=1" in out.stderr
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_peak_follows_the_timed_region():
+    peaks = dict(bf16_burst=1900.0, bf16_sustained=1700.0, source="measured")
+    assert bench.timed_region_peak(peaks, 420.0)[0] == 1900.0
+    assert "burst" in bench.timed_region_peak(peaks, 420.0)[1]
+    assert bench.timed_region_peak(peaks, 5000.0)[0] == 1700.0

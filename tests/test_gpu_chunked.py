@@ -189,3 +189,39 @@ def test_gradient_of_one_argument_only(which):
     else:
         assert x.grad is None
         assert_grad_close(w.grad.double().cpu().numpy(), rw, "bf16", "grad_weight")
+
+
+@pytest.mark.parametrize("V", [20480, 19999])
+@pytest.mark.parametrize("loss_kind", ["device", "callback"])
+def test_grouped_tile_raster_matches_the_oracle(V, loss_kind):
+    """The projection's grouped raster: more column tiles than CTA pairs.
+
+    With V / 256 = 80 column tiles (79 for the ragged V = 19999) a wave of the
+    at most 76 co-resident pairs of a GB300 spans fewer than all column tiles,
+    so the plain GEMM rasters its tiles in groups of row tiles, column after
+    column within a group. N = 1000 in one chunk gives a group of four row
+    tiles, the last one ragged; chunks of 512 rows give groups of two. Both the
+    device-side weighted squared error and the torch callback go through that
+    projection; every element is compared with the oracle.
+    """
+    from linear_cross_entropy_tiled_gb300 import weighted_mse_loss
+    N, H = 1000, 256
+    X, W, Y, r, f, Xd, Wd = case(N, H, V, "bf16", seed=V + 13)
+    for chunk_rows in (None, 512):
+        if loss_kind == "device":
+            x = Xd.clone().requires_grad_(True)
+            w = Wd.clone().requires_grad_(True)
+            fn = weighted_mse_loss(torch.from_numpy(Y).cuda(), torch.from_numpy(r).cuda(),
+                                   torch.from_numpy(f).cuda())
+            lt = chunked_linear_loss(x, w, fn, chunk_rows=chunk_rows)
+            lt.backward()
+            torch.cuda.synchronize()
+            loss, gx, gw = float(lt.item()), x.grad.double().cpu().numpy(), w.grad.double().cpu().numpy()
+        else:
+            loss, gx, gw = run(Xd, Wd, Y, r, f, chunk_rows=chunk_rows)
+        ref, rx, rw = oracle.chunked_linear_loss(X, W, oracle.weighted_mse, Y, r, f,
+                                                 chunk_rows=chunk_rows)
+        tol = 1e-4 if loss_kind == "device" else TOL["bf16"]["loss"]
+        assert abs(loss - ref) <= tol * abs(ref), (chunk_rows, loss, ref)
+        assert_grad_close(gx, rx, "bf16", f"grad_inputs (chunk_rows={chunk_rows})")
+        assert_grad_close(gw, rw, "bf16", f"grad_weight (chunk_rows={chunk_rows})")

@@ -2,7 +2,8 @@
 
 Every mbarrier wait in the tensor-core kernels is bounded. The test starves one
 wait: the forward's producer arms a pipeline stage but never issues its loads,
-a flag nothing sets. It checks three things:
+a flag nothing sets (armed for this host thread by flce_test_fault). It checks
+three things:
 - the kernel gives up after the (shortened) limit and reports FLCE_ERR_TIMEOUT
   through the workspace status word;
 - it frees its tensor memory and returns, with no trap, no fault and no hang;
@@ -22,18 +23,21 @@ from flce_check import assert_loss_close, to_device
 pytestmark = pytest.mark.gpu
 
 
-def test_starved_wait_reports_timeout_and_the_context_survives(monkeypatch):
+def test_starved_wait_reports_timeout_and_the_context_survives():
     d = small_case(600, 256, 3000, seed=17, dtype="bf16", bias=True, ignore_frac=0.1)
     h, w, b, t = to_device(d, "bf16")
     p = _lib.make_params(N=600, H=256, V=3000, dtype=_lib.FLCE_BF16, has_bias=True,
                          reduction="mean")
     stream = torch.cuda.current_stream().cuda_stream
-    monkeypatch.setenv("FLCE_TEST_DROP_KBLOCK", "1")
-    monkeypatch.setenv("FLCE_TEST_WAIT_MS", "100")
-    _, _, _, _, ws = flce_forward(p, h, w, t, b)
+    _lib.test_fault(1, 100)
+    try:
+        loss, lse, nc, ent, ws = flce_forward(p, h, w, t, b, return_metrics=True)
+    finally:
+        _lib.test_fault(-1, 0)
     assert _lib.check_status(ws.data_ptr(), stream) == 7          # FLCE_ERR_TIMEOUT
-    monkeypatch.delenv("FLCE_TEST_DROP_KBLOCK")
-    monkeypatch.delenv("FLCE_TEST_WAIT_MS")
+    # nothing of the aborted forward looks like a result
+    assert np.isnan(loss.item()) and np.isnan(lse.cpu().numpy()).all()
+    assert nc.item() == -1 and np.isnan(ent.item())
     loss, _, _, _, ws = flce_forward(p, h, w, t, b)
     assert _lib.check_status(ws.data_ptr(), stream) == 0
     ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], reduction="mean")

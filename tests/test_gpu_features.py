@@ -46,18 +46,14 @@ def dev_tensor(x, dtype):
 
 @pytest.mark.parametrize("dtype,N,H,V,axis,chunk_cap", [
     ("bf16", 1200, 2560, 16500, "rows", None),  # grad_hidden with 2 K splits, 3 row chunks
-    ("bf16", 700, 136, 900, "rows", "256"),     # 3 row chunks
+    ("bf16", 700, 136, 900, "rows", 256),       # 3 row chunks
     ("bf16", 600, 256, 16500, "vocab", None),   # 4 vocabulary chunks of 4352 columns
-    ("bf16", 700, 136, 900, "vocab", "256"),    # 4 vocabulary chunks of 256 columns
+    ("bf16", 700, 136, 900, "vocab", 256),      # 4 vocabulary chunks of 256 columns
     ("bf16", 200, 64, 250, "vocab", None),      # 1 vocabulary chunk (V < 256)
     ("f32", 150, 64, 700, None, None),
 ])
-def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap, monkeypatch):
-    if axis:
-        monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
-    if chunk_cap:
-        monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS" if axis == "rows" else "FLCE_MAX_CHUNK_COLS",
-                           chunk_cap)
+def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap):
+    schedule = dict(bwd_chunk_axis=axis or "auto", max_chunk=chunk_cap or 0)
     d = small_case(N, H, V, seed=N + V, dtype=dtype, bias=True, ignore_frac=0.1)
     kw = dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3)
     gh, gw, gb = oracle.backward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **kw)
@@ -67,7 +63,7 @@ def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap, mon
     gw0 = exact(g.standard_normal(gw.shape) * np.abs(gw).max(), dtype)
     gb0 = exact(g.standard_normal(gb.shape) * np.abs(gb).max(), dtype)
     h, w, b, t = to_device(d, dtype)
-    p = _lib.make_params(N=N, H=H, V=V, dtype=DT[dtype], has_bias=True, **kw)
+    p = _lib.make_params(N=N, H=H, V=V, dtype=DT[dtype], has_bias=True, **kw, **schedule)
     _, lse, _, _, _ = flce_forward(p, h, w, t, b)
     out = (dev_tensor(gh0, dtype), dev_tensor(gw0, dtype), dev_tensor(gb0, dtype))
     flce_backward(p, h, w, t, lse, torch.ones(1, device="cuda"), b, accumulate=True, out=out)
@@ -76,15 +72,14 @@ def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap, mon
         assert_grad_close(got.float().cpu().numpy(), ref, dtype, "accumulated grad_" + name)
 
 
-def test_grad_weight_accumulated_in_weight_dtype(monkeypatch):
+def test_grad_weight_accumulated_in_weight_dtype():
     # Only row chunks accumulate grad_weight across chunks.
-    monkeypatch.setenv("FLCE_BWD_CHUNKS", "rows")
-    monkeypatch.setenv("FLCE_MAX_CHUNK_ROWS", "256")
+    schedule = dict(bwd_chunk_axis="rows", max_chunk=256)
     d = small_case(800, 136, 1100, seed=77, dtype="bf16", bias=True, ignore_frac=0.1)
     kw = dict(reduction="sum", logit_scale=0.8)
     h, w, b, t = to_device(d, "bf16")
     p = _lib.make_params(N=800, H=136, V=1100, dtype=_lib.FLCE_BF16, has_bias=True,
-                         grad_weight_accum="weight", **kw)
+                         grad_weight_accum="weight", **kw, **schedule)
     _, lse, _, _, _ = flce_forward(p, h, w, t, b)
     gh, gw, gb, _ = flce_backward(p, h, w, t, lse, torch.ones(1, device="cuda"), b)
     torch.cuda.synchronize()
@@ -92,7 +87,8 @@ def test_grad_weight_accumulated_in_weight_dtype(monkeypatch):
     assert_grad_close(gw.float().cpu().numpy(), rw, "bf16", "grad_weight (weight-dtype accum)")
     assert_grad_close(gh.float().cpu().numpy(), rh, "bf16", "grad_hidden")
     # the weight-dtype accumulator needs no fp32 [V, H] partial
-    p32 = _lib.make_params(N=800, H=136, V=1100, dtype=_lib.FLCE_BF16, has_bias=True, **kw)
+    p32 = _lib.make_params(N=800, H=136, V=1100, dtype=_lib.FLCE_BF16, has_bias=True, **kw,
+                           **schedule)
     assert _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD) < \
         _lib.workspace_bytes(p32, _lib.FLCE_PASS_BACKWARD)
 

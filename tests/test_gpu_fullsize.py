@@ -7,9 +7,11 @@ rows of grad_hidden and sampled vocabulary rows of grad_weight / grad_bias.
 The oracle computes each sampled output independently (a vocabulary row needs
 the oracle's own lse of every row).
 
-For the vocabulary sweep only sampled rows are compared with the oracle
-(lse, per-row loss, grad_hidden rows). The mean loss is also checked against
-the GPU's own per-row losses, a property that holds at any size.
+For the vocabulary sweep the oracle runs its full forward too, which gives
+the loss and every row's lse. Per-row losses and grad_hidden are compared on
+sampled rows, grad_weight on sampled vocabulary rows. The mean loss is also
+checked against the GPU's own per-row losses, a property that holds at any
+size.
 """
 import numpy as np
 import pytest
@@ -130,9 +132,24 @@ def test_sweep_sampled(V):
     gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows,
                                  reduction=w.reduction, **okw)
     assert_sampled_grad(out["grad_hidden"][rows], gh, "grad_hidden rows")
+    # Sampled grad_weight rows. Each needs the oracle's own lse of every row, so
+    # the oracle runs its full fp64 forward here. The sample takes in the last
+    # column, the last column of the last full 256-column tile and both sides
+    # of every boundary between the backward's vocabulary chunks (a quarter of
+    # V in whole tiles).
+    ref = oracle.forward(d["hidden"], d["weight"], d["targets"], reduction=w.reduction,
+                         row_block=512, **okw)
+    assert_loss_close(out["loss"], ref["loss"], "bf16")
+    assert_lse_close(out["lse"], ref["lse"])
+    J = sample_vocab(w.V, d["targets"], seed=V + 1)
+    chunk = -(-(-(-w.V // 4)) // 256) * 256
+    J = np.union1d(J, [e + k for e in range(chunk, w.V, chunk) for k in (-1, 0)])
+    gw, _ = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
+                                    reduction=w.reduction, **okw)
+    assert_sampled_grad(out["grad_weight"][J], gw, "grad_weight rows")
 
 
-def test_more_than_2_to_the_32_logits(monkeypatch):
+def test_more_than_2_to_the_32_logits():
     """N x V = 65536 x 65537 > 2^32 logits (8.6 GB in bf16, never stored).
 
     The backward runs both ways, on the same inputs:
@@ -160,8 +177,7 @@ def test_more_than_2_to_the_32_logits(monkeypatch):
     gw, gb = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
                                      bias=d["bias"], reduction=w.reduction, **okw)
     for axis in ("rows", "vocab"):
-        monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
-        out = run_gpu(d, "bf16", kw_of(w))
+        out = run_gpu(d, "bf16", kw_of(w), schedule=dict(bwd_chunk_axis=axis))
         assert out["status_fwd"] == 0 and out["status_bwd"] == 0
         assert_loss_close(out["loss"], ref["loss"], "bf16")
         assert_lse_close(out["lse"], ref["lse"])

@@ -4,7 +4,8 @@ The shapes are small enough for the oracle to finish in seconds. They still
 span several 128-row, 256-vocabulary and 64-deep tiles, and they have ragged
 tails in N, V and H. Each 16-bit case runs the backward both ways: as row
 chunks (the fp32 grad_weight partial crosses them) and as vocabulary chunks
-(the fp32 grad_hidden partial crosses them). FLCE_BWD_CHUNKS picks the axis.
+(the fp32 grad_hidden partial crosses them). flce_params.bwd_chunk_axis picks
+the axis.
 """
 import os
 
@@ -34,8 +35,8 @@ def with_argmax_targets(d, kw, frac=0.5, seed=0):
     return d
 
 
-def check_case(d, dtype, kw, grad_loss=1.0):
-    out = run_gpu(d, dtype, kw, grad_loss=grad_loss)
+def check_case(d, dtype, kw, grad_loss=1.0, schedule=None):
+    out = run_gpu(d, dtype, kw, grad_loss=grad_loss, schedule=schedule)
     assert out["status_fwd"] == 0 and out["status_bwd"] == 0
     okw = dict(kw)
     ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **okw)
@@ -73,13 +74,12 @@ BF16_CASES = [
 
 @pytest.mark.parametrize("axis", ["rows", "vocab"])
 @pytest.mark.parametrize("N,H,V,bias,ign,kw", BF16_CASES)
-def test_bf16_parity(N, H, V, bias, ign, kw, axis, monkeypatch):
-    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
+def test_bf16_parity(N, H, V, bias, ign, kw, axis):
     d = small_case(N, H, V, seed=N * 7 + V, dtype="bf16", bias=bias, ignore_frac=ign,
                    hidden_std=1.0)
     d = with_argmax_targets(d, kw)
     gl = np.random.default_rng(1).standard_normal(N).astype(np.float32) if kw["reduction"] == "none" else 0.75
-    check_case(d, "bf16", kw, grad_loss=gl)
+    check_case(d, "bf16", kw, grad_loss=gl, schedule=dict(bwd_chunk_axis=axis))
 
 
 F32_CASES = [
@@ -107,26 +107,23 @@ F16_CASES = [
 
 @pytest.mark.parametrize("axis", ["rows", "vocab"])
 @pytest.mark.parametrize("N,H,V,bias,ign,kw", F16_CASES)
-def test_f16_parity(N, H, V, bias, ign, kw, axis, monkeypatch):
-    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
+def test_f16_parity(N, H, V, bias, ign, kw, axis):
     d = small_case(N, H, V, seed=N * 5 + V, dtype="f16", bias=bias, ignore_frac=ign)
     d = with_argmax_targets(d, kw)
     gl = np.random.default_rng(2).standard_normal(N).astype(np.float32) if kw["reduction"] == "none" else 1.0
-    check_case(d, "f16", kw, grad_loss=gl)
+    check_case(d, "f16", kw, grad_loss=gl, schedule=dict(bwd_chunk_axis=axis))
 
 
-@pytest.mark.parametrize("axis,cap_env", [("rows", "FLCE_MAX_CHUNK_ROWS"),
-                                          ("vocab", "FLCE_MAX_CHUNK_COLS")])
-def test_three_or_more_chunk_backward(axis, cap_env, monkeypatch):
+@pytest.mark.parametrize("axis", ["rows", "vocab"])
+def test_three_or_more_chunk_backward(axis):
     """Force 256-row chunks (3 of them) or 256-column chunks (4 of them).
 
     The fp32 partial that crosses the chunks (grad_weight for rows, grad_hidden
     for columns) is stored, added to, then added and cast.
     """
-    monkeypatch.setenv("FLCE_BWD_CHUNKS", axis)
-    monkeypatch.setenv(cap_env, "256")
     d = small_case(700, 136, 900, seed=11, dtype="bf16", bias=True, ignore_frac=0.1)
-    check_case(d, "bf16", dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3))
+    check_case(d, "bf16", dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3),
+               schedule=dict(bwd_chunk_axis=axis, max_chunk=256))
 
 
 def test_every_row_ignored_with_mean():

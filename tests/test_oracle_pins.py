@@ -357,12 +357,59 @@ def test_metrics_brute_force():
     assert out["entropy_sum"] == pytest.approx(ent, rel=1e-12)
 
 
-def test_metrics_do_not_touch_loss_or_grads():
-    """fused-linear-ce README, "Metrics for free": metrics are forward-only and leave loss and gradients unchanged."""
-    h, W, b, t = rnd(15, 5, 3, 8)
-    a = oracle.forward(h, W, t, bias=b)
-    c = oracle.forward(h, W, t, bias=b)
-    assert a["loss"] == c["loss"]
+def brute_top2_gap(row):
+    """Largest value minus the second largest of a list, by one scan (ties give 0)."""
+    if len(row) < 2:
+        return math.inf
+    best, second = -math.inf, -math.inf
+    for v in row:
+        if v > best:
+            best, second = v, best
+        elif v > second:
+            second = v
+    return best - second
+
+
+def plain_logits(h, W, b, s=1.0, c=None):
+    """z_ij written out element by element (bias, then scale, then the tanh softcap)."""
+    z = []
+    for hi in h.tolist():
+        row = []
+        for j, wj in enumerate(W.tolist()):
+            u = (sum(x * y for x, y in zip(hi, wj)) + (0.0 if b is None else float(b[j]))) * s
+            row.append(c * math.tanh(u / c) if c else u)
+        z.append(row)
+    return z
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 9])
+def test_top2_gap_brute_force(V):
+    """top2_gap, which excuses near-tie rows from the exact num_correct check, is the
+    largest logit minus the second largest, in both forward and forward_rows."""
+    h, W, b, t = rnd(40 + V, 12, 4, V)
+    if V >= 3:
+        W[0] *= 2.0          # column 0 leads in many rows ...
+        b[0] = 2.0
+        W[2] = W[0]          # ... tied with column 2: gap 0 there
+        b[2] = b[0]
+    kw = dict(logit_scale=0.8, softcap=3.0)
+    z = plain_logits(h, W, b, s=0.8, c=3.0)
+    want = np.array([brute_top2_gap(row) for row in z])
+    out = oracle.forward(h, W, t, bias=b, reduction="none", **kw)
+    blk = oracle.forward(h, W, t, bias=b, reduction="none", row_block=5, **kw)
+    rows = [0, 3, 7, 11]
+    fr = oracle.forward_rows(h, W, t, rows, bias=b, **kw)
+    if V == 1:
+        assert np.isinf(out["top2_gap"]).all() and np.isinf(fr["top2_gap"]).all()
+        return
+    np.testing.assert_allclose(out["top2_gap"], want, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(blk["top2_gap"], want, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(fr["top2_gap"], want[rows], rtol=1e-12, atol=1e-13)
+    assert (out["top2_gap"] >= 0).all()
+    if V >= 3:
+        # rows whose top logit is the tied pair (columns 0 and 2) have gap 0
+        tied = [i for i, row in enumerate(z) if max(row) == row[0]]
+        assert tied and all(out["top2_gap"][i] == 0.0 for i in tied)
 
 
 def test_mean_with_every_row_ignored():
