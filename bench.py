@@ -172,6 +172,22 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
     return 0.0
 
 
+def kernel_entry(name: str, launches: int, total_ms: float, sm_mhz: float, flops: float,
+                 all_ms: float) -> dict:
+    """One kernel's line of the timed region: time, share, TFLOP/s and the mean SM clock.
+
+    ``sm_mhz`` is the launches' mean SM clock from the library's clock records
+    (cycles over elapsed time, 0 when the kernel keeps none). TFLOP/s per GHz
+    compares kernels independently of the clock the power cap allowed.
+    """
+    tf = flops / (total_ms * 1e-3) / 1e12 if (flops and total_ms) else None
+    return {"name": name, "launches": launches,
+            "ms_per_launch": total_ms / launches if launches else 0.0,
+            "share": total_ms / max(all_ms, 1e-9), "tflops": tf,
+            "sm_mhz": sm_mhz or None,
+            "tflops_per_ghz": (tf / (sm_mhz * 1e-3)) if (tf and sm_mhz) else None}
+
+
 def fp32_alu_peak(sms: int, sm_max_mhz: float) -> float:
     """fp32 FFMA peak in TFLOP/s: SMs x 128 fp32 lanes x 2 FLOP x the maximum SM clock."""
     return sms * 128 * 2 * sm_max_mhz * 1e6 / 1e12
@@ -504,12 +520,11 @@ def ours_main(args, w):
         flops = w.flops_fwd_bwd
         tflops = flops / (ms * 1e-3) / 1e12
         kern = []
-        for name, n, tot in kernels:
+        for name, n, tot, mhz in kernels:
             per = tot / n if n else 0.0
             f = kernel_flops(name, w)
-            kern.append({"name": name, "launches": n, "ms_per_launch": per,
-                         "share": tot / max(sum(k[2] for k in kernels), 1e-9),
-                         "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
+            kern.append(kernel_entry(name, n, tot, mhz, f * args.steps,
+                                     sum(k[2] for k in kernels)))
         # the committed DRAM counts hold for the default schedule only
         default_variant = args.grad_weight_accum == "fp32" and args.vocab_shards == 1 and \
             w.dtype == wl.WORKLOADS[w.name].dtype and args.bwd_chunk_axis == "auto"
@@ -691,11 +706,10 @@ def chunked_main(args, w):
         peaks = load_peaks()
         tflops = w.flops_fwd_bwd / (ms * 1e-3) / 1e12
         kern = []
-        for name, n, tot in kernels:
+        for name, n, tot, mhz in kernels:
             f = kernel_flops(name, w)
-            kern.append({"name": name, "launches": n, "ms_per_launch": tot / n if n else 0.0,
-                         "share": tot / max(sum(k[2] for k in kernels), 1e-9),
-                         "tflops": (f * args.steps / (tot * 1e-3) / 1e12) if (f and tot) else None})
+            kern.append(kernel_entry(name, n, tot, mhz, f * args.steps,
+                                     sum(k[2] for k in kernels)))
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None
         roof = None

@@ -444,15 +444,21 @@ uint64_t flce_launch_count(void);
 
 /*
  * Per-kernel timing on the launching stream. While enabled, each launch is
- * bracketed by two CUDA events. flce_profiling_read synchronises those events.
- * It fills up to `max` records, in first-launch order, with the kernel name,
- * the number of launches and their total duration in milliseconds. It then
+ * bracketed by two CUDA events, and each tensor-core launch also sums its
+ * CTAs' SM clock cycles and elapsed nanoseconds into a record of a fixed
+ * 4096-entry array in the library's static device memory (no allocation;
+ * launches past the 4096th before a read get no record).
+ * flce_profiling_read synchronises those events. It fills up to `max`
+ * records, in first-launch order, with the kernel name, the number of
+ * launches, their total duration in milliseconds and their mean SM clock in
+ * MHz (cycles over nanoseconds; 0 for kernels without a record). It then
  * clears the counts. *count is set to the number of distinct kernels.
  */
 typedef struct {
   char name[48];
   uint64_t launches;
   double total_ms;
+  double sm_mhz;
 } flce_kernel_time;
 
 int flce_profiling_enable(int on);

@@ -74,7 +74,7 @@ ROW_STATE_BYTES = ctypes.sizeof(FlceRowState)
 
 class FlceKernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_uint64),
-                ("total_ms", ctypes.c_double)]
+                ("total_ms", ctypes.c_double), ("sm_mhz", ctypes.c_double)]
 
 
 class FlceError(RuntimeError):
@@ -261,9 +261,10 @@ def profiling_enable(on: bool) -> None:
     check(load().flce_profiling_enable(1 if on else 0), "flce_profiling_enable")
 
 
-def profiling_read(max_kernels: int = 64) -> list[tuple[str, int, float]]:
+def profiling_read(max_kernels: int = 64) -> list[tuple[str, int, float, float]]:
+    """(name, launches, total ms, mean SM MHz or 0) per kernel since the last read."""
     arr = (FlceKernelTime * max_kernels)()
     n = ctypes.c_int(0)
     check(load().flce_profiling_read(arr, max_kernels, ctypes.byref(n)), "flce_profiling_read")
-    return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms))
-            for i in range(min(n.value, max_kernels))]
+    return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms),
+             float(arr[i].sm_mhz)) for i in range(min(n.value, max_kernels))]

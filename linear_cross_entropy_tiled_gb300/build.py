@@ -3,8 +3,10 @@
     python -m linear_cross_entropy_tiled_gb300.build
 
 Each .cu file under csrc/ compiles in parallel with nvcc. The objects are then
-linked into linear_cross_entropy_tiled_gb300/lib/libflce.so. nvcc cross-compiles,
-so this also works on a machine without a GPU.
+linked into linear_cross_entropy_tiled_gb300/lib/libflce.so. Each .cu file under
+probes/ (stand-alone measurement programs, not part of the library) becomes an
+executable lib/flce_probe_<name>. nvcc cross-compiles, so this also works on a
+machine without a GPU.
 """
 from __future__ import annotations
 
@@ -17,6 +19,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
+PROBES = os.path.join(PKG, "probes")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libflce.so")
@@ -38,14 +41,23 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+def probe_sources() -> list[str]:
+    return sorted(os.path.join(PROBES, f) for f in os.listdir(PROBES) if f.endswith(".cu"))
+
+
+def probe_path(src: str) -> str:
+    return os.path.join(LIBDIR, "flce_probe_" + os.path.basename(src)[:-3])
+
+
 def _deps_mtime() -> float:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + probe_sources()
     files.append(os.path.join(INCLUDE, "flce.h"))
     return max(os.path.getmtime(f) for f in files)
 
 
 def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
+    outs = [LIB] + [probe_path(p) for p in probe_sources()]
+    return all(os.path.exists(o) and os.path.getmtime(o) >= _deps_mtime() for o in outs)
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
@@ -66,8 +78,21 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(sources())) as ex:
-        objs = list(ex.map(compile_one, sources()))
+    def build_probe(src: str) -> str:
+        exe = probe_path(src)
+        r = subprocess.run([cc, *ARCH, "-O3", "-lineinfo", "-std=c++17", *extra, src, "-o", exe],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+        return exe
+
+    srcs = sources()
+    probes = probe_sources()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs) + len(probes)) as ex:
+        probe_jobs = [ex.submit(build_probe, p) for p in probes]
+        objs = list(ex.map(compile_one, srcs))
+        for j in probe_jobs:
+            j.result()
     tmp = LIB + ".tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:

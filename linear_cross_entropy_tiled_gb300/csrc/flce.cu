@@ -83,9 +83,17 @@ int device_info(DeviceInfo* out) {
 }
 
 // -------------------------------------------------------------- profiling
+// While profiling is on, each tensor-core launch also sums its CTAs' SM clock
+// cycles and nanoseconds into one record of this fixed array (static device
+// memory of the library image; nothing is allocated). flce_profiling_read
+// turns them into each kernel's mean SM clock.
+constexpr int kClockSlots = 4096;
+__device__ ClockRecord g_clock_records[kClockSlots];
+
 struct Pending {
   int name;
   cudaEvent_t e0, e1;
+  int dev, slot;   // clock record, or slot -1 when none
 };
 std::mutex g_prof_mu;
 bool g_prof = false;
@@ -94,6 +102,25 @@ std::vector<uint64_t> g_counts;
 std::vector<double> g_ms;
 std::vector<Pending> g_pending;
 std::vector<cudaEvent_t> g_pool;
+std::vector<double> g_cycles, g_clock_ns;
+ClockRecord* g_clock_base[64] = {};
+int g_clock_next[64] = {};
+thread_local ClockRecord* g_cur_clk = nullptr;   // record of the launch being issued
+
+// A zeroed clock record on device `dev` for the next launch, or nullptr.
+ClockRecord* take_clock_record(int dev, cudaStream_t s, int* slot) {
+  *slot = -1;
+  if (dev < 0 || dev >= 64 || g_clock_next[dev] >= kClockSlots) return nullptr;
+  if (g_clock_base[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_clock_records) != cudaSuccess || p == nullptr) return nullptr;
+    g_clock_base[dev] = static_cast<ClockRecord*>(p);
+  }
+  ClockRecord* r = g_clock_base[dev] + g_clock_next[dev];
+  if (cudaMemsetAsync(r, 0, sizeof(ClockRecord), s) != cudaSuccess) return nullptr;
+  *slot = g_clock_next[dev]++;
+  return r;
+}
 
 cudaEvent_t pool_event() {
   if (!g_pool.empty()) {
@@ -112,6 +139,8 @@ int name_index(const char* n) {
   g_names.emplace_back(n);
   g_counts.push_back(0);
   g_ms.push_back(0.0);
+  g_cycles.push_back(0.0);
+  g_clock_ns.push_back(0.0);
   return static_cast<int>(g_names.size() - 1);
 }
 
@@ -121,13 +150,18 @@ int launch(const char* name, cudaStream_t s, F&& f) {
   std::unique_lock<std::mutex> lk(g_prof_mu);
   const bool prof = g_prof;
   Pending p{};
+  p.slot = -1;
+  g_cur_clk = nullptr;
   if (prof) {
     p.name = name_index(name);
+    cudaGetDevice(&p.dev);
+    g_cur_clk = take_clock_record(p.dev, s, &p.slot);
     p.e0 = pool_event();
     cudaEventRecord(p.e0, s);
   }
   lk.unlock();
   const cudaError_t e = f();
+  g_cur_clk = nullptr;
   if (prof) {
     lk.lock();
     p.e1 = pool_event();
@@ -425,6 +459,7 @@ int gemm_group_m(const GemmArgs& ga, int pairs) {
 cudaError_t launch_gemm(const GemmOperand& op_a, const GemmOperand& op_b, GemmArgs ga, bool f16,
                         int pairs, cudaStream_t st) {
   ga.group_m = gemm_group_m(ga, pairs);
+  ga.clk = g_cur_clk;
   return launch_gemm_tc(op_a, op_b, ga, f16, pairs, st);
 }
 
@@ -648,6 +683,7 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
     if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
     const bool f16 = p->dtype == FLCE_F16;
     v = launch("flce_fwd_tc", st, [&] {
+      fa.clk = g_cur_clk;
       return launch_fwd_tc(tm_h, tm_w, fa, f16, bias != nullptr, p->softcap > 0.f, grid, st);
     });
   } else {
@@ -916,6 +952,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
       da.num_units = da.num_panels * da.n_blocks;
       v = launch("flce_dlogits_tc", st, [&] {
+        da.clk = g_cur_clk;
         return launch_ds_tc(tm_h, tm_wc, da, f16, bias != nullptr, p->softcap > 0.f, grid, st);
       });
       if (v != FLCE_OK) return v;
@@ -1008,6 +1045,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.ds_t = grad_weight != nullptr ? ws + L.ds_t : nullptr;
       da.ld_t = L.ds_t_ld;
       v = launch("flce_dlogits_tc", st, [&] {
+        da.clk = g_cur_clk;
         return launch_ds_tc(tm_h, tm_w, da, f16, bias != nullptr, p->softcap > 0.f, grid, st);
       });
       if (v != FLCE_OK) return v;
@@ -1499,6 +1537,8 @@ int flce_profiling_enable(int on) {
 
 int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
   for (const Pending& p : g_pending) {
     cudaError_t e = cudaEventSynchronize(p.e1);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
@@ -1506,10 +1546,20 @@ int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
     cudaEventElapsedTime(&ms, p.e0, p.e1);
     g_counts[p.name] += 1;
     g_ms[p.name] += ms;
+    if (p.slot >= 0) {
+      ClockRecord r{};
+      cudaSetDevice(p.dev);
+      e = cudaMemcpy(&r, g_clock_base[p.dev] + p.slot, sizeof(r), cudaMemcpyDeviceToHost);
+      cudaSetDevice(cur);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (clock record)");
+      g_cycles[p.name] += static_cast<double>(r.cycles);
+      g_clock_ns[p.name] += static_cast<double>(r.ns);
+    }
     g_pool.push_back(p.e0);
     g_pool.push_back(p.e1);
   }
   g_pending.clear();
+  for (int& n : g_clock_next) n = 0;
   int n = 0;
   for (size_t i = 0; i < g_names.size(); ++i) {
     if (g_counts[i] == 0) continue;
@@ -1518,10 +1568,13 @@ int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
       strncpy(out[n].name, g_names[i].c_str(), sizeof(out[n].name) - 1);
       out[n].launches = g_counts[i];
       out[n].total_ms = g_ms[i];
+      out[n].sm_mhz = g_clock_ns[i] > 0 ? g_cycles[i] / g_clock_ns[i] * 1e3 : 0.0;
     }
     ++n;
     g_counts[i] = 0;
     g_ms[i] = 0.0;
+    g_cycles[i] = 0.0;
+    g_clock_ns[i] = 0.0;
   }
   if (count != nullptr) *count = n;
   return FLCE_OK;

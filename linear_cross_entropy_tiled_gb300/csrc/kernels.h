@@ -59,8 +59,17 @@ __host__ __device__ inline void decode_unit(int u, int n_blocks, int group_block
   nb = g * group_blocks + (r - panel * gb);
 }
 
+// Clock record of one launch, filled only while profiling is on: the sum over
+// the launch's CTAs of SM clock cycles (clock64) and of nanoseconds
+// (%globaltimer) from the CTA's start to its end. Their ratio is the launch's
+// mean SM clock.
+struct ClockRecord {
+  unsigned long long cycles, ns;
+};
+
 struct FwdArgs {
   int N, H, V;
+  ClockRecord* clk;            // nullable (profiling)
   int group_blocks;
   long long vocab_start;       // global id of this call's first vocabulary row
   unsigned long long wait_ns;  // limit of every bounded wait (kWaitLimitNs unless testing)
@@ -163,6 +172,7 @@ struct RowCoefArgs {
 
 struct DsArgs {
   int rows, row0, H, V, V_pad;
+  ClockRecord* clk;            // nullable (profiling)
   int group_blocks;
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
   float scale, softcap, inv_softcap;
@@ -201,6 +211,7 @@ enum GemmMode : int {
 // time share their K range.
 struct GemmArgs {
   int M, N, K;
+  ClockRecord* clk;            // nullable (profiling)
   int m_tiles, n_tiles, k_blocks, num_tiles;
   int k_splits, kb_per_split;
   int group_m;                 // row tiles per raster group (decode_unit; 1: row after row)

@@ -99,6 +99,23 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_
   return *s.tmem_slot;
 }
 
+// Start of a CTA's clock record (thread 0 only; see ClockRecord).
+struct ClockStart {
+  unsigned long long c0 = 0, t0 = 0;
+  __device__ __forceinline__ explicit ClockStart(const ClockRecord* rec) {
+    if (rec != nullptr && threadIdx.x == 0) {
+      c0 = clock64();
+      t0 = global_timer_ns();
+    }
+  }
+  __device__ __forceinline__ void finish(ClockRecord* rec) const {
+    if (rec != nullptr && threadIdx.x == 0) {
+      atomicAdd(&rec->cycles, static_cast<unsigned long long>(clock64()) - c0);
+      atomicAdd(&rec->ns, global_timer_ns() - t0);
+    }
+  }
+};
+
 // The even CTA's MMAs read the odd CTA's shared memory and write its TMEM.
 // So neither CTA releases TMEM or exits before the whole pair is done.
 __device__ __forceinline__ void tc_teardown(uint32_t tmem, int warp) {
@@ -386,6 +403,7 @@ template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                   const FwdArgs a) {
+  const ClockStart clock_start(a.clk);
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -474,6 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   }
   tc_teardown(tmem, warp);
+  clock_start.finish(a.clk);
 }
 
 // ====================================================== dlogits kernel
@@ -570,6 +589,7 @@ template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const DsArgs a) {
+  const ClockStart clock_start(a.clk);
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -691,6 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     }
   }
   tc_teardown(tmem, warp);
+  clock_start.finish(a.clk);
 }
 
 // ========================================================= plain GEMM
@@ -707,6 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_a3,
                    const __grid_constant__ CUtensorMap tm_b3, const GemmArgs a) {
+  const ClockStart clock_start(a.clk);
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -935,6 +957,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   }
   tc_teardown(tmem, warp);
+  clock_start.finish(a.clk);
 }
 
 template <class K>
