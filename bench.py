@@ -172,20 +172,24 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
     return 0.0
 
 
-def kernel_entry(name: str, launches: int, total_ms: float, sm_mhz: float, flops: float,
+def kernel_entry(name: str, launches: int, total_ms: float, sm_mhz: float, waits, flops: float,
                  all_ms: float) -> dict:
     """One kernel's line of the timed region: time, share, TFLOP/s and the mean SM clock.
 
     ``sm_mhz`` is the launches' mean SM clock from the library's clock records
     (cycles over elapsed time, 0 when the kernel keeps none). TFLOP/s per GHz
     compares kernels independently of the clock the power cap allowed.
+    ``waits`` are the shares of the MMA thread's cycles spent waiting for
+    operands and for a free accumulator.
     """
     tf = flops / (total_ms * 1e-3) / 1e12 if (flops and total_ms) else None
     return {"name": name, "launches": launches,
             "ms_per_launch": total_ms / launches if launches else 0.0,
             "share": total_ms / max(all_ms, 1e-9), "tflops": tf,
             "sm_mhz": sm_mhz or None,
-            "tflops_per_ghz": (tf / (sm_mhz * 1e-3)) if (tf and sm_mhz) else None}
+            "tflops_per_ghz": (tf / (sm_mhz * 1e-3)) if (tf and sm_mhz) else None,
+            "mma_wait_operands": waits[0] if sm_mhz else None,
+            "mma_wait_accumulator": waits[1] if sm_mhz else None}
 
 
 def fp32_alu_peak(sms: int, sm_max_mhz: float) -> float:
@@ -520,10 +524,9 @@ def ours_main(args, w):
         flops = w.flops_fwd_bwd
         tflops = flops / (ms * 1e-3) / 1e12
         kern = []
-        for name, n, tot, mhz in kernels:
-            per = tot / n if n else 0.0
+        for name, n, tot, mhz, waits in kernels:
             f = kernel_flops(name, w)
-            kern.append(kernel_entry(name, n, tot, mhz, f * args.steps,
+            kern.append(kernel_entry(name, n, tot, mhz, waits, f * args.steps,
                                      sum(k[2] for k in kernels)))
         # the committed DRAM counts hold for the default schedule only
         default_variant = args.grad_weight_accum == "fp32" and args.vocab_shards == 1 and \
@@ -706,9 +709,9 @@ def chunked_main(args, w):
         peaks = load_peaks()
         tflops = w.flops_fwd_bwd / (ms * 1e-3) / 1e12
         kern = []
-        for name, n, tot, mhz in kernels:
+        for name, n, tot, mhz, waits in kernels:
             f = kernel_flops(name, w)
-            kern.append(kernel_entry(name, n, tot, mhz, f * args.steps,
+            kern.append(kernel_entry(name, n, tot, mhz, waits, f * args.steps,
                                      sum(k[2] for k in kernels)))
         kern.sort(key=lambda k: -k["share"])
         dom = kern[0] if kern else None

@@ -451,14 +451,20 @@ uint64_t flce_launch_count(void);
  * flce_profiling_read synchronises those events. It fills up to `max`
  * records, in first-launch order, with the kernel name, the number of
  * launches, their total duration in milliseconds and their mean SM clock in
- * MHz (cycles over nanoseconds; 0 for kernels without a record). It then
- * clears the counts. *count is set to the number of distinct kernels.
+ * MHz (cycles over nanoseconds; 0 for kernels without a record). For the
+ * tensor-core kernels it adds the share of the MMA-issuing thread's cycles
+ * spent waiting for operands to land in shared memory, and waiting for the
+ * epilogue to free an accumulator; the rest is issuing MMAs and waiting for
+ * the tensor cores to take them. It then clears the counts. *count is set to
+ * the number of distinct kernels.
  */
 typedef struct {
   char name[48];
   uint64_t launches;
   double total_ms;
   double sm_mhz;
+  double mma_wait_operands;     /* fraction of the MMA thread's cycles, 0..1 */
+  double mma_wait_accumulator;  /* fraction of the MMA thread's cycles, 0..1 */
 } flce_kernel_time;
 
 int flce_profiling_enable(int on);

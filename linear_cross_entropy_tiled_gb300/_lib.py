@@ -74,7 +74,8 @@ ROW_STATE_BYTES = ctypes.sizeof(FlceRowState)
 
 class FlceKernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_uint64),
-                ("total_ms", ctypes.c_double), ("sm_mhz", ctypes.c_double)]
+                ("total_ms", ctypes.c_double), ("sm_mhz", ctypes.c_double),
+                ("mma_wait_operands", ctypes.c_double), ("mma_wait_accumulator", ctypes.c_double)]
 
 
 class FlceError(RuntimeError):
@@ -261,10 +262,16 @@ def profiling_enable(on: bool) -> None:
     check(load().flce_profiling_enable(1 if on else 0), "flce_profiling_enable")
 
 
-def profiling_read(max_kernels: int = 64) -> list[tuple[str, int, float, float]]:
-    """(name, launches, total ms, mean SM MHz or 0) per kernel since the last read."""
+def profiling_read(max_kernels: int = 64) -> list[tuple]:
+    """(name, launches, total ms, mean SM MHz or 0, MMA wait shares) per kernel since the last read.
+
+    The last element is (share of the MMA thread's cycles waiting for operands,
+    share waiting for a free accumulator), zeros for kernels without a record.
+    """
     arr = (FlceKernelTime * max_kernels)()
     n = ctypes.c_int(0)
     check(load().flce_profiling_read(arr, max_kernels, ctypes.byref(n)), "flce_profiling_read")
     return [(arr[i].name.decode(), int(arr[i].launches), float(arr[i].total_ms),
-             float(arr[i].sm_mhz)) for i in range(min(n.value, max_kernels))]
+             float(arr[i].sm_mhz),
+             (float(arr[i].mma_wait_operands), float(arr[i].mma_wait_accumulator)))
+            for i in range(min(n.value, max_kernels))]

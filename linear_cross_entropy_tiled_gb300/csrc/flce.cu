@@ -102,7 +102,7 @@ std::vector<uint64_t> g_counts;
 std::vector<double> g_ms;
 std::vector<Pending> g_pending;
 std::vector<cudaEvent_t> g_pool;
-std::vector<double> g_cycles, g_clock_ns;
+std::vector<double> g_cycles, g_clock_ns, g_mma_cycles, g_mma_wait_ops, g_mma_wait_acc;
 ClockRecord* g_clock_base[64] = {};
 int g_clock_next[64] = {};
 thread_local ClockRecord* g_cur_clk = nullptr;   // record of the launch being issued
@@ -141,6 +141,9 @@ int name_index(const char* n) {
   g_ms.push_back(0.0);
   g_cycles.push_back(0.0);
   g_clock_ns.push_back(0.0);
+  g_mma_cycles.push_back(0.0);
+  g_mma_wait_ops.push_back(0.0);
+  g_mma_wait_acc.push_back(0.0);
   return static_cast<int>(g_names.size() - 1);
 }
 
@@ -1554,6 +1557,9 @@ int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (clock record)");
       g_cycles[p.name] += static_cast<double>(r.cycles);
       g_clock_ns[p.name] += static_cast<double>(r.ns);
+      g_mma_cycles[p.name] += static_cast<double>(r.mma_cycles);
+      g_mma_wait_ops[p.name] += static_cast<double>(r.mma_wait_operands);
+      g_mma_wait_acc[p.name] += static_cast<double>(r.mma_wait_accumulator);
     }
     g_pool.push_back(p.e0);
     g_pool.push_back(p.e1);
@@ -1569,12 +1575,17 @@ int flce_profiling_read(flce_kernel_time* out, int max, int* count) {
       out[n].launches = g_counts[i];
       out[n].total_ms = g_ms[i];
       out[n].sm_mhz = g_clock_ns[i] > 0 ? g_cycles[i] / g_clock_ns[i] * 1e3 : 0.0;
+      out[n].mma_wait_operands = g_mma_cycles[i] > 0 ? g_mma_wait_ops[i] / g_mma_cycles[i] : 0.0;
+      out[n].mma_wait_accumulator = g_mma_cycles[i] > 0 ? g_mma_wait_acc[i] / g_mma_cycles[i] : 0.0;
     }
     ++n;
     g_counts[i] = 0;
     g_ms[i] = 0.0;
     g_cycles[i] = 0.0;
     g_clock_ns[i] = 0.0;
+    g_mma_cycles[i] = 0.0;
+    g_mma_wait_ops[i] = 0.0;
+    g_mma_wait_acc[i] = 0.0;
   }
   if (count != nullptr) *count = n;
   return FLCE_OK;

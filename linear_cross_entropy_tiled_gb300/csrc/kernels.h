@@ -62,9 +62,12 @@ __host__ __device__ inline void decode_unit(int u, int n_blocks, int group_block
 // Clock record of one launch, filled only while profiling is on: the sum over
 // the launch's CTAs of SM clock cycles (clock64) and of nanoseconds
 // (%globaltimer) from the CTA's start to its end. Their ratio is the launch's
-// mean SM clock.
+// mean SM clock. The MMA-issuing threads also add the cycles of their role,
+// and the cycles they spent waiting for operands (TMA loads) and for a free
+// accumulator (the epilogue).
 struct ClockRecord {
   unsigned long long cycles, ns;
+  unsigned long long mma_cycles, mma_wait_operands, mma_wait_accumulator;
 };
 
 struct FwdArgs {

@@ -179,29 +179,38 @@ __device__ __forceinline__ void producer_role(const TcSmem& s, const WaitGuard& 
 // Runs in the even CTA only. Descs(ta, tb, sa, sb, kk, adesc, bdesc, idesc)
 // builds the operand and instruction descriptors of the kk-th 16-deep K
 // step within a 64-deep stage of tile (ta, tb).
+// With `rec` (profiling), the role's cycles and its waits for operands and
+// for a free accumulator are added to the launch's clock record.
 template <class ForEachTile, class KBlocks, class Descs>
 __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, uint32_t tmem,
                                          KBlocks kblocks_of, ForEachTile for_each_tile,
-                                         Descs descs) {
+                                         Descs descs, ClockRecord* rec) {
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool dead = false;
+  const bool prof = rec != nullptr;
+  const unsigned long long t_start = prof ? clock64() : 0;
+  unsigned long long w_ops = 0, w_acc = 0;
   for_each_tile([&](int ta, int tb) {
     if (dead) return;
     const int kblocks = kblocks_of(ta, tb);
+    const unsigned long long c0 = prof ? clock64() : 0;
     if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, g)) {
       dead = true;
       return;
     }
+    if (prof) w_acc += clock64() - c0;
     tc_fence_after();
     const uint32_t d = tmem + static_cast<uint32_t>(acc * kBN);
     for (int kb = 0; kb < kblocks; ++kb) {
+      const unsigned long long c1 = prof ? clock64() : 0;
       if (!mbar_wait(&s.full[stage], phase, g)) {
         dead = true;
         return;
       }
+      if (prof) w_ops += clock64() - c1;
       tc_fence_after();
       const uint32_t sa = smem_u32(s.a + stage * kStageA);
       const uint32_t sb = smem_u32(s.b + stage * kStageB);
@@ -225,6 +234,11 @@ __device__ __forceinline__ void mma_role(const TcSmem& s, const WaitGuard& g, ui
   // Every MMA must have finished before TMEM is released.
   umma_commit_pair(s.mma_done);
   drain_wait(s.mma_done, 0);
+  if (prof) {
+    atomicAdd(&rec->mma_cycles, static_cast<unsigned long long>(clock64()) - t_start);
+    atomicAdd(&rec->mma_wait_operands, w_ops);
+    atomicAdd(&rec->mma_wait_accumulator, w_acc);
+  }
 }
 
 // Both operands K-major; the pair computes M = 256, N = 256.
@@ -442,7 +456,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>,
+               a.clk);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -624,7 +639,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>);
+      mma_role(s, g, tmem, [&](int, int) { return kblocks; }, for_each_tile, kmajor_descs<T>,
+               a.clk);
   } else {
     // warps 2-5 take columns 0-127 of each tile, warps 6-9 columns 128-255
     const int q = warp & 3;
@@ -808,7 +824,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                  ad = operand_desc(sa, a_mn, kk);
                  bd = operand_desc(sb, b_mn, kk);
                  idesc = id;
-               });
+               },
+               a.clk);
     }
   } else {
     const int q = warp & 3;

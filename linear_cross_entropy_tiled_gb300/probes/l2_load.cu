@@ -1,0 +1,169 @@
+// Bytes per SM clock that bulk copies can move from global memory into shared
+// memory, with every SM loading at once.
+//
+// The tensor-core kernels stage each CTA's operands through shared memory: at
+// full MMA rate a 256 x 256 pair tile with 64-deep K slices needs 32 KB per
+// CTA per 512 SM clocks, 64 bytes per clock per SM, most of it from L2. This
+// program measures what the memory system delivers per SM when all SMs
+// stream at once, from an L2-resident window and from one much larger than
+// L2. One thread per CTA (one CTA per SM) keeps a ring of 16 KB
+// cp.async.bulk copies in flight, each completing on its stage's mbarrier.
+// Every wait is bounded: a stage that does not complete within a second sets
+// an error flag, and the program reports it instead of a rate.
+//
+// Output: one JSON object per line.
+//   flce_probe_l2_load
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <vector>
+
+namespace {
+
+constexpr int kChunk = 16384;  // bytes per copy
+constexpr int kMaxStages = 12;
+
+#define CHECK(x)                                                                       \
+  do {                                                                                 \
+    cudaError_t e_ = (x);                                                              \
+    if (e_ != cudaSuccess) {                                                           \
+      fprintf(stderr, "%s:%d %s: %s\n", __FILE__, __LINE__, #x, cudaGetErrorString(e_)); \
+      exit(1);                                                                         \
+    }                                                                                  \
+  } while (0)
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of the mbarrier at shared address `bar`, at most
+// one second. Returns false if it gave up.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = now_ns();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (now_ns() - t0 > 1000000000ull) return false;
+  }
+}
+
+// CTA c copies chunk (c + i * gridDim.x) mod nchunks of the window, for i in
+// [0, iters), through `stages` shared-memory buffers. out[c] = {cycles, ns}.
+__global__ void __launch_bounds__(32) bulk_load_kernel(const char* src, long long nchunks,
+                                                       long long iters, int stages,
+                                                       unsigned long long* out, int* error) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ __align__(8) uint64_t bars[kMaxStages];
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < stages; ++s)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[s])) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const unsigned long long c0 = clock64(), t0 = now_ns();
+  long long chunk = blockIdx.x % nchunks;
+  bool ok = true;
+  for (long long i = 0; i < iters && ok; ++i) {
+    const int s = static_cast<int>(i % stages);
+    const uint32_t bar = smem_addr(&bars[s]);
+    if (i >= stages) ok = wait_phase(bar, static_cast<uint32_t>(((i / stages) - 1) & 1));
+    if (!ok) break;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kChunk)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem + s * kChunk)),
+        "l"(src + chunk * kChunk), "r"(kChunk), "r"(bar)
+        : "memory");
+    for (chunk += gridDim.x; chunk >= nchunks;) chunk -= nchunks;
+  }
+  // the copies still in flight
+  for (long long i = iters > stages ? iters - stages : 0; i < iters && ok; ++i) {
+    const int s = static_cast<int>(i % stages);
+    ok = wait_phase(smem_addr(&bars[s]), static_cast<uint32_t>((i / stages) & 1));
+  }
+  if (!ok) atomicOr(error, 1);
+  out[2 * blockIdx.x] = clock64() - c0;
+  out[2 * blockIdx.x + 1] = now_ns() - t0;
+}
+
+}  // namespace
+
+int main() {
+  int dev = 0, sms = 0;
+  CHECK(cudaGetDevice(&dev));
+  CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const size_t max_window = size_t(2048) << 20;
+  char* buf = nullptr;
+  CHECK(cudaMalloc(&buf, max_window));
+  CHECK(cudaMemset(buf, 1, max_window));
+  unsigned long long* rec = nullptr;
+  int* err = nullptr;
+  CHECK(cudaMalloc(&rec, sizeof(unsigned long long) * 2 * sms));
+  CHECK(cudaMalloc(&err, sizeof(int)));
+  CHECK(cudaFuncSetAttribute(bulk_load_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxStages * kChunk));
+  printf("{\"sms\": %d, \"chunk_bytes\": %d}\n", sms, kChunk);
+  const long long windows_mb[] = {24, 64, 2048};
+  for (long long wmb : windows_mb) {
+    for (int stages : {4, 8, 12}) {
+      const long long nchunks = (wmb << 20) / kChunk;
+      const long long iters = (48ll << 30) / (static_cast<long long>(sms) * kChunk);
+      CHECK(cudaMemset(err, 0, sizeof(int)));
+      auto launch = [&] {
+        // the full ring's shared memory in every case, so that one CTA runs per SM
+        bulk_load_kernel<<<sms, 32, kMaxStages * kChunk>>>(buf, nchunks, iters, stages, rec, err);
+      };
+      launch();
+      CHECK(cudaDeviceSynchronize());
+      cudaEvent_t e0, e1;
+      CHECK(cudaEventCreate(&e0));
+      CHECK(cudaEventCreate(&e1));
+      CHECK(cudaEventRecord(e0));
+      launch();
+      CHECK(cudaEventRecord(e1));
+      CHECK(cudaEventSynchronize(e1));
+      CHECK(cudaGetLastError());
+      float ms = 0.f;
+      CHECK(cudaEventElapsedTime(&ms, e0, e1));
+      std::vector<unsigned long long> h(2 * sms);
+      CHECK(cudaMemcpy(h.data(), rec, h.size() * 8, cudaMemcpyDeviceToHost));
+      int herr = 0;
+      CHECK(cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost));
+      double cyc = 0, ns = 0;
+      for (int i = 0; i < sms; ++i) {
+        cyc += static_cast<double>(h[2 * i]);
+        ns += static_cast<double>(h[2 * i + 1]);
+      }
+      const double bytes = static_cast<double>(sms) * iters * kChunk;
+      const double mhz = cyc / ns * 1e3;
+      const double per_sm_clk = bytes / sms / (cyc / sms);
+      printf("{\"probe\": \"bulk_load\", \"window_bytes\": %lld, \"stages\": %d, \"bytes\": %.0f, "
+             "\"ms\": %.4f, \"gbps\": %.1f, \"sm_mhz\": %.0f, \"bytes_per_sm_clock\": %.2f, "
+             "\"status\": \"%s\"}\n",
+             wmb << 20, stages, bytes, ms, bytes / (ms * 1e-3) / 1e9, mhz, per_sm_clk,
+             herr ? "a wait expired" : "ok");
+      fflush(stdout);
+      CHECK(cudaEventDestroy(e0));
+      CHECK(cudaEventDestroy(e1));
+    }
+  }
+  CHECK(cudaFree(buf));
+  CHECK(cudaFree(rec));
+  CHECK(cudaFree(err));
+  return 0;
+}
