@@ -6,14 +6,22 @@
 // CTA per 512 SM clocks, 64 bytes per clock per SM, most of it from L2. This
 // program measures what the memory system delivers per SM when all SMs
 // stream at once, from an L2-resident window and from one much larger than
-// L2. One thread per CTA (one CTA per SM) keeps a ring of 16 KB
-// cp.async.bulk copies in flight, each completing on its stage's mbarrier.
-// Every wait is bounded: a stage that does not complete within a second sets
-// an error flag, and the program reports it instead of a rate.
+// L2. One thread per CTA (one CTA per SM) keeps a ring of 16 KB copies in
+// flight, each completing on its stage's mbarrier:
+//   bulk     cp.async.bulk of 16 KB contiguous bytes;
+//   tensor   cp.async.bulk.tensor.2d of a 64 x 128 bf16 box with the 128-byte
+//            swizzle, the kernels' own operand load.
+// `share` CTAs read the same sequence of chunks at about the same time (the
+// kernels' CTA pairs share each operand slab among several pairs); share = 1
+// gives every CTA its own data. Every wait is bounded: a stage that does not
+// complete within a second sets an error flag, and the program reports it
+// instead of a rate.
 //
 // Output: one JSON object per line.
 //   flce_probe_l2_load
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -63,10 +71,14 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
   }
 }
 
-// CTA c copies chunk (c + i * gridDim.x) mod nchunks of the window, for i in
-// [0, iters), through `stages` shared-memory buffers. out[c] = {cycles, ns}.
-__global__ void __launch_bounds__(32) bulk_load_kernel(const char* src, long long nchunks,
-                                                       long long iters, int stages,
+// CTA c belongs to group g = c / share of `share` CTAs; it copies chunk
+// (g + i * groups) mod nchunks of the window, for i in [0, iters), through
+// `stages` shared-memory buffers. With a tensor map the chunk is the box at
+// rows 128 * chunk of a [rows][64] bf16 view of the window. out[c] = {cycles, ns}.
+__global__ void __launch_bounds__(32) bulk_load_kernel(const char* src,
+                                                       const __grid_constant__ CUtensorMap tmap,
+                                                       bool tensor, long long nchunks,
+                                                       long long iters, int stages, int share,
                                                        unsigned long long* out, int* error) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ __align__(8) uint64_t bars[kMaxStages];
@@ -75,7 +87,8 @@ __global__ void __launch_bounds__(32) bulk_load_kernel(const char* src, long lon
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[s])) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   const unsigned long long c0 = clock64(), t0 = now_ns();
-  long long chunk = blockIdx.x % nchunks;
+  const long long groups = (gridDim.x + share - 1) / share;
+  long long chunk = (blockIdx.x / share) % nchunks;
   bool ok = true;
   for (long long i = 0; i < iters && ok; ++i) {
     const int s = static_cast<int>(i % stages);
@@ -84,12 +97,21 @@ __global__ void __launch_bounds__(32) bulk_load_kernel(const char* src, long lon
     if (!ok) break;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kChunk)
                  : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(smem + s * kChunk)),
-        "l"(src + chunk * kChunk), "r"(kChunk), "r"(bar)
-        : "memory");
-    for (chunk += gridDim.x; chunk >= nchunks;) chunk -= nchunks;
+    if (tensor) {
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+          " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem + s * kChunk)),
+          "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(0), "r"(static_cast<int>(chunk * 128)),
+          "r"(bar)
+          : "memory");
+    } else {
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(smem + s * kChunk)),
+          "l"(src + chunk * kChunk), "r"(kChunk), "r"(bar)
+          : "memory");
+    }
+    for (chunk += groups; chunk >= nchunks;) chunk -= nchunks;
   }
   // the copies still in flight
   for (long long i = iters > stages ? iters - stages : 0; i < iters && ok; ++i) {
@@ -118,15 +140,44 @@ int main() {
   CHECK(cudaFuncSetAttribute(bulk_load_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxStages * kChunk));
   printf("{\"sms\": %d, \"chunk_bytes\": %d}\n", sms, kChunk);
-  const long long windows_mb[] = {24, 64, 2048};
-  for (long long wmb : windows_mb) {
-    for (int stages : {4, 8, 12}) {
+  // [rows][64] bf16 view of the whole buffer, 64 x 128 boxes, 128-byte swizzle
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    CHECK(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      fprintf(stderr, "cuTensorMapEncodeTiled not found\n");
+      return 1;
+    }
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  CUtensorMap tmap;
+  {
+    const cuuint64_t dims[2] = {64, max_window / 128};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, buf, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      fprintf(stderr, "cuTensorMapEncodeTiled failed\n");
+      return 1;
+    }
+  }
+  const long long windows_mb[] = {64, 2048};
+  for (long long wmb : windows_mb)
+  for (int tensor : {0, 1})
+  for (int share : {1, 4, 16, 152}) {
+    {
+      const int stages = 8;
       const long long nchunks = (wmb << 20) / kChunk;
       const long long iters = (48ll << 30) / (static_cast<long long>(sms) * kChunk);
       CHECK(cudaMemset(err, 0, sizeof(int)));
       auto launch = [&] {
         // the full ring's shared memory in every case, so that one CTA runs per SM
-        bulk_load_kernel<<<sms, 32, kMaxStages * kChunk>>>(buf, nchunks, iters, stages, rec, err);
+        bulk_load_kernel<<<sms, 32, kMaxStages * kChunk>>>(buf, tmap, tensor != 0, nchunks, iters,
+                                                           stages, share, rec, err);
       };
       launch();
       CHECK(cudaDeviceSynchronize());
@@ -152,11 +203,11 @@ int main() {
       const double bytes = static_cast<double>(sms) * iters * kChunk;
       const double mhz = cyc / ns * 1e3;
       const double per_sm_clk = bytes / sms / (cyc / sms);
-      printf("{\"probe\": \"bulk_load\", \"window_bytes\": %lld, \"stages\": %d, \"bytes\": %.0f, "
-             "\"ms\": %.4f, \"gbps\": %.1f, \"sm_mhz\": %.0f, \"bytes_per_sm_clock\": %.2f, "
-             "\"status\": \"%s\"}\n",
-             wmb << 20, stages, bytes, ms, bytes / (ms * 1e-3) / 1e9, mhz, per_sm_clk,
-             herr ? "a wait expired" : "ok");
+      printf("{\"probe\": \"%s\", \"window_bytes\": %lld, \"share\": %d, \"stages\": %d, "
+             "\"bytes\": %.0f, \"ms\": %.4f, \"gbps\": %.1f, \"sm_mhz\": %.0f, "
+             "\"bytes_per_sm_clock\": %.2f, \"status\": \"%s\"}\n",
+             tensor ? "tensor_load" : "bulk_load", wmb << 20, share, stages, bytes, ms,
+             bytes / (ms * 1e-3) / 1e9, mhz, per_sm_clk, herr ? "a wait expired" : "ok");
       fflush(stdout);
       CHECK(cudaEventDestroy(e0));
       CHECK(cudaEventDestroy(e1));
