@@ -56,6 +56,12 @@
  *   to add its gradients into the buffers it is given.
  * - Results do not depend on launch timing. Every reduction runs in a fixed
  *   order, so repeated calls on the same inputs give bit-identical outputs.
+ * - The debug build of this library (libflce_debug.so, compiled with
+ *   FLCE_DEBUG) checks every kernel store against the buffer it belongs to.
+ *   A store that would land outside is skipped and flagged; each entry point
+ *   then synchronises its stream and returns FLCE_ERR_BOUNDS. It is meant for
+ *   tests, in place of a memory checker; the release build does no checks
+ *   and never synchronises.
  */
 #ifndef FLCE_H_
 #define FLCE_H_
@@ -124,7 +130,9 @@ enum {
   FLCE_ERR_WORKSPACE = 4,    /* NULL workspace or ws_bytes below the required size */
   FLCE_ERR_CUDA = 5,         /* a CUDA runtime call failed                          */
   FLCE_ERR_TARGET_RANGE = 6, /* device: a target outside [0,V) and != ignore_index  */
-  FLCE_ERR_TIMEOUT = 7       /* device: a bounded wait in a kernel expired          */
+  FLCE_ERR_TIMEOUT = 7,      /* device: a bounded wait in a kernel expired          */
+  FLCE_ERR_BOUNDS = 8        /* device, debug build only: a kernel store would have
+                                fallen outside its buffer and was skipped           */
 };
 
 typedef struct {
@@ -174,6 +182,25 @@ typedef struct {
  * Returns FLCE_OK and sets *bytes, or an argument error.
  */
 int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
+
+/*
+ * The regions of a pass's workspace that its kernels may write, in address
+ * order: name, byte offset from the start of the workspace and byte count.
+ * Every byte of the workspace outside them is left as the caller gave it.
+ * This is the layout flce_workspace_bytes sizes; the same p and pass give the
+ * same regions. It is a diagnostic: tests fill the workspace with a pattern
+ * and check, after a call, that no byte outside a region changed (a stand-in
+ * for a memory checker). Writes up to `max` records to `out` and the number
+ * of regions to *count. Returns FLCE_OK or an argument error.
+ */
+typedef struct {
+  char name[24];
+  uint64_t offset;
+  uint64_t bytes;
+} flce_region;
+
+int flce_workspace_regions(const flce_params* p, int pass, flce_region* out, int max,
+                           int* count);
 
 /*
  * Forward: loss, per-row log-sum-exp and optional metrics.
@@ -411,8 +438,9 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
 
 /*
  * Synchronises `stream`, then returns the device-detected status of the last
- * pass that used `workspace`. The status is FLCE_OK, FLCE_ERR_TARGET_RANGE or
- * FLCE_ERR_TIMEOUT, or FLCE_ERR_CUDA if the synchronisation itself failed.
+ * pass that used `workspace`. The status is FLCE_OK, FLCE_ERR_TARGET_RANGE,
+ * FLCE_ERR_TIMEOUT or (debug build) FLCE_ERR_BOUNDS, or FLCE_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 int flce_check_status(const void* workspace, flce_stream_t stream);
 

@@ -12,6 +12,9 @@ from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libflce.so")
+# The same library built with FLCE_DEBUG: every kernel store is checked against
+# its buffer and every call synchronises (include/flce.h). For tests.
+DEBUG_LIB_PATH = os.path.join(_HERE, "lib", "libflce_debug.so")
 
 FLCE_F32, FLCE_BF16, FLCE_F16 = 0, 1, 2
 FLCE_SUM, FLCE_MEAN, FLCE_NONE = 0, 1, 2
@@ -28,6 +31,7 @@ REDUCTIONS = {"sum": FLCE_SUM, "mean": FLCE_MEAN, "none": FLCE_NONE}
 ERRORS = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_ALIGNMENT",
     4: "FLCE_ERR_WORKSPACE", 5: "FLCE_ERR_CUDA", 6: "FLCE_ERR_TARGET_RANGE", 7: "FLCE_ERR_TIMEOUT",
+    8: "FLCE_ERR_BOUNDS",
 }
 
 # Every exported symbol of include/flce.h.
@@ -36,7 +40,7 @@ EXPORTS = (
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
     "flce_forward_partial", "flce_forward_combine", "flce_chunk_logits", "flce_chunk_grads",
-    "flce_chunk_weighted_mse", "flce_test_fault",
+    "flce_chunk_weighted_mse", "flce_test_fault", "flce_workspace_regions",
 )
 
 
@@ -72,6 +76,10 @@ class FlceRowState(ctypes.Structure):
 ROW_STATE_BYTES = ctypes.sizeof(FlceRowState)
 
 
+class FlceRegion(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("offset", ctypes.c_uint64), ("bytes", ctypes.c_uint64)]
+
+
 class FlceKernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_uint64),
                 ("total_ms", ctypes.c_double), ("sm_mhz", ctypes.c_double),
@@ -88,6 +96,14 @@ class FlceError(RuntimeError):
 
 
 _lib: Optional[ctypes.CDLL] = None
+
+
+def use_debug_library() -> None:
+    """Load the FLCE_DEBUG build instead of the release library (before the first call)."""
+    global LIB_PATH
+    if _lib is not None and LIB_PATH != DEBUG_LIB_PATH:
+        raise RuntimeError("the release library is already loaded in this process")
+    LIB_PATH = DEBUG_LIB_PATH
 
 
 def load() -> ctypes.CDLL:
@@ -123,6 +139,9 @@ def load() -> ctypes.CDLL:
                                             ctypes.c_int64, vp, ctypes.c_int64, vp,
                                             ctypes.c_int32, vp, sz, vp]
     lib.flce_chunk_weighted_mse.restype = ctypes.c_int
+    lib.flce_workspace_regions.argtypes = [P, ctypes.c_int, ctypes.POINTER(FlceRegion), ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_int)]
+    lib.flce_workspace_regions.restype = ctypes.c_int
     lib.flce_test_fault.argtypes = [ctypes.c_int32, ctypes.c_int32]
     lib.flce_test_fault.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
@@ -184,6 +203,15 @@ def workspace_bytes(p: FlceParams, pass_: int) -> int:
     check(load().flce_workspace_bytes(ctypes.byref(p), pass_, ctypes.byref(n)),
           "flce_workspace_bytes")
     return n.value
+
+
+def workspace_regions(p: FlceParams, pass_: int) -> list[tuple[str, int, int]]:
+    """(name, byte offset, bytes) of every workspace region the pass's kernels may write."""
+    arr = (FlceRegion * 32)()
+    n = ctypes.c_int(0)
+    check(load().flce_workspace_regions(ctypes.byref(p), pass_, arr, 32, ctypes.byref(n)),
+          "flce_workspace_regions")
+    return [(arr[i].name.decode(), int(arr[i].offset), int(arr[i].bytes)) for i in range(n.value)]
 
 
 def forward_raw(p: FlceParams, hidden: int, weight: int, bias: int, targets: int, loss: int,

@@ -3,7 +3,9 @@
     python -m linear_cross_entropy_tiled_gb300.build
 
 Each .cu file under csrc/ compiles in parallel with nvcc. The objects are then
-linked into linear_cross_entropy_tiled_gb300/lib/libflce.so. Each .cu file under
+linked into linear_cross_entropy_tiled_gb300/lib/libflce.so, and compiled again with
+FLCE_DEBUG (every kernel store checked against its buffer) into
+lib/libflce_debug.so. Each .cu file under
 probes/ (stand-alone measurement programs, not part of the library) becomes an
 executable lib/flce_probe_<name>. nvcc cross-compiles, so this also works on a
 machine without a GPU.
@@ -23,6 +25,7 @@ PROBES = os.path.join(PKG, "probes")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libflce.so")
+DEBUG_LIB = os.path.join(LIBDIR, "libflce_debug.so")   # FLCE_DEBUG: checked stores
 BUILD = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -56,7 +59,7 @@ def _deps_mtime() -> float:
 
 
 def up_to_date() -> bool:
-    outs = [LIB] + [probe_path(p) for p in probe_sources()]
+    outs = [LIB, DEBUG_LIB] + [probe_path(p) for p in probe_sources()]
     return all(os.path.exists(o) and os.path.getmtime(o) >= _deps_mtime() for o in outs)
 
 
@@ -68,9 +71,10 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     cc = nvcc()
     extra = extra or []
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(job: tuple[str, bool]) -> str:
+        src, debug = job
+        obj = os.path.join(BUILD, os.path.basename(src) + (".debug.o" if debug else ".o"))
+        cmd = [cc, *ARCH, *FLAGS, *extra, *(["-DFLCE_DEBUG"] if debug else []), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -88,16 +92,18 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     srcs = sources()
     probes = probe_sources()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs) + len(probes)) as ex:
+    jobs = [(src, False) for src in srcs] + [(src, True) for src in srcs]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(jobs) + len(probes)) as ex:
         probe_jobs = [ex.submit(build_probe, p) for p in probes]
-        objs = list(ex.map(compile_one, srcs))
+        objs = list(ex.map(compile_one, jobs))
         for j in probe_jobs:
             j.result()
-    tmp = LIB + ".tmp"
-    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    for out, part in ((LIB, objs[:len(srcs)]), (DEBUG_LIB, objs[len(srcs):])):
+        tmp = out + ".tmp"
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *part], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
     return LIB
 
 

@@ -42,6 +42,28 @@ thread_local char g_detail[256] = "";
 thread_local int g_test_drop_kb = -1;
 thread_local unsigned long long g_test_wait_ns = 0;
 
+// Builds with FLCE_DEBUG check every kernel store against its buffer (see
+// DevRegion). There, each entry point ends by synchronising its stream and
+// returns FLCE_ERR_BOUNDS if a store fell outside; other builds return `v`
+// at once and stay asynchronous.
+int debug_finish(const void* ws, cudaStream_t st, int v) {
+#ifdef FLCE_DEBUG
+  if (v != FLCE_OK || ws == nullptr) return v;
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (word & kDevErrBounds) {
+    snprintf(g_detail, sizeof(g_detail), "debug build: a kernel store fell outside its buffer");
+    return FLCE_ERR_BOUNDS;
+  }
+#else
+  (void)ws;
+  (void)st;
+#endif
+  return v;
+}
+
 int cuda_fail(cudaError_t e, const char* what) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s", what, cudaGetErrorString(e));
   return FLCE_ERR_CUDA;
@@ -244,6 +266,7 @@ struct FwdLayout {
   int num_panels_max;
   int nblk;
   size_t partials, zt, blk_loss, blk_ent, blk_correct, blk_valid, total;
+  size_t partials_bytes, zt_bytes, blk_bytes;   // bytes the kernels may write in each region
 };
 
 FwdLayout fwd_layout(const flce_params* p) {
@@ -254,19 +277,22 @@ FwdLayout fwd_layout(const flce_params* p) {
   else
     L.num_panels_max = static_cast<int>(ceil_div(V, kSimtPanelCols));
   L.nblk = static_cast<int>(ceil_div(N, kMergeThreads));
+  L.partials_bytes = size_t(L.num_panels_max) * N * sizeof(float4);
+  L.zt_bytes = size_t(N) * 4;
+  L.blk_bytes = size_t(L.nblk) * 8;
   size_t o = kHeader;
   L.partials = o;
-  o = align_up(o + size_t(L.num_panels_max) * N * sizeof(float4), 256);
+  o = align_up(o + L.partials_bytes, 256);
   L.zt = o;
-  o = align_up(o + size_t(N) * 4, 256);
+  o = align_up(o + L.zt_bytes, 256);
   L.blk_loss = o;
-  o = align_up(o + size_t(L.nblk) * 8, 256);
+  o = align_up(o + L.blk_bytes, 256);
   L.blk_ent = o;
-  o = align_up(o + size_t(L.nblk) * 8, 256);
+  o = align_up(o + L.blk_bytes, 256);
   L.blk_correct = o;
-  o = align_up(o + size_t(L.nblk) * 8, 256);
+  o = align_up(o + L.blk_bytes, 256);
   L.blk_valid = o;
-  o = align_up(o + size_t(L.nblk) * 8, 256);
+  o = align_up(o + L.blk_bytes, 256);
   L.total = o;
   return L;
 }
@@ -278,6 +304,8 @@ struct BwdLayout {
   int64_t ds_t_ld;          // row stride of the transposed dlogits buffer (tensor path)
   int nchunks, rowblk, n_rowblocks;
   size_t coef, ds, ds_t, dw, dh_part, bias_part, total;
+  // bytes the kernels may write in each region (0: the region is absent)
+  size_t coef_bytes, ds_bytes, ds_t_bytes, dw_bytes, dh_bytes, bias_bytes;
 };
 
 // The backward stores dlogits for one chunk at a time and contracts it into
@@ -324,18 +352,23 @@ BwdLayout bwd_layout(const flce_params* p) {
     L.ds_t_ld = (N + 7) / 8 * 8;
     L.rowblk = kBM;
     L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
+    L.coef_bytes = size_t(N) * sizeof(float4);
+    L.ds_bytes = size_t(N) * L.ds_ld * elem;
+    L.ds_t_bytes = size_t(L.chunk) * L.ds_t_ld * elem;
+    L.dh_bytes = L.nchunks > 1 ? size_t(N) * H * 4 : 0;
+    L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
     size_t o = kHeader;
     L.coef = o;
-    o = align_up(o + size_t(N) * sizeof(float4), 256);
+    o = align_up(o + L.coef_bytes, 256);
     L.ds = o;
-    o = align_up(o + size_t(N) * L.ds_ld * elem, 1024);
+    o = align_up(o + L.ds_bytes, 1024);
     L.ds_t = o;
-    o = align_up(o + size_t(L.chunk) * L.ds_t_ld * elem, 1024);
+    o = align_up(o + L.ds_t_bytes, 1024);
     L.dw = o;
     L.dh_part = o;
-    if (L.nchunks > 1) o = align_up(o + size_t(N) * H * 4, 1024);
+    if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
     L.bias_part = o;
-    if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
+    if (L.bias_bytes) o = align_up(o + L.bias_bytes, 256);
     L.total = o;
     return L;
   }
@@ -363,26 +396,32 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.nchunks = N > 0 ? static_cast<int>(ceil_div(N, L.chunk)) : 0;
   L.rowblk = tensor_path(p) ? kBM : kSimtTile;
   L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
-  size_t o = kHeader;
-  L.coef = o;
-  o = align_up(o + size_t(N) * sizeof(float4), 256);
-  L.ds = o;
-  o = align_up(o + size_t(L.chunk) * L.V_pad * elem, 1024);
-  L.ds_t = o;
   L.ds_t_ld = (L.chunk + 7) / 8 * 8;
-  if (tensor_path(p)) o = align_up(o + size_t(V) * L.ds_t_ld * elem, 1024);
-  L.dw = o;
-  if (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
-    o = align_up(o + size_t(V) * H * 4, 1024);
-  L.dh_part = o;
+  L.coef_bytes = size_t(N) * sizeof(float4);
+  L.ds_bytes = size_t(L.chunk) * L.V_pad * elem;
+  L.ds_t_bytes = tensor_path(p) ? size_t(V) * L.ds_t_ld * elem : 0;
+  L.dw_bytes = (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
+                   ? size_t(V) * H * 4 : 0;
   if (tensor_path(p)) {
-    o = align_up(o + size_t(kMaxKSplits) * L.chunk * H * 4, 1024);
+    L.dh_bytes = size_t(kMaxKSplits) * L.chunk * H * 4;
   } else if (N > 0) {
     const int s = simt_k_splits(L.chunk, H, V);   // fp32 grad_hidden split partials
-    if (s > 1) o = align_up(o + size_t(s) * L.chunk * H * 4, 1024);
+    L.dh_bytes = s > 1 ? size_t(s) * L.chunk * H * 4 : 0;
   }
+  L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
+  size_t o = kHeader;
+  L.coef = o;
+  o = align_up(o + L.coef_bytes, 256);
+  L.ds = o;
+  o = align_up(o + L.ds_bytes, 1024);
+  L.ds_t = o;
+  if (L.ds_t_bytes) o = align_up(o + L.ds_t_bytes, 1024);
+  L.dw = o;
+  if (L.dw_bytes) o = align_up(o + L.dw_bytes, 1024);
+  L.dh_part = o;
+  if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
   L.bias_part = o;
-  if (p->has_bias) o = align_up(o + size_t(L.n_rowblocks) * L.V_pad * 4, 256);
+  if (L.bias_bytes) o = align_up(o + L.bias_bytes, 256);
   L.total = o;
   return L;
 }
@@ -554,23 +593,69 @@ CUtensorMapDataType map_type(const flce_params* p) {
 // grad_weight_accum = weight the chunks accumulate in grad_weight itself.
 struct ChunkLayout {
   size_t dw_part, dh_part, total;
+  size_t dw_bytes, dh_bytes;
 };
 
 ChunkLayout chunk_layout(const flce_params* p) {
   ChunkLayout L{};
-  size_t o = kHeader;
-  L.dw_part = o;
-  if (tensor_path(p) && p->grad_weight_accum == FLCE_ACCUM_FP32)
-    o = align_up(o + size_t(p->V) * p->H * 4, 1024);
-  L.dh_part = o;
+  L.dw_bytes = (tensor_path(p) && p->grad_weight_accum == FLCE_ACCUM_FP32)
+                   ? size_t(p->V) * p->H * 4 : 0;
   if (tensor_path(p)) {
-    o = align_up(o + size_t(kMaxKSplits) * p->N * p->H * 4, 1024);
+    L.dh_bytes = size_t(kMaxKSplits) * p->N * p->H * 4;
   } else {
     const int s = simt_k_splits(p->N, p->H, p->V);
-    if (s > 1) o = align_up(o + size_t(s) * p->N * p->H * 4, 1024);
+    L.dh_bytes = s > 1 ? size_t(s) * p->N * p->H * 4 : 0;
   }
+  size_t o = kHeader;
+  L.dw_part = o;
+  if (L.dw_bytes) o = align_up(o + L.dw_bytes, 1024);
+  L.dh_part = o;
+  if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
   L.total = o;
   return L;
+}
+
+size_t mse_loss_part_bytes(const flce_params* p) {
+  return size_t(ceil_div(p->V, kBN)) * ceil_div(p->N, 32) * 4;
+}
+
+// The regions of one pass's workspace that the kernels may write, in
+// address order: everything else in the workspace stays untouched.
+struct WsRegion {
+  const char* name;
+  size_t offset, bytes;
+};
+
+std::vector<WsRegion> workspace_regions(const flce_params* p, int pass) {
+  std::vector<WsRegion> r;
+  r.push_back({"header", 0, kHeader});
+  auto add = [&](const char* n, size_t off, size_t bytes) {
+    if (bytes > 0) r.push_back({n, off, bytes});
+  };
+  if (pass == FLCE_PASS_FORWARD) {
+    const FwdLayout L = fwd_layout(p);
+    add("partial_states", L.partials, L.partials_bytes);
+    add("target_logits", L.zt, L.zt_bytes);
+    add("block_loss", L.blk_loss, L.blk_bytes);
+    add("block_entropy", L.blk_ent, L.blk_bytes);
+    add("block_correct", L.blk_correct, L.blk_bytes);
+    add("block_valid", L.blk_valid, L.blk_bytes);
+  } else if (pass == FLCE_PASS_BACKWARD) {
+    const BwdLayout L = bwd_layout(p);
+    add("row_coefficients", L.coef, L.coef_bytes);
+    add("dlogits", L.ds, L.ds_bytes);
+    add("dlogits_transposed", L.ds_t, L.ds_t_bytes);
+    add("grad_weight_fp32", L.dw, L.dw_bytes);
+    add("grad_hidden_fp32", L.dh_part, L.dh_bytes);
+    add("grad_bias_partials", L.bias_part, L.bias_bytes);
+  } else if (pass == FLCE_PASS_CHUNK_GRADS) {
+    const ChunkLayout L = chunk_layout(p);
+    add("grad_weight_fp32", L.dw_part, L.dw_bytes);
+    add("grad_hidden_fp32", L.dh_part, L.dh_bytes);
+  } else if (pass == FLCE_PASS_CHUNK_MSE) {
+    add("loss_partials", kHeader, mse_loss_part_bytes(p));
+  }
+  return r;
 }
 
 }  // namespace
@@ -592,11 +677,29 @@ const char* flce_error_string(int code) {
     case FLCE_ERR_CUDA: return "CUDA runtime error";
     case FLCE_ERR_TARGET_RANGE: return "target outside [0, V) and not ignore_index";
     case FLCE_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case FLCE_ERR_BOUNDS: return "a kernel store fell outside its buffer (debug build)";
     default: return "unknown error code";
   }
 }
 
 const char* flce_last_error_detail(void) { return g_detail; }
+
+int flce_workspace_regions(const flce_params* p, int pass, flce_region* out, int max, int* count) {
+  const int v = validate(p);
+  if (v != FLCE_OK) return v;
+  if (pass < FLCE_PASS_FORWARD || pass > FLCE_PASS_CHUNK_MSE || count == nullptr ||
+      (max > 0 && out == nullptr))
+    return FLCE_ERR_INVALID_ARG;
+  const std::vector<WsRegion> r = workspace_regions(p, pass);
+  for (int i = 0; i < static_cast<int>(r.size()) && i < max; ++i) {
+    memset(&out[i], 0, sizeof(out[i]));
+    strncpy(out[i].name, r[i].name, sizeof(out[i].name) - 1);
+    out[i].offset = r[i].offset;
+    out[i].bytes = r[i].bytes;
+  }
+  *count = static_cast<int>(r.size());
+  return FLCE_OK;
+}
 
 int flce_test_fault(int32_t drop_kblock, int32_t wait_ms) {
   if (drop_kblock < -1 || wait_ms < 0) return FLCE_ERR_INVALID_ARG;
@@ -620,7 +723,7 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes) {
   } else if (pass == FLCE_PASS_CHUNK_GRADS) {
     *bytes = chunk_layout(p).total;
   } else if (pass == FLCE_PASS_CHUNK_MSE) {
-    *bytes = align_up(kHeader + size_t(ceil_div(p->V, kBN)) * ceil_div(p->N, 32) * 4, 256);
+    *bytes = align_up(kHeader + mse_loss_part_bytes(p), 256);
   } else {
     return FLCE_ERR_INVALID_ARG;
   }
@@ -666,6 +769,8 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   fa.ignore_index = p->ignore_index;
   fa.partials = reinterpret_cast<float4*>(ws + L.partials);
   fa.zt = reinterpret_cast<float*>(ws + L.zt);
+  fa.r_partials = DevRegion{ws + L.partials, L.partials_bytes};
+  fa.r_zt = DevRegion{ws + L.zt, L.zt_bytes};
   fa.status = reinterpret_cast<int*>(ws);
   // flce_test_fault arms these for the calling thread only; otherwise no
   // stage is starved and every wait has the default limit.
@@ -765,7 +870,9 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
     v = launch("flce_merge", st, [&] { return launch_merge(ma, L.nblk, st); });
     if (v != FLCE_OK) return v;
   }
-  return forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct, entropy_sum, st);
+  return debug_finish(ws, st,
+                      forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct,
+                                       entropy_sum, st));
 }
 
 int flce_forward_partial(const flce_params* p, const void* hidden, const void* weight,
@@ -796,7 +903,8 @@ int flce_forward_partial(const flce_params* p, const void* hidden, const void* w
   sa.zt = fa.zt;
   sa.targets = targets;
   sa.out = reinterpret_cast<ShardState*>(states);
-  return launch("flce_shard_state", st, [&] { return launch_shard_state(sa, st); });
+  return debug_finish(ws, st,
+                      launch("flce_shard_state", st, [&] { return launch_shard_state(sa, st); }));
 }
 
 int flce_forward_combine(const flce_params* p, const flce_row_state* states, int32_t num_shards,
@@ -840,7 +948,9 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
     v = launch("flce_combine", st, [&] { return launch_combine(ca, L.nblk, st); });
     if (v != FLCE_OK) return v;
   }
-  return forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct, entropy_sum, st);
+  return debug_finish(ws, st,
+                      forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct,
+                                       entropy_sum, st));
 }
 
 int flce_backward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
@@ -918,6 +1028,13 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   da.bias_ld = static_cast<int>(L.V_pad);
   da.tgt_base = 0;
   da.status = status;
+  da.r_ds = DevRegion{ws + L.ds, L.ds_bytes};
+  da.r_ds_t = DevRegion{ws + L.ds_t, L.ds_t_bytes};
+  da.r_bias = DevRegion{ws + L.bias_part, L.bias_bytes};
+  const DevRegion r_gh{grad_hidden, grad_hidden ? size_t(N) * H * elem : 0};
+  const DevRegion r_gw{grad_weight, grad_weight ? size_t(V) * H * elem : 0};
+  const DevRegion r_dh{ws + L.dh_part, L.dh_bytes};
+  const DevRegion r_dw{ws + L.dw, L.dw_bytes};
 
   if (tensor_path(p)) {
     const CUtensorMapDataType dt = map_type(p);
@@ -993,6 +1110,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.ld_part = H;
         ga.acc_scale = acc_scale;
         ga.status = status;
+        ga.r_out = r_gh;
+        ga.r_part = r_dh;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_hidden_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
@@ -1026,6 +1145,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.ld_part = H;
         ga.acc_scale = acc_scale;
         ga.status = status;
+        ga.r_out = r_gw;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
@@ -1079,6 +1199,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.split_stride = static_cast<long long>(L.chunk) * H;
         ga.acc_scale = acc_scale;
         ga.status = status;
+        ga.r_out = r_gh;
+        ga.r_part = r_dh;
         const int units = ga.num_tiles * ga.k_splits;
         const int g2 = units < d.pairs ? units : d.pairs;
         v = launch("flce_grad_hidden_tc", st,
@@ -1139,6 +1261,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.ld_part = H;
         ga.acc_scale = acc_scale;
         ga.status = status;
+        ga.r_out = r_gw;
+        ga.r_part = r_dw;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
@@ -1175,6 +1299,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         // the full chunk so that the workspace holds every chunk's partials
         ga.k_splits = simt_k_splits(L.chunk, H, V);
         ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.status = status;
+        ga.r_c = r_gh;
+        ga.r_part = r_dh;
         v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
@@ -1192,6 +1319,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.C = static_cast<float*>(grad_weight);
         ga.ldc = H;
         ga.accumulate = (c > 0 || p->accumulate) ? 1 : 0;
+        ga.status = status;
+        ga.r_c = r_gw;
         v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
@@ -1208,7 +1337,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     v = launch("flce_bias_reduce", st, [&] { return launch_bias_reduce(ba, p->dtype, st); });
     if (v != FLCE_OK) return v;
   }
-  return FLCE_OK;
+  return debug_finish(ws, st, FLCE_OK);
 }
 
 // ---------------------------------------------------------------------------
@@ -1257,10 +1386,12 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
     ga.part = nullptr;
     ga.ld_part = 0;
     ga.status = reinterpret_cast<int*>(ws);
+    ga.r_out = DevRegion{logits, size_t(N) * ld_logits * 2};
     const bool f16 = p->dtype == FLCE_F16;
     const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
-    return launch("flce_chunk_logits_tc", st,
-                  [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
+    return debug_finish(ws, st, launch("flce_chunk_logits_tc", st, [&] {
+                          return launch_gemm(op_a, op_b, ga, f16, g2, st);
+                        }));
   }
   SimtGemmArgs ga{};
   ga.M = N;
@@ -1275,7 +1406,10 @@ int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weig
   ga.C = static_cast<float*>(logits);
   ga.ldc = ld_logits;
   ga.accumulate = 0;
-  return launch("flce_chunk_logits_simt", st, [&] { return launch_gemm_simt(ga, st); });
+  ga.status = reinterpret_cast<int*>(ws);
+  ga.r_c = DevRegion{logits, size_t(N) * ld_logits * 4};
+  return debug_finish(ws, st,
+                      launch("flce_chunk_logits_simt", st, [&] { return launch_gemm_simt(ga, st); }));
 }
 
 int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void* weight,
@@ -1298,7 +1432,7 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   if (dlogits_t != nullptr && !aligned16(dlogits_t)) return FLCE_ERR_ALIGNMENT;
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const int n_tiles = static_cast<int>(ceil_div(V, kBN));
-  const size_t need = align_up(kHeader + size_t(n_tiles) * ceil_div(N, 32) * 4, 256);
+  const size_t need = align_up(kHeader + mse_loss_part_bytes(p), 256);
   if (workspace == nullptr || ws_bytes < need) return FLCE_ERR_WORKSPACE;
   if (!aligned16(hidden) || !aligned16(weight) || !aligned16(target) ||
       (reinterpret_cast<uintptr_t>(row_weight) & 3u) != 0 || !aligned16(feature_weight) ||
@@ -1339,6 +1473,9 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   ga.loss_part = reinterpret_cast<float*>(ws + kHeader);
   ga.out_t = dlogits_t;
   ga.ld_out_t = ld_dlogits_t;
+  ga.r_out = DevRegion{dlogits, size_t(N) * ld_dlogits * 2};
+  ga.r_out_t = DevRegion{dlogits_t, dlogits_t ? size_t(V) * ld_dlogits_t * 2 : 0};
+  ga.r_loss = DevRegion{ws + kHeader, mse_loss_part_bytes(p)};
   const bool f16 = p->dtype == FLCE_F16;
   const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
   v = launch("flce_chunk_mse_tc", st, [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
@@ -1348,7 +1485,8 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
   la.count = static_cast<long long>(n_tiles) * ceil_div(N, 32);
   la.loss = loss;
   la.accumulate = accumulate_loss;
-  return launch("flce_loss_reduce", st, [&] { return launch_loss_reduce(la, st); });
+  return debug_finish(ws, st,
+                      launch("flce_loss_reduce", st, [&] { return launch_loss_reduce(la, st); }));
 }
 
 int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weight,
@@ -1400,6 +1538,9 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
       ga.accumulate = p->accumulate;
       ga.k_splits = simt_k_splits(N, H, V);
       ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+      ga.status = status;
+      ga.r_c = DevRegion{grad_hidden, size_t(N) * H * 4};
+      ga.r_part = DevRegion{ws + L.dh_part, L.dh_bytes};
       v = launch("flce_chunk_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
       if (v != FLCE_OK) return v;
     }
@@ -1417,10 +1558,12 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
       ga.C = static_cast<float*>(grad_weight);
       ga.ldc = H;
       ga.accumulate = (later || p->accumulate) ? 1 : 0;
+      ga.status = status;
+      ga.r_c = DevRegion{grad_weight, size_t(V) * H * 4};
       v = launch("flce_chunk_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
       if (v != FLCE_OK) return v;
     }
-    return FLCE_OK;
+    return debug_finish(ws, st, FLCE_OK);
   }
   const CUtensorMapDataType dt = map_type(p);
   const bool f16 = p->dtype == FLCE_F16;
@@ -1450,6 +1593,8 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     ga.ld_part = H;
     ga.split_stride = static_cast<long long>(N) * H;
     ga.status = status;
+    ga.r_out = DevRegion{grad_hidden, size_t(N) * H * 2};
+    ga.r_part = DevRegion{ws + L.dh_part, L.dh_bytes};
     const int units = ga.num_tiles * ga.k_splits;
     const int g2 = units < d.pairs ? units : d.pairs;
     v = launch("flce_chunk_grad_hidden_tc", st,
@@ -1512,12 +1657,14 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     ga.part = reinterpret_cast<float*>(ws + L.dw_part);
     ga.ld_part = H;
     ga.status = status;
+    ga.r_out = DevRegion{grad_weight, size_t(V) * H * 2};
+    ga.r_part = DevRegion{ws + L.dw_part, L.dw_bytes};
     const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
     v = launch("flce_chunk_grad_weight_tc", st,
                [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
     if (v != FLCE_OK) return v;
   }
-  return FLCE_OK;
+  return debug_finish(ws, st, FLCE_OK);
 }
 
 int flce_check_status(const void* workspace, flce_stream_t stream) {
@@ -1527,6 +1674,7 @@ int flce_check_status(const void* workspace, flce_stream_t stream) {
   cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (word & kDevErrBounds) return FLCE_ERR_BOUNDS;
   if (word & kDevErrTimeout) return FLCE_ERR_TIMEOUT;
   if (word & kDevErrTargetRange) return FLCE_ERR_TARGET_RANGE;
   return FLCE_OK;

@@ -9,8 +9,18 @@
 namespace flce {
 
 // Device status bits written to the workspace status word. The host maps
-// them to FLCE_ERR_* codes.
-enum : int { kDevErrTargetRange = 1, kDevErrTimeout = 2 };
+// them to FLCE_ERR_* codes. kDevErrBounds is set only by builds with
+// FLCE_DEBUG (see DevRegion).
+enum : int { kDevErrTargetRange = 1, kDevErrTimeout = 2, kDevErrBounds = 4 };
+
+// A buffer a kernel may write: [base, base + bytes). Builds with FLCE_DEBUG
+// check every store of the kernels against the region of its buffer; a store
+// that would land outside sets kDevErrBounds in the status word and is
+// skipped. Other builds ignore the regions.
+struct DevRegion {
+  const void* base;
+  unsigned long long bytes;
+};
 
 // ---- tcgen05 tile shape shared by every bf16 kernel -----------------------
 // CTAs run in pairs (clusters of 2) with the 2-SM MMA (cta_group::2).
@@ -86,6 +96,7 @@ struct FwdArgs {
   float4* partials;            // [num_panels][N]
   float* zt;                   // [N] transformed target logit
   int* status;
+  DevRegion r_partials, r_zt;
 };
 
 // A forward whose bounded wait expired skipped some partial-state stores, so
@@ -190,6 +201,7 @@ struct DsArgs {
   int bias_blk0;               // first row block of this chunk
   int tgt_base;                // shard-local column of this chunk's first column
   int* status;
+  DevRegion r_ds, r_ds_t, r_bias;
 };
 
 enum GemmMode : int {
@@ -236,6 +248,7 @@ struct GemmArgs {
   float* loss_part;            // [n_tiles][ceil(M / 32)]
   void* out_t;                 // nullable: out transposed as well, [N][ld_out_t]
   long long ld_out_t;
+  DevRegion r_out, r_part, r_out_t, r_loss;
 };
 
 // loss = (accumulate ? loss : 0) + sum of part[0 .. count), in a fixed order.
@@ -272,6 +285,8 @@ struct SimtGemmArgs {
   // tiles and a long K.
   int k_splits;
   float* part;
+  int* status;                 // nullable; receives kDevErrBounds (FLCE_DEBUG builds)
+  DevRegion r_c, r_part;
 };
 
 struct BiasReduceArgs {

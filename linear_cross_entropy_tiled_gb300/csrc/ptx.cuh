@@ -79,6 +79,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Whether a store of `n` bytes at `p` may go ahead: always, except in builds
+// with FLCE_DEBUG, where it must lie inside region `r`; otherwise the status
+// word gets kDevErrBounds and the store is skipped.
+__device__ __forceinline__ bool store_allowed(const void* p, unsigned n, const DevRegion& r,
+                                              int* status) {
+#ifdef FLCE_DEBUG
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(r.base);
+  if (r.base == nullptr || a < b || a + n > b + r.bytes) {
+    if (status != nullptr) atomicOr(status, kDevErrBounds);
+    return false;
+  }
+#else
+  (void)p;
+  (void)n;
+  (void)r;
+  (void)status;
+#endif
+  return true;
+}
+
 // Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

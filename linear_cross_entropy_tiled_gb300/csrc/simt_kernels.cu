@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kSimtThreads)
       const int nc = min(T, a.V - c0);
       for (int j = 0; j < nc; ++j) {
         const float z = Z[tid][j];
-        if (c0 + j == tgt) a.zt[row] = z;
+        if (c0 + j == tgt && store_allowed(&a.zt[row], 4, a.r_zt, a.status)) a.zt[row] = z;
         if (z > m) {
           const float f = expf(m - z);
           ssum = ssum * f + 1.f;
@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kSimtThreads)
           const float zc = z * a.inv_softcap;
           g *= (1.f - zc * zc);
         }
-        ds[static_cast<size_t>(rl) * a.V_pad + col] = g;
+        float* const dst = ds + static_cast<size_t>(rl) * a.V_pad + col;
+        if (store_allowed(dst, 4, a.r_ds, a.status)) *dst = g;
       }
       G[ty * 4 + i][tx * 4 + j] = g;
     }
@@ -162,7 +163,8 @@ __global__ void __launch_bounds__(kSimtThreads)
     if (tid < T && c0 + tid < a.V) {
       float sum = 0.f;
       for (int i = 0; i < T; ++i) sum += G[i][tid];
-      a.bias_part[static_cast<size_t>(a.bias_blk0 + rb) * a.bias_ld + c0 + tid] = sum;
+      float* const dst = a.bias_part + static_cast<size_t>(a.bias_blk0 + rb) * a.bias_ld + c0 + tid;
+      if (store_allowed(dst, 4, a.r_bias, a.status)) *dst = sum;
     }
   }
 }
@@ -214,10 +216,11 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
       const int n = n0 + tx * 4 + j;
       if (n >= a.N) continue;
       if (a.k_splits > 1) {
-        a.part[(static_cast<size_t>(blockIdx.z) * a.M + m) * a.N + n] = acc[i][j];
+        float* const dst = a.part + (static_cast<size_t>(blockIdx.z) * a.M + m) * a.N + n;
+        if (store_allowed(dst, 4, a.r_part, a.status)) *dst = acc[i][j];
       } else {
         float* c = a.C + m * a.ldc + n;
-        *c = a.accumulate ? *c + acc[i][j] : acc[i][j];
+        if (store_allowed(c, 4, a.r_c, a.status)) *c = a.accumulate ? *c + acc[i][j] : acc[i][j];
       }
     }
   }
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(256) simt_split_reduce_kernel(const SimtGemmAr
     for (int z = 0; z < a.k_splits; ++z) s += a.part[z * total + i];
     const int m = static_cast<int>(i / a.N), n = static_cast<int>(i - static_cast<long long>(m) * a.N);
     float* c = a.C + m * a.ldc + n;
-    *c = a.accumulate ? *c + s : s;
+    if (store_allowed(c, 4, a.r_c, a.status)) *c = a.accumulate ? *c + s : s;
   }
 }
 

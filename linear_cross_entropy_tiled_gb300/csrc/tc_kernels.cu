@@ -375,7 +375,8 @@ __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs
   // The target logit lives in exactly one chunk of the whole vocabulary sweep.
   const long long rel = tgt - col0;
   if (row_ok && rel >= 0 && rel < 32) {
-    a.zt[row] = select32(z, static_cast<int>(rel));
+    const float zt = select32(z, static_cast<int>(rel));
+    if (store_allowed(&a.zt[row], 4, a.r_zt, a.status)) a.zt[row] = zt;
   }
   // Chunk max and first index that attains it, as a pairwise tree. The left
   // operand wins ties, so the lowest index is kept.
@@ -501,9 +502,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (row_ok && !dead)
-        a.partials[static_cast<size_t>(panel) * a.N + row] =
-            make_float4(m, ssum, tsum, __int_as_float(amax));
+      float4* const dst = a.partials + static_cast<size_t>(panel) * a.N + row;
+      if (row_ok && !dead && store_allowed(dst, 16, a.r_partials, a.status))
+        *dst = make_float4(m, ssum, tsum, __int_as_float(amax));
     }
   }
   tc_teardown(tmem, warp);
@@ -561,10 +562,10 @@ __device__ __forceinline__ void pack32(const float (&g)[32], float mul, uint32_t
 // multiple of 8 columns receives the packed zeros).
 template <typename T>
 __device__ __forceinline__ void store_row_packed(const uint32_t (&w)[16], T* dst, int col0,
-                                                 int cols) {
+                                                 int cols, const DevRegion& r, int* status) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    if (col0 + q * 8 < cols)
+    if (col0 + q * 8 < cols && store_allowed(dst + q * 8, 16, r, status))
       *reinterpret_cast<uint4*>(dst + q * 8) =
           make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
@@ -580,7 +581,8 @@ __device__ __forceinline__ void store_row_packed(const uint32_t (&w)[16], T* dst
 template <typename T>
 __device__ __forceinline__ void store_transposed_packed(const uint32_t (&w)[16], T* dst_t,
                                                         long long ld_t, int col0, int row_w,
-                                                        int lane, int rows, int cols, bool live) {
+                                                        int lane, int rows, int cols, bool live,
+                                                        const DevRegion& r, int* status) {
   const bool odd = (lane & 1) != 0;
   const int row_pair = row_w + (lane & ~1);  // the first of this lane's two rows
   // even lane: (own low half, partner's low half); odd: (partner's high, own high)
@@ -595,7 +597,8 @@ __device__ __forceinline__ void store_transposed_packed(const uint32_t (&w)[16],
   for (int i = 0; i < 16; ++i) {
     const uint32_t recv = __shfl_xor_sync(kFull, w[i], 1);
     const uint32_t out = __byte_perm(w[i], recv, sel);
-    if (inside || (row_in && c_first + 2 * i < cols))
+    if ((inside || (row_in && c_first + 2 * i < cols)) &&
+        store_allowed(base + i * step, 4, r, status))
       *reinterpret_cast<uint32_t*>(base + i * step) = out;
   }
 }
@@ -697,11 +700,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
           pack32<T>(gv, Elem<T>::kBf16 ? 1.f : ds_mul, w);
           if (!dead && row_ok && col0 < a.V) {
             T* const row = static_cast<T*>(a.ds) + static_cast<size_t>(row_local) * a.V_pad;
-            store_row_packed<T>(w, row + col0, col0, a.V);
+            store_row_packed<T>(w, row + col0, col0, a.V, a.r_ds, a.status);
           }
           if (a.ds_t != nullptr)
             store_transposed_packed<T>(w, static_cast<T*>(a.ds_t), a.ld_t, col0, row_local - lane,
-                                       lane, a.rows, a.V, !dead);
+                                       lane, a.rows, a.V, !dead, a.r_ds_t, a.status);
           if (a.bias_part != nullptr) {
             const float cs = warp_transpose_sum32(gv, lane);
             colsum[q * kBN + c * 32 + lane] = cs;
@@ -717,7 +720,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
           if (col < a.V && blk_ok) {
             const float t = ((colsum[j] + colsum[kBN + j]) + colsum[2 * kBN + j]) +
                             colsum[3 * kBN + j];
-            a.bias_part[static_cast<size_t>(a.bias_blk0 + blk_local) * a.bias_ld + col] = t;
+            float* const dst = a.bias_part + static_cast<size_t>(a.bias_blk0 + blk_local) * a.bias_ld + col;
+            if (store_allowed(dst, 4, a.r_bias, a.status)) *dst = t;
           }
         }
         tile_par ^= 1;
@@ -903,8 +907,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             pack32<T>(d, 1.f, w);
             if (a.out_t != nullptr)
               store_transposed_packed<T>(w, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane,
-                                         lane, M, N, true);
-            if (row_ok) store_row_packed<T>(w, out + static_cast<size_t>(m) * ld_out + col0, col0, N);
+                                         lane, M, N, true, a.r_out_t, a.status);
+            if (row_ok)
+              store_row_packed<T>(w, out + static_cast<size_t>(m) * ld_out + col0, col0, N, a.r_out,
+                                  a.status);
             continue;
           }
           if (add_part) {
@@ -941,7 +947,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (col0 + i * 4 < N)
-                dst[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+                if (store_allowed(dst + i, 16, a.r_part, a.status))
+                  dst[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
           } else {
             T* dst = out + static_cast<size_t>(m) * ld_out + col0;
 #pragma unroll
@@ -952,7 +959,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                 w.y = Elem<T>::pack(d[8 * i + 2], d[8 * i + 3]);
                 w.z = Elem<T>::pack(d[8 * i + 4], d[8 * i + 5]);
                 w.w = Elem<T>::pack(d[8 * i + 6], d[8 * i + 7]);
-                *reinterpret_cast<uint4*>(dst + i * 8) = w;
+                if (store_allowed(dst + i * 8, 16, a.r_out, a.status))
+                  *reinterpret_cast<uint4*>(dst + i * 8) = w;
               }
             }
           }
@@ -964,8 +972,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
           const int m_base = m - lane;
-          if (lane == 0 && m_base < M)
-            a.loss_part[static_cast<size_t>(nt) * ((M + 31) / 32) + (m_base >> 5)] = t;
+          if (lane == 0 && m_base < M) {
+            float* const dst = a.loss_part + static_cast<size_t>(nt) * ((M + 31) / 32) + (m_base >> 5);
+            if (store_allowed(dst, 4, a.r_loss, a.status)) *dst = t;
+          }
         }
         epi_release(s, acc, lane);
       }

@@ -18,7 +18,9 @@
 // instead of a rate.
 //
 // Output: one JSON object per line.
-//   flce_probe_l2_load
+//   flce_probe_l2_load                                 every configuration once
+//   flce_probe_l2_load WINDOW_MB SHARE TENSOR SECONDS  one configuration, repeated
+//                                                      for SECONDS (to read power)
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(32) bulk_load_kernel(const char* src,
 
 }  // namespace
 
-int main() {
+int main(int argc, char** argv) {
+  const bool one = argc == 5;
   int dev = 0, sms = 0;
   CHECK(cudaGetDevice(&dev));
   CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -165,10 +168,23 @@ int main() {
       return 1;
     }
   }
-  const long long windows_mb[] = {64, 2048};
+  std::vector<long long> windows_mb = {64, 2048};
+  std::vector<int> tensors = {0, 1}, shares = {1, 4, 16, 152};
+  double seconds = 0.0;
+  if (one) {
+    windows_mb = {atoll(argv[1])};
+    shares = {atoi(argv[2])};
+    tensors = {atoi(argv[3])};
+    seconds = atof(argv[4]);
+    if (windows_mb[0] < 1 || (windows_mb[0] << 20) > static_cast<long long>(max_window) ||
+        shares[0] < 1) {
+      fprintf(stderr, "window must be 1..2048 MB and share >= 1\n");
+      return 1;
+    }
+  }
   for (long long wmb : windows_mb)
-  for (int tensor : {0, 1})
-  for (int share : {1, 4, 16, 152}) {
+  for (int tensor : tensors)
+  for (int share : shares) {
     {
       const int stages = 8;
       const long long nchunks = (wmb << 20) / kChunk;
@@ -181,6 +197,22 @@ int main() {
       };
       launch();
       CHECK(cudaDeviceSynchronize());
+      if (seconds > 0) {   // repeat for the requested time, then time one more run
+        cudaEvent_t a, b;
+        CHECK(cudaEventCreate(&a));
+        CHECK(cudaEventCreate(&b));
+        CHECK(cudaEventRecord(a));
+        launch();
+        CHECK(cudaEventRecord(b));
+        CHECK(cudaEventSynchronize(b));
+        float one_ms = 1.f;
+        CHECK(cudaEventElapsedTime(&one_ms, a, b));
+        const int reps = static_cast<int>(seconds * 1e3 / std::max(one_ms, 0.01f));
+        for (int r = 0; r < reps; ++r) launch();
+        CHECK(cudaDeviceSynchronize());
+        CHECK(cudaEventDestroy(a));
+        CHECK(cudaEventDestroy(b));
+      }
       cudaEvent_t e0, e1;
       CHECK(cudaEventCreate(&e0));
       CHECK(cudaEventCreate(&e1));
