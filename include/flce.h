@@ -437,6 +437,18 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
                             flce_stream_t stream);
 
 /*
+ * dst[i] = src[i] * (*scale) for i < count, in dtype (flce_dtype): the
+ * chunked linear loss's backward, which returns the gradients computed in
+ * the forward scaled by the upstream scalar gradient ("Chunked Linear Loss",
+ * "Gradient handling"). scale is one device float, read by the kernel, so the
+ * call never synchronises. src == dst scales in place; then a scale of 1
+ * costs one launch and no memory traffic. src and dst must not overlap
+ * otherwise, and must be aligned to their element size.
+ */
+int flce_scale(const void* src, void* dst, int64_t count, int32_t dtype, const float* scale,
+               flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device-detected status of the last
  * pass that used `workspace`. The status is FLCE_OK, FLCE_ERR_TARGET_RANGE,
  * FLCE_ERR_TIMEOUT or (debug build) FLCE_ERR_BOUNDS, or FLCE_ERR_CUDA if the

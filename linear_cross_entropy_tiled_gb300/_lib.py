@@ -40,7 +40,7 @@ EXPORTS = (
     "flce_error_string", "flce_last_error_detail", "flce_launch_count",
     "flce_profiling_enable", "flce_profiling_read", "flce_forward_noalloc",
     "flce_forward_partial", "flce_forward_combine", "flce_chunk_logits", "flce_chunk_grads",
-    "flce_chunk_weighted_mse", "flce_test_fault", "flce_workspace_regions",
+    "flce_chunk_weighted_mse", "flce_test_fault", "flce_workspace_regions", "flce_scale",
 )
 
 
@@ -142,6 +142,8 @@ def load() -> ctypes.CDLL:
     lib.flce_workspace_regions.argtypes = [P, ctypes.c_int, ctypes.POINTER(FlceRegion), ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_int)]
     lib.flce_workspace_regions.restype = ctypes.c_int
+    lib.flce_scale.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
+    lib.flce_scale.restype = ctypes.c_int
     lib.flce_test_fault.argtypes = [ctypes.c_int32, ctypes.c_int32]
     lib.flce_test_fault.restype = ctypes.c_int
     lib.flce_check_status.argtypes = [vp, vp]
@@ -276,6 +278,10 @@ def chunk_weighted_mse_raw(p: FlceParams, hidden: int, weight: int, target: int,
 def test_fault(drop_kblock: int, wait_ms: int) -> None:
     """flce_test_fault: starve one stage of this thread's forward launches (-1, 0: off)."""
     check(load().flce_test_fault(drop_kblock, wait_ms), "flce_test_fault")
+
+
+def scale_raw(src: int, dst: int, count: int, dtype: int, scale: int, stream: int) -> int:
+    return load().flce_scale(src, dst, count, dtype, scale, stream)
 
 
 def check_status(ws: int, stream: int) -> int:

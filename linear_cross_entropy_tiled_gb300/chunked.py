@@ -194,11 +194,24 @@ class _ChunkedLinearLoss(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, grad_out):
+        # The gradients computed in the forward, times the upstream scalar
+        # ("Gradient handling"), by the library's scale kernel. It writes new
+        # tensors, so a second backward (retain_graph) still starts from the
+        # unscaled ones.
         gx, gw = ctx.saved_tensors
+        g = grad_out.to(dtype=torch.float32).reshape(1).contiguous()
+        out = []
+        for t in (gx, gw):
+            if t is None:
+                out.append(None)
+                continue
+            o = torch.empty_like(t)
+            _lib.check(_lib.scale_raw(_ptr(t), _ptr(o), t.numel(), _DTYPES[t.dtype], _ptr(g),
+                                      _stream(t.device)), "flce_scale")
+            out.append(o)
+        gx, gw = out
         if gx is not None:
-            gx = (gx * grad_out.to(gx.dtype)).reshape(ctx.shape)
-        if gw is not None:
-            gw = gw * grad_out.to(gw.dtype)
+            gx = gx.reshape(ctx.shape)
         return gx, gw, None, None
 
 

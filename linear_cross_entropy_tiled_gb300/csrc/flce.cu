@@ -20,9 +20,33 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#ifndef FLCE_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 using namespace flce;
 
 namespace {
+
+// An NVTX range over one entry point, so that profilers (ncu --nvtx, nsys)
+// can select a pass by name. Without an attached tool the calls cost a few
+// nanoseconds. Builds with FLCE_NO_NVTX leave them out.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) {
+#ifndef FLCE_NO_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~NvtxRange() {
+#ifndef FLCE_NO_NVTX
+    nvtxRangePop();
+#endif
+  }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ------------------------------------------------------------ device state
 struct DeviceInfo {
@@ -827,6 +851,7 @@ static int forward_finalize(const flce_params* p, uint8_t* ws, const FwdLayout& 
 int flce_forward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
                  const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
                  float* entropy_sum, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_forward");
   FwdLayout L;
   DeviceInfo d;
   int v = forward_prologue(p, hidden, weight, bias, targets, lse, workspace, ws_bytes, &L, &d);
@@ -878,6 +903,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
 int flce_forward_partial(const flce_params* p, const void* hidden, const void* weight,
                          const void* bias, const int64_t* targets, flce_row_state* states,
                          void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_forward_partial");
   static_assert(sizeof(flce_row_state) == sizeof(ShardState), "row state layout");
   FwdLayout L;
   DeviceInfo d;
@@ -911,6 +937,7 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
                          const int64_t* targets, float* loss, float* lse, int64_t* num_correct,
                          float* entropy_sum, void* workspace, size_t ws_bytes,
                          flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_forward_combine");
   int v = validate(p);
   if (v != FLCE_OK) return v;
   const bool rows = p->N > 0;
@@ -957,6 +984,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
                   const int64_t* targets, const float* lse, const float* grad_loss,
                   void* grad_hidden, void* grad_weight, void* grad_bias, void* workspace,
                   size_t ws_bytes, flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_backward");
   int v = validate(p);
   if (v != FLCE_OK) return v;
   const bool rows = p->N > 0;
@@ -1345,6 +1373,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
 // folding of its dlogits into the gradients ("Chunked Linear Loss").
 int flce_chunk_logits(const flce_params* p, const void* hidden, const void* weight, void* logits,
                       int64_t ld_logits, void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_chunk_logits");
   int v = validate(p);
   if (v != FLCE_OK) return v;
   if (weight == nullptr || (p->N > 0 && (hidden == nullptr || logits == nullptr)))
@@ -1418,6 +1447,7 @@ int flce_chunk_weighted_mse(const flce_params* p, const void* hidden, const void
                             void* dlogits_t, int64_t ld_dlogits_t, double* loss,
                             int32_t accumulate_loss, void* workspace, size_t ws_bytes,
                             flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_chunk_weighted_mse");
   int v = validate(p);
   if (v != FLCE_OK) return v;
   if (!tensor_path(p)) return FLCE_ERR_UNSUPPORTED;
@@ -1493,6 +1523,7 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
                      const void* dlogits, int64_t ld_dlogits, const void* dlogits_t,
                      int64_t ld_dlogits_t, int32_t phase, void* grad_hidden, void* grad_weight,
                      void* workspace, size_t ws_bytes, flce_stream_t stream) {
+  const NvtxRange nvtx_range("flce_chunk_grads");
   int v = validate(p);
   if (v != FLCE_OK) return v;
   if (p->N < 1 || phase < FLCE_CHUNK_ONLY || phase > FLCE_CHUNK_LAST) return FLCE_ERR_INVALID_ARG;
@@ -1665,6 +1696,24 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
     if (v != FLCE_OK) return v;
   }
   return debug_finish(ws, st, FLCE_OK);
+}
+
+int flce_scale(const void* src, void* dst, int64_t count, int32_t dtype, const float* scale,
+               flce_stream_t stream) {
+  if (count < 0 || (dtype != FLCE_F32 && dtype != FLCE_BF16 && dtype != FLCE_F16) ||
+      scale == nullptr || (count > 0 && (src == nullptr || dst == nullptr)))
+    return FLCE_ERR_INVALID_ARG;
+  const size_t elem = dtype == FLCE_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) % elem != 0 ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+    return FLCE_ERR_ALIGNMENT;
+  if (count == 0) return FLCE_OK;
+  DeviceInfo d;
+  int v = device_info(&d);
+  if (v != FLCE_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ScaleArgs a{src, dst, static_cast<long long>(count), dtype, scale};
+  return launch("flce_scale", st, [&] { return launch_scale(a, d.sms, st); });
 }
 
 int flce_check_status(const void* workspace, flce_stream_t stream) {

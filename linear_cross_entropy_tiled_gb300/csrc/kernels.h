@@ -251,6 +251,17 @@ struct GemmArgs {
   DevRegion r_out, r_part, r_out_t, r_loss;
 };
 
+// dst[i] = src[i] * (*scale), i < count, in the element type (dtype 0 fp32,
+// 1 bf16, 2 fp16). src == dst is allowed. With *scale == 1 and src == dst
+// every thread returns at once.
+struct ScaleArgs {
+  const void* src;
+  void* dst;
+  long long count;
+  int dtype;
+  const float* scale;
+};
+
 // loss = (accumulate ? loss : 0) + sum of part[0 .. count), in a fixed order.
 struct LossReduceArgs {
   const float* part;
@@ -334,6 +345,7 @@ cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s);
 cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s);
+cudaError_t launch_scale(const ScaleArgs& a, int sms, cudaStream_t s);
 
 constexpr int kMergeThreads = 256;
 

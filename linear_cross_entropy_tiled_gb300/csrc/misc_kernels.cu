@@ -393,6 +393,44 @@ __global__ void __launch_bounds__(1024) loss_reduce_kernel(const LossReduceArgs 
   if (threadIdx.x == 0) a.loss[0] = (a.accumulate ? a.loss[0] : 0.0) + s;
 }
 
+// 16 bytes per thread and step when both pointers are 16-byte aligned; the
+// rest (or everything, if they are not) element by element.
+template <typename T>
+__global__ void __launch_bounds__(256) scale_kernel(const ScaleArgs a) {
+  const float s = *a.scale;
+  if (s == 1.f && a.src == a.dst) return;
+  constexpr int kPer = 16 / static_cast<int>(sizeof(T));
+  const T* src = static_cast<const T*>(a.src);
+  T* dst = static_cast<T*>(a.dst);
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0;
+  const long long nv = vec ? a.count / kPer : 0;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  for (long long i = t0; i < nv; i += stride) {
+    union {
+      uint4 v;
+      T e[kPer];
+    } u;
+    u.v = reinterpret_cast<const uint4*>(src)[i];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) u.e[k] = from_f32<T>(to_f32(u.e[k]) * s);
+    reinterpret_cast<uint4*>(dst)[i] = u.v;
+  }
+  for (long long i = nv * kPer + t0; i < a.count; i += stride) dst[i] = from_f32<T>(to_f32(src[i]) * s);
+}
+
+cudaError_t launch_scale(const ScaleArgs& a, int sms, cudaStream_t s) {
+  const long long blocks = (a.count / 4 + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(blocks < 1 ? 1 : (blocks < 8ll * sms ? blocks : 8ll * sms));
+  if (a.dtype == 1)
+    scale_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+  else if (a.dtype == 2)
+    scale_kernel<__half><<<grid, 256, 0, s>>>(a);
+  else
+    scale_kernel<float><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s) {
   loss_reduce_kernel<<<1, 1024, 0, s>>>(a);
   return cudaGetLastError();

@@ -26,7 +26,7 @@ from flce_check import (assert_entropy_close, assert_grad_close, assert_loss_clo
 
 pytestmark = pytest.mark.gpu
 
-DT = {"bf16": _lib.FLCE_BF16, "f32": _lib.FLCE_F32}
+DT = {"bf16": _lib.FLCE_BF16, "f16": _lib.FLCE_F16, "f32": _lib.FLCE_F32}
 
 
 def exact(x, dtype):
@@ -159,3 +159,26 @@ def test_autograd_options_fuse_grad_accum_and_weight_accum():
                       "weight.grad after fused accumulation")
     assert_grad_close(h.grad.float().cpu().numpy(), rh, "bf16", "grad_hidden")
     assert_grad_close(b.grad.float().cpu().numpy(), rb, "bf16", "grad_bias")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_scale_kernel_is_exact(dtype):
+    """flce_scale: dst = src * s rounded once to the element type, any count and alignment."""
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+    st = torch.cuda.current_stream().cuda_stream
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for count, off in ((1, 0), (8, 0), (1003, 0), (4099, 1), (100000, 3)):
+        src_full = torch.randn(count + off, device="cuda", generator=g).to(tdt)
+        src = src_full[off:]
+        dst = torch.full_like(src, 7.0)
+        s = torch.tensor([0.3], device="cuda")
+        _lib.check(_lib.scale_raw(src.data_ptr(), dst.data_ptr(), count, DT[dtype], s.data_ptr(), st),
+                   "flce_scale")
+        want = (src.float() * 0.3).to(tdt)        # the product in fp32, rounded once
+        assert torch.equal(dst, want), (dtype, count, off)
+        before = src.clone()
+        one = torch.ones(1, device="cuda")
+        _lib.check(_lib.scale_raw(src.data_ptr(), src.data_ptr(), count, DT[dtype], one.data_ptr(), st),
+                   "flce_scale in place")
+        assert torch.equal(src, before)
+    torch.cuda.synchronize()
