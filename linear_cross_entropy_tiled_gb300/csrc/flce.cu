@@ -274,16 +274,33 @@ constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_s
 
 // K splits of a SIMT (fp32) GEMM: enough 64 x 64 output tiles times splits to
 // fill the GPU (about 256 blocks), at least 512 of K per split, at most 16,
-// and at most K / (2 N), so that the split partials (s x M x N) hold no more
-// than half of the A operand (M x K, the dlogits chunk). A function of the
-// shape only, so the workspace query and the launch agree.
+// and at most K / N + 1, so that the split partials ((s - 1) x M x N; split 0
+// writes the output itself) hold no more than the A operand (M x K, the
+// dlogits chunk). A function of the shape only, so the workspace query and
+// the launch agree.
 int simt_k_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
   int64_t s = (256 + tiles - 1) / tiles;
   if (s > K / 512) s = K / 512;
-  if (s > K / (2 * N)) s = K / (2 * N);
+  if (s > K / N + 1) s = K / N + 1;
   if (s > 16) s = 16;
   return s < 1 ? 1 : static_cast<int>(s);
+}
+
+// Bytes of the fp32 K-split partials of a SIMT GEMM (split 0 needs none).
+size_t simt_part_bytes(int64_t M, int64_t N, int64_t K) {
+  return size_t(simt_k_splits(M, N, K) - 1) * M * N * 4;
+}
+
+// 64-column tiles per panel of the fp32 forward: the widest of 4, 2 and 1
+// tiles that still gives at least 152 blocks (one per SM of a GB300), so that
+// small problems spread over the GPU, while the merge's per-row loop over the
+// panels stays short. A function of the shape only.
+int simt_panel_tiles(int64_t N, int64_t V) {
+  const int64_t n_blocks = ceil_div(N, kSimtTile);
+  for (int pt = kSimtPanelCols / kSimtTile; pt > 1; pt /= 2)
+    if (n_blocks * ceil_div(V, int64_t(pt) * kSimtTile) >= 152) return pt;
+  return 1;
 }
 
 struct FwdLayout {
@@ -299,7 +316,7 @@ FwdLayout fwd_layout(const flce_params* p) {
   if (tensor_path(p))
     L.num_panels_max = static_cast<int>(ceil_div(ceil_div(V, kBN), kMinPanelTiles));
   else
-    L.num_panels_max = static_cast<int>(ceil_div(V, kSimtPanelCols));
+    L.num_panels_max = static_cast<int>(ceil_div(V, int64_t(simt_panel_tiles(N, V)) * kSimtTile));
   L.nblk = static_cast<int>(ceil_div(N, kMergeThreads));
   L.partials_bytes = size_t(L.num_panels_max) * N * sizeof(float4);
   L.zt_bytes = size_t(N) * 4;
@@ -344,7 +361,7 @@ struct BwdLayout {
 // rows. flce_params.bwd_chunk_axis fixes the axis, so that callers and tests
 // can reach both schedules at any size; the result is the same either way.
 bool vocab_chunked(const flce_params* p) {
-  if (!tensor_path(p) || p->N == 0) return false;
+  if (p->N == 0) return false;
   if (p->bwd_chunk_axis == FLCE_CHUNK_AXIS_ROWS) return false;
   if (p->bwd_chunk_axis == FLCE_CHUNK_AXIS_VOCAB) return true;
   return p->N < p->V;
@@ -357,29 +374,38 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.V_pad = (V + 7) / 8 * 8;
   L.vocab = vocab_chunked(p);
   if (L.vocab) {
-    // Four column chunks of whole 256-column tiles (two copies of a quarter
-    // of the columns), fewer columns per chunk if N rows of them would pass
-    // the 4 GiB cap; then the columns are spread evenly over the chunks.
+    // Four column chunks of whole tiles (256 columns on the tensor path, 64 on
+    // the fp32 path): two 16-bit copies, or one fp32 copy, of a quarter of the
+    // columns for all rows. Fewer columns per chunk if N rows of them would
+    // pass the 4 GiB cap; then the columns are spread evenly over the chunks.
     // flce_params.max_chunk (rounded down to whole tiles) lowers the cap.
-    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * 2)) / kBN * kBN;
-    if (cap < kBN) cap = kBN;
+    const int copies = tensor_path(p) ? 2 : 1;
+    const int64_t gran = tensor_path(p) ? kBN : kSimtTile;
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * copies)) / gran * gran;
+    if (cap < gran) cap = gran;
     if (p->max_chunk > 0) {
-      const int64_t c = p->max_chunk < kBN ? kBN : p->max_chunk / kBN * kBN;
+      const int64_t c = p->max_chunk < gran ? gran : p->max_chunk / gran * gran;
       if (c < cap) cap = c;
     }
-    int64_t w = ceil_div(ceil_div(V, 4), kBN) * kBN;
+    int64_t w = ceil_div(ceil_div(V, 4), gran) * gran;
     if (w > cap) w = cap;
     L.nchunks = static_cast<int>(ceil_div(V, w));
-    L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), kBN) * kBN;
+    L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), gran) * gran;
     L.nchunks = static_cast<int>(ceil_div(V, L.chunk));
     L.ds_ld = (L.chunk + 7) / 8 * 8;
     L.ds_t_ld = (N + 7) / 8 * 8;
-    L.rowblk = kBM;
+    L.rowblk = tensor_path(p) ? kBM : kSimtTile;
     L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
     L.coef_bytes = size_t(N) * sizeof(float4);
     L.ds_bytes = size_t(N) * L.ds_ld * elem;
-    L.ds_t_bytes = size_t(L.chunk) * L.ds_t_ld * elem;
-    L.dh_bytes = L.nchunks > 1 ? size_t(N) * H * 4 : 0;
+    L.ds_t_bytes = tensor_path(p) ? size_t(L.chunk) * L.ds_t_ld * elem : 0;
+    if (tensor_path(p)) {
+      L.dh_bytes = L.nchunks > 1 ? size_t(N) * H * 4 : 0;
+    } else {
+      // fp32: grad_hidden accumulates in its own fp32 output; only the K-split
+      // partials of one chunk's contraction need room
+      L.dh_bytes = simt_part_bytes(N, H, L.chunk);
+    }
     L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
     size_t o = kHeader;
     L.coef = o;
@@ -387,7 +413,7 @@ BwdLayout bwd_layout(const flce_params* p) {
     L.ds = o;
     o = align_up(o + L.ds_bytes, 1024);
     L.ds_t = o;
-    o = align_up(o + L.ds_t_bytes, 1024);
+    if (L.ds_t_bytes) o = align_up(o + L.ds_t_bytes, 1024);
     L.dw = o;
     L.dh_part = o;
     if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
@@ -429,8 +455,7 @@ BwdLayout bwd_layout(const flce_params* p) {
   if (tensor_path(p)) {
     L.dh_bytes = size_t(kMaxKSplits) * L.chunk * H * 4;
   } else if (N > 0) {
-    const int s = simt_k_splits(L.chunk, H, V);   // fp32 grad_hidden split partials
-    L.dh_bytes = s > 1 ? size_t(s) * L.chunk * H * 4 : 0;
+    L.dh_bytes = simt_part_bytes(L.chunk, H, V);   // fp32 grad_hidden split partials
   }
   L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
   size_t o = kHeader;
@@ -627,8 +652,7 @@ ChunkLayout chunk_layout(const flce_params* p) {
   if (tensor_path(p)) {
     L.dh_bytes = size_t(kMaxKSplits) * p->N * p->H * 4;
   } else {
-    const int s = simt_k_splits(p->N, p->H, p->V);
-    L.dh_bytes = s > 1 ? size_t(s) * p->N * p->H * 4 : 0;
+    L.dh_bytes = simt_part_bytes(p->N, p->H, p->V);
   }
   size_t o = kHeader;
   L.dw_part = o;
@@ -820,7 +844,8 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
     });
   } else {
     fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
-    fa.num_panels = static_cast<int>(ceil_div(V, kSimtPanelCols));
+    fa.panel_tiles = simt_panel_tiles(N, V);
+    fa.num_panels = static_cast<int>(ceil_div(V, int64_t(fa.panel_tiles) * kSimtTile));
     fa.num_units = fa.num_panels * fa.n_blocks;
     v = launch("flce_fwd_simt", st, [&] {
       return launch_fwd_simt(static_cast<const float*>(hidden), static_cast<const float*>(weight),
@@ -1294,6 +1319,70 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
+        if (v != FLCE_OK) return v;
+      }
+    }
+  } else if (L.vocab) {
+    // fp32, vocabulary chunks (N < V): dlogits for columns [v0, v0 + vc) of
+    // all rows, one fp32 copy. Each chunk's grad_weight rows are complete after
+    // one contraction over all N rows; grad_hidden accumulates in its own fp32
+    // output across the chunks, in chunk order.
+    const float* hf = static_cast<const float*>(hidden);
+    const float* wf = static_cast<const float*>(weight);
+    for (int c = 0; c < L.nchunks; ++c) {
+      const int v0 = static_cast<int>(c * L.chunk);
+      const int vc = static_cast<int>(V - v0 < L.chunk ? V - v0 : L.chunk);
+      da.rows = N;
+      da.row0 = 0;
+      da.V = vc;
+      da.V_pad = static_cast<int>(L.ds_ld);
+      da.bias = bias != nullptr ? static_cast<const float*>(bias) + v0 : nullptr;
+      da.bias_part = bias_part != nullptr ? bias_part + v0 : nullptr;
+      da.bias_blk0 = 0;
+      da.tgt_base = v0;
+      const float* wc = wf + size_t(v0) * H;
+      v = launch("flce_dlogits_simt", st, [&] { return launch_ds_simt(hf, wc, da, st); });
+      if (v != FLCE_OK) return v;
+      const float* ds = reinterpret_cast<const float*>(da.ds);
+      if (grad_hidden) {
+        SimtGemmArgs ga{};
+        ga.M = N;
+        ga.N = H;
+        ga.K = vc;
+        ga.A = ds;
+        ga.sam = L.ds_ld;
+        ga.sak = 1;
+        ga.B = wc;
+        ga.sbk = H;
+        ga.sbn = 1;
+        ga.C = static_cast<float*>(grad_hidden);
+        ga.ldc = H;
+        ga.accumulate = (c > 0 || p->accumulate) ? 1 : 0;
+        ga.k_splits = simt_k_splits(N, H, vc);
+        ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.status = status;
+        ga.r_c = r_gh;
+        ga.r_part = r_dh;
+        v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
+        if (v != FLCE_OK) return v;
+      }
+      if (grad_weight) {
+        SimtGemmArgs ga{};
+        ga.M = vc;
+        ga.N = H;
+        ga.K = N;
+        ga.A = ds;  // A(m, k) = dlogits[k][m]
+        ga.sam = 1;
+        ga.sak = L.ds_ld;
+        ga.B = hf;
+        ga.sbk = H;
+        ga.sbn = 1;
+        ga.C = static_cast<float*>(grad_weight) + size_t(v0) * H;
+        ga.ldc = H;
+        ga.accumulate = p->accumulate;
+        ga.status = status;
+        ga.r_c = r_gw;
+        v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
         if (v != FLCE_OK) return v;
       }
     }

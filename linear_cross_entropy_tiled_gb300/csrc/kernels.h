@@ -48,7 +48,7 @@ constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;
 
 // ---- fp32 SIMT path tile shape -------------------------------------------
 constexpr int kSimtTile = 64;        // 64 x 64 logit tiles
-constexpr int kSimtPanelCols = 256;  // columns per partial-state panel (fp32 forward)
+constexpr int kSimtPanelCols = 256;  // widest partial-state panel of the fp32 forward (columns)
 constexpr int kSimtThreads = 256;
 
 // Per (panel, row) partial state of the online log-sum-exp:
@@ -290,10 +290,10 @@ struct SimtGemmArgs {
   float* C;                    // C[m*ldc + n]
   long long ldc;
   int accumulate;              // 1: C += A B, 0: C = A B
-  // k_splits > 1: split s of the K range stores its fp32 product to
-  // part + s * M * N ([M][N], row-major), and a second kernel sums the splits
-  // in order into C (adding C when accumulate). For outputs with few 64 x 64
-  // tiles and a long K.
+  // k_splits > 1: split 0 of the K range writes C (adds to it when
+  // accumulate); split s > 0 stores its fp32 product to part + (s - 1) * M * N
+  // ([M][N], row-major), and a second kernel adds those to C in split order.
+  // For outputs with few 64 x 64 tiles and a long K.
   int k_splits;
   float* part;
   int* status;                 // nullable; receives kDevErrBounds (FLCE_DEBUG builds)

@@ -7,8 +7,9 @@
 // as the bf16 path: vocabulary panels with an online log-sum-exp (forward),
 // and a recompute -> dlogits -> two contractions backward. Only the tile
 // arithmetic differs. Speed is secondary to the 1e-5 accuracy bar; the work is
-// spread over enough blocks for small problems (256-column forward panels,
-// and a fixed-order K split for grad_hidden, whose output is small).
+// spread over enough blocks for small problems (forward panels of 64 to 256
+// columns, vocabulary chunks over all rows in the backward, and a fixed-order
+// K split for grad_hidden, whose output is small).
 #include <math.h>
 
 #include "kernels.h"
@@ -32,14 +33,29 @@ __device__ __forceinline__ void simt_logit_tile(const float* __restrict__ h,
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  // The next K slice is loaded into registers while the current one is
+  // multiplied from shared memory, so global latency overlaps the FMAs.
+  constexpr int kPer = T * TK / kSimtThreads;   // elements of each operand per thread
+  float ra[kPer], rb[kPer];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kSimtThreads;
+      const int rr = e / TK, k = k0 + e % TK;
+      ra[q] = (r0 + rr < nrows && k < H) ? h[static_cast<size_t>(r0 + rr) * H + k] : 0.f;
+      rb[q] = (c0 + rr < ncols && k < H) ? w[static_cast<size_t>(c0 + rr) * H + k] : 0.f;
+    }
+  };
+  load(0);
   for (int k0 = 0; k0 < H; k0 += TK) {
-    for (int e = tid; e < T * TK; e += kSimtThreads) {
-      const int rr = e / TK, kk = e % TK;
-      const int k = k0 + kk;
-      As[kk][rr] = (r0 + rr < nrows && k < H) ? h[static_cast<size_t>(r0 + rr) * H + k] : 0.f;
-      Bs[kk][rr] = (c0 + rr < ncols && k < H) ? w[static_cast<size_t>(c0 + rr) * H + k] : 0.f;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kSimtThreads;
+      As[e % TK][e / TK] = ra[q];
+      Bs[e % TK][e / TK] = rb[q];
     }
     __syncthreads();
+    if (k0 + TK < H) load(k0 + TK);
 #pragma unroll 8
     for (int kk = 0; kk < TK; ++kk) {
       float av[4], bv[4];
@@ -63,7 +79,7 @@ __device__ __forceinline__ float transform_f32(float a, const float* bias, int c
   return u;
 }
 
-// One block per (panel of kSimtPanelCols columns, block of 64 rows).
+// One block per (panel of 64 x panel_tiles columns, block of 64 rows).
 __global__ void __launch_bounds__(kSimtThreads)
     fwd_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const FwdArgs a) {
   __shared__ float As[TK][T + 4];
@@ -79,8 +95,8 @@ __global__ void __launch_bounds__(kSimtThreads)
   const int row = r0 + tid;
   long long tgt = (tid < T && row < a.N) ? a.targets[row] : a.ignore_index;
   tgt = (tgt == a.ignore_index) ? -(1ll << 40) : tgt - a.vocab_start;  // shard-local id
-  const int c_begin = panel * kSimtPanelCols;
-  const int c_end = min(a.V, c_begin + kSimtPanelCols);
+  const int c_begin = panel * a.panel_tiles * T;
+  const int c_end = min(a.V, c_begin + a.panel_tiles * T);
   for (int c0 = c_begin; c0 < c_end; c0 += T) {
     float acc[4][4];
     simt_logit_tile(h, w, a.H, r0, a.N, c0, a.V, As, Bs, acc);
@@ -185,14 +201,40 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  // Neighbouring threads read neighbouring addresses: along K for an operand
+  // whose K stride is 1, else along M (or N). The next K slice is loaded into
+  // registers while the current one is multiplied from shared memory.
+  const bool a_k_contig = a.sak == 1, b_k_contig = a.sbk == 1 && a.sbn != 1;
+  constexpr int kPer = T * GK / kSimtThreads;   // elements of each operand per thread
+  float ra[kPer], rb[kPer];
+  auto coords = [&](int e, bool k_contig, int& k, int& mn) {
+    k = k_contig ? e % GK : e / T;
+    mn = k_contig ? e / GK : e % T;
+  };
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kSimtThreads;
+      int ka, ma, kbb, nb;
+      coords(e, a_k_contig, ka, ma);
+      coords(e, b_k_contig, kbb, nb);
+      ra[q] = (m0 + ma < a.M && k0 + ka < ke) ? a.A[(m0 + ma) * a.sam + (k0 + ka) * a.sak] : 0.f;
+      rb[q] = (n0 + nb < a.N && k0 + kbb < ke) ? a.B[(k0 + kbb) * a.sbk + (n0 + nb) * a.sbn] : 0.f;
+    }
+  };
+  if (kb < ke) load(kb);
   for (int k0 = kb; k0 < ke; k0 += GK) {
-    for (int e = tid; e < T * GK; e += kSimtThreads) {
-      const int kk = e / T, mm = e % T;
-      const int k = k0 + kk;
-      As[kk][mm] = (m0 + mm < a.M && k < ke) ? a.A[(m0 + mm) * a.sam + k * a.sak] : 0.f;
-      Bs[kk][mm] = (n0 + mm < a.N && k < ke) ? a.B[k * a.sbk + (n0 + mm) * a.sbn] : 0.f;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kSimtThreads;
+      int ka, ma, kbb, nb;
+      coords(e, a_k_contig, ka, ma);
+      coords(e, b_k_contig, kbb, nb);
+      As[ka][ma] = ra[q];
+      Bs[kbb][nb] = rb[q];
     }
     __syncthreads();
+    if (k0 + GK < ke) load(k0 + GK);
 #pragma unroll
     for (int kk = 0; kk < GK; ++kk) {
       float av[4], bv[4];
@@ -215,8 +257,8 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= a.N) continue;
-      if (a.k_splits > 1) {
-        float* const dst = a.part + (static_cast<size_t>(blockIdx.z) * a.M + m) * a.N + n;
+      if (blockIdx.z > 0) {
+        float* const dst = a.part + (static_cast<size_t>(blockIdx.z - 1) * a.M + m) * a.N + n;
         if (store_allowed(dst, 4, a.r_part, a.status)) *dst = acc[i][j];
       } else {
         float* c = a.C + m * a.ldc + n;
@@ -226,15 +268,16 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
   }
 }
 
-// C[m][n] (+)= sum over s of part[s][m][n], in split order.
+// Split 0 of a K-split product has already written C (or added to it); this
+// adds the other splits' partials part[0 .. k_splits - 2] in split order.
 __global__ void __launch_bounds__(256) simt_split_reduce_kernel(const SimtGemmArgs a) {
   const long long total = static_cast<long long>(a.M) * a.N;
   for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += 256ll * gridDim.x) {
     float s = 0.f;
-    for (int z = 0; z < a.k_splits; ++z) s += a.part[z * total + i];
+    for (int z = 0; z + 1 < a.k_splits; ++z) s += a.part[z * total + i];
     const int m = static_cast<int>(i / a.N), n = static_cast<int>(i - static_cast<long long>(m) * a.N);
     float* c = a.C + m * a.ldc + n;
-    if (store_allowed(c, 4, a.r_c, a.status)) *c = a.accumulate ? *c + s : s;
+    if (store_allowed(c, 4, a.r_c, a.status)) *c += s;
   }
 }
 
