@@ -802,7 +802,7 @@ static int forward_prologue(const flce_params* p, const void* hidden, const void
 // The vocabulary sweep: per-panel online states and the target logits.
 static int forward_tiles(const flce_params* p, const void* hidden, const void* weight,
                          const void* bias, const int64_t* targets, uint8_t* ws, const FwdLayout& L,
-                         const DeviceInfo& d, cudaStream_t st, FwdArgs* out) {
+                         const DeviceInfo& d, bool metrics, cudaStream_t st, FwdArgs* out) {
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   FwdArgs fa{};
   fa.N = N;
@@ -840,7 +840,8 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
     const bool f16 = p->dtype == FLCE_F16;
     v = launch("flce_fwd_tc", st, [&] {
       fa.clk = g_cur_clk;
-      return launch_fwd_tc(tm_h, tm_w, fa, f16, bias != nullptr, p->softcap > 0.f, grid, st);
+      return launch_fwd_tc(tm_h, tm_w, fa, f16, bias != nullptr, p->softcap > 0.f, metrics, grid,
+                           st);
     });
   } else {
     fa.n_blocks = static_cast<int>(ceil_div(N, kSimtTile));
@@ -897,7 +898,9 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
   const int N = static_cast<int>(p->N);
   if (N > 0) {
     FwdArgs fa;
-    if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, st, &fa)) != FLCE_OK) return v;
+    const bool metrics = num_correct != nullptr || entropy_sum != nullptr;
+    if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, metrics, st, &fa)) != FLCE_OK)
+      return v;
     MergeArgs ma{};
     ma.N = N;
     ma.V = static_cast<int>(p->V);
@@ -942,7 +945,9 @@ int flce_forward_partial(const flce_params* p, const void* hidden, const void* w
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   if (p->N == 0) return FLCE_OK;
   FwdArgs fa;
-  if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, st, &fa)) != FLCE_OK) return v;
+  // the shard states carry the argmax and sum z exp(z - m) for the merge's metrics
+  if ((v = forward_tiles(p, hidden, weight, bias, targets, ws, L, d, true, st, &fa)) != FLCE_OK)
+    return v;
   ShardStateArgs sa{};
   sa.N = static_cast<int>(p->N);
   sa.V = static_cast<int>(p->V);

@@ -310,8 +310,12 @@ struct BiasReduceArgs {
 // tcgen05 / TMA kernels (bf16). `grid` is the number of CTA pairs.
 cudaError_t tc_max_active_pairs(int* pairs);
 // f16 selects fp16 operands and outputs; otherwise bf16.
+// metrics: also keep each row's argmax and sum z exp(z - m) (needed for
+// num_correct, entropy_sum and exported shard states); loss and lse are the
+// same bits either way.
 cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
-                          bool f16, bool has_bias, bool softcap, int grid, cudaStream_t s);
+                          bool f16, bool has_bias, bool softcap, bool metrics, int grid,
+                          cudaStream_t s);
 cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,
                          bool f16, bool has_bias, bool softcap, int grid, cudaStream_t s);
 // A GEMM operand in global memory. `map` is its 2-D tensor map: 64 x 128

@@ -348,6 +348,70 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Two fp32 lanes in one 64-bit register pair, for the packed fp32 arithmetic
+// of sm_100+ (fma / mul / add .f32x2). Each lane is rounded as the scalar
+// instruction rounds it, so packed and scalar code give identical bits.
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// d[j] = a[j] * b + c[j] (c may be nullptr: d[j] = a[j] * b) for even N, in
+// pairs of lanes.
+template <int N>
+__device__ __forceinline__ void fma_pairs(float (&d)[N], const float (&a)[N], float b,
+                                          const float (&c)[N]) {
+  const unsigned long long bb = f2pack(b, b);
+#pragma unroll
+  for (int j = 0; j < N; j += 2)
+    f2unpack(fma2(f2pack(a[j], a[j + 1]), bb, f2pack(c[j], c[j + 1])), d[j], d[j + 1]);
+}
+template <int N>
+__device__ __forceinline__ void fma_pairs(float (&d)[N], const float (&a)[N], float b, float c) {
+  const unsigned long long bb = f2pack(b, b), cc = f2pack(c, c);
+#pragma unroll
+  for (int j = 0; j < N; j += 2) f2unpack(fma2(f2pack(a[j], a[j + 1]), bb, cc), d[j], d[j + 1]);
+}
+template <int N>
+__device__ __forceinline__ void mul_pairs(float (&d)[N], const float (&a)[N], float b) {
+  const unsigned long long bb = f2pack(b, b);
+#pragma unroll
+  for (int j = 0; j < N; j += 2) f2unpack(mul2(f2pack(a[j], a[j + 1]), bb), d[j], d[j + 1]);
+}
+template <int N>
+__device__ __forceinline__ void mul_pairs(float (&d)[N], const float (&a)[N], const float (&b)[N]) {
+#pragma unroll
+  for (int j = 0; j < N; j += 2)
+    f2unpack(mul2(f2pack(a[j], a[j + 1]), f2pack(b[j], b[j + 1])), d[j], d[j + 1]);
+}
+// x[j] += x[j + W] for j < W (W even), in pairs of lanes.
+template <int W, int N>
+__device__ __forceinline__ void add_half_pairs(float (&x)[N]) {
+#pragma unroll
+  for (int j = 0; j < W; j += 2)
+    f2unpack(add2(f2pack(x[j], x[j + 1]), f2pack(x[j + W], x[j + W + 1])), x[j], x[j + 1]);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -321,27 +321,28 @@ __device__ __forceinline__ float transform(uint32_t raw, float bs, float scale, 
 }
 
 // ======================================================= forward kernel
-// One level of a pairwise (max, first index) tree over W pairs. The left
-// element wins ties, so the lowest index survives.
-template <int W>
-__device__ __forceinline__ void argmax_level(float (&mv)[16], int (&mi)[16]) {
-#pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const bool l = mv[2 * j] >= mv[2 * j + 1];
-    mv[j] = l ? mv[2 * j] : mv[2 * j + 1];
-    mi[j] = l ? mi[2 * j] : mi[2 * j + 1];
-  }
+// Sum of the 32 values of x by a pairwise tree, the first four levels in
+// packed pairs of lanes (x is overwritten).
+__device__ __forceinline__ float tree_sum32(float (&x)[32]) {
+  add_half_pairs<16>(x);
+  add_half_pairs<8>(x);
+  add_half_pairs<4>(x);
+  add_half_pairs<2>(x);
+  return x[0] + x[1];
 }
 
-// One level of a pairwise sum tree over W pairs, for two arrays at once.
-template <int W>
-__device__ __forceinline__ void sum_level(float (&e)[32], float (&ze)[32]) {
+// Largest of the 32 values, by a pairwise tree.
+__device__ __forceinline__ float tree_max32(const float (&z)[32]) {
+  float t[16];
 #pragma unroll
-  for (int j = 0; j < W; ++j) {
-    e[j] = e[j] + e[j + W];
-    ze[j] = ze[j] + ze[j + W];
-  }
+  for (int j = 0; j < 16; ++j) t[j] = fmaxf(z[2 * j], z[2 * j + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+  return t[0];
 }
+
 // x[i] for a runtime i in [0, 32), as a 5-level multiplexer on the bits of
 // i. Every array index stays a compile-time constant, so x stays in
 // registers.
@@ -358,19 +359,34 @@ __device__ __forceinline__ float select32(const float (&x)[32], int i) {
   return (i & 1) ? t2[1] : t2[0];
 }
 
-template <typename T, bool kRagged, bool kBias, bool kSoftcap>
+// The 256 x 256 logit tile's 32 columns col0 .. col0 + 31 of one row, folded
+// into the row's online state (fused-linear-ce README, "Algorithm"): the
+// transform, the running max m, sum exp(z - m) and, with kMetrics, the first
+// index of the max and sum z exp(z - m) ("Metrics for free"). The arithmetic
+// that m and ssum see is the same with and without kMetrics, so loss and lse
+// are bit-identical either way. The element-wise steps run in packed pairs of
+// lanes (f32x2), rounded as the scalar steps are.
+template <typename T, bool kRagged, bool kBias, bool kSoftcap, bool kMetrics>
 __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs& a, int col0,
                                           long long tgt, int row, bool row_ok, float& m,
                                           float& ssum, float& tsum, int& amax) {
-  float bs[32];
-  if (kBias) load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
   float z[32];
+  {
+    float raw[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) raw[j] = __uint_as_float(v[j]);
+    if (kBias) {
+      float bs[32];
+      load_bias32<T, kRagged>(static_cast<const T*>(a.bias), col0, a.V, a.scale, bs);
+      fma_pairs(z, raw, a.scale, bs);       // (a + b) s, as fma(a, s, b s)
+    } else {
+      mul_pairs(z, raw, a.scale);
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    float zz = transform<kBias, kSoftcap>(v[j], kBias ? bs[j] : 0.f, a.scale, a.softcap,
-                                          a.inv_softcap);
-    if (kRagged && col0 + j >= a.V) zz = -INFINITY;
-    z[j] = zz;
+    if (kSoftcap) z[j] = a.softcap * tanh_via_exp2(z[j] * a.inv_softcap);
+    if (kRagged && col0 + j >= a.V) z[j] = -INFINITY;
   }
   // The target logit lives in exactly one chunk of the whole vocabulary sweep.
   const long long rel = tgt - col0;
@@ -378,43 +394,38 @@ __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs
     const float zt = select32(z, static_cast<int>(rel));
     if (store_allowed(&a.zt[row], 4, a.r_zt, a.status)) a.zt[row] = zt;
   }
-  // Chunk max and first index that attains it, as a pairwise tree. The left
-  // operand wins ties, so the lowest index is kept.
-  float mv[16];
-  int mi[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const bool l = z[2 * j] >= z[2 * j + 1];
-    mv[j] = l ? z[2 * j] : z[2 * j + 1];
-    mi[j] = l ? 2 * j : 2 * j + 1;
-  }
-  argmax_level<8>(mv, mi);
-  argmax_level<4>(mv, mi);
-  argmax_level<2>(mv, mi);
-  argmax_level<1>(mv, mi);
-  const float cmax = mv[0];
+  const float cmax = tree_max32(z);
   const float mnew = fmaxf(m, cmax);
-  if (cmax > m) amax = col0 + mi[0];  // strict: an earlier chunk keeps a tie
-  const float alpha = ex2_approx((m - mnew) * kLog2e);
-  const float nb = -mnew * kLog2e;
-  float e[32], ze[32];
+  if (kMetrics && cmax > m) {
+    // strictly larger: an earlier chunk keeps a tie; within the chunk the
+    // lowest index that attains the max
+    int idx = 31;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    e[j] = ex2_approx(fmaf(z[j], kLog2e, nb));
-    const float zc = (kRagged && col0 + j >= a.V) ? 0.f : z[j];
-    ze[j] = zc * e[j];
+    for (int j = 30; j >= 0; --j) idx = (z[j] == cmax) ? j : idx;
+    amax = col0 + idx;
   }
-  sum_level<16>(e, ze);
-  sum_level<8>(e, ze);
-  sum_level<4>(e, ze);
-  sum_level<2>(e, ze);
-  sum_level<1>(e, ze);
-  ssum = fmaf(ssum, alpha, e[0]);
-  tsum = fmaf(tsum, alpha, ze[0]);
+  const float alpha = ex2_approx((m - mnew) * kLog2e);
+  float e[32];
+  fma_pairs(e, z, kLog2e, -mnew * kLog2e);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) e[j] = ex2_approx(e[j]);
+  if (kMetrics) {
+    float ze[32];
+    if (kRagged) {
+      float zc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) zc[j] = (col0 + j >= a.V) ? 0.f : z[j];
+      mul_pairs(ze, zc, e);
+    } else {
+      mul_pairs(ze, z, e);
+    }
+    tsum = fmaf(tsum, alpha, tree_sum32(ze));
+  }
+  ssum = fmaf(ssum, alpha, tree_sum32(e));
   m = mnew;
 }
 
-template <typename T, bool kBias, bool kSoftcap>
+template <typename T, bool kBias, bool kSoftcap, bool kMetrics>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                   const FwdArgs a) {
@@ -490,10 +501,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             tmem_ld_wait(v);
             const int col0 = vt * kBN + c * 32;
             if (!ragged) {
-              fwd_chunk<T, false, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
+              fwd_chunk<T, false, kBias, kSoftcap, kMetrics>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
                                                    amax);
             } else if (col0 < a.V) {
-              fwd_chunk<T, true, kBias, kSoftcap>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
+              fwd_chunk<T, true, kBias, kSoftcap, kMetrics>(v, a, col0, tgt, row, row_ok, m, ssum, tsum,
                                                   amax);
             }
           }
@@ -995,7 +1006,7 @@ cudaError_t set_smem_attr(K kernel) {
 }  // namespace
 
 cudaError_t tc_max_active_pairs(int* pairs) {
-  auto k = fwd_tc_kernel<__nv_bfloat16, false, false>;
+  auto k = fwd_tc_kernel<__nv_bfloat16, false, false, false>;
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1010,11 +1021,13 @@ cudaError_t tc_max_active_pairs(int* pairs) {
 }
 
 namespace {
-template <typename T>
+template <typename T, bool kMetrics>
 cudaError_t launch_fwd_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
                          bool has_bias, bool softcap, int grid, cudaStream_t st) {
-  auto k = has_bias ? (softcap ? fwd_tc_kernel<T, true, true> : fwd_tc_kernel<T, true, false>)
-                    : (softcap ? fwd_tc_kernel<T, false, true> : fwd_tc_kernel<T, false, false>);
+  auto k = has_bias ? (softcap ? fwd_tc_kernel<T, true, true, kMetrics>
+                               : fwd_tc_kernel<T, true, false, kMetrics>)
+                    : (softcap ? fwd_tc_kernel<T, false, true, kMetrics>
+                               : fwd_tc_kernel<T, false, false, kMetrics>);
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
@@ -1045,9 +1058,13 @@ cudaError_t launch_gemm_t(const GemmOperand& op_a, const GemmOperand& op_b, cons
 
 // `grid` counts CTA pairs; the launch has 2 * grid CTAs.
 cudaError_t launch_fwd_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const FwdArgs& a,
-                          bool f16, bool has_bias, bool softcap, int grid, cudaStream_t st) {
-  return f16 ? launch_fwd_t<__half>(tm_h, tm_w, a, has_bias, softcap, grid, st)
-             : launch_fwd_t<__nv_bfloat16>(tm_h, tm_w, a, has_bias, softcap, grid, st);
+                          bool f16, bool has_bias, bool softcap, bool metrics, int grid,
+                          cudaStream_t st) {
+  if (metrics)
+    return f16 ? launch_fwd_t<__half, true>(tm_h, tm_w, a, has_bias, softcap, grid, st)
+               : launch_fwd_t<__nv_bfloat16, true>(tm_h, tm_w, a, has_bias, softcap, grid, st);
+  return f16 ? launch_fwd_t<__half, false>(tm_h, tm_w, a, has_bias, softcap, grid, st)
+             : launch_fwd_t<__nv_bfloat16, false>(tm_h, tm_w, a, has_bias, softcap, grid, st);
 }
 
 cudaError_t launch_ds_tc(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const DsArgs& a,

@@ -150,14 +150,17 @@ def test_out_of_range_target_reports_status_without_fault():
     assert out["status_fwd"] == 6 and out["status_bwd"] == 6
 
 
-def test_deterministic_and_metrics_bit_identical():
+@pytest.mark.parametrize("dtype,softcap,bias", [("bf16", 20.0, True), ("bf16", None, True),
+                                                ("f16", None, False)])
+def test_deterministic_and_metrics_bit_identical(dtype, softcap, bias):
     """Repeated calls give the same bits. return_metrics leaves loss, lse and gradients
-    bit-identical (fused-linear-ce README, 'Metrics for free')."""
-    d = small_case(700, 264, 1300, seed=9, dtype="bf16", bias=True, ignore_frac=0.1)
-    kw = dict(reduction="mean", softcap=20.0, z_loss_multiplier=1e-4, deterministic=True)
-    a = run_gpu(d, "bf16", kw, return_metrics=True)
-    b = run_gpu(d, "bf16", kw, return_metrics=False)
-    c = run_gpu(d, "bf16", kw, return_metrics=True)
+    bit-identical (fused-linear-ce README, 'Metrics for free'): the forward kernel built
+    without the metrics' bookkeeping must agree bit for bit with the one built with it."""
+    d = small_case(700, 264, 1300, seed=9, dtype=dtype, bias=bias, ignore_frac=0.1)
+    kw = dict(reduction="mean", softcap=softcap, z_loss_multiplier=1e-4, deterministic=True)
+    a = run_gpu(d, dtype, kw, return_metrics=True)
+    b = run_gpu(d, dtype, kw, return_metrics=False)
+    c = run_gpu(d, dtype, kw, return_metrics=True)
     for k in ("loss", "lse", "grad_hidden", "grad_weight", "grad_bias"):
         np.testing.assert_array_equal(a[k], b[k], err_msg=k)
         np.testing.assert_array_equal(a[k], c[k], err_msg=k)
