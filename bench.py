@@ -169,6 +169,8 @@ def kernel_flops(name: str, w: wl.Workload) -> float:
                 "flce_chunk_grad_weight_tc", "flce_fwd_simt", "flce_dlogits_simt",
                 "flce_grad_hidden_simt", "flce_grad_weight_simt"):
         return 2.0 * w.N * w.H * w.V
+    if name == "flce_grads_simt":   # both gradient contractions in one launch
+        return 4.0 * w.N * w.H * w.V
     return 0.0
 
 

@@ -1349,8 +1349,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       v = launch("flce_dlogits_simt", st, [&] { return launch_ds_simt(hf, wc, da, st); });
       if (v != FLCE_OK) return v;
       const float* ds = reinterpret_cast<const float*>(da.ds);
+      SimtGemmArgs gh_args{}, gw_args{};
       if (grad_hidden) {
-        SimtGemmArgs ga{};
+        SimtGemmArgs& ga = gh_args;
         ga.M = N;
         ga.N = H;
         ga.K = vc;
@@ -1368,11 +1369,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.status = status;
         ga.r_c = r_gh;
         ga.r_part = r_dh;
-        v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(ga, st); });
-        if (v != FLCE_OK) return v;
       }
       if (grad_weight) {
-        SimtGemmArgs ga{};
+        SimtGemmArgs& ga = gw_args;
         ga.M = vc;
         ga.N = H;
         ga.K = N;
@@ -1387,9 +1386,16 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.accumulate = p->accumulate;
         ga.status = status;
         ga.r_c = r_gw;
-        v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(ga, st); });
-        if (v != FLCE_OK) return v;
       }
+      // Both contractions of the chunk in one grid when both are wanted: each
+      // alone is too small to fill the GPU at the sizes this path serves.
+      if (grad_hidden && grad_weight)
+        v = launch("flce_grads_simt", st, [&] { return launch_gemm_simt2(gh_args, gw_args, st); });
+      else if (grad_hidden)
+        v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(gh_args, st); });
+      else if (grad_weight)
+        v = launch("flce_grad_weight_simt", st, [&] { return launch_gemm_simt(gw_args, st); });
+      if (v != FLCE_OK) return v;
     }
   } else {
     const float* hf = static_cast<const float*>(hidden);

@@ -339,6 +339,8 @@ cudaError_t launch_gemm_tc(const GemmOperand& op_a, const GemmOperand& op_b, con
 cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s);
+// Two independent products in one launch (then each one's split reduction).
+cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, cudaStream_t s);
 
 // dtype-generic small kernels (dtype: 0 = f32, 1 = bf16, 2 = fp16)
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);

@@ -187,14 +187,15 @@ __global__ void __launch_bounds__(kSimtThreads)
 
 constexpr int GK = 16;
 
-__global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmArgs a) {
+// Output tile (bx, by) of 64 x 64 and K split bz of one product.
+__device__ __forceinline__ void gemm_simt_block(const SimtGemmArgs& a, int bx, int by, int bz) {
   __shared__ float As[GK][T + 4];
   __shared__ float Bs[GK][T + 4];
-  const int m0 = blockIdx.y * T, n0 = blockIdx.x * T;
+  const int m0 = by * T, n0 = bx * T;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  // this block's K range: all of K, or split blockIdx.z of k_splits
+  // this block's K range: all of K, or split bz of k_splits
   const int kc = a.k_splits > 1 ? (a.K + a.k_splits - 1) / a.k_splits : a.K;
-  const int kb = static_cast<int>(blockIdx.z) * kc;
+  const int kb = bz * kc;
   const int ke = min(a.K, kb + kc);
   float acc[4][4];
 #pragma unroll
@@ -257,8 +258,8 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= a.N) continue;
-      if (blockIdx.z > 0) {
-        float* const dst = a.part + (static_cast<size_t>(blockIdx.z - 1) * a.M + m) * a.N + n;
+      if (bz > 0) {
+        float* const dst = a.part + (static_cast<size_t>(bz - 1) * a.M + m) * a.N + n;
         if (store_allowed(dst, 4, a.r_part, a.status)) *dst = acc[i][j];
       } else {
         float* c = a.C + m * a.ldc + n;
@@ -266,6 +267,22 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmA
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const SimtGemmArgs a) {
+  gemm_simt_block(a, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// Two independent products in one grid: blocks [0, n1) compute the first,
+// the rest the second. The two contractions of a backward chunk are each too
+// small to fill the GPU alone; together they do.
+__global__ void __launch_bounds__(kSimtThreads) gemm_simt2_kernel(const SimtGemmArgs a1,
+                                                                  const SimtGemmArgs a2, int n1) {
+  const bool first = static_cast<int>(blockIdx.x) < n1;
+  const SimtGemmArgs& a = first ? a1 : a2;
+  const int i = first ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - n1;
+  const int gx = (a.N + T - 1) / T, gy = (a.M + T - 1) / T;
+  gemm_simt_block(a, i % gx, (i / gx) % gy, i / (gx * gy));
 }
 
 // Split 0 of a K-split product has already written C (or added to it); this
@@ -292,6 +309,28 @@ cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cuda
   dim3 grid((a.V + T - 1) / T, (a.rows + T - 1) / T);
   ds_simt_kernel<<<grid, kSimtThreads, 0, s>>>(h, w, a);
   return cudaGetLastError();
+}
+
+namespace {
+int simt_blocks(const SimtGemmArgs& a) {
+  return ((a.N + T - 1) / T) * ((a.M + T - 1) / T) * (a.k_splits > 1 ? a.k_splits : 1);
+}
+cudaError_t split_reduce_after(const SimtGemmArgs& a, cudaStream_t s) {
+  if (a.k_splits <= 1) return cudaSuccess;
+  const long long total = static_cast<long long>(a.M) * a.N;
+  const int blocks = static_cast<int>(min(4096ll, (total + 255) / 256));
+  simt_split_reduce_kernel<<<blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, cudaStream_t s) {
+  const int n1 = simt_blocks(a1), n2 = simt_blocks(a2);
+  gemm_simt2_kernel<<<n1 + n2, kSimtThreads, 0, s>>>(a1, a2, n1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = split_reduce_after(a1, s)) != cudaSuccess) return e;
+  return split_reduce_after(a2, s);
 }
 
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s) {

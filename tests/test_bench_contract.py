@@ -40,6 +40,9 @@ def test_kernel_flops_count_each_contraction_once_per_step():
     names = ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc")
     assert sum(bench.kernel_flops(n, w) for n in names) == w.flops_fwd_bwd
     assert bench.kernel_flops("flce_merge", w) == 0.0
+    t = wl.WORKLOADS["tiny_f32"]
+    names = ("flce_fwd_simt", "flce_dlogits_simt", "flce_grads_simt")
+    assert sum(bench.kernel_flops(n, t) for n in names) == t.flops_fwd_bwd
     r = wl.REGRESSION_WORKLOADS["mse_v32768"]
     names = ("flce_chunk_mse_tc", "flce_chunk_grad_hidden_tc", "flce_chunk_grad_weight_tc")
     assert sum(bench.kernel_flops(n, r) for n in names) == r.flops_fwd_bwd
