@@ -267,7 +267,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // ------------------------------------------------------ workspace layouts
 constexpr int kMinPanelTiles = 4;
 constexpr int kMaxPanelTiles = 32;
-constexpr size_t kHeader = 256;   // status word at 0, fp16 dlogits scale {S, 1/S} at 64
+constexpr size_t kHeader = 256;   // status word at 0, fp16 dlogits scale {S, 1/S} at 64,
+                                  // the GEMMs' tile counters at 128
 constexpr size_t kScaleOffset = 64;
 constexpr size_t kChunkByteCap = size_t(4) << 30;
 constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_splits)
@@ -547,10 +548,21 @@ int gemm_group_m(const GemmArgs& ga, int pairs) {
   return static_cast<int>(g < ga.m_tiles ? g : ga.m_tiles);
 }
 
+// The GEMMs take their units from an atomic counter in the workspace header
+// (two ints at kTileCounterOffset, zeroed with the header at every entry and
+// left zero by each launch), so that a pair that finishes early takes the
+// next unit. Builds with FLCE_STATIC_GEMM_SCHEDULE hand the units out
+// round-robin instead.
+constexpr size_t kTileCounterOffset = 128;
+
 cudaError_t launch_gemm(const GemmOperand& op_a, const GemmOperand& op_b, GemmArgs ga, bool f16,
                         int pairs, cudaStream_t st) {
   ga.group_m = gemm_group_m(ga, pairs);
   ga.clk = g_cur_clk;
+#ifndef FLCE_STATIC_GEMM_SCHEDULE
+  if (ga.status != nullptr)
+    ga.tile_counter = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ga.status) + kTileCounterOffset);
+#endif
   return launch_gemm_tc(op_a, op_b, ga, f16, pairs, st);
 }
 

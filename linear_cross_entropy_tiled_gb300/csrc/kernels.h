@@ -249,6 +249,10 @@ struct GemmArgs {
   void* out_t;                 // nullable: out transposed as well, [N][ld_out_t]
   long long ld_out_t;
   DevRegion r_out, r_part, r_out_t, r_loss;
+  // Dynamic schedule: two ints, zero before the launch and left zero after it.
+  // [0] hands out units in order, [1] counts the pairs that have finished
+  // taking units. nullptr: every pair takes units u = pair, pair + npairs, ...
+  int* tile_counter;
 };
 
 // dst[i] = src[i] * (*scale), i < count, in the element type (dtype 0 fp32,

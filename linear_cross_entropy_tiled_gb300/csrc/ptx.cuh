@@ -99,6 +99,42 @@ __device__ __forceinline__ bool store_allowed(const void* p, unsigned n, const D
   return true;
 }
 
+// try_wait with acquire at cluster scope: the completing arrive came from the
+// other CTA of the pair, and data it wrote before arriving must be visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitGuard& g) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if (*g.abort) return false;
+    if (global_timer_ns() - t0 > g.limit_ns) {
+      *g.abort = 1;
+      atomicOr(g.status, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
+// 32-bit store to shared memory of a CTA of this cluster, by its
+// shared::cluster address (from mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -52,7 +52,17 @@ struct TcSmem {
   uint64_t* mma_done;    // 1: all MMAs complete (teardown)
   uint32_t* tmem_slot;
   int* abort;
+  // Unit queue of the dynamic GEMM schedule (see TileQueue): the even CTA's
+  // producer publishes each unit to both CTAs of the pair.
+  uint64_t* q_full;      // kQueue: the slot holds a unit (in each CTA)
+  uint64_t* q_empty;     // kQueue: every consumer has read it (even CTA only)
+  int* q_unit;           // kQueue
 };
+
+constexpr int kQueue = 4;
+// Readers of each queue slot: the MMA thread, the odd CTA's producer, and the
+// four epilogue warps of each CTA.
+constexpr int kQueueReaders = 2 + 2 * 4;
 
 __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
   TcSmem s;
@@ -69,6 +79,9 @@ __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
   s.mma_done = s.tempty + 2;
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.mma_done + 1);
   s.abort = reinterpret_cast<int*>(s.tmem_slot + 1);
+  s.q_full = s.mma_done + 2;   // after tmem_slot and abort (8 bytes)
+  s.q_empty = s.q_full + kQueue;
+  s.q_unit = reinterpret_cast<int*>(s.q_empty + kQueue);
   return s;
 }
 
@@ -86,6 +99,10 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_
       mbar_init(&s.tempty[i], 2 * epi_warps);  // even CTA: every epilogue warp of both CTAs
     }
     mbar_init(s.mma_done, 1);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], kQueueReaders);
+    }
     *s.abort = 0;
     fence_mbar_init();
   }
@@ -745,6 +762,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
   clock_start.finish(a.clk);
 }
 
+// ==================================================== dynamic schedule
+// Units handed out by an atomic counter instead of round-robin (the prior
+// art's tile semaphore, quack diff, GemmWrapperBase): a pair that finishes
+// early takes the next unit. Only the even CTA's producer thread touches the
+// counter; it publishes each unit (or -1 when none is left) through a ring of
+// kQueue shared-memory slots, written in both CTAs of the pair, and every
+// other role of both CTAs reads the units from its own CTA's copy. A slot is
+// reused only after all kQueueReaders readers have released it. Every wait
+// is bounded (WaitGuard).
+struct TileQueue {
+  const TcSmem& s;
+  const WaitGuard& g;
+  uint32_t rank;
+  int i = 0;   // units published or read so far
+
+  // Even CTA's producer: the next unit, published to both CTAs; -1 when the
+  // units are exhausted; -2 if a wait gave up.
+  __device__ __forceinline__ int publish(int* counter, int units) {
+    const int slot = i % kQueue;
+    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
+    if (!mbar_wait_cluster(&s.q_empty[slot], ph ^ 1u, g)) return -2;
+    int u = atomicAdd(counter, 1);
+    if (u >= units) u = -1;
+    s.q_unit[slot] = u;
+    st_shared_cluster_u32(mapa_shared(smem_u32(&s.q_unit[slot]), 1), static_cast<uint32_t>(u));
+    mbar_arrive(&s.q_full[slot]);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_full[slot]), 1));
+    ++i;
+    return u;
+  }
+
+  // Any other role: the next unit from this CTA's slot (-1: none left, -2: a
+  // wait gave up). Each reader then calls release() once it has the value;
+  // in a warp that reads together, one lane releases after a __syncwarp.
+  __device__ __forceinline__ int read() {
+    const int slot = i % kQueue;
+    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
+    const bool ok = rank == 0 ? mbar_wait(&s.q_full[slot], ph, g)
+                              : mbar_wait_cluster(&s.q_full[slot], ph, g);
+    if (!ok) return -2;
+    return *reinterpret_cast<volatile int*>(&s.q_unit[slot]);
+  }
+  __device__ __forceinline__ void release() {
+    const int slot = i % kQueue;
+    if (rank == 0)
+      mbar_arrive(&s.q_empty[slot]);
+    else
+      mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_empty[slot]), 0));
+    ++i;
+  }
+};
+
 // ========================================================= plain GEMM
 // D = A B with fp32 accumulation; the two gradient contractions. Units
 // (split, tile) go round-robin over the pairs: consecutive units are
@@ -777,12 +846,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   // Every unit of this pair as (row tile << 8 | split, column tile), decoded
   // once per tile: the per-stage work of the single producer thread stays
   // free of divisions. Splits number at most 255 (the host uses at most 2).
+  // With a tile counter the units come from the dynamic schedule (TileQueue):
+  // the even CTA's producer takes them off the counter and every other role
+  // reads them from the queue, in the same order.
+  const bool dynamic = a.tile_counter != nullptr;
+  auto decode = [&](int u, int& ta, int& nt) {
+    const int sp = u / num_tiles;
+    int mt;
+    decode_unit(u - sp * num_tiles, m_tiles, group_m, n_tiles, nt, mt);
+    ta = (mt << 8) | sp;
+  };
   auto for_each_tile = [&](auto&& f) {
-    for (int u = pair; u < units; u += npairs) {
-      const int sp = u / num_tiles;
-      int mt, nt;
-      decode_unit(u - sp * num_tiles, m_tiles, group_m, n_tiles, nt, mt);
-      f((mt << 8) | sp, nt);
+    int ta, nt;
+    if (!dynamic) {
+      for (int u = pair; u < units; u += npairs) {
+        decode(u, ta, nt);
+        f(ta, nt);
+      }
+      return;
+    }
+    TileQueue q{s, g, rank};
+    if (warp == 0 && rank == 0) {
+      while (true) {
+        const int u = q.publish(a.tile_counter, units);
+        if (u == -1) {
+          // the last pair to run out leaves the counters at zero for the next launch
+          if (atomicAdd(a.tile_counter + 1, 1) == npairs - 1) {
+            a.tile_counter[0] = 0;
+            a.tile_counter[1] = 0;
+          }
+        }
+        if (u < 0) return;
+        decode(u, ta, nt);
+        f(ta, nt);
+      }
+    }
+    while (true) {   // the odd CTA's producer, or the MMA thread
+      const int u = q.read();
+      if (u == -2) return;
+      q.release();
+      if (u < 0) return;
+      decode(u, ta, nt);
+      f(ta, nt);
     }
   };
   auto kblocks_of = [&](int ta, int) {
@@ -860,7 +965,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
-    for (int u = pair; u < units; u += npairs) {
+    auto unit_epilogue = [&](int u) {
       const int sp = u / num_tiles, t = u - sp * num_tiles;
       int mt, nt;
       decode_unit(t, m_tiles, group_m, n_tiles, nt, mt);
@@ -992,6 +1097,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    };
+    if (!dynamic) {
+      for (int u = pair; u < units; u += npairs) unit_epilogue(u);
+    } else {
+      TileQueue q{s, g, rank};
+      while (true) {
+        const int u = q.read();   // the same value in every lane that got one
+        if (!__all_sync(kFull, u != -2)) break;
+        __syncwarp();
+        if (lane == 0) q.release();
+        else ++q.i;
+        if (u < 0) break;
+        unit_epilogue(u);
+      }
     }
   }
   tc_teardown(tmem, warp);
