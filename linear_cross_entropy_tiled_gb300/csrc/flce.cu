@@ -195,7 +195,6 @@ int name_index(const char* n) {
 
 template <class F>
 int launch(const char* name, cudaStream_t s, F&& f) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
   std::unique_lock<std::mutex> lk(g_prof_mu);
   const bool prof = g_prof;
   Pending p{};
@@ -268,7 +267,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int kMinPanelTiles = 4;
 constexpr int kMaxPanelTiles = 32;
 constexpr size_t kHeader = 256;   // status word at 0, fp16 dlogits scale {S, 1/S} at 64,
-                                  // the GEMMs' tile counters at 128
+                                  // the GEMMs' tile counters at 128, the merge's
+                                  // blocks-done counter at 136
 constexpr size_t kScaleOffset = 64;
 constexpr size_t kChunkByteCap = size_t(4) << 30;
 constexpr int kMaxKSplits = 2;   // K splits of the grad_hidden GEMM (choose_k_splits)
@@ -306,7 +306,8 @@ int simt_panel_tiles(int64_t N, int64_t V) {
 
 struct FwdLayout {
   int num_panels_max;
-  int nblk;
+  int lanes;   // merge threads per row
+  int nblk;    // merge blocks
   size_t partials, zt, blk_loss, blk_ent, blk_correct, blk_valid, total;
   size_t partials_bytes, zt_bytes, blk_bytes;   // bytes the kernels may write in each region
 };
@@ -318,7 +319,10 @@ FwdLayout fwd_layout(const flce_params* p) {
     L.num_panels_max = static_cast<int>(ceil_div(ceil_div(V, kBN), kMinPanelTiles));
   else
     L.num_panels_max = static_cast<int>(ceil_div(V, int64_t(simt_panel_tiles(N, V)) * kSimtTile));
-  L.nblk = static_cast<int>(ceil_div(N, kMergeThreads));
+  // about four panels per merge thread, up to a warp per row
+  L.lanes = 1;
+  while (L.lanes < 32 && L.lanes * 4 < L.num_panels_max) L.lanes *= 2;
+  L.nblk = static_cast<int>(ceil_div(N * L.lanes, kMergeThreads));
   L.partials_bytes = size_t(L.num_panels_max) * N * sizeof(float4);
   L.zt_bytes = size_t(N) * 4;
   L.blk_bytes = size_t(L.nblk) * 8;
@@ -345,10 +349,18 @@ struct BwdLayout {
   int64_t ds_ld;            // row stride of the dlogits buffer, in elements
   int64_t ds_t_ld;          // row stride of the transposed dlogits buffer (tensor path)
   int nchunks, rowblk, n_rowblocks;
-  size_t coef, ds, ds_t, dw, dh_part, bias_part, total;
+  size_t cnt, coef, ds, ds_t, dw, dh_part, bias_part, total;
   // bytes the kernels may write in each region (0: the region is absent)
-  size_t coef_bytes, ds_bytes, ds_t_bytes, dw_bytes, dh_bytes, bias_bytes;
+  size_t cnt_bytes, coef_bytes, ds_bytes, ds_t_bytes, dw_bytes, dh_bytes, bias_bytes;
 };
+
+// The fp32 path's K-split GEMMs count the finished splits of each output tile
+// in a region right after the header; the backward's first kernel zeroes both.
+void place_counters(const flce_params* p, BwdLayout* L, size_t* o) {
+  L->cnt = *o;
+  L->cnt_bytes = tensor_path(p) ? 0 : size_t(kSimtSplitTiles) * 4;
+  if (L->cnt_bytes) *o = align_up(*o + L->cnt_bytes, 256);
+}
 
 // The backward stores dlogits for one chunk at a time and contracts it into
 // both gradients. The tensor path keeps two copies: row-major for grad_hidden
@@ -409,6 +421,7 @@ BwdLayout bwd_layout(const flce_params* p) {
     }
     L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
     size_t o = kHeader;
+    place_counters(p, &L, &o);
     L.coef = o;
     o = align_up(o + L.coef_bytes, 256);
     L.ds = o;
@@ -460,6 +473,7 @@ BwdLayout bwd_layout(const flce_params* p) {
   }
   L.bias_bytes = p->has_bias ? size_t(L.n_rowblocks) * L.V_pad * 4 : 0;
   size_t o = kHeader;
+  place_counters(p, &L, &o);
   L.coef = o;
   o = align_up(o + L.coef_bytes, 256);
   L.ds = o;
@@ -702,6 +716,7 @@ std::vector<WsRegion> workspace_regions(const flce_params* p, int pass) {
     add("block_valid", L.blk_valid, L.blk_bytes);
   } else if (pass == FLCE_PASS_BACKWARD) {
     const BwdLayout L = bwd_layout(p);
+    add("tile_counters", L.cnt, L.cnt_bytes);
     add("row_coefficients", L.coef, L.coef_bytes);
     add("dlogits", L.ds, L.ds_bytes);
     add("dlogits_transposed", L.ds_t, L.ds_t_bytes);
@@ -719,6 +734,8 @@ std::vector<WsRegion> workspace_regions(const flce_params* p, int pass) {
 }
 
 }  // namespace
+
+void flce::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void flce::set_error_detail(const char* msg) {
   snprintf(g_detail, sizeof(g_detail), "%s", msg);
@@ -869,9 +886,12 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   return v;
 }
 
-static int forward_finalize(const flce_params* p, uint8_t* ws, const FwdLayout& L, int nblk,
-                            float* loss, int64_t* num_correct, float* entropy_sum,
-                            cudaStream_t st) {
+// The merge's (or combine's) blocks-done counter: a word of the header, which
+// every forward entry zeroes before its first kernel.
+constexpr size_t kMergeDoneOffset = 136;
+
+static FinalizeArgs finalize_args(const flce_params* p, uint8_t* ws, const FwdLayout& L, int nblk,
+                                  float* loss, int64_t* num_correct, float* entropy_sum) {
   FinalizeArgs fz{};
   fz.nblk = nblk;
   fz.status = reinterpret_cast<const int*>(ws);
@@ -883,6 +903,15 @@ static int forward_finalize(const flce_params* p, uint8_t* ws, const FwdLayout& 
   fz.loss = p->reduction == FLCE_NONE ? nullptr : loss;
   fz.num_correct = num_correct;
   fz.entropy_sum = entropy_sum;
+  return fz;
+}
+
+// Reduced outputs of a call without rows (the merge, which otherwise writes
+// them, does not run).
+static int forward_finalize_empty(const flce_params* p, uint8_t* ws, const FwdLayout& L,
+                                  float* loss, int64_t* num_correct, float* entropy_sum,
+                                  cudaStream_t st) {
+  const FinalizeArgs fz = finalize_args(p, ws, L, 0, loss, num_correct, entropy_sum);
   return launch("flce_finalize", st, [&] { return launch_finalize(fz, st); });
 }
 
@@ -919,6 +948,7 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
     ma.vocab_start = 0;
     ma.vocab_total = p->V;
     ma.num_panels = fa.num_panels;
+    ma.lanes = L.lanes;
     ma.reduction = p->reduction;
     ma.ignore_index = p->ignore_index;
     ma.zeta = p->z_loss_multiplier;
@@ -932,12 +962,12 @@ int flce_forward(const flce_params* p, const void* hidden, const void* weight, c
     ma.blk_correct = reinterpret_cast<long long*>(ws + L.blk_correct);
     ma.blk_valid = reinterpret_cast<long long*>(ws + L.blk_valid);
     ma.status = reinterpret_cast<int*>(ws);
+    ma.done = reinterpret_cast<int*>(ws + kMergeDoneOffset);
+    ma.fin = finalize_args(p, ws, L, L.nblk, loss, num_correct, entropy_sum);
     v = launch("flce_merge", st, [&] { return launch_merge(ma, L.nblk, st); });
-    if (v != FLCE_OK) return v;
+    return debug_finish(ws, st, v);
   }
-  return debug_finish(ws, st,
-                      forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct,
-                                       entropy_sum, st));
+  return debug_finish(ws, st, forward_finalize_empty(p, ws, L, loss, num_correct, entropy_sum, st));
 }
 
 int flce_forward_partial(const flce_params* p, const void* hidden, const void* weight,
@@ -1014,12 +1044,12 @@ int flce_forward_combine(const flce_params* p, const flce_row_state* states, int
     ca.blk_correct = reinterpret_cast<long long*>(ws + L.blk_correct);
     ca.blk_valid = reinterpret_cast<long long*>(ws + L.blk_valid);
     ca.status = reinterpret_cast<int*>(ws);
+    ca.done = reinterpret_cast<int*>(ws + kMergeDoneOffset);
+    ca.fin = finalize_args(p, ws, L, L.nblk, loss, num_correct, entropy_sum);
     v = launch("flce_combine", st, [&] { return launch_combine(ca, L.nblk, st); });
-    if (v != FLCE_OK) return v;
+    return debug_finish(ws, st, v);
   }
-  return debug_finish(ws, st,
-                      forward_finalize(p, ws, L, N > 0 ? L.nblk : 0, loss, num_correct,
-                                       entropy_sum, st));
+  return debug_finish(ws, st, forward_finalize_empty(p, ws, L, loss, num_correct, entropy_sum, st));
 }
 
 int flce_backward(const flce_params* p, const void* hidden, const void* weight, const void* bias,
@@ -1047,11 +1077,14 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const size_t elem = tensor_path(p) ? 2 : 4;
-
+  cudaError_t e = cudaSuccess;
+  const bool no_rows = N == 0 || (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr);
+  // Without rows the status word is cleared here; otherwise the row
+  // coefficients kernel, which runs first, clears it with the tile counters.
+  if (no_rows && (e = cudaMemsetAsync(ws, 0, kHeader, st)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemsetAsync");
   if (grad_hidden == nullptr && grad_weight == nullptr && grad_bias == nullptr) return FLCE_OK;
   if (N == 0) {
     if (p->accumulate) return FLCE_OK;  // nothing to add
@@ -1079,6 +1112,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   float* ds_scale = p->dtype == FLCE_F16 ? reinterpret_cast<float*>(ws + kScaleOffset) : nullptr;
   ra.ds_scale = ds_scale;
   ra.status = status;
+  ra.zero = status;
+  ra.zero_words = static_cast<int>((L.cnt + L.cnt_bytes) / 4);
   v = launch("flce_row_coef", st, [&] { return launch_row_coef(ra, st); });
   if (v != FLCE_OK) return v;
 
@@ -1378,6 +1413,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.accumulate = (c > 0 || p->accumulate) ? 1 : 0;
         ga.k_splits = simt_k_splits(N, H, vc);
         ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.tile_count = reinterpret_cast<int*>(ws + L.cnt);
         ga.status = status;
         ga.r_c = r_gh;
         ga.r_part = r_dh;
@@ -1439,6 +1475,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         // the full chunk so that the workspace holds every chunk's partials
         ga.k_splits = simt_k_splits(L.chunk, H, V);
         ga.part = reinterpret_cast<float*>(ws + L.dh_part);
+        ga.tile_count = reinterpret_cast<int*>(ws + L.cnt);
         ga.status = status;
         ga.r_c = r_gh;
         ga.r_part = r_dh;

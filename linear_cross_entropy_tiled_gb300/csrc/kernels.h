@@ -49,7 +49,8 @@ constexpr int kTcSmemBytes = 1024 + kStages * kStageBytes + 8192 + 1024;
 // ---- fp32 SIMT path tile shape -------------------------------------------
 constexpr int kSimtTile = 64;        // 64 x 64 logit tiles
 constexpr int kSimtPanelCols = 256;  // widest partial-state panel of the fp32 forward (columns)
-constexpr int kSimtThreads = 256;
+constexpr int kSimtThreads = 128;
+constexpr int kSimtSplitTiles = 256;  // K-split SIMT GEMMs have fewer output tiles than this
 
 // Per (panel, row) partial state of the online log-sum-exp:
 // x = running max m, y = sum exp(z - m), z = sum z exp(z - m), w = argmax (int bits).
@@ -99,12 +100,31 @@ struct FwdArgs {
   DevRegion r_partials, r_zt;
 };
 
+struct FinalizeArgs {
+  int nblk, reduction;
+  const int* status;           // kDevErrTimeout set: loss and entropy NaN, num_correct -1
+  const double* blk_loss;
+  const double* blk_ent;
+  const long long* blk_correct;
+  const long long* blk_valid;
+  float* loss;                 // [1] for sum/mean, nullptr for none
+  int64_t* num_correct;        // nullable
+  float* entropy_sum;          // nullable
+};
+
+// The merge's blocks count themselves on `done` (a zeroed word of the
+// workspace header) after storing their block sums; the last one to arrive
+// sums all blocks' sums in block order and writes the reduced outputs, as
+// finalize_kernel does, so the forward needs no separate finalize launch.
+// done == nullptr: the block sums are left for finalize_kernel.
+
 // A forward whose bounded wait expired skipped some partial-state stores, so
 // the merge would combine whatever the workspace held before. merge_kernel
 // reads the status word first (the stream orders it after the forward) and
 // then writes NaN to every lse and loss instead.
 struct MergeArgs {
   int N, V, num_panels, reduction;
+  int lanes;                   // threads per row (a power of two <= 32); the grid covers N x lanes
   long long vocab_start, vocab_total;   // shard placement; vocab_total = V when not sharded
   long long ignore_index;
   float zeta;
@@ -118,6 +138,8 @@ struct MergeArgs {
   long long* blk_correct;
   long long* blk_valid;
   int* status;
+  int* done;                   // nullable: blocks-done counter, zero at launch
+  FinalizeArgs fin;            // the reduced outputs, when done != nullptr
 };
 
 // Exported per-row state of one vocabulary shard (20 bytes): running max,
@@ -155,18 +177,8 @@ struct CombineArgs {
   long long* blk_correct;
   long long* blk_valid;
   int* status;
-};
-
-struct FinalizeArgs {
-  int nblk, reduction;
-  const int* status;           // kDevErrTimeout set: loss and entropy NaN, num_correct -1
-  const double* blk_loss;
-  const double* blk_ent;
-  const long long* blk_correct;
-  const long long* blk_valid;
-  float* loss;                 // [1] for sum/mean, nullptr for none
-  int64_t* num_correct;        // nullable
-  float* entropy_sum;          // nullable
+  int* done;                   // nullable: as in MergeArgs
+  FinalizeArgs fin;
 };
 
 // Backward per-row coefficients: x = s*gamma*(1 + 2 zeta lse), y = s*gamma,
@@ -182,6 +194,11 @@ struct RowCoefArgs {
   float4* coef;
   float* ds_scale;             // nullable: receives {S, 1/S}, S = 2^k with max |dlogits| * S <= 2^14
   int* status;
+  // The first words of the workspace (the header with the status word, then
+  // the tile counters of the K-split GEMMs), zeroed before anything else: the
+  // backward's first kernel does this in place of a memset.
+  int* zero;
+  int zero_words;
 };
 
 struct DsArgs {
@@ -296,10 +313,13 @@ struct SimtGemmArgs {
   int accumulate;              // 1: C += A B, 0: C = A B
   // k_splits > 1: split 0 of the K range writes C (adds to it when
   // accumulate); split s > 0 stores its fp32 product to part + (s - 1) * M * N
-  // ([M][N], row-major), and a second kernel adds those to C in split order.
-  // For outputs with few 64 x 64 tiles and a long K.
+  // ([M][N], row-major). Those are added to C in split order by the last of
+  // a tile's splits to finish when tile_count is given (one zeroed counter
+  // per 64 x 64 output tile, left zero again), else by a second kernel. For
+  // outputs with few 64 x 64 tiles and a long K.
   int k_splits;
   float* part;
+  int* tile_count;
   int* status;                 // nullable; receives kDevErrBounds (FLCE_DEBUG builds)
   DevRegion r_c, r_part;
 };
@@ -310,6 +330,10 @@ struct BiasReduceArgs {
   const float* bias_part;      // [nblk][V_pad]
   void* grad_bias;             // dtype of the pass
 };
+
+// Counts one kernel launch of this library (flce_launch_count); called after
+// every kernel launch statement.
+void note_launch();
 
 // tcgen05 / TMA kernels (bf16). `grid` is the number of CTA pairs.
 cudaError_t tc_max_active_pairs(int* pairs);

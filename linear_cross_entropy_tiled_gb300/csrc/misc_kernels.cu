@@ -1,7 +1,8 @@
 // Small kernels shared by both dtypes:
 //   merge       per-row merge of the vocabulary-panel partial states into
 //               lse, loss_i, entropy_i and correct_i, plus per-block sums;
-//   finalize    fixed-order sum of the block sums into the reduced outputs;
+//   finalize    fixed-order sum of the block sums into the reduced outputs
+//               (run by the last merge block to finish, or as its own kernel);
 //   row_coef    per-row backward coefficients (gamma with the reduction and
 //               the z-loss folded in);
 //   bias_reduce fixed-order sum of per-row-block grad_bias partials;
@@ -36,43 +37,122 @@ __device__ __forceinline__ Tv block_sum(Tv v, Tv* sh) {
   return r;  // valid in thread 0
 }
 
-// Merge of the online-softmax states of all vocabulary panels of one row, in
-// panel order (fused-linear-ce README, "Algorithm": the flash-attention style
-// rescaling). Panels are merged in increasing column order. A later panel
-// takes the argmax only with a strictly larger max, so ties keep the lowest
-// column index.
+// Fixed-order sum of the block sums (each thread a fixed strided subset, then
+// a fixed tree) into the reduced outputs. Called by every thread of one block.
+__device__ void finalize_block(const FinalizeArgs& a) {
+  __shared__ double sh_d[32];
+  __shared__ long long sh_i[32];
+  double l = 0.0, e = 0.0;
+  long long c = 0, v = 0;
+  for (int b = threadIdx.x; b < a.nblk; b += blockDim.x) {
+    // L2 loads: other blocks of the same launch may have written these
+    l += __ldcg(a.blk_loss + b);
+    e += __ldcg(a.blk_ent + b);
+    c += __ldcg(a.blk_correct + b);
+    v += __ldcg(a.blk_valid + b);
+  }
+  l = block_sum(l, sh_d);
+  e = block_sum(e, sh_d);
+  c = block_sum(c, sh_i);
+  v = block_sum(v, sh_i);
+  if (threadIdx.x == 0 && a.status != nullptr && (*a.status & kDevErrTimeout) != 0) {
+    if (a.loss != nullptr) *a.loss = NAN;
+    if (a.num_correct != nullptr) *a.num_correct = -1;
+    if (a.entropy_sum != nullptr) *a.entropy_sum = NAN;
+  } else if (threadIdx.x == 0) {
+    if (a.loss != nullptr) {
+      if (a.reduction == 0) {
+        *a.loss = static_cast<float>(l);
+      } else {
+        *a.loss = v > 0 ? static_cast<float>(l / static_cast<double>(v)) : NAN;
+      }
+    }
+    if (a.num_correct != nullptr) *a.num_correct = c;
+    if (a.entropy_sum != nullptr) *a.entropy_sum = static_cast<float>(e);
+  }
+}
+
+// After a block has stored its block sums: the last block of the grid to get
+// here runs finalize_block (threadfence-reduction pattern: each block makes
+// its stores visible before it counts itself, and the last one reads the
+// others' stores only after it has seen the full count).
+__device__ void finalize_if_last(int* done, const FinalizeArgs& fin) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  finalize_block(fin);
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) { finalize_block(a); }
+
+// Two online-softmax states of one row merged, `left` covering lower columns
+// than `right`: the right one takes the argmax only with a strictly larger
+// max, so ties keep the lowest column index. An empty right state (max
+// -inf: no panel) leaves the left one as it is.
+struct SoftmaxState {
+  float m, s, t;
+  int a;
+};
+
+__device__ __forceinline__ void merge_right(SoftmaxState& l, const SoftmaxState& r) {
+  if (r.m == -INFINITY) return;
+  if (r.m > l.m) {
+    const float f = expf(l.m - r.m);
+    l.s = fmaf(l.s, f, r.s);
+    l.t = fmaf(l.t, f, r.t);
+    l.m = r.m;
+    l.a = r.a;
+  } else {
+    const float f = expf(r.m - l.m);
+    l.s = fmaf(r.s, f, l.s);
+    l.t = fmaf(r.t, f, l.t);
+  }
+}
+
+// Merge of the online-softmax states of all vocabulary panels of one row
+// (fused-linear-ce README, "Algorithm": the flash-attention style
+// rescaling). `lanes` threads share a row: each merges a contiguous range of
+// panels in panel order, then the lanes combine in a fixed tree, lower panels
+// on the left. The order depends on the shape only, not on timing.
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
   __shared__ double sh_d[32];
   __shared__ long long sh_i[32];
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lanes = a.lanes;
+  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int i = static_cast<int>(g / lanes), lane = static_cast<int>(g % lanes);
   double loss_i = 0.0, ent_i = 0.0;
   long long corr = 0, valid = 0;
   const bool timed_out = (*a.status & kDevErrTimeout) != 0;
-  if (i < a.N && timed_out) {
+  SoftmaxState st{-INFINITY, 0.f, 0.f, 0};
+  if (i < a.N && !timed_out) {
+    const int p0 = static_cast<int>(static_cast<long long>(lane) * a.num_panels / lanes);
+    const int p1 = static_cast<int>(static_cast<long long>(lane + 1) * a.num_panels / lanes);
+    for (int p = p0; p < p1; ++p) {
+      const float4 q = a.partials[static_cast<size_t>(p) * a.N + i];
+      merge_right(st, SoftmaxState{q.x, q.y, q.z, __float_as_int(q.w)});
+    }
+  }
+  for (int o = 1; o < lanes; o <<= 1) {
+    SoftmaxState r;
+    r.m = __shfl_down_sync(0xffffffffu, st.m, o, lanes);
+    r.s = __shfl_down_sync(0xffffffffu, st.s, o, lanes);
+    r.t = __shfl_down_sync(0xffffffffu, st.t, o, lanes);
+    r.a = __shfl_down_sync(0xffffffffu, st.a, o, lanes);
+    if ((lane & (2 * o - 1)) == 0) merge_right(st, r);
+  }
+  if (i < a.N && lane == 0 && timed_out) {
     // The forward gave up before storing all of its partial states: no
     // output of this call may look like a result.
     a.lse[i] = NAN;
     loss_i = NAN;
     ent_i = NAN;
     if (a.loss_rows != nullptr) a.loss_rows[i] = NAN;
-  } else if (i < a.N) {
-    float M = -INFINITY, S = 0.f, Tt = 0.f;
-    int A = 0;
-    for (int p = 0; p < a.num_panels; ++p) {
-      const float4 st = a.partials[static_cast<size_t>(p) * a.N + i];
-      if (st.x > M) {
-        const float f = expf(M - st.x);
-        S = fmaf(S, f, st.y);
-        Tt = fmaf(Tt, f, st.z);
-        M = st.x;
-        A = __float_as_int(st.w);
-      } else {
-        const float f = expf(st.x - M);
-        S = fmaf(st.y, f, S);
-        Tt = fmaf(st.z, f, Tt);
-      }
-    }
-    const float lse = M + logf(S);
+  } else if (i < a.N && lane == 0) {
+    const float lse = st.m + logf(st.s);
     a.lse[i] = lse;
     const long long t = a.targets[i];
     float li = 0.f;
@@ -83,8 +163,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
         li = NAN;
       } else {
         li = lse - a.zt[i] + a.zeta * lse * lse;
-        ent_i = static_cast<double>(lse - Tt / S);
-        corr = (static_cast<long long>(A) + a.vocab_start == t) ? 1 : 0;
+        ent_i = static_cast<double>(lse - st.t / st.s);
+        corr = (static_cast<long long>(st.a) + a.vocab_start == t) ? 1 : 0;
       }
     }
     loss_i = li;
@@ -100,6 +180,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     a.blk_correct[blockIdx.x] = bc;
     a.blk_valid[blockIdx.x] = bv;
   }
+  if (a.done != nullptr) finalize_if_last(a.done, a.fin);
 }
 
 // Per-row state of one vocabulary shard: the panels of this call merged in
@@ -199,46 +280,19 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
     a.blk_correct[blockIdx.x] = bc;
     a.blk_valid[blockIdx.x] = bv;
   }
+  if (a.done != nullptr) finalize_if_last(a.done, a.fin);
 }
 
-__global__ void __launch_bounds__(256) finalize_kernel(const FinalizeArgs a) {
-  __shared__ double sh_d[32];
-  __shared__ long long sh_i[32];
-  double l = 0.0, e = 0.0;
-  long long c = 0, v = 0;
-  for (int b = threadIdx.x; b < a.nblk; b += blockDim.x) {
-    l += a.blk_loss[b];
-    e += a.blk_ent[b];
-    c += a.blk_correct[b];
-    v += a.blk_valid[b];
-  }
-  l = block_sum(l, sh_d);
-  e = block_sum(e, sh_d);
-  c = block_sum(c, sh_i);
-  v = block_sum(v, sh_i);
-  if (threadIdx.x == 0 && a.status != nullptr && (*a.status & kDevErrTimeout) != 0) {
-    if (a.loss != nullptr) *a.loss = NAN;
-    if (a.num_correct != nullptr) *a.num_correct = -1;
-    if (a.entropy_sum != nullptr) *a.entropy_sum = NAN;
-  } else if (threadIdx.x == 0) {
-    if (a.loss != nullptr) {
-      if (a.reduction == 0) {
-        *a.loss = static_cast<float>(l);
-      } else {
-        *a.loss = v > 0 ? static_cast<float>(l / static_cast<double>(v)) : NAN;
-      }
-    }
-    if (a.num_correct != nullptr) *a.num_correct = c;
-    if (a.entropy_sum != nullptr) *a.entropy_sum = static_cast<float>(e);
-  }
-}
 
-// One block. It first counts the valid rows (needed for the mean), then
-// writes the coefficients of every row.
+// One block, the backward's first kernel. It zeroes the workspace header and
+// tile counters, counts the valid rows (needed for the mean), then writes the
+// coefficients of every row.
 __global__ void __launch_bounds__(1024) row_coef_kernel(const RowCoefArgs a) {
   __shared__ long long sh_i[32];
   __shared__ long long s_valid;
   __shared__ float sh_max[32];
+  for (int i = threadIdx.x; i < a.zero_words; i += blockDim.x) a.zero[i] = 0;
+  __syncthreads();
   long long v = 0;
   for (int i = threadIdx.x; i < a.N; i += blockDim.x) v += (a.targets[i] != a.ignore_index) ? 1 : 0;
   v = block_sum(v, sh_i);
@@ -355,31 +409,37 @@ cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s) {
     split_reduce_kernel<__half><<<grid, 256, 0, s>>>(a);
   else
     split_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s) {
   merge_kernel<<<nblk, kMergeThreads, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_shard_state(const ShardStateArgs& a, cudaStream_t s) {
   shard_state_kernel<<<(a.N + 255) / 256, 256, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s) {
   combine_kernel<<<nblk, kMergeThreads, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
   finalize_kernel<<<1, 256, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s) {
   row_coef_kernel<<<1, 1024, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -428,11 +488,13 @@ cudaError_t launch_scale(const ScaleArgs& a, int sms, cudaStream_t s) {
     scale_kernel<__half><<<grid, 256, 0, s>>>(a);
   else
     scale_kernel<float><<<grid, 256, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s) {
   loss_reduce_kernel<<<1, 1024, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -444,6 +506,7 @@ cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t 
     bias_reduce_kernel<__half><<<grid, 256, 0, s>>>(a);
   else
     bias_reduce_kernel<float><<<grid, 256, 0, s>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 

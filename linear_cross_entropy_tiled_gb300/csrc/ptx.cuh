@@ -484,4 +484,20 @@ struct Elem<__half> {
   __device__ static __forceinline__ float to_float(__half x) { return __half2float(x); }
 };
 
+// ---------------------------------------------------------------- cp.async
+// Asynchronous 4-byte global -> shared copy through L1; with valid = false
+// nothing is read and the destination is zero-filled (src-size 0).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's committed groups are still in flight.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
 }  // namespace flce

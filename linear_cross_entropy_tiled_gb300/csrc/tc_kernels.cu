@@ -1150,6 +1150,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -1161,6 +1162,7 @@ cudaError_t launch_ds_t(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const 
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   k<<<2 * grid, kDsThreads, kTcSmemBytes, st>>>(tm_h, tm_w, a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -1171,6 +1173,7 @@ cudaError_t launch_gemm_t(const GemmOperand& op_a, const GemmOperand& op_b, cons
   cudaError_t e = set_smem_attr(k);
   if (e != cudaSuccess) return e;
   k<<<2 * grid, kTcThreads, kTcSmemBytes, st>>>(op_a.map, op_b.map, op_a.map3, op_b.map3, a);
+  note_launch();
   return cudaGetLastError();
 }
 }  // namespace

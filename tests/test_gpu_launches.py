@@ -1,0 +1,83 @@
+"""Kernels per call, and the in-kernel reductions that replaced separate launches.
+
+* The forward's merge sums the block sums itself (its last block to finish),
+  so a forward with rows launches the logit-tile kernel and the merge only.
+* The backward's first kernel (the row coefficients) clears the workspace
+  header and the fp32 tile counters, so the backward issues no memset.
+* The fp32 path's K-split contraction adds its split partials to grad_hidden
+  in the last split of each tile to finish, in split order, so no
+  split-reduce kernel follows it; its counters are left zero for the next
+  call, and repeated calls give the same bits.
+"""
+import pytest
+import torch
+
+import oracle
+from linear_cross_entropy_tiled_gb300 import _lib
+from linear_cross_entropy_tiled_gb300.functional import flce_backward, flce_forward
+from linear_cross_entropy_tiled_gb300.workloads import small_case
+
+from flce_check import assert_grad_close, assert_loss_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": _lib.FLCE_BF16, "f32": _lib.FLCE_F32}
+
+
+def kernels_of(fn):
+    torch.cuda.synchronize()
+    n0 = _lib.launch_count()
+    out = fn()
+    torch.cuda.synchronize()
+    return _lib.launch_count() - n0, out
+
+
+@pytest.mark.parametrize("dtype,N,H,V,bias", [
+    ("f32", 256, 512, 8192, False),   # the fp32 workload's sizes: 4 vocabulary chunks
+    ("f32", 130, 72, 600, True),
+    ("bf16", 600, 256, 4100, True),
+])
+def test_kernels_per_call(dtype, N, H, V, bias):
+    d = small_case(N, H, V, seed=3, dtype=dtype, bias=bias, ignore_frac=0.1)
+    h, w, b, t = to_device(d, dtype)
+    p = _lib.make_params(N=N, H=H, V=V, dtype=DT[dtype], has_bias=bias, reduction="sum")
+    n_fwd, (loss, lse, _, _, _) = kernels_of(lambda: flce_forward(p, h, w, t, b))
+    assert n_fwd == 2                         # logit tiles, merge (with the reduction)
+    gl = torch.ones(1, device="cuda")
+    n_bwd, _ = kernels_of(lambda: flce_backward(p, h, w, t, lse, gl, b))
+    # N < V: four vocabulary chunks, each dlogits and both contractions (one
+    # grid on the fp32 path); row coefficients first, grad_bias's sum last
+    per_chunk = 2 if dtype == "f32" else 3
+    assert n_bwd == 1 + per_chunk * 4 + (1 if bias else 0)
+
+
+@pytest.mark.parametrize("N,H,V,axis", [
+    (256, 512, 8192, "vocab"),    # grad_hidden: 32 tiles x 4 K splits per chunk
+    (200, 136, 3000, "rows"),     # grad_hidden K = V split per row chunk
+    (70, 64, 9000, "vocab"),      # ragged row tile, 4 K splits
+])
+def test_fp32_split_counters_reset_and_repeatable(N, H, V, axis):
+    d = small_case(N, H, V, seed=N, dtype="f32", bias=False, ignore_frac=0.1)
+    h, w, _, t = to_device(d, "f32")
+    p = _lib.make_params(N=N, H=H, V=V, dtype=_lib.FLCE_F32, reduction="sum",
+                         bwd_chunk_axis=axis, max_chunk=64 if axis == "rows" else 0)
+    loss, lse, _, _, _ = flce_forward(p, h, w, t)
+    ref = oracle.forward(d["hidden"], d["weight"], d["targets"], reduction="sum")
+    assert_loss_close(loss.item(), ref["loss"], "f32")
+    gl = torch.ones(1, device="cuda")
+    ws = torch.full((_lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD),), 0x7F, dtype=torch.uint8,
+                    device="cuda")   # counters start as garbage: the first kernel clears them
+    outs = []
+    for _ in range(3):
+        gh, gw, _, ws = flce_backward(p, h, w, t, lse, gl, workspace=ws)
+        torch.cuda.synchronize()
+        regions = {n: (o, s) for n, o, s in _lib.workspace_regions(p, _lib.FLCE_PASS_BACKWARD)}
+        o, s = regions["tile_counters"]
+        assert torch.count_nonzero(ws[o:o + s]).item() == 0
+        assert _lib.check_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+        outs.append((gh.clone(), gw.clone()))
+    for gh, gw in outs[1:]:
+        assert torch.equal(gh, outs[0][0]) and torch.equal(gw, outs[0][1])
+    rgh, rgw, _ = oracle.backward(d["hidden"], d["weight"], d["targets"], reduction="sum")
+    assert_grad_close(outs[0][0].cpu().numpy(), rgh, "f32", "grad_hidden")
+    assert_grad_close(outs[0][1].cpu().numpy(), rgw, "f32", "grad_weight")
