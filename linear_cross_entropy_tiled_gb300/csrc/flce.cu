@@ -355,10 +355,11 @@ struct BwdLayout {
 };
 
 // The fp32 path's K-split GEMMs count the finished splits of each output tile
-// in a region right after the header; the backward's first kernel zeroes both.
+// in a region right after the header, followed by the unit counter of the
+// persistent contraction grid; the backward's first kernel zeroes all of it.
 void place_counters(const flce_params* p, BwdLayout* L, size_t* o) {
   L->cnt = *o;
-  L->cnt_bytes = tensor_path(p) ? 0 : size_t(kSimtSplitTiles) * 4;
+  L->cnt_bytes = tensor_path(p) ? 0 : size_t(kSimtSplitTiles + kSimtSchedWords) * 4;
   if (L->cnt_bytes) *o = align_up(*o + L->cnt_bytes, 256);
 }
 
@@ -1438,7 +1439,10 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       // Both contractions of the chunk in one grid when both are wanted: each
       // alone is too small to fill the GPU at the sizes this path serves.
       if (grad_hidden && grad_weight)
-        v = launch("flce_grads_simt", st, [&] { return launch_gemm_simt2(gh_args, gw_args, st); });
+        v = launch("flce_grads_simt", st, [&] {
+          return launch_gemm_simt2(gh_args, gw_args,
+                                   reinterpret_cast<int*>(ws + L.cnt) + kSimtSplitTiles, st);
+        });
       else if (grad_hidden)
         v = launch("flce_grad_hidden_simt", st, [&] { return launch_gemm_simt(gh_args, st); });
       else if (grad_weight)

@@ -51,6 +51,7 @@ constexpr int kSimtTile = 64;        // 64 x 64 logit tiles
 constexpr int kSimtPanelCols = 256;  // widest partial-state panel of the fp32 forward (columns)
 constexpr int kSimtThreads = 128;
 constexpr int kSimtSplitTiles = 256;  // K-split SIMT GEMMs have fewer output tiles than this
+constexpr int kSimtSchedWords = 2;    // unit counter and finished-block count of a persistent SIMT grid
 
 // Per (panel, row) partial state of the online log-sum-exp:
 // x = running max m, y = sum exp(z - m), z = sum z exp(z - m), w = argmax (int bits).
@@ -368,7 +369,10 @@ cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cu
 cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s);
 // Two independent products in one launch (then each one's split reduction).
-cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, cudaStream_t s);
+// Both products in one grid. sched: nullable, two zeroed ints (left zero)
+// that make the grid persistent, taking (tile, split) units longest first.
+cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, int* sched,
+                              cudaStream_t s);
 
 // dtype-generic small kernels (dtype: 0 = f32, 1 = bf16, 2 = fp16)
 cudaError_t launch_merge(const MergeArgs& a, int nblk, cudaStream_t s);

@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG)
     ds_simt_kernel(const float* __restrict__ h, const float* __restrict__ w, const DsArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<KG>& sm = *reinterpret_cast<SimtSmem<KG>*>(smem_raw);
-  float (&G)[T][T + 1] = *reinterpret_cast<float (*)[T][T + 1]>(smem_raw + sizeof(SimtSmem<KG>));
+  // per-column sums for grad_bias: the tile's dlogits, staged in 16-byte pieces
+  float (&G)[T][T + 4] = *reinterpret_cast<float (*)[T][T + 4]>(smem_raw + sizeof(SimtSmem<KG>));
   const int c0 = blockIdx.x * T;
   const int rb = blockIdx.y;
   const int r0 = rb * T;  // local to the chunk
@@ -364,8 +365,10 @@ __global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG)
             g[jj] *= (1.f - zc * zc);
           }
         }
-        G[ty * 4 + i][tile_col(tx, 4 * half + jj)] = g[jj];
       }
+      if (a.bias_part != nullptr)
+        *reinterpret_cast<float4*>(&G[ty * 4 + i][tile_col(tx, 4 * half)]) =
+            make_float4(g[0], g[1], g[2], g[3]);
       if (row_ok && col0 < a.V) {
         float* const dst = ds + static_cast<size_t>(rl) * a.V_pad + col0;
         // four neighbouring columns: one 16-byte store when all are in the row
@@ -482,17 +485,40 @@ __global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG) gemm_simt_kernel(co
   gemm_simt_block<KG>(a, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// Two independent products in one grid: blocks [0, n1) compute the first,
-// the rest the second. The two contractions of a backward chunk are each too
-// small to fill the GPU alone; together they do.
+// Two independent products in one grid: units [0, n1) are the first
+// product's (tile, split) blocks, the rest the second's; each alone is too
+// small to fill the GPU at the sizes this path serves. With sched == nullptr
+// block b computes unit b. Otherwise the grid is persistent and takes units
+// in order from sched[0] (the host puts the product with the longer K per
+// unit first, so the long units start first and the short ones fill in);
+// sched[1] counts the blocks that have finished, and the last one zeroes
+// both for the next launch. Which block computes a unit does not change its
+// result.
 template <int KG>
-__global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG) gemm_simt2_kernel(const SimtGemmArgs a1,
-                                                                  const SimtGemmArgs a2, int n1) {
-  const bool first = static_cast<int>(blockIdx.x) < n1;
-  const SimtGemmArgs& a = first ? a1 : a2;
-  const int i = first ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - n1;
-  const int gx = (a.N + T - 1) / T, gy = (a.M + T - 1) / T;
-  gemm_simt_block<KG>(a, i % gx, (i / gx) % gy, i / (gx * gy));
+__global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG)
+    gemm_simt2_kernel(const SimtGemmArgs a1, const SimtGemmArgs a2, int n1, int n_units,
+                      int* sched) {
+  __shared__ int s_unit;
+  for (int it = 0;; ++it) {
+    if (threadIdx.x == 0)
+      s_unit = sched != nullptr ? atomicAdd(sched, 1)
+                                : (it == 0 ? static_cast<int>(blockIdx.x) : n_units);
+    __syncthreads();
+    const int u = s_unit;
+    __syncthreads();   // every thread has read s_unit before it changes
+    if (u >= n_units) break;
+    const bool first = u < n1;
+    const SimtGemmArgs& a = first ? a1 : a2;
+    const int i = first ? u : u - n1;
+    const int gx = (a.N + T - 1) / T, gy = (a.M + T - 1) / T;
+    gemm_simt_block<KG>(a, i % gx, (i / gx) % gy, i / (gx * gy));
+  }
+  if (sched != nullptr && threadIdx.x == 0 &&
+      atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    // every block is past its last fetch
+    sched[0] = 0;
+    sched[1] = 0;
+  }
 }
 
 // Split 0 of a K-split product has already written C (or added to it); this
@@ -521,13 +547,15 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 // the grid has at most two blocks per SM, so that few tiles still bring many
 // warps; otherwise one (128 threads, four blocks per SM), so that a larger
 // grid runs in one wave.
-int groups_for(long long blocks) {
+int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 0;
-  return blocks <= 2ll * sms ? 2 : 1;
+  return sms;
 }
+
+int groups_for(long long blocks) { return blocks <= 2ll * sm_count() ? 2 : 1; }
 
 template <int KG>
 cudaError_t launch_fwd_kg(const float* h, const float* w, const FwdArgs& a, cudaStream_t s) {
@@ -542,7 +570,7 @@ cudaError_t launch_fwd_kg(const float* h, const float* w, const FwdArgs& a, cuda
 template <int KG>
 cudaError_t launch_ds_kg(const float* h, const float* w, const DsArgs& a, dim3 grid,
                          cudaStream_t s) {
-  const size_t bytes = sizeof(SimtSmem<KG>) + sizeof(float) * T * (T + 1);
+  const size_t bytes = sizeof(SimtSmem<KG>) + sizeof(float) * T * (T + 4);
   cudaError_t e = set_smem(ds_simt_kernel<KG>, bytes);
   if (e != cudaSuccess) return e;
   ds_simt_kernel<KG><<<grid, KG * kSimtThreads, bytes, s>>>(h, w, a);
@@ -552,11 +580,11 @@ cudaError_t launch_ds_kg(const float* h, const float* w, const DsArgs& a, dim3 g
 
 template <int KG>
 cudaError_t launch_gemm2_kg(const SimtGemmArgs& a1, const SimtGemmArgs& a2, int n1, int n2,
-                            cudaStream_t s) {
+                            int grid, int* sched, cudaStream_t s) {
   const size_t bytes = sizeof(SimtSmem<KG>);
   cudaError_t e = set_smem(gemm_simt2_kernel<KG>, bytes);
   if (e != cudaSuccess) return e;
-  gemm_simt2_kernel<KG><<<n1 + n2, KG * kSimtThreads, bytes, s>>>(a1, a2, n1);
+  gemm_simt2_kernel<KG><<<grid, KG * kSimtThreads, bytes, s>>>(a1, a2, n1, n1 + n2, sched);
   note_launch();
   return cudaGetLastError();
 }
@@ -597,10 +625,26 @@ cudaError_t split_reduce_after(const SimtGemmArgs& a, cudaStream_t s) {
 }
 }  // namespace
 
-cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, cudaStream_t s) {
-  const int n1 = simt_blocks(a1), n2 = simt_blocks(a2);
-  cudaError_t e = groups_for(n1 + n2) == 2 ? launch_gemm2_kg<2>(a1, a2, n1, n2, s)
-                                           : launch_gemm2_kg<1>(a1, a2, n1, n2, s);
+cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, int* sched,
+                              cudaStream_t s) {
+  // K per unit: the longer units go first
+  auto unit_k = [](const SimtGemmArgs& a) {
+    return a.k_splits > 1 ? (a.K + a.k_splits - 1) / a.k_splits : a.K;
+  };
+  const bool swap = unit_k(a2) > unit_k(a1);
+  const SimtGemmArgs& p1 = swap ? a2 : a1;
+  const SimtGemmArgs& p2 = swap ? a1 : a2;
+  const int n1 = simt_blocks(p1), n2 = simt_blocks(p2);
+  cudaError_t e;
+  if (sched != nullptr) {
+    // persistent: two 256-thread blocks per SM
+    const int cap = 2 * sm_count();
+    const int grid = n1 + n2 < cap || cap < 1 ? n1 + n2 : cap;
+    e = launch_gemm2_kg<2>(p1, p2, n1, n2, grid, sched, s);
+  } else {
+    e = groups_for(n1 + n2) == 2 ? launch_gemm2_kg<2>(p1, p2, n1, n2, n1 + n2, nullptr, s)
+                                 : launch_gemm2_kg<1>(p1, p2, n1, n2, n1 + n2, nullptr, s);
+  }
   if (e != cudaSuccess) return e;
   if ((e = split_reduce_after(a1, s)) != cudaSuccess) return e;
   return split_reduce_after(a2, s);
