@@ -223,8 +223,9 @@ __global__ void __launch_bounds__(256) shard_state_kernel(const ShardStateArgs a
 }
 
 // Merge of the states of R vocabulary shards, in shard order, into lse,
-// loss_i, entropy_i and correct_i per row, plus per-block sums for
-// finalize_kernel. The shards must be given in increasing vocabulary order:
+// loss_i, entropy_i and correct_i per row, plus per-block sums, which the
+// last block to finish reduces (finalize_block). The shards must be given in
+// increasing vocabulary order:
 // a later shard takes the argmax only with a strictly larger max, so ties keep
 // the lowest global id. The target logit is the sum over shards; only the owning
 // shard contributes a nonzero value.
