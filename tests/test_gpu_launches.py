@@ -81,3 +81,29 @@ def test_fp32_split_counters_reset_and_repeatable(N, H, V, axis):
     rgh, rgw, _ = oracle.backward(d["hidden"], d["weight"], d["targets"], reduction="sum")
     assert_grad_close(outs[0][0].cpu().numpy(), rgh, "f32", "grad_hidden")
     assert_grad_close(outs[0][1].cpu().numpy(), rgw, "f32", "grad_weight")
+
+
+def test_fp32_large_grids_one_group_and_persistent_loop():
+    """fp32 at N=1200, H=136, V=20000 (vocabulary chunks of 5056 columns).
+
+    The forward (1501 units) and dlogits (1501 tiles) grids exceed two blocks
+    per SM, so they run the 128-thread single-group kernels; the two
+    contractions (285 + 237 units) run on the persistent grid of two blocks
+    per SM, each block taking several units. Everything against the oracle.
+    """
+    N, H, V = 1200, 136, 20000
+    d = small_case(N, H, V, seed=11, dtype="f32", bias=True, ignore_frac=0.1)
+    h, w, b, t = to_device(d, "f32")
+    kw = dict(reduction="mean", z_loss_multiplier=1e-3, softcap=20.0)
+    p = _lib.make_params(N=N, H=H, V=V, dtype=_lib.FLCE_F32, has_bias=True, **kw)
+    loss, lse, _, _, _ = flce_forward(p, h, w, t, b)
+    ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **kw)
+    assert_loss_close(loss.item(), ref["loss"], "f32")
+    gl = torch.ones(1, device="cuda")
+    gh, gw, gb, ws = flce_backward(p, h, w, t, lse, gl, b)
+    torch.cuda.synchronize()
+    assert _lib.check_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    rgh, rgw, rgb = oracle.backward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **kw)
+    assert_grad_close(gh.cpu().numpy(), rgh, "f32", "grad_hidden")
+    assert_grad_close(gw.cpu().numpy(), rgw, "f32", "grad_weight")
+    assert_grad_close(gb.cpu().numpy(), rgb, "f32", "grad_bias")
