@@ -467,8 +467,9 @@ const char* flce_last_error_detail(void);
 /*
  * Test hook for the bounded waits; not for production use. From this call on,
  * every forward pass launched from the calling host thread starves one TMA
- * pipeline stage: the even CTA of the first CTA pair arms the stage of K slice
- * `drop_kblock` of its first tile but never issues its loads, so the MMA's
+ * pipeline stage: the even CTA of the CTA pair that takes the first unit (row
+ * block 0, vocabulary tile 0) arms the stage of K slice `drop_kblock` of that
+ * tile but never issues its loads, so the MMA's
  * wait on it must expire. wait_ms > 0 shortens every wait of those launches
  * to that many milliseconds (0 keeps the default of 4 s). The kernel then
  * records FLCE_ERR_TIMEOUT in the status word, stops its other roles, drains

@@ -854,6 +854,9 @@ static int forward_tiles(const flce_params* p, const void* hidden, const void* w
   // stage is starved and every wait has the default limit.
   fa.wait_ns = g_test_wait_ns > 0 ? g_test_wait_ns : kWaitLimitNs;
   fa.drop_kb = g_test_drop_kb;
+  // the header's GEMM counters, zeroed at every forward entry (the forward
+  // launches no GEMM)
+  fa.tile_counter = reinterpret_cast<int*>(ws + kTileCounterOffset);
   int v;
   if (tensor_path(p)) {
     const CUtensorMapDataType dt = map_type(p);
@@ -1134,6 +1137,9 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
   da.bias_ld = static_cast<int>(L.V_pad);
   da.tgt_base = 0;
   da.status = status;
+  // the header's unit counters, zeroed by the row coefficients kernel and left
+  // zero by every launch that takes units from them
+  da.tile_counter = tensor_path(p) ? reinterpret_cast<int*>(ws + kTileCounterOffset) : nullptr;
   da.r_ds = DevRegion{ws + L.ds, L.ds_bytes};
   da.r_ds_t = DevRegion{ws + L.ds_t, L.ds_t_bytes};
   da.r_bias = DevRegion{ws + L.bias_part, L.bias_bytes};

@@ -88,9 +88,14 @@ struct FwdArgs {
   int group_blocks;
   long long vocab_start;       // global id of this call's first vocabulary row
   unsigned long long wait_ns;  // limit of every bounded wait (kWaitLimitNs unless testing)
-  int drop_kb;                 // fault injection, off (-1) unless testing: the even CTA of pair 0
-                               // arms but never issues the loads of this K slice of its first tile
+  int drop_kb;                 // fault injection, off (-1) unless testing: the even CTA of the
+                               // pair that has unit 0 arms but never issues the loads of this
+                               // K slice of that unit's first tile
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;
+  // Dynamic schedule, as GemmArgs::tile_counter: two zeroed ints (left zero)
+  // from which the pairs take (panel, pair block) units in order; nullptr:
+  // round-robin.
+  int* tile_counter;
   float scale, softcap, inv_softcap;
   const void* bias;            // dtype of the pass, or nullptr
   const int64_t* targets;
@@ -204,6 +209,7 @@ struct RowCoefArgs {
 
 struct DsArgs {
   int rows, row0, H, V, V_pad;
+  int* tile_counter;           // dynamic schedule as in FwdArgs; nullptr: round-robin
   ClockRecord* clk;            // nullable (profiling)
   int group_blocks;
   int n_blocks, v_tiles, panel_tiles, num_panels, num_units;

@@ -57,12 +57,16 @@ struct TcSmem {
   uint64_t* q_full;      // kQueue: the slot holds a unit (in each CTA)
   uint64_t* q_empty;     // kQueue: every consumer has read it (even CTA only)
   int* q_unit;           // kQueue
+  int* ep_unit;          // 2: a unit passed from the dlogits kernel's queue reader to its epilogue warps
 };
 
 constexpr int kQueue = 4;
 // Readers of each queue slot: the MMA thread, the odd CTA's producer, and the
-// four epilogue warps of each CTA.
+// four epilogue warps of each CTA (the GEMM and the forward), or one epilogue
+// warp of each CTA (the dlogits kernel, whose epilogue warps share units
+// through shared memory).
 constexpr int kQueueReaders = 2 + 2 * 4;
+constexpr int kDsQueueReaders = 2 + 2 * 1;
 
 __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
   TcSmem s;
@@ -82,13 +86,15 @@ __device__ __forceinline__ TcSmem carve_smem(uint8_t* raw) {
   s.q_full = s.mma_done + 2;   // after tmem_slot and abort (8 bytes)
   s.q_empty = s.q_full + kQueue;
   s.q_unit = reinterpret_cast<int*>(s.q_empty + kQueue);
+  s.ep_unit = s.q_unit + kQueue;
   return s;
 }
 
 // Barriers and TMEM of both CTAs of the pair. The cluster barrier at the end
 // makes every barrier initialised before any remote arrive or
 // remote-signalling TMA can target it.
-__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_warps = 4) {
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_warps = 4,
+                                             int queue_readers = kQueueReaders) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);   // even CTA: its own arrive.expect_tx
@@ -101,7 +107,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& s, int warp, int epi_
     mbar_init(s.mma_done, 1);
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], kQueueReaders);
+      mbar_init(&s.q_empty[i], queue_readers);
     }
     *s.abort = 0;
     fence_mbar_init();
@@ -442,6 +448,58 @@ __device__ __forceinline__ void fwd_chunk(const uint32_t (&v)[32], const FwdArgs
   m = mnew;
 }
 
+// ==================================================== dynamic schedule
+// Units handed out by an atomic counter instead of round-robin (the prior
+// art's tile semaphore, quack diff, GemmWrapperBase): a pair that finishes
+// early takes the next unit. Only the even CTA's producer thread touches the
+// counter; it publishes each unit (or -1 when none is left) through a ring of
+// kQueue shared-memory slots, written in both CTAs of the pair, and every
+// other role of both CTAs reads the units from its own CTA's copy. A slot is
+// reused only after all kQueueReaders readers have released it. Every wait
+// is bounded (WaitGuard).
+struct TileQueue {
+  const TcSmem& s;
+  const WaitGuard& g;
+  uint32_t rank;
+  int i = 0;   // units published or read so far
+
+  // Even CTA's producer: the next unit, published to both CTAs; -1 when the
+  // units are exhausted; -2 if a wait gave up.
+  __device__ __forceinline__ int publish(int* counter, int units) {
+    const int slot = i % kQueue;
+    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
+    if (!mbar_wait_cluster(&s.q_empty[slot], ph ^ 1u, g)) return -2;
+    int u = atomicAdd(counter, 1);
+    if (u >= units) u = -1;
+    s.q_unit[slot] = u;
+    st_shared_cluster_u32(mapa_shared(smem_u32(&s.q_unit[slot]), 1), static_cast<uint32_t>(u));
+    mbar_arrive(&s.q_full[slot]);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_full[slot]), 1));
+    ++i;
+    return u;
+  }
+
+  // Any other role: the next unit from this CTA's slot (-1: none left, -2: a
+  // wait gave up). Each reader then calls release() once it has the value;
+  // in a warp that reads together, one lane releases after a __syncwarp.
+  __device__ __forceinline__ int read() {
+    const int slot = i % kQueue;
+    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
+    const bool ok = rank == 0 ? mbar_wait(&s.q_full[slot], ph, g)
+                              : mbar_wait_cluster(&s.q_full[slot], ph, g);
+    if (!ok) return -2;
+    return *reinterpret_cast<volatile int*>(&s.q_unit[slot]);
+  }
+  __device__ __forceinline__ void release() {
+    const int slot = i % kQueue;
+    if (rank == 0)
+      mbar_arrive(&s.q_empty[slot]);
+    else
+      mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_empty[slot]), 0));
+    ++i;
+  }
+};
+
 template <typename T, bool kBias, bool kSoftcap, bool kMetrics>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
@@ -456,14 +514,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const WaitGuard g{a.status, s.abort, a.wait_ns};
   const int kblocks = (a.H + kBK - 1) / kBK;
 
+  // Units (panel, pair block) round-robin, or with a tile counter from the
+  // dynamic schedule: the even CTA's producer takes them off the counter and
+  // every other role reads them from the queue, in the same order. Taken in
+  // order, the units in flight stay a window of consecutive units, so the
+  // pairs keep working on the same few W panels however far apart their
+  // progress drifts.
+  const bool dynamic = a.tile_counter != nullptr;
+  auto for_each_unit = [&](auto&& f) {
+    if (!dynamic) {
+      for (int u = pair; u < a.num_units; u += npairs) f(u);
+      return;
+    }
+    TileQueue q{s, g, rank};
+    if (warp == 0 && rank == 0) {
+      while (true) {
+        const int u = q.publish(a.tile_counter, a.num_units);
+        if (u == -1) {
+          // the last pair to run out leaves the counters at zero for the next launch
+          if (atomicAdd(a.tile_counter + 1, 1) == npairs - 1) {
+            a.tile_counter[0] = 0;
+            a.tile_counter[1] = 0;
+          }
+        }
+        if (u < 0) return;
+        f(u);
+      }
+    }
+    while (true) {   // the odd CTA's producer, or the MMA thread
+      const int u = q.read();
+      if (u == -2) return;
+      q.release();
+      if (u < 0) return;
+      f(u);
+    }
+  };
   auto for_each_tile = [&](auto&& f) {
-    for (int u = pair; u < a.num_units; u += npairs) {
+    for_each_unit([&](int u) {
       int panel, nb;
       decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
       for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
-    }
+    });
   };
 
   if (warp == 0) {
@@ -476,9 +569,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     [&](int nb, int vt, int kb, uint8_t* da, uint8_t* db, uint32_t bar) {
                       // Fault injection for the bounded-wait test: the stage is armed
                       // but its loads never come, so the MMA's wait must time out.
-                      if (kb == a.drop_kb && pair == 0 && rank == 0 &&
-                          nb == 0 && vt == 0)
-                        return;
+                      // (nb, vt) = (0, 0) is the first tile of unit 0.
+                      if (kb == a.drop_kb && rank == 0 && nb == 0 && vt == 0) return;
                       tma_load_2d_pair(da, &tm_h, bar, kb * kBK, nb * kPairM + rank * kBM, pol_h);
                       tma_load_2d_pair(db, &tm_w, bar, kb * kBK, vt * kBN + rank * kBNHalf, pol_w);
                     });
@@ -493,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool dead = false;
-    for (int u = pair; u < a.num_units; u += npairs) {
+    auto unit_epilogue = [&](int u) {
       int panel, nb;
       decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int row = nb * kPairM + static_cast<int>(rank) * kBM + r;
@@ -533,6 +625,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       float4* const dst = a.partials + static_cast<size_t>(panel) * a.N + row;
       if (row_ok && !dead && store_allowed(dst, 16, a.r_partials, a.status))
         *dst = make_float4(m, ssum, tsum, __int_as_float(amax));
+    };
+    if (!dynamic) {
+      for (int u = pair; u < a.num_units; u += npairs) unit_epilogue(u);
+    } else {
+      TileQueue q{s, g, rank};
+      while (true) {
+        const int u = q.read();   // the same value in every lane that got one
+        if (!__all_sync(kFull, u != -2)) break;
+        __syncwarp();
+        if (lane == 0) q.release();
+        else ++q.i;
+        if (u < 0) break;
+        unit_epilogue(u);
+      }
     }
   }
   tc_teardown(tmem, warp);
@@ -639,20 +745,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const TcSmem s = carve_smem(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tmem = tc_setup(s, warp, 8);
+  const uint32_t tmem = tc_setup(s, warp, 8, kDsQueueReaders);
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd CTA
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const WaitGuard g{a.status, s.abort};
   const int kblocks = (a.H + kBK - 1) / kBK;
 
+  // Units round-robin, or in order from the dynamic schedule, as in the
+  // forward kernel.
+  const bool dynamic = a.tile_counter != nullptr;
+  auto for_each_unit = [&](auto&& f) {
+    if (!dynamic) {
+      for (int u = pair; u < a.num_units; u += npairs) f(u);
+      return;
+    }
+    TileQueue q{s, g, rank};
+    if (warp == 0 && rank == 0) {
+      while (true) {
+        const int u = q.publish(a.tile_counter, a.num_units);
+        if (u == -1) {
+          // the last pair to run out leaves the counters at zero for the next launch
+          if (atomicAdd(a.tile_counter + 1, 1) == npairs - 1) {
+            a.tile_counter[0] = 0;
+            a.tile_counter[1] = 0;
+          }
+        }
+        if (u < 0) return;
+        f(u);
+      }
+    }
+    while (true) {   // the odd CTA's producer, or the MMA thread
+      const int u = q.read();
+      if (u == -2) return;
+      q.release();
+      if (u < 0) return;
+      f(u);
+    }
+  };
   auto for_each_tile = [&](auto&& f) {
-    for (int u = pair; u < a.num_units; u += npairs) {
+    for_each_unit([&](int u) {
       int panel, nb;
       decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int vt0 = panel * a.panel_tiles;
       const int vt1 = min(a.v_tiles, vt0 + a.panel_tiles);
       for (int vt = vt0; vt < vt1; ++vt) f(nb, vt);
-    }
+    });
   };
 
   if (warp == 0) {
@@ -683,7 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     uint32_t acc_phase = 0;
     bool dead = false;
     int tile_par = 0;
-    for (int u = pair; u < a.num_units; u += npairs) {
+    auto unit_epilogue = [&](int u) {
       int panel, nb;
       decode_unit(u, a.n_blocks, a.group_blocks, a.num_panels, panel, nb);
       const int blk_local = nb * 2 + static_cast<int>(rank);  // this CTA's 128-row block
@@ -756,63 +893,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
+    };
+    if (!dynamic) {
+      for (int u = pair; u < a.num_units; u += npairs) unit_epilogue(u);
+    } else {
+      // Warp 2 reads the queue for this CTA's eight epilogue warps and passes
+      // each unit (or the end: -1, or -2 after a wait gave up) through
+      // alternating shared slots, so that all eight stop at the same unit and
+      // the per-tile barrier of the bias sums stays balanced. A slot is
+      // rewritten two units later, after every warp has passed the barrier
+      // that follows its read of the unit in between.
+      TileQueue q{s, g, rank};
+      for (int it = 0;; ++it) {
+        if (warp == 2) {
+          int u = q.read();
+          u = __all_sync(kFull, u != -2) ? u : -2;
+          __syncwarp();
+          if (u != -2) {
+            if (lane == 0) q.release();
+            else ++q.i;
+          }
+          if (lane == 0) s.ep_unit[it & 1] = u;
+        }
+        named_barrier(2, 256);
+        const int u = *reinterpret_cast<volatile int*>(&s.ep_unit[it & 1]);
+        if (u < 0) break;
+        unit_epilogue(u);
+      }
     }
   }
   tc_teardown(tmem, warp);
   clock_start.finish(a.clk);
 }
 
-// ==================================================== dynamic schedule
-// Units handed out by an atomic counter instead of round-robin (the prior
-// art's tile semaphore, quack diff, GemmWrapperBase): a pair that finishes
-// early takes the next unit. Only the even CTA's producer thread touches the
-// counter; it publishes each unit (or -1 when none is left) through a ring of
-// kQueue shared-memory slots, written in both CTAs of the pair, and every
-// other role of both CTAs reads the units from its own CTA's copy. A slot is
-// reused only after all kQueueReaders readers have released it. Every wait
-// is bounded (WaitGuard).
-struct TileQueue {
-  const TcSmem& s;
-  const WaitGuard& g;
-  uint32_t rank;
-  int i = 0;   // units published or read so far
-
-  // Even CTA's producer: the next unit, published to both CTAs; -1 when the
-  // units are exhausted; -2 if a wait gave up.
-  __device__ __forceinline__ int publish(int* counter, int units) {
-    const int slot = i % kQueue;
-    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
-    if (!mbar_wait_cluster(&s.q_empty[slot], ph ^ 1u, g)) return -2;
-    int u = atomicAdd(counter, 1);
-    if (u >= units) u = -1;
-    s.q_unit[slot] = u;
-    st_shared_cluster_u32(mapa_shared(smem_u32(&s.q_unit[slot]), 1), static_cast<uint32_t>(u));
-    mbar_arrive(&s.q_full[slot]);
-    mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_full[slot]), 1));
-    ++i;
-    return u;
-  }
-
-  // Any other role: the next unit from this CTA's slot (-1: none left, -2: a
-  // wait gave up). Each reader then calls release() once it has the value;
-  // in a warp that reads together, one lane releases after a __syncwarp.
-  __device__ __forceinline__ int read() {
-    const int slot = i % kQueue;
-    const uint32_t ph = static_cast<uint32_t>(i / kQueue) & 1u;
-    const bool ok = rank == 0 ? mbar_wait(&s.q_full[slot], ph, g)
-                              : mbar_wait_cluster(&s.q_full[slot], ph, g);
-    if (!ok) return -2;
-    return *reinterpret_cast<volatile int*>(&s.q_unit[slot]);
-  }
-  __device__ __forceinline__ void release() {
-    const int slot = i % kQueue;
-    if (rank == 0)
-      mbar_arrive(&s.q_empty[slot]);
-    else
-      mbar_arrive_cluster(mapa_shared(smem_u32(&s.q_empty[slot]), 0));
-    ++i;
-  }
-};
 
 // ========================================================= plain GEMM
 // D = A B with fp32 accumulation; the two gradient contractions. Units
