@@ -1258,6 +1258,10 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.acc_scale = acc_scale;
         ga.status = status;
         ga.r_out = r_gw;
+        // h (64 MB at H = 4096, N = 8192) is read by every wave of tiles; the
+        // transposed dlogits stream through once
+        ga.a_evict_first = 1;
+        ga.b_evict_last = 1;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });

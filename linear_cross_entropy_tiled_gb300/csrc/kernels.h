@@ -277,6 +277,10 @@ struct GemmArgs {
   // [0] hands out units in order, [1] counts the pairs that have finished
   // taking units. nullptr: every pair takes units u = pair, pair + npairs, ...
   int* tile_counter;
+  // L2 policy of the operand loads: 1 marks A's lines evict-first (a stream
+  // read once) or B's evict-last (an operand every tile of a wave re-reads);
+  // 0 leaves the normal policy.
+  int a_evict_first, b_evict_last;
 };
 
 // dst[i] = src[i] * (*scale), i < count, in the element type (dtype 0 fp32,

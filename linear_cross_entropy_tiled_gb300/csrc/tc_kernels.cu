@@ -1014,7 +1014,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_b);
       if (a_atoms > 0) tma_prefetch_desc(&tm_a3);
       if (b_atoms > 0) tma_prefetch_desc(&tm_b3);
-      const uint64_t pol = l2_policy_evict_normal();
+      const uint64_t pol_n = l2_policy_evict_normal();
+      const uint64_t pol_a = a.a_evict_first ? l2_policy_evict_first() : pol_n;
+      const uint64_t pol_b = a.b_evict_last ? l2_policy_evict_last() : pol_n;
       const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
       producer_role(s, g, kblocks_of, rank == 0, for_each_tile,
                     [&](int ta, int nt, int kb_rel, uint8_t* da, uint8_t* db, uint32_t bar) {
@@ -1026,25 +1028,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                         // this CTA's 128 rows of M, one 64 x 64 box each
                         const int at = m0 >> 6;
                         if (at + 2 <= a_atoms) {
-                          tma_load_3d_pair(da, &tm_a3, bar, 0, k0, at, pol);
+                          tma_load_3d_pair(da, &tm_a3, bar, 0, k0, at, pol_a);
                         } else {
-                          tma_load_2d_pair(da, &tm_a, bar, m0, k0, pol);
-                          tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, k0, pol);
+                          tma_load_2d_pair(da, &tm_a, bar, m0, k0, pol_a);
+                          tma_load_2d_pair(da + 8192, &tm_a, bar, m0 + 64, k0, pol_a);
                         }
                       } else {
-                        tma_load_2d_pair(da, &tm_a, bar, k0, m0, pol);
+                        tma_load_2d_pair(da, &tm_a, bar, k0, m0, pol_a);
                       }
                       if (b_mn) {
                         // [K rows][N cols] in memory: two atoms cover this CTA's 128 columns
                         const int at = n0 >> 6;
                         if (at + 2 <= b_atoms) {
-                          tma_load_3d_pair(db, &tm_b3, bar, 0, k0, at, pol);
+                          tma_load_3d_pair(db, &tm_b3, bar, 0, k0, at, pol_b);
                         } else {
-                          tma_load_2d_pair(db, &tm_b, bar, n0, k0, pol);
-                          tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, k0, pol);
+                          tma_load_2d_pair(db, &tm_b, bar, n0, k0, pol_b);
+                          tma_load_2d_pair(db + 8192, &tm_b, bar, n0 + 64, k0, pol_b);
                         }
                       } else {
-                        tma_load_2d_pair(db, &tm_b, bar, k0, n0, pol);
+                        tma_load_2d_pair(db, &tm_b, bar, k0, n0, pol_b);
                       }
                     });
     }
