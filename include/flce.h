@@ -488,7 +488,9 @@ uint64_t flce_launch_count(void);
  * bracketed by two CUDA events, and each tensor-core launch also sums its
  * CTAs' SM clock cycles and elapsed nanoseconds into a record of a fixed
  * 4096-entry array in the library's static device memory (no allocation;
- * launches past the 4096th before a read get no record).
+ * launches past the 4096th before a read get no record; the first profiled
+ * launch after a read zeroes the whole array on its stream, and a launch on
+ * another stream zeroes its own record).
  * flce_profiling_read synchronises those events. It fills up to `max`
  * records, in first-launch order, with the kernel name, the number of
  * launches, their total duration in milliseconds and their mean SM clock in

@@ -151,9 +151,13 @@ std::vector<cudaEvent_t> g_pool;
 std::vector<double> g_cycles, g_clock_ns, g_mma_cycles, g_mma_wait_ops, g_mma_wait_acc;
 ClockRecord* g_clock_base[64] = {};
 int g_clock_next[64] = {};
+cudaStream_t g_clock_stream[64] = {};   // stream that zeroed the array for this read epoch
 thread_local ClockRecord* g_cur_clk = nullptr;   // record of the launch being issued
 
-// A zeroed clock record on device `dev` for the next launch, or nullptr.
+// A zeroed clock record on device `dev` for the next launch, or nullptr. The
+// first record of a read epoch zeroes the whole array once, on the launching
+// stream, so that the timed launches are not interleaved with a memset each;
+// a launch on another stream zeroes its own record.
 ClockRecord* take_clock_record(int dev, cudaStream_t s, int* slot) {
   *slot = -1;
   if (dev < 0 || dev >= 64 || g_clock_next[dev] >= kClockSlots) return nullptr;
@@ -163,7 +167,14 @@ ClockRecord* take_clock_record(int dev, cudaStream_t s, int* slot) {
     g_clock_base[dev] = static_cast<ClockRecord*>(p);
   }
   ClockRecord* r = g_clock_base[dev] + g_clock_next[dev];
-  if (cudaMemsetAsync(r, 0, sizeof(ClockRecord), s) != cudaSuccess) return nullptr;
+  if (g_clock_next[dev] == 0) {
+    if (cudaMemsetAsync(g_clock_base[dev], 0, sizeof(ClockRecord) * kClockSlots, s) != cudaSuccess)
+      return nullptr;
+    g_clock_stream[dev] = s;
+  } else if (s != g_clock_stream[dev] &&
+             cudaMemsetAsync(r, 0, sizeof(ClockRecord), s) != cudaSuccess) {
+    return nullptr;
+  }
   *slot = g_clock_next[dev]++;
   return r;
 }
