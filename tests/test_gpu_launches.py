@@ -107,3 +107,37 @@ def test_fp32_large_grids_one_group_and_persistent_loop():
     assert_grad_close(gh.cpu().numpy(), rgh, "f32", "grad_hidden")
     assert_grad_close(gw.cpu().numpy(), rgw, "f32", "grad_weight")
     assert_grad_close(gb.cpu().numpy(), rgb, "f32", "grad_bias")
+
+
+def test_profiling_records_per_kernel():
+    """flce_profiling_read: per-kernel launch counts, durations, clocks and MMA wait shares.
+
+    Two read epochs in a row: each read returns only the launches since the
+    previous one, and the clock records (zeroed once per epoch) give a clock
+    within the GPU's range for every tensor-core kernel.
+    """
+    N, H, V = 1024, 512, 9000
+    d = small_case(N, H, V, seed=21, dtype="bf16", bias=True, ignore_frac=0.05)
+    h, w, b, t = to_device(d, "bf16")
+    p = _lib.make_params(N=N, H=H, V=V, dtype=_lib.FLCE_BF16, has_bias=True, reduction="mean")
+    gl = torch.ones(1, device="cuda")
+    _lib.profiling_read()   # drop anything pending
+    for steps in (1, 3):
+        _lib.profiling_enable(True)
+        for _ in range(steps):
+            loss, lse, _, _, _ = flce_forward(p, h, w, t, b)
+            flce_backward(p, h, w, t, lse, gl, b)
+        _lib.profiling_enable(False)
+        recs = {r[0]: r for r in _lib.profiling_read()}
+        # forward: tiles + merge; backward: row coefficients, 4 x (dlogits, two GEMMs), bias sums
+        assert recs["flce_fwd_tc"][1] == steps and recs["flce_merge"][1] == steps
+        assert recs["flce_dlogits_tc"][1] == 4 * steps
+        assert recs["flce_grad_hidden_tc"][1] == 4 * steps
+        assert recs["flce_grad_weight_tc"][1] == 4 * steps
+        for name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
+            _, n, ms, mhz, (w_ops, w_acc) = recs[name]
+            assert ms > 0.0, name
+            assert 300.0 < mhz < 2600.0, (name, mhz)
+            assert 0.0 <= w_ops <= 1.0 and 0.0 <= w_acc <= 1.0, (name, w_ops, w_acc)
+        assert recs["flce_merge"][3] == 0.0   # the small kernels keep no clock record
+    assert _lib.profiling_read() == []
