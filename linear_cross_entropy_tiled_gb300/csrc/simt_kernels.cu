@@ -9,7 +9,10 @@
 // arithmetic differs. Speed is secondary to the 1e-5 accuracy bar; the work is
 // spread over enough blocks for small problems (forward panels of 64 to 256
 // columns, vocabulary chunks over all rows in the backward, and a fixed-order
-// K split for grad_hidden, whose output is small).
+// K split for grad_hidden, whose output is small). Every kernel multiplies
+// 64 x 64 tiles with 4 x 8 outputs per thread from operand slices that
+// cp.async brings into a shared-memory ring (tile_product); the backward's
+// two contractions share one persistent grid.
 #include <math.h>
 
 #include "kernels.h"
