@@ -359,10 +359,12 @@ struct BwdLayout {
   int64_t chunk, V_pad;     // rows (or columns) per chunk
   int64_t ds_ld;            // row stride of the dlogits buffer, in elements
   int64_t ds_t_ld;          // row stride of the transposed dlogits buffer (tensor path)
+  int64_t ht_ld;            // row stride of the transposed hidden (tensor path, vocabulary chunks)
+  bool wt;                  // grad_weight computed transposed, from h^T and the row-major dlogits
   int nchunks, rowblk, n_rowblocks;
-  size_t cnt, coef, ds, ds_t, dw, dh_part, bias_part, total;
+  size_t cnt, coef, ds, ds_t, ht, dw, dh_part, bias_part, total;
   // bytes the kernels may write in each region (0: the region is absent)
-  size_t cnt_bytes, coef_bytes, ds_bytes, ds_t_bytes, dw_bytes, dh_bytes, bias_bytes;
+  size_t cnt_bytes, coef_bytes, ds_bytes, ds_t_bytes, ht_bytes, dw_bytes, dh_bytes, bias_bytes;
 };
 
 // The fp32 path's K-split GEMMs count the finished splits of each output tile
@@ -399,12 +401,18 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.V_pad = (V + 7) / 8 * 8;
   L.vocab = vocab_chunked(p);
   if (L.vocab) {
-    // Four column chunks of whole tiles (256 columns on the tensor path, 64 on
-    // the fp32 path): two 16-bit copies, or one fp32 copy, of a quarter of the
-    // columns for all rows. Fewer columns per chunk if N rows of them would
-    // pass the 4 GiB cap; then the columns are spread evenly over the chunks.
+    // Column chunks of whole tiles (256 columns on the tensor path, 64 on the
+    // fp32 path) over all rows, whose dlogits copies hold about N x V bytes
+    // together: one 16-bit row-major copy of half of the columns (the tensor
+    // path: grad_weight is then computed transposed, as (h^T dS)^T, from a
+    // transposed copy of h); two 16-bit copies, row-major and transposed, of
+    // a quarter of the columns (the tensor path when the gradients are added
+    // into existing buffers); or one fp32 copy of a quarter (the fp32 path).
+    // Fewer columns per chunk if N rows of them would pass the 4 GiB cap;
+    // then the columns are spread evenly over the chunks.
     // flce_params.max_chunk (rounded down to whole tiles) lowers the cap.
-    const int copies = tensor_path(p) ? 2 : 1;
+    L.wt = tensor_path(p) && !p->accumulate;
+    const int copies = tensor_path(p) && !L.wt ? 2 : 1;
     const int64_t gran = tensor_path(p) ? kBN : kSimtTile;
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * copies)) / gran * gran;
     if (cap < gran) cap = gran;
@@ -412,18 +420,20 @@ BwdLayout bwd_layout(const flce_params* p) {
       const int64_t c = p->max_chunk < gran ? gran : p->max_chunk / gran * gran;
       if (c < cap) cap = c;
     }
-    int64_t w = ceil_div(ceil_div(V, 4), gran) * gran;
+    int64_t w = ceil_div(ceil_div(V, int64_t(copies) * int64_t(elem)), gran) * gran;
     if (w > cap) w = cap;
     L.nchunks = static_cast<int>(ceil_div(V, w));
     L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), gran) * gran;
     L.nchunks = static_cast<int>(ceil_div(V, L.chunk));
     L.ds_ld = (L.chunk + 7) / 8 * 8;
     L.ds_t_ld = (N + 7) / 8 * 8;
+    L.ht_ld = (N + 7) / 8 * 8;
     L.rowblk = tensor_path(p) ? kBM : kSimtTile;
     L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
     L.coef_bytes = size_t(N) * sizeof(float4);
     L.ds_bytes = size_t(N) * L.ds_ld * elem;
-    L.ds_t_bytes = tensor_path(p) ? size_t(L.chunk) * L.ds_t_ld * elem : 0;
+    L.ds_t_bytes = tensor_path(p) && !L.wt ? size_t(L.chunk) * L.ds_t_ld * elem : 0;
+    L.ht_bytes = L.wt ? size_t(H) * L.ht_ld * 2 : 0;
     if (tensor_path(p)) {
       L.dh_bytes = L.nchunks > 1 ? size_t(N) * H * 4 : 0;
     } else {
@@ -440,6 +450,8 @@ BwdLayout bwd_layout(const flce_params* p) {
     o = align_up(o + L.ds_bytes, 1024);
     L.ds_t = o;
     if (L.ds_t_bytes) o = align_up(o + L.ds_t_bytes, 1024);
+    L.ht = o;
+    if (L.ht_bytes) o = align_up(o + L.ht_bytes, 1024);
     L.dw = o;
     L.dh_part = o;
     if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
@@ -732,6 +744,7 @@ std::vector<WsRegion> workspace_regions(const flce_params* p, int pass) {
     add("row_coefficients", L.coef, L.coef_bytes);
     add("dlogits", L.ds, L.ds_bytes);
     add("dlogits_transposed", L.ds_t, L.ds_t_bytes);
+    add("hidden_transposed", L.ht, L.ht_bytes);
     add("grad_weight_fp32", L.dw, L.dw_bytes);
     add("grad_hidden_fp32", L.dh_part, L.dh_bytes);
     add("grad_bias_partials", L.bias_part, L.bias_bytes);
@@ -1169,6 +1182,20 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
     float* dw_part = reinterpret_cast<float*>(ws + L.dw);
     const int nchunks_rows = L.vocab ? 0 : L.nchunks;
+    if (L.vocab && L.wt && grad_weight) {
+      // h^T [H][ht_ld], the K-major A operand of the transposed grad_weight
+      TransposeArgs ta{};
+      ta.src = static_cast<const uint16_t*>(hidden);
+      ta.dst = reinterpret_cast<uint16_t*>(ws + L.ht);
+      ta.rows = N;
+      ta.cols = H;
+      ta.ld_src = H;
+      ta.ld_dst = L.ht_ld;
+      ta.status = status;
+      ta.r_dst = DevRegion{ws + L.ht, L.ht_bytes};
+      v = launch("flce_transpose_hidden", st, [&] { return launch_transpose16(ta, st); });
+      if (v != FLCE_OK) return v;
+    }
     for (int c = 0; L.vocab && c < L.nchunks; ++c) {
       // Columns [v0, v0 + vc) of the vocabulary, all N rows.
       const int v0 = static_cast<int>(c * L.chunk);
@@ -1185,7 +1212,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.bias_part = bias_part != nullptr ? bias_part + v0 : nullptr;
       da.bias_blk0 = 0;
       da.tgt_base = v0;
-      da.ds_t = grad_weight != nullptr ? ws + L.ds_t : nullptr;
+      da.ds_t = grad_weight != nullptr && !L.wt ? ws + L.ds_t : nullptr;
       da.ld_t = L.ds_t_ld;
       da.n_blocks = static_cast<int>(ceil_div(N, kPairM));
       da.v_tiles = static_cast<int>(ceil_div(vc, kBN));
@@ -1240,10 +1267,47 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
-      if (grad_weight) {
-        // grad_weight[v0:v0+vc, H] = dS^T[vc, N] (K-major, the transposed copy)
-        // x h[N, H] (MN-major): complete after this one GEMM, so it goes
-        // straight to the output.
+      if (grad_weight && L.wt) {
+        // grad_weight[v0:v0+vc, H] = (h^T[H, N] (K-major, the transposed copy
+        // of h) x dS[N, vc] (MN-major through the 3-D view))^T: complete after
+        // this one GEMM, whose epilogue stores its tiles transposed straight
+        // into the output.
+        GemmOperand op_a, op_b;
+        GemmArgs ga{};
+        if ((v = make_k_operand(&op_a, ws + L.ht, N, H, uint64_t(L.ht_ld) * 2, kBM, dt)) != FLCE_OK)
+          return v;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, da.ds, vc, N, ds_row_bytes, dt)) != FLCE_OK)
+          return v;
+        ga.M = H;
+        ga.N = vc;
+        ga.K = N;
+        ga.m_tiles = static_cast<int>(ceil_div(H, kPairM));
+        ga.n_tiles = static_cast<int>(ceil_div(vc, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(N, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = 1;
+        ga.kb_per_split = ga.k_blocks;
+        ga.a_mn = 0;
+        ga.b_mn = 1;
+        ga.mode = kStoreOutT;
+        ga.out_t = static_cast<uint8_t*>(grad_weight) + size_t(v0) * H * 2;
+        ga.ld_out_t = H;
+        ga.part = nullptr;
+        ga.acc_scale = acc_scale;
+        ga.status = status;
+        ga.r_out_t = r_gw;
+        // h^T (64 MB at H = 4096, N = 8192) is read by every wave of tiles; the
+        // dlogits chunk streams through once per group of row tiles
+        ga.a_l2 = kL2EvictLast;
+        ga.b_l2 = kL2EvictFirst;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+        v = launch("flce_grad_weight_tc", st,
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
+        if (v != FLCE_OK) return v;
+      } else if (grad_weight) {
+        // grad_weight[v0:v0+vc, H] (+)= dS^T[vc, N] (K-major, the transposed
+        // copy) x h[N, H] (MN-major): complete after this one GEMM, so it goes
+        // straight to the output (or is added to it).
         GemmOperand op_a, op_b;
         GemmArgs ga{};
         if ((v = make_k_operand(&op_a, da.ds_t, N, vc, uint64_t(L.ds_t_ld) * 2, kBM, dt)) != FLCE_OK)
@@ -1271,8 +1335,8 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.r_out = r_gw;
         // h (64 MB at H = 4096, N = 8192) is read by every wave of tiles; the
         // transposed dlogits stream through once
-        ga.a_evict_first = 1;
-        ga.b_evict_last = 1;
+        ga.a_l2 = kL2EvictFirst;
+        ga.b_l2 = kL2EvictLast;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });

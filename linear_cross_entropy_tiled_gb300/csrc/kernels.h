@@ -239,7 +239,10 @@ enum GemmMode : int {
   // logits are never stored: out = 2 r_m f_n (acc - y_mn) in the output dtype,
   // and loss_part[n_tile][m / 32] = sum over the tile's columns and the 32
   // rows m / 32 of r_m f_n (acc - y_mn)^2 (fp32). Needs k_splits == 1.
-  kWeightedMse = 6
+  kWeightedMse = 6,
+  // out_t = acc transposed, in the output dtype: out_t[n * ld_out_t + m] for
+  // the tile's rows m and columns n. Needs k_splits == 1.
+  kStoreOutT = 7
 };
 
 // One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With
@@ -277,10 +280,22 @@ struct GemmArgs {
   // [0] hands out units in order, [1] counts the pairs that have finished
   // taking units. nullptr: every pair takes units u = pair, pair + npairs, ...
   int* tile_counter;
-  // L2 policy of the operand loads: 1 marks A's lines evict-first (a stream
-  // read once) or B's evict-last (an operand every tile of a wave re-reads);
-  // 0 leaves the normal policy.
-  int a_evict_first, b_evict_last;
+  // L2 policy of each operand's loads: kL2Normal, kL2EvictFirst (a stream
+  // read once) or kL2EvictLast (an operand every wave of tiles re-reads).
+  int a_l2, b_l2;
+};
+
+enum L2Policy : int { kL2Normal = 0, kL2EvictFirst = 1, kL2EvictLast = 2 };
+
+// dst[c * ld_dst + r] = src[r * ld_src + c] for a rows x cols matrix of 16-bit
+// elements (bf16 or fp16: the bits are moved, not converted).
+struct TransposeArgs {
+  const uint16_t* src;
+  uint16_t* dst;
+  int rows, cols;
+  long long ld_src, ld_dst;
+  int* status;
+  DevRegion r_dst;
 };
 
 // dst[i] = src[i] * (*scale), i < count, in the element type (dtype 0 fp32,
@@ -390,6 +405,7 @@ cudaError_t launch_shard_state(const ShardStateArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_row_coef(const RowCoefArgs& a, cudaStream_t s);
+cudaError_t launch_transpose16(const TransposeArgs& a, cudaStream_t s);
 cudaError_t launch_bias_reduce(const BiasReduceArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_split_reduce(const SplitReduceArgs& a, cudaStream_t s);
 cudaError_t launch_loss_reduce(const LossReduceArgs& a, cudaStream_t s);

@@ -285,6 +285,28 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
 }
 
 
+// 32 x 32 tiles through shared memory (one element per 32-bit word, a
+// 33-word row pitch, so that neither the row reads nor the column reads
+// conflict); 32 x 8 threads, four rows each.
+__global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a) {
+  __shared__ uint32_t tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty + 8 * i, c = c0 + tx;
+    tile[ty + 8 * i][tx] = (r < a.rows && c < a.cols) ? a.src[r * a.ld_src + c] : 0u;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + ty + 8 * i, r = r0 + tx;
+    uint16_t* const dst = a.dst + c * a.ld_dst + r;
+    if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
+      *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
+  }
+}
+
 // One block, the backward's first kernel. It zeroes the workspace header and
 // tile counters, counts the valid rows (needed for the mean), then writes the
 // coefficients of every row.
@@ -434,6 +456,13 @@ cudaError_t launch_combine(const CombineArgs& a, int nblk, cudaStream_t s) {
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
   finalize_kernel<<<1, 256, 0, s>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose16(const TransposeArgs& a, cudaStream_t s) {
+  const dim3 grid((a.cols + 31) / 32, (a.rows + 31) / 32);
+  transpose16_kernel<<<grid, 256, 0, s>>>(a);
   note_launch();
   return cudaGetLastError();
 }

@@ -1014,9 +1014,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&tm_b);
       if (a_atoms > 0) tma_prefetch_desc(&tm_a3);
       if (b_atoms > 0) tma_prefetch_desc(&tm_b3);
-      const uint64_t pol_n = l2_policy_evict_normal();
-      const uint64_t pol_a = a.a_evict_first ? l2_policy_evict_first() : pol_n;
-      const uint64_t pol_b = a.b_evict_last ? l2_policy_evict_last() : pol_n;
+      auto policy = [](int k) {
+        return k == kL2EvictFirst ? l2_policy_evict_first()
+               : k == kL2EvictLast ? l2_policy_evict_last()
+                                   : l2_policy_evict_normal();
+      };
+      const uint64_t pol_a = policy(a.a_l2), pol_b = policy(a.b_l2);
       const int m_off = static_cast<int>(rank) * kBM, n_off = static_cast<int>(rank) * kBNHalf;
       producer_role(s, g, kblocks_of, rank == 0, for_each_tile,
                     [&](int ta, int nt, int kb_rel, uint8_t* da, uint8_t* db, uint32_t bar) {
@@ -1069,6 +1072,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
     const bool add_out = mode0 == kAddOutToOut || mode0 == kAddOutToPart;
     const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
+    const bool t_only = mode0 == kStoreOutT;
     constexpr bool mse = kMse;  // the kWeightedMse epilogue is its own instantiation
     const float* const tgt = a.target;
     const float* const feat = a.feat_w;
@@ -1099,12 +1103,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                     v);
           tmem_ld_wait(v);
           const int col0 = nt * kBN + c * 32;
-          // The loss epilogue keeps every lane of a warp (the transposed store
-          // shuffles); a row past M has zero logits and zero weight there.
-          if (mse ? col0 >= N : (!row_ok || col0 >= N)) continue;
+          // The loss epilogue and the transposed store keep every lane of a
+          // warp (the transposed store shuffles); a row past M has zero logits
+          // and zero weight there.
+          if ((mse || t_only) ? col0 >= N : (!row_ok || col0 >= N)) continue;
           float d[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
+          if (!mse && t_only) {
+            uint32_t w[16];
+            pack32<T>(d, 1.f, w);
+            store_transposed_packed<T>(w, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane,
+                                       lane, M, N, true, a.r_out_t, a.status);
+            continue;
+          }
           if (mse) {
             // d holds the logits z of this row's 32 columns; they become
             // 2 r f (z - y), and r f (z - y)^2 goes into the row's loss.

@@ -49,14 +49,25 @@ def test_workspace_sizes(lib):
     p = params(N=8192, H=4096, V=128256, has_bias=True)
     fwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_FORWARD)
     assert fwd < 64 << 20                       # a few MB of partial states
-    # N < V: vocabulary chunks. Two bf16 copies of dlogits (row-major and
-    # transposed) for all rows and a quarter of the columns (32064 rounded up
-    # to whole 256-column tiles), and the fp32 grad_hidden partial that
-    # crosses the four chunks.
+    # N < V: vocabulary chunks. One bf16 row-major copy of dlogits for all
+    # rows and half of the columns (64128 rounded up to whole 256-column
+    # tiles), h transposed (grad_weight is computed as (h^T dS)^T), and the
+    # fp32 grad_hidden partial that crosses the two chunks.
     bwd = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
-    chunk = 2 * 8192 * 32256 * 2
+    chunk = 8192 * 64256 * 2
+    ht = 4096 * 8192 * 2
     dh = 8192 * 4096 * 4
-    assert chunk + dh < bwd < chunk + dh + (64 << 20)
+    assert chunk + ht + dh < bwd < chunk + ht + dh + (64 << 20)
+    regions = {n: b for n, _, b in _lib.workspace_regions(p, _lib.FLCE_PASS_BACKWARD)}
+    assert regions["dlogits"] == chunk and regions["hidden_transposed"] == ht
+    assert "dlogits_transposed" not in regions
+    # adding into existing gradients keeps the transposed dlogits copy (two
+    # copies of a quarter of the columns) and needs no transposed h
+    pa = _lib.FlceParams.from_buffer_copy(p)
+    pa.accumulate = 1
+    ra = {n: b for n, _, b in _lib.workspace_regions(pa, _lib.FLCE_PASS_BACKWARD)}
+    assert ra["dlogits"] == 8192 * 32256 * 2 and ra["dlogits_transposed"] == 32256 * 8192 * 2
+    assert "hidden_transposed" not in ra
     assert bwd < 8192 * 128256 * 2              # less than one N x V buffer
     # row chunks: two copies of a quarter of the rows, the fp32 grad_weight
     # partial and two fp32 K-split partials of grad_hidden
@@ -229,8 +240,8 @@ def test_schedule_fields(lib):
     full = _lib.workspace_bytes(base, _lib.FLCE_PASS_BACKWARD)
     capped = params(N=8192, H=4096, V=128256, max_chunk=8192)
     small = _lib.workspace_bytes(capped, _lib.FLCE_PASS_BACKWARD)
-    # vocabulary chunks of 8192 columns instead of 32256: two copies of N x chunk shrink
-    assert full - small == pytest.approx(2 * 8192 * (32256 - 8192) * 2, rel=1e-3)
+    # vocabulary chunks of 8192 columns instead of 64256: the copy of N x chunk shrinks
+    assert full - small == pytest.approx(8192 * (64256 - 8192) * 2, rel=1e-3)
     # below one tile it is one tile (256 columns), not an error
     tiny = params(N=8192, H=4096, V=128256, max_chunk=1)
     assert _lib.workspace_bytes(tiny, _lib.FLCE_PASS_BACKWARD) < small

@@ -45,10 +45,14 @@ def test_kernels_per_call(dtype, N, H, V, bias):
     assert n_fwd == 2                         # logit tiles, merge (with the reduction)
     gl = torch.ones(1, device="cuda")
     n_bwd, _ = kernels_of(lambda: flce_backward(p, h, w, t, lse, gl, b))
-    # N < V: four vocabulary chunks, each dlogits and both contractions (one
-    # grid on the fp32 path); row coefficients first, grad_bias's sum last
-    per_chunk = 2 if dtype == "f32" else 3
-    assert n_bwd == 1 + per_chunk * 4 + (1 if bias else 0)
+    # N < V: vocabulary chunks (four on the fp32 path, two on the 16-bit path,
+    # whose one dlogits copy holds half of the columns), each dlogits and both
+    # contractions (one grid on the fp32 path); row coefficients first (and
+    # h transposed on the 16-bit path), grad_bias's sum last
+    if dtype == "f32":
+        assert n_bwd == 1 + 2 * 4 + (1 if bias else 0)
+    else:
+        assert n_bwd == 2 + 3 * 2 + (1 if bias else 0)
 
 
 @pytest.mark.parametrize("N,H,V,axis", [
@@ -129,11 +133,13 @@ def test_profiling_records_per_kernel():
             flce_backward(p, h, w, t, lse, gl, b)
         _lib.profiling_enable(False)
         recs = {r[0]: r for r in _lib.profiling_read()}
-        # forward: tiles + merge; backward: row coefficients, 4 x (dlogits, two GEMMs), bias sums
+        # forward: tiles + merge; backward: row coefficients, h transposed,
+        # 2 x (dlogits, two GEMMs), bias sums
         assert recs["flce_fwd_tc"][1] == steps and recs["flce_merge"][1] == steps
-        assert recs["flce_dlogits_tc"][1] == 4 * steps
-        assert recs["flce_grad_hidden_tc"][1] == 4 * steps
-        assert recs["flce_grad_weight_tc"][1] == 4 * steps
+        assert recs["flce_transpose_hidden"][1] == steps
+        assert recs["flce_dlogits_tc"][1] == 2 * steps
+        assert recs["flce_grad_hidden_tc"][1] == 2 * steps
+        assert recs["flce_grad_weight_tc"][1] == 2 * steps
         for name in ("flce_fwd_tc", "flce_dlogits_tc", "flce_grad_hidden_tc", "flce_grad_weight_tc"):
             _, n, ms, mhz, (w_ops, w_acc) = recs[name]
             assert ms > 0.0, name
