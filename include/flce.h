@@ -28,11 +28,14 @@
  * - The backward recomputes each logit tile and forms dlogits from it in
  *   registers (same section). dlogits goes to HBM in 16 bits for one chunk
  *   at a time: a range of vocabulary columns for all rows when N < V, else
- *   a range of rows. Each chunk is stored row-major and transposed. The two
- *   copies together hold about half of the N x V logits, and at most 4 GiB.
- *   Two tensor-core contractions then accumulate grad_hidden = dlogits W and
- *   grad_weight = dlogits^T h, as the quack diff and "Chunked Linear Loss",
- *   section "Gradient handling", do per chunk.
+ *   a range of rows. Two tensor-core contractions then accumulate
+ *   grad_hidden = dlogits W and grad_weight = dlogits^T h, as the quack diff
+ *   and "Chunked Linear Loss", section "Gradient handling", do per chunk.
+ *   With vocabulary chunks grad_weight is computed transposed, (h^T dlogits)^T,
+ *   so one row-major dlogits copy of half of the columns serves both; with row
+ *   chunks, or when adding into existing gradients, each chunk is also stored
+ *   transposed. The copies together hold about half of the N x V logits, and
+ *   at most 4 GiB.
  *
  * Conventions common to every entry point:
  * - Pointers named "device" must point to device memory of the current CUDA
@@ -170,10 +173,11 @@ typedef struct {
  * Device bytes the caller must provide as `workspace` for one pass. The
  * forward and backward need different amounts, and one workspace may serve
  * both passes in turn. For the headline size (N=8192, H=4096, V=128256,
- * bf16, with bias) the forward needs 16.5 MB and the backward 1.22 GB:
- * - N < V, so the backward chunks the vocabulary: a quarter of V (32256
- *   columns) of dlogits for all rows, row-major and transposed
- *   (2 x 528 MB);
+ * bf16, with bias) the forward needs 16.6 MB and the backward 1.29 GB:
+ * - N < V, so the backward chunks the vocabulary: half of V (64256 columns)
+ *   of dlogits for all rows, row-major (1.05 GB), and h transposed (67 MB);
+ *   with flce_params.accumulate, a quarter of V (32256 columns), row-major
+ *   and transposed (2 x 528 MB), instead;
  * - the fp32 grad_hidden partial carried across the chunks (134 MB);
  * - per-128-row bias partial sums (33 MB).
  * With N >= V it chunks rows instead and holds the fp32 grad_weight partial

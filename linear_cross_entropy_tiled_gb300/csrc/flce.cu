@@ -377,10 +377,14 @@ void place_counters(const flce_params* p, BwdLayout* L, size_t* o) {
 }
 
 // The backward stores dlogits for one chunk at a time and contracts it into
-// both gradients. The tensor path keeps two copies: row-major for grad_hidden
-// (K = vocabulary) and transposed for grad_weight (K = rows), so that both
-// GEMMs read their dlogits operand K-major. Together the copies hold about
-// half of the N x V logits, and at most 4 GiB. Whatever crosses chunks is
+// both gradients. grad_hidden (K = vocabulary) reads the row-major copy
+// K-major. With vocabulary chunks the tensor path computes grad_weight
+// transposed, (h^T dS)^T, reading that same copy as its MN-major B operand
+// and a transposed copy of h as its K-major A, so one dlogits copy suffices;
+// with row chunks, or when the gradients are added into existing buffers, it
+// keeps a second, transposed dlogits copy that grad_weight (K = rows) reads
+// K-major. Together the copies hold about half of the N x V logits, and at
+// most 4 GiB. Whatever crosses chunks is
 // summed in an fp32 partial: grad_weight [V, H] when the chunks are row
 // ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
 // chunks the vocabulary whenever N < V, where that partial is the smaller one:
