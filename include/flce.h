@@ -33,8 +33,7 @@
  *   and "Chunked Linear Loss", section "Gradient handling", do per chunk.
  *   With vocabulary chunks grad_weight is computed transposed, (h^T dlogits)^T,
  *   so one row-major dlogits copy of half of the columns serves both; with row
- *   chunks, or when adding into existing gradients, each chunk is also stored
- *   transposed. The copies together hold about half of the N x V logits, and
+ *   chunks each chunk is also stored transposed. The copies together hold about half of the N x V logits, and
  *   at most 4 GiB.
  *
  * Conventions common to every entry point:
@@ -176,8 +175,6 @@ typedef struct {
  * bf16, with bias) the forward needs 16.6 MB and the backward 1.29 GB:
  * - N < V, so the backward chunks the vocabulary: half of V (64256 columns)
  *   of dlogits for all rows, row-major (1.05 GB), and h transposed (67 MB);
- *   with flce_params.accumulate, a quarter of V (32256 columns), row-major
- *   and transposed (2 x 528 MB), instead;
  * - the fp32 grad_hidden partial carried across the chunks (134 MB);
  * - per-128-row bias partial sums (33 MB).
  * With N >= V it chunks rows instead and holds the fp32 grad_weight partial

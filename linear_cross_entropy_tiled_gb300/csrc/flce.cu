@@ -381,9 +381,8 @@ void place_counters(const flce_params* p, BwdLayout* L, size_t* o) {
 // K-major. With vocabulary chunks the tensor path computes grad_weight
 // transposed, (h^T dS)^T, reading that same copy as its MN-major B operand
 // and a transposed copy of h as its K-major A, so one dlogits copy suffices;
-// with row chunks, or when the gradients are added into existing buffers, it
-// keeps a second, transposed dlogits copy that grad_weight (K = rows) reads
-// K-major. Together the copies hold about half of the N x V logits, and at
+// with row chunks it keeps a second, transposed dlogits copy that grad_weight
+// (K = rows) reads K-major. Together the copies hold about half of the N x V logits, and at
 // most 4 GiB. Whatever crosses chunks is
 // summed in an fp32 partial: grad_weight [V, H] when the chunks are row
 // ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
@@ -406,16 +405,14 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.vocab = vocab_chunked(p);
   if (L.vocab) {
     // Column chunks of whole tiles (256 columns on the tensor path, 64 on the
-    // fp32 path) over all rows, whose dlogits copies hold about N x V bytes
-    // together: one 16-bit row-major copy of half of the columns (the tensor
-    // path: grad_weight is then computed transposed, as (h^T dS)^T, from a
-    // transposed copy of h); two 16-bit copies, row-major and transposed, of
-    // a quarter of the columns (the tensor path when the gradients are added
-    // into existing buffers); or one fp32 copy of a quarter (the fp32 path).
+    // fp32 path) over all rows, whose dlogits copy holds about N x V bytes:
+    // one 16-bit row-major copy of half of the columns (the tensor path:
+    // grad_weight is computed transposed, as (h^T dS)^T, from a transposed
+    // copy of h), or one fp32 copy of a quarter (the fp32 path).
     // Fewer columns per chunk if N rows of them would pass the 4 GiB cap;
     // then the columns are spread evenly over the chunks.
     // flce_params.max_chunk (rounded down to whole tiles) lowers the cap.
-    L.wt = tensor_path(p) && !p->accumulate;
+    L.wt = tensor_path(p);
     const int copies = tensor_path(p) && !L.wt ? 2 : 1;
     const int64_t gran = tensor_path(p) ? kBN : kSimtTile;
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * copies)) / gran * gran;
@@ -1293,7 +1290,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         ga.kb_per_split = ga.k_blocks;
         ga.a_mn = 0;
         ga.b_mn = 1;
-        ga.mode = kStoreOutT;
+        ga.mode = p->accumulate ? kAddOutToOutT : kStoreOutT;
         ga.out_t = static_cast<uint8_t*>(grad_weight) + size_t(v0) * H * 2;
         ga.ld_out_t = H;
         ga.part = nullptr;

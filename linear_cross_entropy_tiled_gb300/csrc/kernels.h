@@ -242,7 +242,10 @@ enum GemmMode : int {
   kWeightedMse = 6,
   // out_t = acc transposed, in the output dtype: out_t[n * ld_out_t + m] for
   // the tile's rows m and columns n. Needs k_splits == 1.
-  kStoreOutT = 7
+  kStoreOutT = 7,
+  // out_t = out_t + acc transposed (read-modify-write in the output dtype,
+  // one rounding). Needs k_splits == 1.
+  kAddOutToOutT = 8
 };
 
 // One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With

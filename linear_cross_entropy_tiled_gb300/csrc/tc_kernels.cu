@@ -737,6 +737,36 @@ __device__ __forceinline__ void store_transposed_packed(const uint32_t (&w)[16],
   }
 }
 
+// Adds a warp's 32 rows x 32 fp32 columns, transposed, into dst_t (16-bit):
+// the layout and bounds of store_transposed_packed, with the lane pairs
+// exchanging fp32 values so that each existing value is read, added to in
+// fp32 and rounded once. All 32 lanes must call it (it shuffles).
+template <typename T>
+__device__ __forceinline__ void add_transposed(const float (&d)[32], T* dst_t, long long ld_t,
+                                               int col0, int row_w, int lane, int rows, int cols,
+                                               bool live, const DevRegion& r, int* status) {
+  const bool odd = (lane & 1) != 0;
+  const int row_pair = row_w + (lane & ~1);
+  const int c_first = col0 + (odd ? 1 : 0);
+  T* const base = dst_t + static_cast<size_t>(c_first) * ld_t + row_pair;
+  const size_t step = 2 * static_cast<size_t>(ld_t);
+  const bool inside = live && row_w + 32 <= rows && col0 + 32 <= cols;
+  const bool row_in = live && row_pair < rows;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    // even lane: column 2i of rows (own, partner); odd lane: column 2i + 1 of
+    // rows (partner, own)
+    const float recv = __shfl_xor_sync(kFull, odd ? d[2 * i] : d[2 * i + 1], 1);
+    const float lo = odd ? recv : d[2 * i];
+    const float hi = odd ? d[2 * i + 1] : recv;
+    T* const p = base + i * step;
+    if ((inside || (row_in && c_first + 2 * i < cols)) && store_allowed(p, 4, r, status)) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      *reinterpret_cast<uint32_t*>(p) = Elem<T>::pack(Elem<T>::lo(w) + lo, Elem<T>::hi(w) + hi);
+    }
+  }
+}
+
 template <typename T, bool kBias, bool kSoftcap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kDsThreads, 1)
     ds_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
@@ -1072,7 +1102,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
     const bool add_out = mode0 == kAddOutToOut || mode0 == kAddOutToPart;
     const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
-    const bool t_only = mode0 == kStoreOutT;
+    const bool t_only = mode0 == kStoreOutT || mode0 == kAddOutToOutT;
     constexpr bool mse = kMse;  // the kWeightedMse epilogue is its own instantiation
     const float* const tgt = a.target;
     const float* const feat = a.feat_w;
@@ -1111,10 +1141,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
           if (!mse && t_only) {
-            uint32_t w[16];
-            pack32<T>(d, 1.f, w);
-            store_transposed_packed<T>(w, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane,
-                                       lane, M, N, true, a.r_out_t, a.status);
+            if (mode0 == kAddOutToOutT) {
+              add_transposed<T>(d, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane, lane, M, N,
+                                true, a.r_out_t, a.status);
+            } else {
+              uint32_t w[16];
+              pack32<T>(d, 1.f, w);
+              store_transposed_packed<T>(w, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane,
+                                         lane, M, N, true, a.r_out_t, a.status);
+            }
             continue;
           }
           if (mse) {

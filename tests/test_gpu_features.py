@@ -47,7 +47,7 @@ def dev_tensor(x, dtype):
 @pytest.mark.parametrize("dtype,N,H,V,axis,chunk_cap", [
     ("bf16", 1200, 2560, 16500, "rows", None),  # grad_hidden with 2 K splits, 3 row chunks
     ("bf16", 700, 136, 900, "rows", 256),       # 3 row chunks
-    ("bf16", 600, 256, 16500, "vocab", None),   # 4 vocabulary chunks of 4352 columns
+    ("bf16", 600, 256, 16500, "vocab", None),   # 2 vocabulary chunks of 8448 columns
     ("bf16", 700, 136, 900, "vocab", 256),      # 4 vocabulary chunks of 256 columns
     ("bf16", 200, 64, 250, "vocab", None),      # 1 vocabulary chunk (V < 256)
     ("f32", 150, 64, 700, None, None),
