@@ -374,10 +374,16 @@ int flce_forward_noalloc(const flce_params* p, const void* hidden, const void* w
  *   - dlogits is device memory of N rows of ld_dlogits elements in the input
  *     dtype (ld_dlogits >= V, ld_dlogits % 8 == 0), as the caller's loss
  *     returned it.
+ *   - On the 16-bit path grad_weight is computed transposed, as
+ *     (hidden^T dlogits)^T: the chunk's hidden rows are transposed into the
+ *     workspace and dlogits is read along its rows, so no transposed copy is
+ *     needed.
  *   - dlogits_t (optional, bf16 / fp16): the same values transposed, V rows of
  *     ld_dlogits_t >= N elements (ld_dlogits_t % 8 == 0), as
- *     flce_chunk_weighted_mse writes them. grad_weight then reads them K-major,
- *     about 20 % faster than reading dlogits across its rows. NULL if absent.
+ *     flce_chunk_weighted_mse writes them. Read only when an fp32-accumulated
+ *     grad_weight is added into an existing one (FLCE_ACCUM_FP32 with
+ *     p->accumulate = 1), where grad_weight then reads it K-major, about 20 %
+ *     faster than reading dlogits across its rows. NULL if absent.
  *   - grad_hidden points to the chunk's rows. It is overwritten, or added to
  *     when p->accumulate is 1. NULL skips it.
  *   - grad_weight (V x H) is summed over the chunks of one loss, which the

@@ -131,9 +131,8 @@ class _ChunkedLinearLoss(torch.autograd.Function):
                 raise ValueError("weighted_mse_loss: target [N, V], row_weight [N], "
                                  "feature_weight [V] must match inputs and weight")
             loss64 = torch.zeros(1, dtype=torch.float64, device=dev)
-            # the transposed copy lets grad_weight read dlogits K-major
-            ld_t = _round8(rows)
-            logits_t = torch.empty((V, ld_t), dtype=x.dtype, device=dev)
+            # no transposed dlogits copy: flce_chunk_grads computes grad_weight
+            # transposed, from h^T and the row-major dlogits
             ws_m = torch.empty(max(256, _lib.workspace_bytes(p_max, _lib.FLCE_PASS_CHUNK_MSE)),
                                dtype=torch.uint8, device=dev)
         for c in range(nchunks):
@@ -146,7 +145,7 @@ class _ChunkedLinearLoss(torch.autograd.Function):
                 rc = _lib.chunk_weighted_mse_raw(
                     p, _ptr(xc), _ptr(w), _ptr(tgt), tgt.stride(0), _ptr(fn.row_weight[r0:r1]),
                     _ptr(fn.feature_weight), _ptr(logits), ld, _ptr(loss64), 1 if c > 0 else 0,
-                    _ptr(ws_m), ws_m.numel(), stream, _ptr(logits_t) if need_w else 0, ld_t)
+                    _ptr(ws_m), ws_m.numel(), stream, 0, 0)
                 _lib.check(rc, "flce_chunk_weighted_mse")
                 _maybe_check(ws_m, "flce_chunk_weighted_mse")
                 g = logits[: r1 - r0]
@@ -181,9 +180,7 @@ class _ChunkedLinearLoss(torch.autograd.Function):
                      else _lib.FLCE_CHUNK_LAST if c == nchunks - 1 else _lib.FLCE_CHUNK_NEXT)
             rc = _lib.chunk_grads_raw(p, _ptr(xc), _ptr(w), _ptr(g), g.stride(0), phase,
                                       _ptr(gx[r0:r1]) if gx is not None else 0, _ptr(gw),
-                                      _ptr(ws_g), ws_g.numel(), stream,
-                                      _ptr(logits_t) if (device_loss and need_w) else 0,
-                                      ld_t if device_loss else 0)
+                                      _ptr(ws_g), ws_g.numel(), stream, 0, 0)
             _lib.check(rc, "flce_chunk_grads")
             _maybe_check(ws_g, "flce_chunk_grads")
         if device_loss:

@@ -692,24 +692,47 @@ CUtensorMapDataType map_type(const flce_params* p) {
 // The two partials exist on the tensor path only; with
 // grad_weight_accum = weight the chunks accumulate in grad_weight itself.
 struct ChunkLayout {
-  size_t dw_part, dh_part, total;
-  size_t dw_bytes, dh_bytes;
+  bool wt;              // grad_weight computed transposed, (h^T dlogits)^T
+  int64_t ht_ld, dw_ld; // row strides of h^T and of the fp32 grad_weight partial
+  size_t dw_part, dh_part, ht, total;
+  size_t dw_bytes, dh_bytes, ht_bytes;
 };
+
+// flce_chunk_grads on the tensor path computes grad_weight transposed, from
+// h^T (transposed into the workspace) and the caller's row-major dlogits as
+// an MN-major operand, so it needs no transposed dlogits. The fp32 partial
+// across the chunks then has grad_weight^T's layout [H][V]. Only adding the
+// fp32-accumulated gradient into an existing one keeps the row-major partial
+// and reads dlogits transposed. A function of the parameters, so every chunk
+// of one loss takes the same path.
+bool chunk_grads_transposed(const flce_params* p) {
+  return tensor_path(p) && !(p->grad_weight_accum == FLCE_ACCUM_FP32 && p->accumulate);
+}
 
 ChunkLayout chunk_layout(const flce_params* p) {
   ChunkLayout L{};
+  L.wt = chunk_grads_transposed(p);
+  L.dw_ld = L.wt ? (p->V + 7) / 8 * 8 : p->H;
   L.dw_bytes = (tensor_path(p) && p->grad_weight_accum == FLCE_ACCUM_FP32)
-                   ? size_t(p->V) * p->H * 4 : 0;
+                   ? size_t(L.wt ? p->H : p->V) * L.dw_ld * 4 : 0;
   if (tensor_path(p)) {
     L.dh_bytes = size_t(kMaxKSplits) * p->N * p->H * 4;
   } else {
     L.dh_bytes = simt_part_bytes(p->N, p->H, p->V);
   }
+  L.ht_ld = (p->N + 7) / 8 * 8;
+  L.ht_bytes = L.wt ? size_t(p->H) * L.ht_ld * 2 : 0;
+  // grad_hidden's split partials are done with (split-reduced) before h is
+  // transposed for grad_weight, so both share one scratch region. It comes
+  // last: its size follows the call's N, its start does not, so every chunk
+  // of one loss writes inside the regions of the largest chunk.
   size_t o = kHeader;
   L.dw_part = o;
   if (L.dw_bytes) o = align_up(o + L.dw_bytes, 1024);
   L.dh_part = o;
-  if (L.dh_bytes) o = align_up(o + L.dh_bytes, 1024);
+  L.ht = o;
+  const size_t scratch = L.dh_bytes > L.ht_bytes ? L.dh_bytes : L.ht_bytes;
+  if (scratch) o = align_up(o + scratch, 1024);
   L.total = o;
   return L;
 }
@@ -753,6 +776,7 @@ std::vector<WsRegion> workspace_regions(const flce_params* p, int pass) {
     const ChunkLayout L = chunk_layout(p);
     add("grad_weight_fp32", L.dw_part, L.dw_bytes);
     add("grad_hidden_fp32", L.dh_part, L.dh_bytes);
+    add("hidden_transposed", L.ht, L.ht_bytes);
   } else if (pass == FLCE_PASS_CHUNK_MSE) {
     add("loss_partials", kHeader, mse_loss_part_bytes(p));
   }
@@ -1886,7 +1910,60 @@ int flce_chunk_grads(const flce_params* p, const void* hidden, const void* weigh
       if (v != FLCE_OK) return v;
     }
   }
-  if (grad_weight) {
+  if (grad_weight && L.wt) {
+    // grad_weight[V, H] (+)= (h^T[H, N] (K-major) x dlogits[N, V] (MN-major
+    // through the 3-D view))^T; the epilogue stores (or adds) its tiles
+    // transposed. The fp32 partial across chunks is grad_weight^T [H][dw_ld].
+    TransposeArgs ta{};
+    ta.src = static_cast<const uint16_t*>(hidden);
+    ta.dst = reinterpret_cast<uint16_t*>(ws + L.ht);
+    ta.rows = N;
+    ta.cols = H;
+    ta.ld_src = H;
+    ta.ld_dst = L.ht_ld;
+    ta.status = status;
+    ta.r_dst = DevRegion{ws + L.ht, L.ht_bytes};
+    v = launch("flce_transpose_hidden", st, [&] { return launch_transpose16(ta, st); });
+    if (v != FLCE_OK) return v;
+    GemmOperand op_a, op_b;
+    GemmArgs ga{};
+    if ((v = make_k_operand(&op_a, ws + L.ht, N, H, uint64_t(L.ht_ld) * 2, kBM, dt)) != FLCE_OK)
+      return v;
+    if ((v = make_mn_operand(&op_b, &ga.b_atoms, dlogits, V, N, dl_row_bytes, dt)) != FLCE_OK)
+      return v;
+    ga.M = H;
+    ga.N = V;
+    ga.K = N;
+    ga.m_tiles = static_cast<int>(ceil_div(H, kPairM));
+    ga.n_tiles = static_cast<int>(ceil_div(V, kBN));
+    ga.k_blocks = static_cast<int>(ceil_div(N, kBK));
+    ga.num_tiles = ga.m_tiles * ga.n_tiles;
+    ga.k_splits = 1;
+    ga.kb_per_split = ga.k_blocks;
+    ga.a_mn = 0;
+    ga.b_mn = 1;
+    if (phase == FLCE_CHUNK_ONLY || p->grad_weight_accum == FLCE_ACCUM_WEIGHT)
+      ga.mode = (later || p->accumulate) ? kAddOutToOutT : kStoreOutT;
+    else if (phase == FLCE_CHUNK_FIRST)
+      ga.mode = kStorePart;
+    else if (phase == FLCE_CHUNK_NEXT)
+      ga.mode = kAddPart;
+    else
+      ga.mode = kAddPartToOutT;
+    ga.out_t = grad_weight;
+    ga.ld_out_t = H;
+    ga.part = reinterpret_cast<float*>(ws + L.dw_part);
+    ga.ld_part = L.dw_ld;
+    ga.status = status;
+    ga.r_out_t = DevRegion{grad_weight, size_t(V) * H * 2};
+    ga.r_part = DevRegion{ws + L.dw_part, L.dw_bytes};
+    ga.a_l2 = kL2EvictLast;
+    ga.b_l2 = kL2EvictFirst;
+    const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+    v = launch("flce_chunk_grad_weight_tc", st,
+               [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
+    if (v != FLCE_OK) return v;
+  } else if (grad_weight) {
     // grad_weight[V, H] (+)= dlogits^T[V, N] x h[N, H] (MN-major). dlogits^T is
     // read K-major from the transposed copy when the caller has one, else
     // MN-major from dlogits (about 20 % slower).

@@ -245,7 +245,10 @@ enum GemmMode : int {
   kStoreOutT = 7,
   // out_t = out_t + acc transposed (read-modify-write in the output dtype,
   // one rounding). Needs k_splits == 1.
-  kAddOutToOutT = 8
+  kAddOutToOutT = 8,
+  // out_t = (part + acc) transposed: the fp32 partial is in the tile's own
+  // layout, part[m * ld_part + n]. Needs k_splits == 1.
+  kAddPartToOutT = 9
 };
 
 // One plain GEMM D[M,N] = A[M,K] B[K,N] in 256 x 256 pair tiles. With

@@ -1102,7 +1102,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const bool add_part = mode0 == kAddPart || mode0 == kAddPartToOut;
     const bool add_out = mode0 == kAddOutToOut || mode0 == kAddOutToPart;
     const bool to_part = mode0 == kStorePart || mode0 == kAddPart || mode0 == kAddOutToPart;
-    const bool t_only = mode0 == kStoreOutT || mode0 == kAddOutToOutT;
+    const bool t_only = mode0 == kStoreOutT || mode0 == kAddOutToOutT || mode0 == kAddPartToOutT;
     constexpr bool mse = kMse;  // the kWeightedMse epilogue is its own instantiation
     const float* const tgt = a.target;
     const float* const feat = a.feat_w;
@@ -1141,6 +1141,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(v[j]) * acc_mul;
           if (!mse && t_only) {
+            if (mode0 == kAddPartToOutT && row_ok) {
+              const float4* src =
+                  reinterpret_cast<const float4*>(part + static_cast<size_t>(m) * ld_part + col0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (col0 + i * 4 < N) {
+                  const float4 p4 = src[i];
+                  d[4 * i] += p4.x;
+                  d[4 * i + 1] += p4.y;
+                  d[4 * i + 2] += p4.z;
+                  d[4 * i + 3] += p4.w;
+                }
+              }
+            }
             if (mode0 == kAddOutToOutT) {
               add_transposed<T>(d, static_cast<T*>(a.out_t), a.ld_out_t, col0, m - lane, lane, M, N,
                                 true, a.r_out_t, a.status);

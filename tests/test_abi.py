@@ -176,11 +176,22 @@ def test_chunked_linear_loss_entry_points_validate_before_any_gpu_work(lib):
     """flce_chunk_logits / flce_chunk_grads ("Chunked Linear Loss"): sizes and argument checks."""
     p = params(N=512, H=256, V=1000)
     assert _lib.workspace_bytes(p, _lib.FLCE_PASS_CHUNK_LOGITS) == 256
-    # fp32 grad_weight partial [V, H] and two K-split partials of grad_hidden [N, H]
+    # the fp32 grad_weight partial, in grad_weight^T's layout [H][round8(V)] (the
+    # contraction is computed transposed), then one scratch region for the two
+    # K-split partials of grad_hidden [N, H] and, after them, h^T [H][round8(N)]
+    # in 16 bits
     need = _lib.workspace_bytes(p, _lib.FLCE_PASS_CHUNK_GRADS)
-    assert 1000 * 256 * 4 + 2 * 512 * 256 * 4 < need < 1000 * 256 * 4 + 2 * 512 * 256 * 4 + 8192
+    base = 256 * 1000 * 4 + max(2 * 512 * 256 * 4, 256 * 512 * 2)
+    assert base < need < base + 8192
+    regions = {n: b for n, _, b in _lib.workspace_regions(p, _lib.FLCE_PASS_CHUNK_GRADS)}
+    assert regions["grad_weight_fp32"] == 256 * 1000 * 4 and regions["hidden_transposed"] == 256 * 512 * 2
     pw = params(N=512, H=256, V=1000, grad_weight_accum="weight")
-    assert _lib.workspace_bytes(pw, _lib.FLCE_PASS_CHUNK_GRADS) < need - 1000 * 256 * 4 + 4096
+    assert _lib.workspace_bytes(pw, _lib.FLCE_PASS_CHUNK_GRADS) < need - 256 * 1000 * 4 + 4096
+    # adding an fp32-accumulated grad_weight into an existing one keeps the
+    # row-major partial [V][H] and needs no h^T
+    pa = params(N=512, H=256, V=1000, accumulate=True)
+    ra = {n: b for n, _, b in _lib.workspace_regions(pa, _lib.FLCE_PASS_CHUNK_GRADS)}
+    assert ra["grad_weight_fp32"] == 1000 * 256 * 4 and "hidden_transposed" not in ra
     pf = params(N=512, H=256, V=1000, dtype=_lib.FLCE_F32)
     assert _lib.workspace_bytes(pf, _lib.FLCE_PASS_CHUNK_GRADS) == 256   # SIMT: no partials
     fake = 1 << 20
@@ -267,3 +278,19 @@ def test_no_environment_reads_in_the_library():
     csrc = os.path.join(ROOT, "linear_cross_entropy_tiled_gb300", "csrc")
     for f in os.listdir(csrc):
         assert "getenv" not in open(os.path.join(csrc, f)).read(), f
+
+
+@pytest.mark.parametrize("dtype", [_lib.FLCE_BF16, _lib.FLCE_F32])
+@pytest.mark.parametrize("accum", ["fp32", "weight"])
+def test_chunk_grads_regions_of_smaller_chunks_lie_inside_the_largest(lib, dtype, accum):
+    """The workspace is sized with the largest chunk's N; every chunk of one loss
+    (fewer rows) must write only inside those regions."""
+    big = params(N=700, H=136, V=701, dtype=dtype, grad_weight_accum=accum)
+    ref = {}
+    for name, off, n in _lib.workspace_regions(big, _lib.FLCE_PASS_CHUNK_GRADS):
+        ref.setdefault(name, (off, n))
+    for N in (1, 160, 333, 699, 700):
+        q = params(N=N, H=136, V=701, dtype=dtype, grad_weight_accum=accum)
+        for name, off, n in _lib.workspace_regions(q, _lib.FLCE_PASS_CHUNK_GRADS):
+            roff, rn = ref[name]
+            assert roff == off and n <= rn, (N, name, off, n, roff, rn)
