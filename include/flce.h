@@ -31,10 +31,12 @@
  *   a range of rows. Two tensor-core contractions then accumulate
  *   grad_hidden = dlogits W and grad_weight = dlogits^T h, as the quack diff
  *   and "Chunked Linear Loss", section "Gradient handling", do per chunk.
- *   With vocabulary chunks grad_weight is computed transposed, (h^T dlogits)^T,
- *   so one row-major dlogits copy of half of the columns serves both; with row
- *   chunks each chunk is also stored transposed. The copies together hold about half of the N x V logits, and
- *   at most 4 GiB.
+ *   grad_weight is computed transposed, (h^T dlogits)^T, so one row-major
+ *   dlogits copy serves both contractions: half of the columns for all rows,
+ *   or half of the rows for all columns. Only row chunks that add into
+ *   existing gradients through the fp32 grad_weight partial also store each
+ *   chunk transposed (two copies of a quarter of the rows). The copies hold
+ *   about half of the N x V logits, and at most 4 GiB.
  *
  * Conventions common to every entry point:
  * - Pointers named "device" must point to device memory of the current CUDA
@@ -114,9 +116,9 @@ typedef enum {
 typedef enum { FLCE_ACCUM_FP32 = 0, FLCE_ACCUM_WEIGHT = 1 } flce_accum;
 
 /* Axis along which flce_backward cuts its work into chunks (see
- * flce_workspace_bytes). AUTO takes vocabulary chunks when N < V on the 16-bit
- * path and row chunks otherwise. The results are the same either way; the
- * workspace size and the speed differ. The fp32 path always chunks rows. */
+ * flce_workspace_bytes). AUTO takes vocabulary chunks when N < V and row
+ * chunks otherwise. The results are the same either way; the workspace size
+ * and the speed differ. */
 typedef enum {
   FLCE_CHUNK_AXIS_AUTO = 0,
   FLCE_CHUNK_AXIS_ROWS = 1,
@@ -177,9 +179,10 @@ typedef struct {
  *   of dlogits for all rows, row-major (1.05 GB), and h transposed (67 MB);
  * - the fp32 grad_hidden partial carried across the chunks (134 MB);
  * - per-128-row bias partial sums (33 MB).
- * With N >= V it chunks rows instead and holds the fp32 grad_weight partial
- * (V x H x 4 bytes) with FLCE_ACCUM_FP32. No workspace of either layout
- * reaches the N x V x 2 bytes of the logits in 16 bits.
+ * With N >= V it chunks rows instead (half of the rows of dlogits per chunk,
+ * and h transposed) and holds the fp32 grad_weight partial (H x round_up(V, 8)
+ * x 4 bytes) with FLCE_ACCUM_FP32. No workspace of either layout reaches the
+ * N x V x 2 bytes of the logits in 16 bits.
  * Returns FLCE_OK and sets *bytes, or an argument error.
  */
 int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);

@@ -359,7 +359,8 @@ struct BwdLayout {
   int64_t chunk, V_pad;     // rows (or columns) per chunk
   int64_t ds_ld;            // row stride of the dlogits buffer, in elements
   int64_t ds_t_ld;          // row stride of the transposed dlogits buffer (tensor path)
-  int64_t ht_ld;            // row stride of the transposed hidden (tensor path, vocabulary chunks)
+  int64_t ht_ld;            // row stride of the transposed hidden (tensor path)
+  int64_t dw_ld;            // row stride of the fp32 grad_weight partial (row chunks)
   bool wt;                  // grad_weight computed transposed, from h^T and the row-major dlogits
   int nchunks, rowblk, n_rowblocks;
   size_t cnt, coef, ds, ds_t, ht, dw, dh_part, bias_part, total;
@@ -378,14 +379,16 @@ void place_counters(const flce_params* p, BwdLayout* L, size_t* o) {
 
 // The backward stores dlogits for one chunk at a time and contracts it into
 // both gradients. grad_hidden (K = vocabulary) reads the row-major copy
-// K-major. With vocabulary chunks the tensor path computes grad_weight
-// transposed, (h^T dS)^T, reading that same copy as its MN-major B operand
-// and a transposed copy of h as its K-major A, so one dlogits copy suffices;
-// with row chunks it keeps a second, transposed dlogits copy that grad_weight
-// (K = rows) reads K-major. Together the copies hold about half of the N x V logits, and at
-// most 4 GiB. Whatever crosses chunks is
-// summed in an fp32 partial: grad_weight [V, H] when the chunks are row
-// ranges, grad_hidden [N, H] when they are vocabulary ranges. The tensor path
+// K-major. The tensor path computes grad_weight transposed, (h^T dS)^T,
+// reading that same copy as its MN-major B operand and a transposed copy of h
+// as its K-major A, so one dlogits copy suffices. Only row chunks that add
+// into existing gradients through the fp32 grad_weight partial keep a second,
+// transposed dlogits copy that grad_weight (K = rows) reads K-major, because
+// that partial starts from the output in its own [V, H] layout. The copies
+// hold about half of the N x V logits, and at most 4 GiB. Whatever crosses
+// chunks is summed in an fp32 partial: grad_weight (as [H, V] when computed
+// transposed) when the chunks are row ranges, grad_hidden [N, H] when they
+// are vocabulary ranges. The tensor path
 // chunks the vocabulary whenever N < V, where that partial is the smaller one:
 // each chunk's grad_weight rows are then complete after one GEMM over all N
 // rows. flce_params.bwd_chunk_axis fixes the axis, so that callers and tests
@@ -462,14 +465,20 @@ BwdLayout bwd_layout(const flce_params* p) {
     return L;
   }
   L.ds_ld = L.V_pad;
-  // Row chunks of a quarter of the rows: two 16-bit copies (tensor path) or
-  // one fp32 copy (SIMT path) then hold about N x V bytes, half of the logits
-  // in bf16. Chunk boundaries fall on 256-row pair blocks (tensor path) or
-  // 64-row SIMT tiles.
-  const int copies = tensor_path(p) ? 2 : 1;
+  // Row chunks whose dlogits copies hold about N x V bytes, half of the
+  // logits in bf16: one 16-bit row-major copy of half of the rows (the tensor
+  // path, grad_weight computed transposed from a transposed copy of h), two
+  // 16-bit copies of a quarter (the tensor path adding into existing
+  // gradients through an fp32 grad_weight partial, which starts from the
+  // output in grad_weight's own layout), or one fp32 copy of a quarter (the
+  // fp32 path). Chunk boundaries fall on 256-row pair blocks (tensor path)
+  // or 64-row SIMT tiles.
+  L.wt = tensor_path(p) && !(p->grad_weight_accum == FLCE_ACCUM_FP32 && p->accumulate);
+  const int copies = tensor_path(p) && !L.wt ? 2 : 1;
   const int64_t gran = tensor_path(p) ? kPairM : kSimtTile;
   {
-    const int64_t quarter = ceil_div(ceil_div(N, 4), gran) * gran;
+    const int64_t parts = L.wt ? 2 : 4;
+    const int64_t quarter = ceil_div(ceil_div(N, parts), gran) * gran;
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem * copies)) /
                   gran * gran;
     if (cap < gran) cap = gran;
@@ -486,11 +495,16 @@ BwdLayout bwd_layout(const flce_params* p) {
   L.rowblk = tensor_path(p) ? kBM : kSimtTile;
   L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
   L.ds_t_ld = (L.chunk + 7) / 8 * 8;
+  L.ht_ld = (N + 7) / 8 * 8;
+  // the fp32 grad_weight partial, in the layout the contraction produces:
+  // grad_weight^T [H][V_pad] when it is computed transposed, else [V][H]
+  L.dw_ld = L.wt ? L.V_pad : H;
   L.coef_bytes = size_t(N) * sizeof(float4);
   L.ds_bytes = size_t(L.chunk) * L.V_pad * elem;
-  L.ds_t_bytes = tensor_path(p) ? size_t(V) * L.ds_t_ld * elem : 0;
+  L.ds_t_bytes = tensor_path(p) && !L.wt ? size_t(V) * L.ds_t_ld * elem : 0;
+  L.ht_bytes = L.wt ? size_t(H) * L.ht_ld * 2 : 0;
   L.dw_bytes = (tensor_path(p) && L.nchunks > 1 && p->grad_weight_accum == FLCE_ACCUM_FP32)
-                   ? size_t(V) * H * 4 : 0;
+                   ? size_t(L.wt ? H : V) * L.dw_ld * 4 : 0;
   if (tensor_path(p)) {
     L.dh_bytes = size_t(kMaxKSplits) * L.chunk * H * 4;
   } else if (N > 0) {
@@ -505,6 +519,8 @@ BwdLayout bwd_layout(const flce_params* p) {
   o = align_up(o + L.ds_bytes, 1024);
   L.ds_t = o;
   if (L.ds_t_bytes) o = align_up(o + L.ds_t_bytes, 1024);
+  L.ht = o;
+  if (L.ht_bytes) o = align_up(o + L.ht_bytes, 1024);
   L.dw = o;
   if (L.dw_bytes) o = align_up(o + L.dw_bytes, 1024);
   L.dh_part = o;
@@ -1207,7 +1223,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
     if ((v = make_map(&tm_w, weight, H, V, uint64_t(H) * 2, kBK, kBNHalf, dt)) != FLCE_OK) return v;
     float* dw_part = reinterpret_cast<float*>(ws + L.dw);
     const int nchunks_rows = L.vocab ? 0 : L.nchunks;
-    if (L.vocab && L.wt && grad_weight) {
+    if (L.wt && grad_weight) {
       // h^T [H][ht_ld], the K-major A operand of the transposed grad_weight
       TransposeArgs ta{};
       ta.src = static_cast<const uint16_t*>(hidden);
@@ -1381,7 +1397,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.num_panels = static_cast<int>(ceil_div(da.v_tiles, da.panel_tiles));
       da.num_units = da.num_panels * da.n_blocks;
       da.bias_blk0 = row0 / kBM;
-      da.ds_t = grad_weight != nullptr ? ws + L.ds_t : nullptr;
+      da.ds_t = grad_weight != nullptr && !L.wt ? ws + L.ds_t : nullptr;
       da.ld_t = L.ds_t_ld;
       v = launch("flce_dlogits_tc", st, [&] {
         da.clk = g_cur_clk;
@@ -1438,7 +1454,56 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
           if (v != FLCE_OK) return v;
         }
       }
-      if (grad_weight) {
+      if (grad_weight && L.wt) {
+        // grad_weight[V, H] (+)= (h^T[H, row0:row0+rows] (K-major, columns of
+        // the transposed copy of h) x dS[rows, V] (MN-major through the 3-D
+        // view))^T. Across row chunks: the fp32 partial grad_weight^T
+        // [H][dw_ld] (started by the first chunk, added to by the middle
+        // ones, added and stored transposed by the last), or, accumulating in
+        // the weight dtype, the output read, added and rewritten transposed.
+        GemmOperand op_a, op_b;
+        GemmArgs ga{};
+        const uint8_t* htc = ws + L.ht + size_t(row0) * 2;
+        if ((v = make_k_operand(&op_a, htc, rows, H, uint64_t(L.ht_ld) * 2, kBM, dt)) != FLCE_OK)
+          return v;
+        if ((v = make_mn_operand(&op_b, &ga.b_atoms, da.ds, V, rows, ds_row_bytes, dt)) != FLCE_OK)
+          return v;
+        ga.M = H;
+        ga.N = V;
+        ga.K = rows;
+        ga.m_tiles = static_cast<int>(ceil_div(H, kPairM));
+        ga.n_tiles = static_cast<int>(ceil_div(V, kBN));
+        ga.k_blocks = static_cast<int>(ceil_div(rows, kBK));
+        ga.num_tiles = ga.m_tiles * ga.n_tiles;
+        ga.k_splits = 1;
+        ga.kb_per_split = ga.k_blocks;
+        ga.a_mn = 0;
+        ga.b_mn = 1;
+        if (p->grad_weight_accum == FLCE_ACCUM_WEIGHT || L.nchunks == 1)
+          ga.mode = (c > 0 || p->accumulate) ? kAddOutToOutT : kStoreOutT;
+        else if (c == 0)
+          ga.mode = kStorePart;
+        else if (c == L.nchunks - 1)
+          ga.mode = kAddPartToOutT;
+        else
+          ga.mode = kAddPart;
+        ga.out_t = grad_weight;
+        ga.ld_out_t = H;
+        ga.part = dw_part;
+        ga.ld_part = L.dw_ld;
+        ga.acc_scale = acc_scale;
+        ga.status = status;
+        ga.r_out_t = r_gw;
+        ga.r_part = r_dw;
+        // the chunk's columns of h^T stay in L2 while the dlogits columns
+        // stream through once
+        ga.a_l2 = kL2EvictLast;
+        ga.b_l2 = kL2EvictFirst;
+        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
+        v = launch("flce_grad_weight_tc", st,
+                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
+        if (v != FLCE_OK) return v;
+      } else if (grad_weight) {
         // grad_weight[V, H] (+)= dS^T[V, rows] (K-major, the transposed copy)
         // x h[rows, H] (MN-major)
         GemmOperand op_a, op_b;

@@ -67,21 +67,43 @@ def test_workspace_sizes(lib):
     assert _lib.workspace_regions(pa, _lib.FLCE_PASS_BACKWARD) == \
         _lib.workspace_regions(p, _lib.FLCE_PASS_BACKWARD)
     assert bwd < 8192 * 128256 * 2              # less than one N x V buffer
-    # row chunks: two copies of a quarter of the rows, the fp32 grad_weight
-    # partial and two fp32 K-split partials of grad_hidden
+    # row chunks: one row-major copy of half of the rows, h transposed (grad_weight
+    # is computed as (h^T dS)^T here too), the fp32 grad_weight^T partial [H][V]
+    # and two fp32 K-split partials of grad_hidden
     pr = _lib.FlceParams.from_buffer_copy(p)
     pr.bwd_chunk_axis = _lib.FLCE_CHUNK_AXIS_ROWS
     bwd_rows = _lib.workspace_bytes(pr, _lib.FLCE_PASS_BACKWARD)
-    chunk = 2 * 2048 * 128256 * 2
-    dw = 128256 * 4096 * 4
-    dh = 2 * 2048 * 4096 * 4
-    assert chunk + dw + dh < bwd_rows < chunk + dw + dh + (64 << 20)
+    chunk = 4096 * 128256 * 2
+    dw = 4096 * 128256 * 4
+    dh = 2 * 4096 * 4096 * 4
+    assert chunk + ht + dw + dh < bwd_rows < chunk + ht + dw + dh + (64 << 20)
+    regions = {n: b for n, _, b in _lib.workspace_regions(pr, _lib.FLCE_PASS_BACKWARD)}
+    assert regions["dlogits"] == chunk and regions["hidden_transposed"] == ht
+    assert regions["grad_weight_fp32"] == dw and "dlogits_transposed" not in regions
     assert bwd_rows < 8192 * 128256 * 2 + dw
+    # adding into existing gradients through the fp32 partial: that partial starts
+    # from grad_weight in its [V, H] layout, so grad_weight reads a transposed
+    # dlogits copy (K = rows), and each of the two copies holds a quarter of the rows
+    pra = _lib.FlceParams.from_buffer_copy(pr)
+    pra.accumulate = 1
+    regions = {n: b for n, _, b in _lib.workspace_regions(pra, _lib.FLCE_PASS_BACKWARD)}
+    assert regions["dlogits"] == 2048 * 128256 * 2
+    assert regions["dlogits_transposed"] == 128256 * 2048 * 2
+    assert regions["grad_weight_fp32"] == 128256 * 4096 * 4 and "hidden_transposed" not in regions
+    # accumulating in the weight dtype needs no partial and keeps one copy
+    prw = _lib.FlceParams.from_buffer_copy(pra)
+    prw.grad_weight_accum = _lib.FLCE_ACCUM_WEIGHT
+    regions = {n: b for n, _, b in _lib.workspace_regions(prw, _lib.FLCE_PASS_BACKWARD)}
+    assert regions["dlogits"] == chunk and "dlogits_transposed" not in regions
+    assert "grad_weight_fp32" not in regions
     # N > V: row chunks by default
     q = params(N=65536, H=1024, V=32000)
-    chunk = 2 * 16384 * 32000 * 2
-    dw = 32000 * 1024 * 4
-    assert chunk + dw < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < chunk + dw + (300 << 20)
+    chunk = 32768 * 32000 * 2
+    ht = 1024 * 65536 * 2
+    dw = 1024 * 32000 * 4
+    dh = 2 * 32768 * 1024 * 4
+    assert chunk + ht + dw + dh < _lib.workspace_bytes(q, _lib.FLCE_PASS_BACKWARD) < \
+        chunk + ht + dw + dh + (64 << 20)
     # the fp32 path keeps one copy of a quarter of the rows: together with the
     # 16-bit paths' two copies of a quarter, about N x V bytes
     f = params(N=4096, H=1024, V=3000, dtype=_lib.FLCE_F32)

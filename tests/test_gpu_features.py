@@ -44,16 +44,19 @@ def dev_tensor(x, dtype):
     return torch.from_numpy(x).cuda()
 
 
-@pytest.mark.parametrize("dtype,N,H,V,axis,chunk_cap", [
-    ("bf16", 1200, 2560, 16500, "rows", None),  # grad_hidden with 2 K splits, 3 row chunks
-    ("bf16", 700, 136, 900, "rows", 256),       # 3 row chunks
-    ("bf16", 600, 256, 16500, "vocab", None),   # 2 vocabulary chunks of 8448 columns
-    ("bf16", 700, 136, 900, "vocab", 256),      # 4 vocabulary chunks of 256 columns
-    ("bf16", 200, 64, 250, "vocab", None),      # 1 vocabulary chunk (V < 256)
-    ("f32", 150, 64, 700, None, None),
+@pytest.mark.parametrize("dtype,N,H,V,axis,chunk_cap,accum", [
+    ("bf16", 1200, 2560, 16500, "rows", None, "fp32"),  # grad_hidden with 2 K splits, 3 row chunks
+    ("bf16", 700, 136, 900, "rows", 256, "fp32"),       # 3 row chunks
+    # 3 row chunks, grad_weight (computed transposed) read, added and rewritten by each
+    ("bf16", 700, 136, 900, "rows", 256, "weight"),
+    ("bf16", 600, 256, 16500, "vocab", None, "fp32"),   # 2 vocabulary chunks of 8448 columns
+    ("bf16", 700, 136, 900, "vocab", 256, "fp32"),      # 4 vocabulary chunks of 256 columns
+    ("bf16", 200, 64, 250, "vocab", None, "fp32"),      # 1 vocabulary chunk (V < 256)
+    ("f32", 150, 64, 700, None, None, "fp32"),
 ])
-def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap):
-    schedule = dict(bwd_chunk_axis=axis or "auto", max_chunk=chunk_cap or 0)
+def test_accumulate_into_existing_gradients(dtype, N, H, V, axis, chunk_cap, accum):
+    schedule = dict(bwd_chunk_axis=axis or "auto", max_chunk=chunk_cap or 0,
+                    grad_weight_accum=accum)
     d = small_case(N, H, V, seed=N + V, dtype=dtype, bias=True, ignore_frac=0.1)
     kw = dict(reduction="mean", softcap=15.0, z_loss_multiplier=1e-3)
     gh, gw, gb = oracle.backward(d["hidden"], d["weight"], d["targets"], bias=d["bias"], **kw)
