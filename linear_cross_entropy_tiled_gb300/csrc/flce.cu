@@ -478,7 +478,7 @@ BwdLayout bwd_layout(const flce_params* p) {
   const int64_t gran = tensor_path(p) ? kPairM : kSimtTile;
   {
     const int64_t parts = L.wt ? 2 : 4;
-    const int64_t quarter = ceil_div(ceil_div(N, parts), gran) * gran;
+    const int64_t share = ceil_div(ceil_div(N, parts), gran) * gran;
     int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(L.V_pad) * elem * copies)) /
                   gran * gran;
     if (cap < gran) cap = gran;
@@ -488,7 +488,7 @@ BwdLayout bwd_layout(const flce_params* p) {
       const int64_t r = p->max_chunk < gran ? gran : p->max_chunk / gran * gran;
       if (r < cap) cap = r;
     }
-    L.chunk = quarter < cap ? quarter : cap;
+    L.chunk = share < cap ? share : cap;
     if (L.chunk > N && N > 0) L.chunk = N;
   }
   L.nchunks = N > 0 ? static_cast<int>(ceil_div(N, L.chunk)) : 0;

@@ -287,23 +287,32 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
 
 // 32 x 32 tiles through shared memory (one element per 32-bit word, a
 // 33-word row pitch, so that neither the row reads nor the column reads
-// conflict); 32 x 8 threads, four rows each.
+// conflict); 32 x 8 threads, four rows each. The blocks walk the tiles in
+// order, column tiles fastest, so any number of rows fits one launch.
 __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a) {
   __shared__ uint32_t tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const long long col_tiles = (a.cols + 31) / 32;
+  const long long tiles = col_tiles * ((a.rows + 31) / 32);
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const long long r0 = t / col_tiles * 32;
+    const int c0 = static_cast<int>(t % col_tiles) * 32;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = r0 + ty + 8 * i, c = c0 + tx;
-    tile[ty + 8 * i][tx] = (r < a.rows && c < a.cols) ? a.src[r * a.ld_src + c] : 0u;
-  }
-  __syncthreads();
+    for (int i = 0; i < 4; ++i) {
+      const long long r = r0 + ty + 8 * i;
+      const int c = c0 + tx;
+      tile[ty + 8 * i][tx] = (r < a.rows && c < a.cols) ? a.src[r * a.ld_src + c] : 0u;
+    }
+    __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int c = c0 + ty + 8 * i, r = r0 + tx;
-    uint16_t* const dst = a.dst + c * a.ld_dst + r;
-    if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
-      *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
+    for (int i = 0; i < 4; ++i) {
+      const int c = c0 + ty + 8 * i;
+      const long long r = r0 + tx;
+      uint16_t* const dst = a.dst + c * a.ld_dst + r;
+      if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
+        *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
+    }
+    __syncthreads();   // the tile is read out before the next one is written
   }
 }
 
@@ -461,7 +470,8 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_transpose16(const TransposeArgs& a, cudaStream_t s) {
-  const dim3 grid((a.cols + 31) / 32, (a.rows + 31) / 32);
+  const long long tiles = static_cast<long long>((a.cols + 31) / 32) * ((a.rows + 31) / 32);
+  const unsigned grid = static_cast<unsigned>(tiles < 65536 ? (tiles < 1 ? 1 : tiles) : 65536);
   transpose16_kernel<<<grid, 256, 0, s>>>(a);
   note_launch();
   return cudaGetLastError();

@@ -332,8 +332,11 @@ __global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG)
   SimtSmem<KG>& sm = *reinterpret_cast<SimtSmem<KG>*>(smem_raw);
   // per-column sums for grad_bias: the tile's dlogits, staged in 16-byte pieces
   float (&G)[T][T + 4] = *reinterpret_cast<float (*)[T][T + 4]>(smem_raw + sizeof(SimtSmem<KG>));
-  const int c0 = blockIdx.x * T;
-  const int rb = blockIdx.y;
+  // one 1-D grid over the chunk's tiles, column tiles fastest (a 2-D grid
+  // would cap the row tiles at 65535)
+  const int ct = (a.V + T - 1) / T;
+  const int c0 = static_cast<int>(blockIdx.x % ct) * T;
+  const int rb = static_cast<int>(blockIdx.x / ct);
   const int r0 = rb * T;  // local to the chunk
   const int tid = threadIdx.x, g = tid / kSimtThreads, lt = tid % kSimtThreads;
   const int tx = lt & 7, ty = lt >> 3;
@@ -485,7 +488,10 @@ __device__ __forceinline__ void gemm_simt_block(const SimtGemmArgs& a, int bx, i
 
 template <int KG>
 __global__ void __launch_bounds__(KG * kSimtThreads, 4 / KG) gemm_simt_kernel(const SimtGemmArgs a) {
-  gemm_simt_block<KG>(a, blockIdx.x, blockIdx.y, blockIdx.z);
+  // one 1-D grid: column tiles fastest, then row tiles, then K splits
+  const int nx = (a.N + T - 1) / T, ny = (a.M + T - 1) / T;
+  const int b = static_cast<int>(blockIdx.x);
+  gemm_simt_block<KG>(a, b % nx, (b / nx) % ny, b / (nx * ny));
 }
 
 // Two independent products in one grid: units [0, n1) are the first
@@ -608,10 +614,11 @@ cudaError_t launch_fwd_simt(const float* h, const float* w, const FwdArgs& a, cu
 }
 
 cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cudaStream_t s) {
-  const dim3 grid((a.V + T - 1) / T, (a.rows + T - 1) / T);
-  return groups_for(static_cast<long long>(grid.x) * grid.y) == 2
-             ? launch_ds_kg<2>(h, w, a, grid, s)
-             : launch_ds_kg<1>(h, w, a, grid, s);
+  const long long tiles = static_cast<long long>((a.V + T - 1) / T) * ((a.rows + T - 1) / T);
+  if (tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(tiles));
+  return groups_for(tiles) == 2 ? launch_ds_kg<2>(h, w, a, grid, s)
+                                : launch_ds_kg<1>(h, w, a, grid, s);
 }
 
 namespace {
@@ -655,10 +662,12 @@ cudaError_t launch_gemm_simt2(const SimtGemmArgs& a1, const SimtGemmArgs& a2, in
 
 cudaError_t launch_gemm_simt(const SimtGemmArgs& a, cudaStream_t s) {
   const int splits = a.k_splits > 1 ? a.k_splits : 1;
-  const dim3 grid((a.N + T - 1) / T, (a.M + T - 1) / T, splits);
-  cudaError_t e = groups_for(static_cast<long long>(grid.x) * grid.y * grid.z) == 2
-                      ? launch_gemm_kg<2>(a, grid, s)
-                      : launch_gemm_kg<1>(a, grid, s);
+  const long long blocks =
+      static_cast<long long>((a.N + T - 1) / T) * ((a.M + T - 1) / T) * splits;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  cudaError_t e = groups_for(blocks) == 2 ? launch_gemm_kg<2>(a, grid, s)
+                                          : launch_gemm_kg<1>(a, grid, s);
   if (e != cudaSuccess) return e;
   return split_reduce_after(a, s);
 }

@@ -154,12 +154,13 @@ def test_more_than_2_to_the_32_logits():
 
     The backward runs both ways, on the same inputs:
 
-    * row chunks: a quarter of the rows would pass the 4 GiB cap of the two
-      dlogits copies, so it runs 5 chunks (4 of 16128 rows, then 1024). That
-      drives the fp32 grad_weight partial through store, add and add-and-cast
-      at scale;
-    * vocabulary chunks: 5 chunks (4 of 13312 columns, then 12289), with the
-      fp32 grad_hidden partial through the same three steps.
+    * row chunks: half of the rows would pass the 4 GiB cap of the dlogits
+      copy, so it runs 3 chunks (2 of 32512 rows, then 512). That drives the
+      fp32 grad_weight^T partial through store, add and add-and-store-
+      transposed at scale;
+    * vocabulary chunks: half of the columns would pass the same cap, so it
+      runs 3 chunks (2 of 22016 columns, then 21505), with the fp32
+      grad_hidden partial through the same three steps.
 
     V = 65537 leaves one column in the last vocabulary tile.
     """
@@ -169,11 +170,11 @@ def test_more_than_2_to_the_32_logits():
     okw = oracle_kw(w)
     ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"],
                          reduction=w.reduction, row_block=2048, **okw)
-    rows = sample_rows(w.N, [16128, 32256, 64512], seed=1)
+    rows = sample_rows(w.N, [32512, 65024], seed=1)
     gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows, bias=d["bias"],
                                  reduction=w.reduction, **okw)
     J = sample_vocab(w.V, d["targets"], seed=2)
-    J = np.union1d(J, [13311, 13312, 26623, 26624, 53247, 53248])
+    J = np.union1d(J, [22015, 22016, 44031, 44032])
     gw, gb = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
                                      bias=d["bias"], reduction=w.reduction, **okw)
     for axis in ("rows", "vocab"):
@@ -184,3 +185,33 @@ def test_more_than_2_to_the_32_logits():
         assert_sampled_grad(out["grad_hidden"][rows], gh, f"grad_hidden rows ({axis})")
         assert_sampled_grad(out["grad_weight"][J], gw, f"grad_weight rows ({axis})")
         assert_sampled_grad(out["grad_bias"][J], gb, f"grad_bias entries ({axis})")
+
+
+def test_more_row_tiles_than_a_grid_dimension_holds():
+    """N = 2,100,001 rows of bf16 (H = 64, V = 520, so row chunks: 1050112
+    rows, then 1049889). h then has more 32-row tiles (65626) than the 65535
+    blocks a grid's y dimension holds; its transposition walks the tiles from
+    a 1-D grid. The loss and every row's lse against the oracle's full
+    forward; grad_hidden on sampled rows, including both sides of the chunk
+    boundary and of row 65535 x 32; grad_weight and grad_bias on sampled
+    vocabulary rows, including both sides of the last tile boundary.
+    """
+    w = wl.Workload("many_rows", N=2_100_001, H=64, V=520, bias=True, ignore_frac=0.05,
+                    reduction="mean", z_loss_multiplier=1e-4, seed=777)
+    d = wl.generate(w)
+    okw = oracle_kw(w)
+    ref = oracle.forward(d["hidden"], d["weight"], d["targets"], bias=d["bias"],
+                         reduction=w.reduction, row_block=65536, **okw)
+    rows = sample_rows(w.N, [1050112, 65535 * 32], seed=3)
+    gh = oracle.grad_hidden_rows(d["hidden"], d["weight"], d["targets"], rows, bias=d["bias"],
+                                 reduction=w.reduction, **okw)
+    J = np.union1d(sample_vocab(w.V, d["targets"], seed=4), [255, 256, 511, 512, 519])
+    gw, gb = oracle.grad_weight_rows(d["hidden"], d["weight"], d["targets"], ref["lse"], J,
+                                     bias=d["bias"], reduction=w.reduction, **okw)
+    out = run_gpu(d, "bf16", kw_of(w))
+    assert out["status_fwd"] == 0 and out["status_bwd"] == 0
+    assert_loss_close(out["loss"], ref["loss"], "bf16")
+    assert_lse_close(out["lse"], ref["lse"])
+    assert_sampled_grad(out["grad_hidden"][rows], gh, "grad_hidden rows")
+    assert_sampled_grad(out["grad_weight"][J], gw, "grad_weight rows")
+    assert_sampled_grad(out["grad_bias"][J], gb, "grad_bias entries")
