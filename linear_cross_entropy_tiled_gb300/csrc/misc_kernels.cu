@@ -291,12 +291,17 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
 // order, column tiles fastest, so any number of rows fits one launch.
 __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a) {
   __shared__ uint32_t tile[32][33];
-  const long long col_tiles = (a.cols + 31) / 32;
-  const long long tiles = col_tiles * ((a.rows + 31) / 32);
+  const int col_tiles = (a.cols + 31) / 32, row_tiles = (a.rows + 31) / 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const long long r0 = t / col_tiles * 32;
-    const int c0 = static_cast<int>(t % col_tiles) * 32;
+  // tile (rt, ct) = (t / col_tiles, t % col_tiles) for t = blockIdx.x,
+  // blockIdx.x + gridDim.x, ...: stepped without a division per tile
+  const int step_r = static_cast<int>(gridDim.x) / col_tiles;
+  const int step_c = static_cast<int>(gridDim.x) % col_tiles;
+  int rt = static_cast<int>(blockIdx.x) / col_tiles;
+  int ct = static_cast<int>(blockIdx.x) % col_tiles;
+  for (; rt < row_tiles; rt += step_r) {
+    const long long r0 = static_cast<long long>(rt) * 32;
+    const int c0 = ct * 32;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const long long r = r0 + ty + 8 * i;
@@ -313,6 +318,11 @@ __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a)
         *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
     }
     __syncthreads();   // the tile is read out before the next one is written
+    ct += step_c;
+    if (ct >= col_tiles) {
+      ct -= col_tiles;
+      ++rt;
+    }
   }
 }
 
