@@ -287,21 +287,14 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
 
 // 32 x 32 tiles through shared memory (one element per 32-bit word, a
 // 33-word row pitch, so that neither the row reads nor the column reads
-// conflict); 32 x 8 threads, four rows each. The blocks walk the tiles in
-// order, column tiles fastest, so any number of rows fits one launch.
+// conflict); 32 x 8 threads, four rows each. blockIdx.x is the column tile;
+// blockIdx.y steps through the row tiles by gridDim.y, which is at most
+// 65535, so any number of rows fits one launch.
 __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a) {
   __shared__ uint32_t tile[32][33];
-  const int col_tiles = (a.cols + 31) / 32, row_tiles = (a.rows + 31) / 32;
+  const int c0 = blockIdx.x * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  // tile (rt, ct) = (t / col_tiles, t % col_tiles) for t = blockIdx.x,
-  // blockIdx.x + gridDim.x, ...: stepped without a division per tile
-  const int step_r = static_cast<int>(gridDim.x) / col_tiles;
-  const int step_c = static_cast<int>(gridDim.x) % col_tiles;
-  int rt = static_cast<int>(blockIdx.x) / col_tiles;
-  int ct = static_cast<int>(blockIdx.x) % col_tiles;
-  for (; rt < row_tiles; rt += step_r) {
-    const long long r0 = static_cast<long long>(rt) * 32;
-    const int c0 = ct * 32;
+  for (long long r0 = blockIdx.y * 32ll; r0 < a.rows; r0 += gridDim.y * 32ll) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const long long r = r0 + ty + 8 * i;
@@ -317,12 +310,7 @@ __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a)
       if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
         *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
     }
-    __syncthreads();   // the tile is read out before the next one is written
-    ct += step_c;
-    if (ct >= col_tiles) {
-      ct -= col_tiles;
-      ++rt;
-    }
+    if (r0 + gridDim.y * 32ll < a.rows) __syncthreads();   // read out before the next tile
   }
 }
 
@@ -480,8 +468,8 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_transpose16(const TransposeArgs& a, cudaStream_t s) {
-  const long long tiles = static_cast<long long>((a.cols + 31) / 32) * ((a.rows + 31) / 32);
-  const unsigned grid = static_cast<unsigned>(tiles < 65536 ? (tiles < 1 ? 1 : tiles) : 65536);
+  const int row_tiles = (a.rows + 31) / 32;
+  const dim3 grid((a.cols + 31) / 32, row_tiles < 1 ? 1 : (row_tiles < 65535 ? row_tiles : 65535));
   transpose16_kernel<<<grid, 256, 0, s>>>(a);
   note_launch();
   return cudaGetLastError();
