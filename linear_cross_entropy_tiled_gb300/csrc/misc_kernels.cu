@@ -285,32 +285,44 @@ __global__ void __launch_bounds__(kMergeThreads) combine_kernel(const CombineArg
 }
 
 
-// 32 x 32 tiles through shared memory (one element per 32-bit word, a
-// 33-word row pitch, so that neither the row reads nor the column reads
-// conflict); 32 x 8 threads, four rows each. blockIdx.x is the column tile;
-// blockIdx.y steps through the row tiles by gridDim.y, which is at most
-// 65535, so any number of rows fits one launch.
+// One 32 x 32 tile of the transposition, rows [r0, r0 + 32) and columns
+// [c0, c0 + 32) of the source, through shared memory (one element per 32-bit
+// word, a 33-word row pitch, so that neither the row reads nor the column
+// reads conflict); 32 x 8 threads, four rows each.
+template <typename R>
+__device__ __forceinline__ void transpose_tile(const TransposeArgs& a, uint32_t (&tile)[32][33],
+                                               R r0, int c0, int tx, int ty) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const R r = r0 + ty + 8 * i;
+    const int c = c0 + tx;
+    tile[ty + 8 * i][tx] = (r < a.rows && c < a.cols) ? a.src[r * a.ld_src + c] : 0u;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + ty + 8 * i;
+    const R r = r0 + tx;
+    uint16_t* const dst = a.dst + c * a.ld_dst + r;
+    if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
+      *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
+  }
+}
+
+// blockIdx.x is the column tile and blockIdx.y the row tile. gridDim.y is at
+// most 65535; past 65535 row tiles (2,097,120 rows) each block steps through
+// the row tiles by gridDim.y, so any number of rows fits one launch.
 __global__ void __launch_bounds__(256) transpose16_kernel(const TransposeArgs a) {
   __shared__ uint32_t tile[32][33];
   const int c0 = blockIdx.x * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  if (gridDim.y * 32ll >= a.rows) {
+    transpose_tile<int>(a, tile, static_cast<int>(blockIdx.y) * 32, c0, tx, ty);
+    return;
+  }
   for (long long r0 = blockIdx.y * 32ll; r0 < a.rows; r0 += gridDim.y * 32ll) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const long long r = r0 + ty + 8 * i;
-      const int c = c0 + tx;
-      tile[ty + 8 * i][tx] = (r < a.rows && c < a.cols) ? a.src[r * a.ld_src + c] : 0u;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = c0 + ty + 8 * i;
-      const long long r = r0 + tx;
-      uint16_t* const dst = a.dst + c * a.ld_dst + r;
-      if (c < a.cols && r < a.rows && store_allowed(dst, 2, a.r_dst, a.status))
-        *dst = static_cast<uint16_t>(tile[tx][ty + 8 * i]);
-    }
-    if (r0 + gridDim.y * 32ll < a.rows) __syncthreads();   // read out before the next tile
+    transpose_tile<long long>(a, tile, r0, c0, tx, ty);
+    __syncthreads();   // the tile is read out before the next one is written
   }
 }
 
