@@ -416,27 +416,24 @@ BwdLayout bwd_layout(const flce_params* p) {
     // then the columns are spread evenly over the chunks.
     // flce_params.max_chunk (rounded down to whole tiles) lowers the cap.
     L.wt = tensor_path(p);
-    const int copies = tensor_path(p) && !L.wt ? 2 : 1;
     const int64_t gran = tensor_path(p) ? kBN : kSimtTile;
-    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem * copies)) / gran * gran;
+    int64_t cap = static_cast<int64_t>(kChunkByteCap / (size_t(N) * elem)) / gran * gran;
     if (cap < gran) cap = gran;
     if (p->max_chunk > 0) {
       const int64_t c = p->max_chunk < gran ? gran : p->max_chunk / gran * gran;
       if (c < cap) cap = c;
     }
-    int64_t w = ceil_div(ceil_div(V, int64_t(copies) * int64_t(elem)), gran) * gran;
+    int64_t w = ceil_div(ceil_div(V, int64_t(elem)), gran) * gran;
     if (w > cap) w = cap;
     L.nchunks = static_cast<int>(ceil_div(V, w));
     L.chunk = L.nchunks == 1 ? V : ceil_div(ceil_div(V, L.nchunks), gran) * gran;
     L.nchunks = static_cast<int>(ceil_div(V, L.chunk));
     L.ds_ld = (L.chunk + 7) / 8 * 8;
-    L.ds_t_ld = (N + 7) / 8 * 8;
     L.ht_ld = (N + 7) / 8 * 8;
     L.rowblk = tensor_path(p) ? kBM : kSimtTile;
     L.n_rowblocks = static_cast<int>(ceil_div(N, L.rowblk));
     L.coef_bytes = size_t(N) * sizeof(float4);
     L.ds_bytes = size_t(N) * L.ds_ld * elem;
-    L.ds_t_bytes = tensor_path(p) && !L.wt ? size_t(L.chunk) * L.ds_t_ld * elem : 0;
     L.ht_bytes = L.wt ? size_t(H) * L.ht_ld * 2 : 0;
     if (tensor_path(p)) {
       L.dh_bytes = L.nchunks > 1 ? size_t(N) * H * 4 : 0;
@@ -452,8 +449,7 @@ BwdLayout bwd_layout(const flce_params* p) {
     o = align_up(o + L.coef_bytes, 256);
     L.ds = o;
     o = align_up(o + L.ds_bytes, 1024);
-    L.ds_t = o;
-    if (L.ds_t_bytes) o = align_up(o + L.ds_t_bytes, 1024);
+    L.ds_t = o;   // no transposed copy with vocabulary chunks
     L.ht = o;
     if (L.ht_bytes) o = align_up(o + L.ht_bytes, 1024);
     L.dw = o;
@@ -1253,8 +1249,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
       da.bias_part = bias_part != nullptr ? bias_part + v0 : nullptr;
       da.bias_blk0 = 0;
       da.tgt_base = v0;
-      da.ds_t = grad_weight != nullptr && !L.wt ? ws + L.ds_t : nullptr;
-      da.ld_t = L.ds_t_ld;
+      da.ds_t = nullptr;
       da.n_blocks = static_cast<int>(ceil_div(N, kPairM));
       da.v_tiles = static_cast<int>(ceil_div(vc, kBN));
       da.group_blocks = group_blocks_for(da.n_blocks, H);
@@ -1308,7 +1303,7 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
         if (v != FLCE_OK) return v;
       }
-      if (grad_weight && L.wt) {
+      if (grad_weight) {
         // grad_weight[v0:v0+vc, H] = (h^T[H, N] (K-major, the transposed copy
         // of h) x dS[N, vc] (MN-major through the 3-D view))^T: complete after
         // this one GEMM, whose epilogue stores its tiles transposed straight
@@ -1341,43 +1336,6 @@ int flce_backward(const flce_params* p, const void* hidden, const void* weight, 
         // dlogits chunk streams through once per group of row tiles
         ga.a_l2 = kL2EvictLast;
         ga.b_l2 = kL2EvictFirst;
-        const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
-        v = launch("flce_grad_weight_tc", st,
-                   [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
-        if (v != FLCE_OK) return v;
-      } else if (grad_weight) {
-        // grad_weight[v0:v0+vc, H] (+)= dS^T[vc, N] (K-major, the transposed
-        // copy) x h[N, H] (MN-major): complete after this one GEMM, so it goes
-        // straight to the output (or is added to it).
-        GemmOperand op_a, op_b;
-        GemmArgs ga{};
-        if ((v = make_k_operand(&op_a, da.ds_t, N, vc, uint64_t(L.ds_t_ld) * 2, kBM, dt)) != FLCE_OK)
-          return v;
-        if ((v = make_mn_operand(&op_b, &ga.b_atoms, hidden, H, N, uint64_t(H) * 2, dt)) != FLCE_OK)
-          return v;
-        ga.M = vc;
-        ga.N = H;
-        ga.K = N;
-        ga.m_tiles = static_cast<int>(ceil_div(vc, kPairM));
-        ga.n_tiles = static_cast<int>(ceil_div(H, kBN));
-        ga.k_blocks = static_cast<int>(ceil_div(N, kBK));
-        ga.num_tiles = ga.m_tiles * ga.n_tiles;
-        ga.k_splits = 1;
-        ga.kb_per_split = ga.k_blocks;
-        ga.a_mn = 0;
-        ga.b_mn = 1;
-        ga.mode = p->accumulate ? kAddOutToOut : kStoreOut;
-        ga.out = static_cast<uint8_t*>(grad_weight) + size_t(v0) * H * 2;
-        ga.ld_out = H;
-        ga.part = nullptr;
-        ga.ld_part = H;
-        ga.acc_scale = acc_scale;
-        ga.status = status;
-        ga.r_out = r_gw;
-        // h (64 MB at H = 4096, N = 8192) is read by every wave of tiles; the
-        // transposed dlogits stream through once
-        ga.a_l2 = kL2EvictFirst;
-        ga.b_l2 = kL2EvictLast;
         const int g2 = ga.num_tiles < d.pairs ? ga.num_tiles : d.pairs;
         v = launch("flce_grad_weight_tc", st,
                    [&] { return launch_gemm(op_a, op_b, ga, f16, g2, st); });
