@@ -181,8 +181,10 @@ typedef struct {
  * - per-128-row bias partial sums (33 MB).
  * With N >= V it chunks rows instead (half of the rows of dlogits per chunk,
  * and h transposed) and holds the fp32 grad_weight partial (H x round_up(V, 8)
- * x 4 bytes) with FLCE_ACCUM_FP32. No workspace of either layout reaches the
- * N x V x 2 bytes of the logits in 16 bits.
+ * x 4 bytes) with FLCE_ACCUM_FP32. Adding into existing gradients with
+ * FLCE_ACCUM_FP32 keeps two dlogits copies of a quarter of the rows (row-major
+ * and transposed) and a V x H x 4-byte partial instead. No workspace of either
+ * layout reaches the N x V x 2 bytes of the logits in 16 bits.
  * Returns FLCE_OK and sets *bytes, or an argument error.
  */
 int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
