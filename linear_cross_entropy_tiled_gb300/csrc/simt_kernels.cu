@@ -617,6 +617,8 @@ cudaError_t launch_ds_simt(const float* h, const float* w, const DsArgs& a, cuda
   const long long tiles = static_cast<long long>((a.V + T - 1) / T) * ((a.rows + T - 1) / T);
   if (tiles > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(tiles));
+  // at most one tile per SM: four K groups (16 warps) per block
+  if (tiles <= sm_count()) return launch_ds_kg<4>(h, w, a, grid, s);
   return groups_for(tiles) == 2 ? launch_ds_kg<2>(h, w, a, grid, s)
                                 : launch_ds_kg<1>(h, w, a, grid, s);
 }
