@@ -35,7 +35,8 @@ def kernels_of(fn):
 @pytest.mark.parametrize("dtype,N,H,V,bias", [
     ("f32", 256, 512, 8192, False),   # the fp32 workload's sizes: 4 vocabulary chunks
     ("f32", 130, 72, 600, True),
-    ("bf16", 600, 256, 4100, True),
+    ("bf16", 600, 256, 4100, True),   # N < V: 2 vocabulary chunks
+    ("bf16", 1200, 256, 600, True),   # N >= V: 2 row chunks of 768 and 432 rows
 ])
 def test_kernels_per_call(dtype, N, H, V, bias):
     d = small_case(N, H, V, seed=3, dtype=dtype, bias=bias, ignore_frac=0.1)
@@ -45,14 +46,36 @@ def test_kernels_per_call(dtype, N, H, V, bias):
     assert n_fwd == 2                         # logit tiles, merge (with the reduction)
     gl = torch.ones(1, device="cuda")
     n_bwd, _ = kernels_of(lambda: flce_backward(p, h, w, t, lse, gl, b))
-    # N < V: vocabulary chunks (four on the fp32 path, two on the 16-bit path,
-    # whose one dlogits copy holds half of the columns), each dlogits and both
-    # contractions (one grid on the fp32 path); row coefficients first (and
-    # h transposed on the 16-bit path), grad_bias's sum last
+    # vocabulary chunks (four on the fp32 path, two on the 16-bit path, whose
+    # one dlogits copy holds half of the columns) or, with N >= V, two row
+    # chunks of half of the rows: each dlogits and both contractions (one grid
+    # on the fp32 path; no K split at V = 600); row coefficients first (and h
+    # transposed on the 16-bit path), grad_bias's sum last
     if dtype == "f32":
         assert n_bwd == 1 + 2 * 4 + (1 if bias else 0)
     else:
         assert n_bwd == 2 + 3 * 2 + (1 if bias else 0)
+
+
+def test_row_chunks_adding_fp32_accumulated_grad_weight_keep_two_copies():
+    """Row chunks that add into existing gradients with fp32 accumulation: the
+    fp32 grad_weight partial starts from the output in its [V, H] layout, so
+    grad_weight reads a transposed dlogits copy and h is not transposed. Two
+    copies of a quarter of the rows: 3 chunks of 512, 512 and 176 rows."""
+    N, H, V = 1200, 256, 600
+    d = small_case(N, H, V, seed=8, dtype="bf16", bias=True, ignore_frac=0.1)
+    h, w, b, t = to_device(d, "bf16")
+    p = _lib.make_params(N=N, H=H, V=V, dtype=_lib.FLCE_BF16, has_bias=True, reduction="mean")
+    _, lse, _, _, _ = flce_forward(p, h, w, t, b)
+    out = (torch.zeros_like(h), torch.zeros_like(w), torch.zeros_like(b))
+    gl = torch.ones(1, device="cuda")
+    n_bwd, _ = kernels_of(lambda: flce_backward(p, h, w, t, lse, gl, b, accumulate=True, out=out))
+    assert n_bwd == 1 + 3 * 3 + 1
+    rgh, rgw, rgb = oracle.backward(d["hidden"], d["weight"], d["targets"], bias=d["bias"],
+                                    reduction="mean")
+    assert_grad_close(out[0].float().cpu().numpy(), rgh, "bf16", "grad_hidden")
+    assert_grad_close(out[1].float().cpu().numpy(), rgw, "bf16", "grad_weight")
+    assert_grad_close(out[2].float().cpu().numpy(), rgb, "bf16", "grad_bias")
 
 
 @pytest.mark.parametrize("N,H,V,axis", [
