@@ -13,6 +13,10 @@ The pins are:
   chunked sums ("Chunked Linear Loss", "Reduction semantics"), online merge over
   vocabulary splits (fused-linear-ce README, "Algorithm").
 * brute force for the metrics (fused-linear-ce README, "Metrics for free").
+* the row-sampled entry points (one row of grad_hidden, one vocabulary row of
+  grad_weight, a few rows of the forward), which the full-size GPU tests use,
+  against the full backward and forward, with softcap, z-loss, bias and
+  ignored rows.
 
 Each pin is chosen so that a plausible slip fails at least one of them: a
 dropped term, a wrong sign, a transposed operand or a wrong reduction.
@@ -85,6 +89,35 @@ def test_matches_torch_cross_entropy(reduction, with_bias, scale):
     fr = oracle.forward_rows(h, W, t, rows, bias=b, logit_scale=scale)
     np.testing.assert_allclose(fr["loss"], out["loss_rows"][rows], rtol=1e-13)
     np.testing.assert_allclose(fr["lse"], out["lse"][rows], rtol=1e-13)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean", "none"])
+@pytest.mark.parametrize("softcap,zeta,scale", [(None, 0.3, 1.0), (2.0, 0.0, 0.6),
+                                                (1.5, 0.2, -0.8)])
+def test_row_sampled_entry_points_with_softcap_and_zloss(reduction, softcap, zeta, scale):
+    """The sampled entry points the full-size GPU tests use (one row of
+    grad_hidden, one vocabulary row of grad_weight / grad_bias, the forward of
+    a few rows) agree with the full backward and forward, which the finite
+    differences and torch autograd pin, with the softcap and z-loss factors,
+    ignored rows and a bias."""
+    h, W, b, t = rnd(5, 10, 6, 11, bias=True, ignore=(1, 6))
+    g = np.random.default_rng(9).standard_normal(10) if reduction == "none" else 1.3
+    kw = dict(bias=b, logit_scale=scale, softcap=softcap, z_loss_multiplier=zeta)
+    out = oracle.forward(h, W, t, reduction=reduction, **kw)
+    gh, gw, gb = oracle.backward(h, W, t, reduction=reduction, grad_loss=g, **kw)
+    rows = [0, 1, 4, 9]
+    np.testing.assert_allclose(
+        oracle.grad_hidden_rows(h, W, t, rows, reduction=reduction, grad_loss=g, **kw),
+        gh[rows], rtol=1e-12, atol=1e-14)
+    J = [0, 3, 10]
+    gwJ, gbJ = oracle.grad_weight_rows(h, W, t, out["lse"], J, reduction=reduction,
+                                       grad_loss=g, **kw)
+    np.testing.assert_allclose(gwJ, gw[J], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gbJ, gb[J], rtol=1e-12, atol=1e-14)
+    fr = oracle.forward_rows(h, W, t, rows, **kw)
+    np.testing.assert_allclose(fr["loss"], out["loss_rows"][rows], rtol=1e-13)
+    np.testing.assert_allclose(fr["lse"], out["lse"][rows], rtol=1e-13)
+    np.testing.assert_allclose(fr["entropy"], out["entropy_rows"][rows], rtol=1e-12)
 
 
 def test_lse_matches_torch_logsumexp():
