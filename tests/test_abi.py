@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from linear_cross_entropy_tiled_gb300 import _lib
@@ -316,3 +317,44 @@ def test_chunk_grads_regions_of_smaller_chunks_lie_inside_the_largest(lib, dtype
         for name, off, n in _lib.workspace_regions(q, _lib.FLCE_PASS_CHUNK_GRADS):
             roff, rn = ref[name]
             assert roff == off and n <= rn, (N, name, off, n, roff, rn)
+
+
+def test_backward_layouts_over_random_shapes(lib):
+    """Every backward workspace layout, over a seeded sweep of shapes, dtypes and
+    schedule options: the regions lie in address order without overlap, inside
+    the size flce_workspace_bytes reports, on 256-byte boundaries; the dlogits
+    copies respect the 4 GiB bound whenever one tile of them fits under it; h
+    is transposed exactly on the 16-bit path outside fp32-accumulated adds into
+    existing row-chunked gradients, which alone keep a transposed dlogits copy."""
+    g = np.random.default_rng(2024)
+    dtypes = {"f32": _lib.FLCE_F32, "bf16": _lib.FLCE_BF16, "f16": _lib.FLCE_F16}
+    for _ in range(400):
+        dt = str(g.choice(list(dtypes)))
+        N = int(g.choice([1, 7, 255, 256, 1000, 8192, 65536, 300000]))
+        H = int(g.choice([8, 64, 136, 4096]))
+        V = int(g.choice([1, 5, 600, 8193, 65537, 128256]))
+        axis = str(g.choice(["auto", "rows", "vocab"]))
+        accum = str(g.choice(["fp32", "weight"]))
+        accumulate = bool(g.integers(0, 2))
+        bias = bool(g.integers(0, 2))
+        max_chunk = int(g.choice([0, 0, 1, 300, 5000]))
+        p = params(N=N, H=H, V=V, dtype=dtypes[dt], bwd_chunk_axis=axis, grad_weight_accum=accum,
+                   accumulate=accumulate, has_bias=bias, max_chunk=max_chunk)
+        total = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
+        regions = _lib.workspace_regions(p, _lib.FLCE_PASS_BACKWARD)
+        case = (dt, N, H, V, axis, accum, accumulate, bias, max_chunk)
+        end = 0
+        for name, off, n in regions:
+            assert off >= end and n > 0 and off % 256 == 0, (case, name, off, n, end)
+            end = off + n
+        assert end <= total, (case, end, total)
+        r = {name: n for name, _, n in regions}
+        rows_axis = axis == "rows" or (axis == "auto" and N >= V)
+        tensor = dt != "f32"
+        two_copies = tensor and rows_axis and accum == "fp32" and accumulate
+        assert ("dlogits_transposed" in r) == two_copies, (case, sorted(r))
+        assert ("hidden_transposed" in r) == (tensor and not two_copies), (case, sorted(r))
+        elem = 2 if tensor else 4
+        one_tile = (256 if tensor else 64) * (N if not rows_axis else (V + 7) // 8 * 8) * elem
+        if one_tile <= 4 << 30:
+            assert r["dlogits"] <= 4 << 30, (case, r["dlogits"])
