@@ -192,6 +192,8 @@ int flce_workspace_bytes(const flce_params* p, int pass, size_t* bytes);
 /*
  * The regions of a pass's workspace that its kernels may write, in address
  * order: name, byte offset from the start of the workspace and byte count.
+ * Two regions share their bytes only where the pass uses them one after the
+ * other (flce_chunk_grads: grad_hidden's split partials, then h transposed).
  * Every byte of the workspace outside them is left as the caller gave it.
  * This is the layout flce_workspace_bytes sizes; the same p and pass give the
  * same regions. It is a diagnostic: tests fill the workspace with a pattern

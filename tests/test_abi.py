@@ -320,9 +320,12 @@ def test_chunk_grads_regions_of_smaller_chunks_lie_inside_the_largest(lib, dtype
 
 
 def test_backward_layouts_over_random_shapes(lib):
-    """Every backward workspace layout, over a seeded sweep of shapes, dtypes and
-    schedule options: the regions lie in address order without overlap, inside
-    the size flce_workspace_bytes reports, on 256-byte boundaries; the dlogits
+    """Every forward, chunked-loss-gradient and backward workspace layout, over a
+    seeded sweep of shapes, dtypes and schedule options: the regions lie in
+    address order without overlap (but for the one scratch region that
+    flce_chunk_grads uses first for grad_hidden's split partials, then for h^T),
+    inside the size flce_workspace_bytes reports, on 256-byte boundaries. In
+    the backward, the dlogits
     copies respect the 4 GiB bound whenever one tile of them fits under it; h
     is transposed exactly on the 16-bit path outside fp32-accumulated adds into
     existing row-chunked gradients, which alone keep a transposed dlogits copy."""
@@ -340,14 +343,23 @@ def test_backward_layouts_over_random_shapes(lib):
         max_chunk = int(g.choice([0, 0, 1, 300, 5000]))
         p = params(N=N, H=H, V=V, dtype=dtypes[dt], bwd_chunk_axis=axis, grad_weight_accum=accum,
                    accumulate=accumulate, has_bias=bias, max_chunk=max_chunk)
-        total = _lib.workspace_bytes(p, _lib.FLCE_PASS_BACKWARD)
-        regions = _lib.workspace_regions(p, _lib.FLCE_PASS_BACKWARD)
         case = (dt, N, H, V, axis, accum, accumulate, bias, max_chunk)
-        end = 0
-        for name, off, n in regions:
-            assert off >= end and n > 0 and off % 256 == 0, (case, name, off, n, end)
-            end = off + n
-        assert end <= total, (case, end, total)
+        for pass_ in (_lib.FLCE_PASS_FORWARD, _lib.FLCE_PASS_CHUNK_GRADS,
+                      _lib.FLCE_PASS_BACKWARD):
+            total = _lib.workspace_bytes(p, pass_)
+            regions = _lib.workspace_regions(p, pass_)
+            end, prev = 0, None
+            for name, off, n in regions:
+                # flce_chunk_grads finishes grad_hidden's split partials before it
+                # transposes h, so those two share one scratch region
+                shared = (pass_ == _lib.FLCE_PASS_CHUNK_GRADS and name == "hidden_transposed"
+                          and prev is not None and prev[0] == "grad_hidden_fp32"
+                          and prev[1] == off)
+                assert (off >= end or shared) and n > 0 and off % 256 == 0, \
+                    (case, pass_, name, off, n, end)
+                end = max(end, off + n)
+                prev = (name, off)
+            assert end <= total, (case, pass_, end, total)
         r = {name: n for name, _, n in regions}
         rows_axis = axis == "rows" or (axis == "auto" and N >= V)
         tensor = dt != "f32"
