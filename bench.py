@@ -13,9 +13,11 @@ Timing:
   launching stream; the K steps as a whole have a barrier and a device
   synchronize on both sides. The slowest rank's median counts.
 - ``e2e`` is the same metric through the public PyTorch API with host
-  buffers. Each step copies the step's inputs from pinned host memory and
-  reads the loss back. The copy for the next step runs on a side stream,
-  into a second set of device buffers, while the current step computes.
+  buffers, over the same number of steps. Each step copies the step's inputs
+  from pinned host memory and reads the loss back. The copy for the next
+  step runs on a side stream, into a second set of device buffers, while the
+  current step computes; only the first step's copy overlaps nothing (its
+  time alone is reported as ``h2d_ms_alone``).
 - The inputs are larger than L2 (W alone is 1.05 GB), so no L2 flush is
   needed between steps.
 
